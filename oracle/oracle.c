@@ -1,0 +1,163 @@
+/*
+ * CPU oracle for the skinny BF16 linear layer  out[M,N] = x[M,K] @ W[N,K]^T (+ bias[N]).
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is compiled into a separate shared
+ * object that only the test suite, the smoke check and the CPU-baseline leg
+ * of the benchmark load.  The CUDA library never links, includes or calls it,
+ * and it shares no header, helper or table with the CUDA sources.
+ *
+ * What it computes (the plain definition, written out):
+ *
+ *   acc[m,n] = sum_{k=0}^{K-1} f64(x[m,k]) * f64(W[n,k])        ascending k
+ *   acc[m,n] += f64(bias[n])                                      if bias given
+ *   out[m,n] = RNE_bf16(acc[m,n])                                 one rounding
+ *
+ * Source of the definition: sglang PR #30117 page, section "关键源码片段",
+ * header comment of the TGV BF16 GEMM kernel (out[M,N] = x[M,K] @ weight[N,K].T
+ * (+ bias[N]); bf16 in and out; fp32 accumulation inside).  The oracle widens
+ * to f64 instead of f32 so that only the final rounding matters: a product of
+ * two bf16 values has at most 16 significant bits and is exact in f64, so the
+ * only other error is the f64 summation (~1e-16 relative).
+ *
+ * Readings where the page is silent (also listed in the design notes):
+ *  - bias enters before the single rounding (the FP8 wrapper on the
+ *    sglang PR #28333 page adds bias after the GEMM in the output dtype;
+ *    the difference is one extra rounding, inside the test tolerance);
+ *  - rounding is IEEE round-to-nearest, ties to even;
+ *  - the router variant of the vLLM PR #42562 page writes fp32 logits
+ *    (LLBf16SplitK, out_dtype=Float32): oracle_linear_f32 rounds the same
+ *    f64 sum once to binary32 instead of bf16.
+ *
+ * The narrowing conversion (rne_narrow) is written from the IEEE 754 binary
+ * interchange format definition (sign, biased exponent, trailing significand)
+ * on the bit pattern of the f64 value; it calls no library cast.
+ */
+#include <stdint.h>
+#include <string.h>
+
+/* bf16 is the upper 16 bits of an IEEE binary32; widening is exact. */
+static double bf16_to_f64(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/*
+ * Round an f64 value to the nearest value of a narrower IEEE binary format with
+ * `ebits` exponent bits and `mbits` trailing-significand bits, ties to even.
+ * Returns the bit pattern of the narrow format (sign in bit ebits+mbits).
+ * NaN maps to the canonical quiet NaN; overflow rounds to infinity.
+ */
+static uint32_t rne_narrow(double v, int ebits, int mbits)
+{
+    uint64_t b;
+    memcpy(&b, &v, sizeof b);
+    const uint32_t sign = (uint32_t)(b >> 63) << (ebits + mbits);
+    const int e = (int)((b >> 52) & 0x7FF);
+    const uint64_t f = b & ((1ULL << 52) - 1);
+    const uint32_t exp_ones = ((1u << ebits) - 1u) << mbits;
+
+    if (e == 0x7FF)                         /* NaN or infinity */
+        return f ? (exp_ones | (1u << (mbits - 1))) : (sign | exp_ones);
+    if (e == 0)                             /* f64 zero or f64 subnormal (< 2^-1022) */
+        return sign;                        /* far below half the narrow format's smallest subnormal */
+
+    const int bias = (1 << (ebits - 1)) - 1;
+    const int E = e - 1023;                 /* v = S * 2^(E-52), S the 53-bit significand */
+    const int emin = 1 - bias;              /* exponent of the smallest normal */
+    if (E > bias)                           /* at or above 2^(bias+1): infinity */
+        return sign | exp_ones;
+
+    const uint64_t S = (1ULL << 52) | f;
+    const int q = (E >= emin ? E : emin) - mbits;   /* exponent of one unit in the last place */
+    const int shift = q - (E - 52);                  /* low bits of S that fall below that unit */
+    if (shift > 54)                         /* |v| < 2^(q-2): rounds to zero */
+        return sign;
+
+    uint64_t kept = S >> shift;
+    const uint64_t rem = S & ((1ULL << shift) - 1);
+    const uint64_t half = 1ULL << (shift - 1);
+    if (rem > half || (rem == half && (kept & 1)))
+        kept++;
+
+    uint32_t bits;
+    if (E >= emin)                          /* kept in [2^mbits, 2^(mbits+1)]; a carry bumps the exponent */
+        bits = ((uint32_t)(E + bias - 1) << mbits) + (uint32_t)kept;
+    else                                    /* subnormal: kept <= 2^mbits (== 2^mbits is the smallest normal) */
+        bits = (uint32_t)kept;
+    return sign | bits;
+}
+
+uint16_t oracle_rne_bf16(double v) { return (uint16_t)rne_narrow(v, 8, 7); }
+uint32_t oracle_rne_f32(double v) { return rne_narrow(v, 8, 23); }
+double oracle_bf16_to_f64(uint16_t h) { return bf16_to_f64(h); }
+
+/* One output element, unrounded: ascending-k f64 sum, then bias. */
+static double dot_row(const uint16_t *xrow, const uint16_t *wrow, const uint16_t *bias,
+                      int64_t n, int64_t K)
+{
+    double acc = 0.0;
+    for (int64_t k = 0; k < K; ++k)
+        acc += bf16_to_f64(xrow[k]) * bf16_to_f64(wrow[k]);
+    if (bias)
+        acc += bf16_to_f64(bias[n]);
+    return acc;
+}
+
+/* acc[M*N] (row-major), unrounded f64.  bias may be NULL. */
+void oracle_linear_f64(const uint16_t *x, const uint16_t *W, const uint16_t *bias,
+                       int64_t M, int64_t N, int64_t K, double *acc)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            acc[m * N + n] = dot_row(x + m * K, W + n * K, bias, n, K);
+}
+
+/* out[M*N] bf16 bits (row-major): the defined result. */
+void oracle_linear_bf16(const uint16_t *x, const uint16_t *W, const uint16_t *bias,
+                        int64_t M, int64_t N, int64_t K, uint16_t *out)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            out[m * N + n] = oracle_rne_bf16(dot_row(x + m * K, W + n * K, bias, n, K));
+}
+
+/* out[M*N] binary32 bits: the fp32-logits variant (one rounding to binary32). */
+void oracle_linear_f32(const uint16_t *x, const uint16_t *W, const uint16_t *bias,
+                       int64_t M, int64_t N, int64_t K, uint32_t *out)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            out[m * N + n] = oracle_rne_f32(dot_row(x + m * K, W + n * K, bias, n, K));
+}
+
+/*
+ * Selected output rows only: out[r*N + n] for m = rows[r].  Used to check
+ * sampled rows of shapes too large to evaluate in full on the CPU.
+ */
+void oracle_linear_rows_bf16(const uint16_t *x, const uint16_t *W, const uint16_t *bias,
+                             int64_t M, int64_t N, int64_t K,
+                             const int64_t *rows, int64_t nrows, uint16_t *out)
+{
+    (void)M;
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t m = rows[r];
+        for (int64_t n = 0; n < N; ++n)
+            out[r * N + n] = oracle_rne_bf16(dot_row(x + m * K, W + n * K, bias, n, K));
+    }
+}
+
+/* Unrounded selected rows (for the per-row cosine check at full size). */
+void oracle_linear_rows_f64(const uint16_t *x, const uint16_t *W, const uint16_t *bias,
+                            int64_t M, int64_t N, int64_t K,
+                            const int64_t *rows, int64_t nrows, double *acc)
+{
+    (void)M;
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t m = rows[r];
+        for (int64_t n = 0; n < N; ++n)
+            acc[r * N + n] = dot_row(x + m * K, W + n * K, bias, n, K);
+    }
+}
