@@ -1,0 +1,165 @@
+/*
+ * bf16_linear.h — C ABI of the GB300 (sm_103a) skinny BF16 linear layer.
+ *
+ *     out[M,N] = x[M,K] @ W[N,K]^T (+ bias[N])
+ *
+ * Operation: the unquantised serving linear layer defined in the header comment
+ * of the TGV BF16 GEMM kernel (sglang PR #30117 page, "关键源码片段": out[M, N]
+ * = x[M, K] @ weight[N, K].T (+ bias[N]); bf16 inputs and output, fp32
+ * accumulation inside).  Its hot regime is the decode / MoE-router shape with
+ * M <= 16 tokens (vLLM PR #42562 page, "实现拆解" items 1-4), where reading W
+ * from HBM sets the cost.
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller, on the
+ *    current CUDA device.  The library keeps no reference after the call
+ *    returns (the launch is asynchronous: buffers must stay valid until the
+ *    stream reaches it).
+ *  - Layouts are dense row-major with no padding: x[M][K], W[N][K] (the
+ *    nn.Linear weight layout), out[M][N], bias[N].  Elements are IEEE bfloat16
+ *    (the upper 16 bits of a binary32), except out of bf16_linear_f32out.
+ *  - Pointers must be 16-byte aligned (the vLLM PR #42562 review lowered the
+ *    assumed alignment of these kernels to 16 bytes).  out must not overlap
+ *    x, W or bias.
+ *  - Arithmetic: every product and sum in fp32, then out = RNE_bf16(acc + bias)
+ *    (bias, when given, is added in fp32 before the single rounding).  The
+ *    summation order depends on the kernel the plan picks; for a fixed plan the
+ *    result is bitwise deterministic from run to run.
+ *  - Nothing allocates device memory, nothing synchronises the stream, and the
+ *    calls are safe to make from several host threads at once.  A call may be
+ *    captured in a CUDA graph once the device has been initialised by one
+ *    earlier non-captured call on it (initialisation sets kernel attributes).
+ *  - Device: compute capability 10.3 (GB300) only; any other device returns
+ *    BF16L_EARCH (the TGV page notes its kernel is built for SM10x only and
+ *    errors elsewhere; this library is built for sm_103a alone).
+ *  - Errors are reported by return value; no entry point aborts the process.
+ */
+#ifndef BF16_LINEAR_H
+#define BF16_LINEAR_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* CUDA stream handle (a cudaStream_t / CUstream); NULL means the legacy default stream. */
+typedef void *bf16l_stream_t;
+
+typedef enum {
+    BF16L_OK = 0,
+    BF16L_EINVAL = -1,       /* bad size, NULL required pointer, or a plan that cannot run this shape */
+    BF16L_EALIGN = -2,       /* a pointer is not 16-byte aligned */
+    BF16L_EARCH = -3,        /* current device is not compute capability 10.3 */
+    BF16L_ELAUNCH = -4,      /* the CUDA launch (or device query) failed; see bf16_linear_cuda_error */
+    BF16L_ETIMEOUT = -5,     /* a kernel's bounded wait gave up (read via bf16_linear_device_status) */
+    BF16L_EUNSUPPORTED = -6  /* the requested kernel does not support this shape (e.g. K % 8 != 0 for a TMA kernel) */
+} bf16l_status;
+
+/* Kernels behind the dispatcher. */
+typedef enum {
+    BF16L_KERNEL_DOTPROD = 0, /* CUDA-core dot product, 128-bit weight loads, one CTA per slice of W rows */
+    BF16L_KERNEL_SPLITK = 1,  /* TMA -> tcgen05 (weights on the MMA M side), K split over a thread-block
+                                 cluster, fp32 partials reduced through distributed shared memory */
+    BF16L_KERNEL_TILE = 2     /* persistent warp-specialised TMA -> tcgen05 -> TMEM tile GEMM */
+} bf16l_kernel;
+
+/*
+ * A launch plan: which kernel and its parameters.  Mirrors the dispatch key of
+ * the vLLM LL-BF16 router GEMM (vLLM PR #42562 page, LLBf16Gemm.CompileKey:
+ * backend, M, K, bs, split_k, num_stages), extended with the fields the
+ * tcgen05 kernels need.  Fields a kernel does not use are 0.
+ */
+typedef struct {
+    int32_t kernel;        /* bf16l_kernel */
+    int32_t threads;       /* threads per CTA */
+    int32_t rows_per_cta;  /* DOTPROD: W rows per CTA;  SPLITK / TILE: W rows per tile (MMA M or N) */
+    int32_t tokens_per_cta;/* SPLITK: tokens per MMA (M padded to 16);  TILE: x rows per tile */
+    int32_t split_k;       /* SPLITK: CTAs per cluster along K (1..16) */
+    int32_t stages;        /* SPLITK / TILE: shared-memory ring depth (64-wide K chunks) */
+    int32_t grid;          /* CTAs launched (informational; computed by the plan) */
+    int32_t flags;         /* reserved, 0 */
+} bf16l_plan;
+
+/*
+ * Describe the device a plan is made for.  bf16_linear() fills this from the
+ * current device; tests pass fake devices (the mock-device pattern of the
+ * sglang PR #34042 page's backend tests).
+ */
+typedef struct {
+    int32_t cc_major;      /* compute capability, 10 */
+    int32_t cc_minor;      /* 3 for GB300 */
+    int32_t num_sms;       /* streaming multiprocessors (152 on GB300) */
+} bf16l_device;
+
+/*
+ * bf16_linear_plan — choose the kernel and parameters for (M, N, K) on `dev`.
+ *
+ * Pure host code: makes no CUDA call and touches no device.  dev == NULL means
+ * a GB300 (cc 10.3, 152 SMs).  Rules (vLLM PR #48774 page, LLBf16Gemm.dispatch
+ * and _arch_tuned_configs, with the thresholds re-measured on GB300): a table
+ * measured on GB300 keyed by (K, N) with one entry per M decides; shapes not in
+ * the table use size rules (dot product for tiny M or K % 8 != 0, cluster
+ * split-K for skinny M, the tile kernel for large M).
+ *
+ * Returns BF16L_OK and fills *plan; BF16L_EINVAL for M < 0, N <= 0, K <= 0 or
+ * plan == NULL; BF16L_EARCH when dev is not compute capability 10.3.  M == 0
+ * yields a plan with grid == 0 (nothing to launch).
+ */
+int bf16_linear_plan(int M, int N, int K, const bf16l_device *dev, bf16l_plan *plan);
+
+/*
+ * bf16_linear — out = x @ W^T (+ bias), bf16 out, on `stream`.
+ *
+ * x: device bf16 [M][K]; W: device bf16 [N][K]; bias: device bf16 [N] or NULL;
+ * out: device bf16 [M][N], written in full (every element), never read.
+ * Asynchronous: returns after enqueueing one kernel launch (none when M == 0).
+ * Returns BF16L_OK, BF16L_EINVAL (sizes, NULL x/W/out), BF16L_EALIGN,
+ * BF16L_EARCH, or BF16L_ELAUNCH.
+ */
+int bf16_linear(const void *x, const void *W, const void *bias, void *out,
+                int M, int N, int K, bf16l_stream_t stream);
+
+/*
+ * bf16_linear_with_plan — as bf16_linear, but run exactly `plan` (for tests,
+ * sweeps and benchmarks).  No fallback: a plan that cannot run this shape
+ * returns BF16L_EINVAL or BF16L_EUNSUPPORTED without launching (an explicit
+ * request errors rather than silently falling back, as the sglang PR #34042
+ * page's backend resolution does).
+ */
+int bf16_linear_with_plan(const void *x, const void *W, const void *bias, void *out,
+                          int M, int N, int K, const bf16l_plan *plan, bf16l_stream_t stream);
+
+/*
+ * bf16_linear_device_status — read (and optionally clear) the current device's
+ * kernel status word.  0 means no kernel gave up; otherwise the first failing
+ * wait's code (BF16L_ETIMEOUT in the low byte, the wait site above it).
+ * Synchronises the device (reads device memory).  Returns BF16L_OK or
+ * BF16L_ELAUNCH.
+ */
+int bf16_linear_device_status(int32_t *status, int clear);
+
+/*
+ * bf16_linear_selftest_wait — diagnostic for the bounded-wait path.  Launches
+ * one thread that waits on a shared-memory barrier nothing ever completes and
+ * gives up after limit_us microseconds, recording BF16L_ETIMEOUT (wait site 6)
+ * in the device status word, exactly as a kernel whose wait ran out would.
+ * The GPU stays usable.  Asynchronous; returns BF16L_OK, BF16L_EARCH or
+ * BF16L_ELAUNCH.
+ */
+int bf16_linear_selftest_wait(uint32_t limit_us, bf16l_stream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *bf16_linear_strerror(int status);
+
+/* The last CUDA error code seen by the library on this host thread (0 if none). */
+int bf16_linear_cuda_error(void);
+
+/* Library version, as major * 10000 + minor * 100 + patch. */
+int bf16_linear_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BF16_LINEAR_H */

@@ -1,0 +1,11 @@
+"""GB300-native skinny BF16 linear layer: out[M,N] = x[M,K] @ W[N,K]^T (+ bias[N]).
+
+The product is the C-ABI library ``libbf16_linear.so`` (include/bf16_linear.h):
+three hand-written sm_103a kernels (CUDA-core dot product, tcgen05 cluster
+split-K with a DSMEM reduction, tcgen05 tile GEMM) behind a measured shape
+dispatcher.  This package is its thin Python binding; build the library with
+``python -m moe_router_gemm_gb300.build``.
+"""
+from ._binding import (BF16LinearError, Device, KERNEL_DOTPROD, KERNEL_NAMES, KERNEL_SPLITK,  # noqa: F401
+                       KERNEL_TILE, LIB_PATH, Plan, bf16_linear, bf16_linear_with_plan, device_status,
+                       load, make_plan, plan, selftest_wait, strerror, version)

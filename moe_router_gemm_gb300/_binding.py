@@ -1,0 +1,201 @@
+"""ctypes binding of libbf16_linear.so — argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+turns torch tensors into (pointer, size, stream) arguments, checks dtype /
+contiguity / device on the Python side (the dtype guards the vLLM PR #42562
+review asked for: both x and W must be bfloat16), and raises on a nonzero
+status.  There is no fallback: if the library is missing the import-time
+loader raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libbf16_linear.so")
+
+OK, EINVAL, EALIGN, EARCH, ELAUNCH, ETIMEOUT, EUNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
+KERNEL_DOTPROD, KERNEL_SPLITK, KERNEL_TILE = 0, 1, 2
+KERNEL_NAMES = {KERNEL_DOTPROD: "dotprod", KERNEL_SPLITK: "splitk", KERNEL_TILE: "tile"}
+
+
+class Plan(ctypes.Structure):
+    """Mirror of bf16l_plan in include/bf16_linear.h."""
+    _fields_ = [("kernel", ctypes.c_int32), ("threads", ctypes.c_int32),
+                ("rows_per_cta", ctypes.c_int32), ("tokens_per_cta", ctypes.c_int32),
+                ("split_k", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("grid", ctypes.c_int32), ("flags", ctypes.c_int32)]
+
+    def as_dict(self) -> dict:
+        d = {f[0]: int(getattr(self, f[0])) for f in self._fields_}
+        d["kernel_name"] = KERNEL_NAMES.get(d["kernel"], "?")
+        return d
+
+    def __repr__(self):
+        return f"Plan({self.as_dict()})"
+
+
+class Device(ctypes.Structure):
+    """Mirror of bf16l_device."""
+    _fields_ = [("cc_major", ctypes.c_int32), ("cc_minor", ctypes.c_int32), ("num_sms", ctypes.c_int32)]
+
+
+class BF16LinearError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the built library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise ImportError(f"{p} is missing: build it with `python -m moe_router_gemm_gb300.build` "
+                              "(there is no CPU fallback)")
+        lib = ctypes.CDLL(p)
+        vp, i32 = ctypes.c_void_p, ctypes.c_int
+        lib.bf16_linear.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp]
+        lib.bf16_linear.restype = i32
+        lib.bf16_linear_with_plan.argtypes = [vp, vp, vp, vp, i32, i32, i32, ctypes.POINTER(Plan), vp]
+        lib.bf16_linear_with_plan.restype = i32
+        lib.bf16_linear_plan.argtypes = [i32, i32, i32, ctypes.POINTER(Device), ctypes.POINTER(Plan)]
+        lib.bf16_linear_plan.restype = i32
+        lib.bf16_linear_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32), i32]
+        lib.bf16_linear_device_status.restype = i32
+        lib.bf16_linear_selftest_wait.argtypes = [ctypes.c_uint32, vp]
+        lib.bf16_linear_selftest_wait.restype = i32
+        lib.bf16_linear_strerror.argtypes = [i32]
+        lib.bf16_linear_strerror.restype = ctypes.c_char_p
+        lib.bf16_linear_cuda_error.argtypes = []
+        lib.bf16_linear_cuda_error.restype = i32
+        lib.bf16_linear_version.argtypes = []
+        lib.bf16_linear_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def strerror(status: int) -> str:
+    return load().bf16_linear_strerror(int(status)).decode()
+
+
+def _raise(status: int, what: str):
+    lib = load()
+    extra = ""
+    if status == ELAUNCH:
+        extra = f" (cuda error {lib.bf16_linear_cuda_error()})"
+    raise BF16LinearError(status, f"{what}: {strerror(status)}{extra}")
+
+
+def plan(M: int, N: int, K: int, device: tuple[int, int, int] | None = None) -> Plan:
+    """The kernel and parameters chosen for (M, N, K); device = (cc_major, cc_minor, num_sms)."""
+    p = Plan()
+    dev = Device(*device) if device is not None else None
+    st = load().bf16_linear_plan(int(M), int(N), int(K), ctypes.byref(dev) if dev is not None else None,
+                                 ctypes.byref(p))
+    if st != OK:
+        _raise(st, f"bf16_linear_plan({M},{N},{K})")
+    return p
+
+
+def make_plan(kernel: int | str, **fields) -> Plan:
+    """Build an explicit plan (for with_plan); unspecified fields are 0."""
+    if isinstance(kernel, str):
+        kernel = {v: k for k, v in KERNEL_NAMES.items()}[kernel]
+    p = Plan()
+    p.kernel = int(kernel)
+    for k, v in fields.items():
+        setattr(p, k, int(v))
+    return p
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _check(x, W, bias, out):
+    import torch
+    if x.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise TypeError(f"x and W must be torch.bfloat16 (got {x.dtype}, {W.dtype})")
+    if bias is not None and bias.dtype != torch.bfloat16:
+        raise TypeError(f"bias must be torch.bfloat16 (got {bias.dtype})")
+    if x.dim() != 2 or W.dim() != 2 or x.shape[1] != W.shape[1]:
+        raise ValueError(f"need x[M,K] and W[N,K], got {tuple(x.shape)} and {tuple(W.shape)}")
+    M, K = x.shape
+    N = W.shape[0]
+    if bias is not None and tuple(bias.shape) != (N,):
+        raise ValueError(f"bias must be [{N}], got {tuple(bias.shape)}")
+    for name, t in (("x", x), ("W", W), ("bias", bias)):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    elif out.dtype != torch.bfloat16 or tuple(out.shape) != (M, N) or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError("out must be a contiguous CUDA bf16 tensor of shape [M, N]")
+    devs = {t.device for t in (x, W, bias, out) if t is not None}
+    if len(devs) != 1:
+        raise ValueError(f"all tensors must be on one device, got {devs}")
+    return M, N, K, out
+
+
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def bf16_linear(x, W, bias=None, out=None, stream=None):
+    """out[M,N] = x[M,K] @ W[N,K]^T (+ bias[N]) in bf16, on the given (or current) stream."""
+    import torch
+    M, N, K, out = _check(x, W, bias, out)
+    with torch.cuda.device(x.device):
+        st = load().bf16_linear(_ptr(x), _ptr(W), _ptr(bias), _ptr(out), M, N, K,
+                                _stream_handle(stream, x.device))
+    if st != OK:
+        _raise(st, f"bf16_linear(M={M}, N={N}, K={K})")
+    return out
+
+
+def bf16_linear_with_plan(x, W, bias=None, out=None, plan_: Plan | None = None, stream=None):
+    """Run exactly `plan_` (no fallback: an unusable plan raises)."""
+    import torch
+    if plan_ is None:
+        raise ValueError("plan_ is required")
+    M, N, K, out = _check(x, W, bias, out)
+    with torch.cuda.device(x.device):
+        st = load().bf16_linear_with_plan(_ptr(x), _ptr(W), _ptr(bias), _ptr(out), M, N, K,
+                                          ctypes.byref(plan_), _stream_handle(stream, x.device))
+    if st != OK:
+        _raise(st, f"bf16_linear_with_plan(M={M}, N={N}, K={K}, {plan_})")
+    return out
+
+
+def device_status(clear: bool = False) -> int:
+    """The device's kernel status word (0 = no kernel wait gave up).  Synchronises."""
+    v = ctypes.c_int32(0)
+    st = load().bf16_linear_device_status(ctypes.byref(v), int(bool(clear)))
+    if st != OK:
+        _raise(st, "bf16_linear_device_status")
+    return int(v.value)
+
+
+def selftest_wait(limit_us: int, stream=None):
+    """Launch the bounded-wait diagnostic (see bf16_linear.h)."""
+    import torch
+    st = load().bf16_linear_selftest_wait(int(limit_us), _stream_handle(stream, torch.cuda.current_device()))
+    if st != OK:
+        _raise(st, "bf16_linear_selftest_wait")
+
+
+def version() -> int:
+    return int(load().bf16_linear_version())

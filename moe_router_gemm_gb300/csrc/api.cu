@@ -1,0 +1,240 @@
+// api.cu — the C ABI: argument validation, per-device initialisation, the
+// kernel status word, TMA descriptor encoding and the launch itself.
+//
+// Validation follows the contract in bf16_linear.h: sizes and pointers are
+// checked before any CUDA call (so the checks also run on hosts without a GPU),
+// then the device is checked (compute capability 10.3 only), then the plan is
+// made and exactly one kernel is launched.  Nothing here allocates device
+// memory or synchronises a stream.
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include <functional>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bf16l {
+
+// The kernel status word (one per device, in this module's device image).
+__device__ int32_t g_status = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    std::once_flag once;
+    int err = 0;  // cudaError_t of the initialisation
+    bf16l_device dev = {0, 0, 0};
+    int32_t *status = nullptr;
+};
+DeviceState g_devices[kMaxDevices];
+
+thread_local int t_last_cuda_error = 0;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int note(int cuda_err) {
+    if (cuda_err != 0) t_last_cuda_error = cuda_err;
+    return cuda_err;
+}
+
+void init_device(DeviceState &s) {
+    int d = 0;
+    int e = (int)cudaGetDevice(&d);
+    if (!e) e = (int)cudaDeviceGetAttribute(&s.dev.cc_major, cudaDevAttrComputeCapabilityMajor, d);
+    if (!e) e = (int)cudaDeviceGetAttribute(&s.dev.cc_minor, cudaDevAttrComputeCapabilityMinor, d);
+    if (!e) e = (int)cudaDeviceGetAttribute(&s.dev.num_sms, cudaDevAttrMultiProcessorCount, d);
+    if (!e && s.dev.cc_major == 10 && s.dev.cc_minor == 3) {
+        // Host code cannot take the address of a __device__ variable directly:
+        // ask the runtime for this device's copy.
+        void *p = nullptr;
+        e = (int)cudaGetSymbolAddress(&p, g_status);
+        s.status = static_cast<int32_t *>(p);
+        if (!e) e = init_dotprod();
+        if (!e) e = init_splitk();
+        if (!e) e = init_tile();
+    }
+    s.err = e;
+}
+
+// Current device's state, initialised once.  Returns a bf16l_status.
+int current_device(DeviceState **out) {
+    int d = 0;
+    const int e = (int)cudaGetDevice(&d);
+    if (e) {
+        note(e);
+        return BF16L_ELAUNCH;
+    }
+    if (d < 0 || d >= kMaxDevices) return BF16L_ELAUNCH;
+    DeviceState &s = g_devices[d];
+    std::call_once(s.once, init_device, std::ref(s));
+    if (s.err) {
+        note(s.err);
+        return BF16L_ELAUNCH;
+    }
+    if (s.dev.cc_major != 10 || s.dev.cc_minor != 3) return BF16L_EARCH;
+    *out = &s;
+    return BF16L_OK;
+}
+
+bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+bool overlaps(const void *a, uint64_t abytes, const void *b, uint64_t bbytes) {
+    if (!a || !b || abytes == 0 || bbytes == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+// Size and pointer checks that need no GPU.  BF16L_OK means "go on".
+int check_args(const void *x, const void *W, const void *bias, void *out, int M, int N, int K) {
+    if (M < 0 || N <= 0 || K <= 0) return BF16L_EINVAL;
+    if (M == 0) return BF16L_OK;
+    if (!x || !W || !out) return BF16L_EINVAL;
+    if (misaligned(x) || misaligned(W) || misaligned(out) || (bias && misaligned(bias))) return BF16L_EALIGN;
+    const uint64_t xb = 2ull * (uint64_t)M * (uint64_t)K, wb = 2ull * (uint64_t)N * (uint64_t)K;
+    const uint64_t ob = 2ull * (uint64_t)M * (uint64_t)N, bb = bias ? 2ull * (uint64_t)N : 0;
+    if (overlaps(out, ob, x, xb) || overlaps(out, ob, W, wb) || overlaps(out, ob, bias, bb)) return BF16L_EINVAL;
+    return BF16L_OK;
+}
+
+int run(const void *x, const void *W, const void *bias, void *out, int M, int N, int K, const bf16l_plan *forced,
+        bf16l_stream_t stream) {
+    int st = check_args(x, W, bias, out, M, N, K);
+    if (st != BF16L_OK) return st;
+    if (M == 0) return BF16L_OK;
+    if (forced) {
+        // Check the requested plan's shape rules before touching the device.
+        bf16l_plan tmp = *forced;
+        const bf16l_device any = {10, 3, kGb300Sms};
+        st = check_plan(M, N, K, any, &tmp);
+        if (st != BF16L_OK) return st;
+    }
+    DeviceState *ds = nullptr;
+    st = current_device(&ds);
+    if (st != BF16L_OK) return st;
+
+    bf16l_plan p;
+    if (forced) {
+        p = *forced;
+        st = check_plan(M, N, K, ds->dev, &p);
+    } else {
+        st = bf16_linear_plan(M, N, K, &ds->dev, &p);
+    }
+    if (st != BF16L_OK) return st;
+
+    LaunchArgs a = {x, W, bias, out, M, N, K, stream, ds->dev.num_sms, ds->status};
+    int e = 0;
+    switch (p.kernel) {
+        case BF16L_KERNEL_DOTPROD: e = launch_dotprod(a, p); break;
+        case BF16L_KERNEL_SPLITK: e = launch_splitk(a, p); break;
+        case BF16L_KERNEL_TILE: e = launch_tile(a, p); break;
+        default: return BF16L_EINVAL;
+    }
+    if (e) {
+        note(e);
+        return BF16L_ELAUNCH;
+    }
+    return BF16L_OK;
+}
+
+// One thread waits on an mbarrier that nothing arrives on, for limit_ns.
+__global__ void selftest_wait_kernel(int32_t *status, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    mbar_wait(&bar, 0, status, kSiteSelftest, limit_ns);
+    // Complete the barrier's phase ourselves so nothing is left pending.
+    mbar_arrive(&bar);
+}
+
+}  // namespace
+
+int make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                      uint32_t box_cols, CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo) {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode) return (int)CUDA_ERROR_NOT_FOUND;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};  // bytes between rows
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return (int)g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace bf16l
+
+// ---------------------------------------------------------------------------
+// Exported entry points.
+// ---------------------------------------------------------------------------
+extern "C" int bf16_linear(const void *x, const void *W, const void *bias, void *out, int M, int N, int K,
+                           bf16l_stream_t stream) {
+    return bf16l::run(x, W, bias, out, M, N, K, nullptr, stream);
+}
+
+extern "C" int bf16_linear_with_plan(const void *x, const void *W, const void *bias, void *out, int M, int N,
+                                     int K, const bf16l_plan *plan, bf16l_stream_t stream) {
+    if (!plan) return BF16L_EINVAL;
+    return bf16l::run(x, W, bias, out, M, N, K, plan, stream);
+}
+
+extern "C" int bf16_linear_device_status(int32_t *status, int clear) {
+    using namespace bf16l;
+    if (!status) return BF16L_EINVAL;
+    DeviceState *ds = nullptr;
+    const int st = current_device(&ds);
+    if (st != BF16L_OK) return st;
+    int32_t v = 0;
+    int e = (int)cudaMemcpy(&v, ds->status, sizeof v, cudaMemcpyDeviceToHost);
+    if (!e && clear) {
+        const int32_t zero = 0;
+        e = (int)cudaMemcpy(ds->status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    }
+    if (e) {
+        note(e);
+        return BF16L_ELAUNCH;
+    }
+    *status = v;
+    return BF16L_OK;
+}
+
+extern "C" int bf16_linear_selftest_wait(uint32_t limit_us, bf16l_stream_t stream) {
+    using namespace bf16l;
+    DeviceState *ds = nullptr;
+    const int st = current_device(&ds);
+    if (st != BF16L_OK) return st;
+    selftest_wait_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(ds->status, (uint64_t)limit_us * 1000ull);
+    const int e = (int)cudaGetLastError();
+    if (e) {
+        note(e);
+        return BF16L_ELAUNCH;
+    }
+    return BF16L_OK;
+}
+
+extern "C" const char *bf16_linear_strerror(int status) {
+    switch (status) {
+        case BF16L_OK: return "ok";
+        case BF16L_EINVAL: return "invalid argument";
+        case BF16L_EALIGN: return "pointer not 16-byte aligned";
+        case BF16L_EARCH: return "device is not compute capability 10.3 (GB300)";
+        case BF16L_ELAUNCH: return "CUDA launch or device query failed";
+        case BF16L_ETIMEOUT: return "a kernel wait timed out";
+        case BF16L_EUNSUPPORTED: return "the requested kernel does not support this shape";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int bf16_linear_cuda_error(void) { return bf16l::t_last_cuda_error; }
+
+extern "C" int bf16_linear_version(void) { return 1 * 10000 + 0 * 100 + 0; }

@@ -1,0 +1,171 @@
+// dotprod.cu — CUDA-core dot-product kernel for the smallest token counts.
+//
+// Prior art: the LLBf16Dotprod kernel on the vLLM PR #42562 page ("实现拆解"
+// item 1 and its source excerpt): one CTA per expert row, 128-bit weight
+// loads, each weight vector widened to fp32 once and used for every token,
+// warp-shuffle then shared-memory reduction; chosen for M <= 4 or K < 2048.
+//
+// This kernel keeps that structure and adds what GB300 needs to keep enough
+// bytes in flight at such small sizes: a CTA owns R consecutive W rows (so each
+// x vector, read from L2, is reused R times), and every thread issues all the
+// 16-byte weight loads of a batch of up to 8 vectors per row before it does any
+// arithmetic.  Tokens are processed MT at a time (MT = M for M <= 8); larger M
+// loops over W again, which only the K % 8 != 0 fallback ever does.
+//
+// Arithmetic: fp32 products and sums (each thread sums its k-slice in
+// ascending order, then a fixed shuffle tree and a fixed in-order sum over
+// warps), bias added in fp32, one RNE rounding to bf16.  Deterministic.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bf16l {
+
+template <int VEC>
+struct Vec;
+template <>
+struct Vec<8> {  // 8 bf16 in 16 bytes
+    uint4 v;
+    __device__ __forceinline__ void load_stream(const uint16_t *p) { v = ldg_stream_v4(p); }
+    __device__ __forceinline__ void load_cached(const uint16_t *p) { v = __ldg(reinterpret_cast<const uint4 *>(p)); }
+    __device__ __forceinline__ float get(int e) const {
+        const uint32_t w = (e < 2) ? v.x : (e < 4) ? v.y : (e < 6) ? v.z : v.w;
+        return (e & 1) ? bf16_hi(w) : bf16_lo(w);
+    }
+};
+template <>
+struct Vec<1> {  // one bf16 (rows not 16-byte aligned when K % 8 != 0)
+    uint16_t v;
+    __device__ __forceinline__ void load_stream(const uint16_t *p) { v = __ldg(p); }
+    __device__ __forceinline__ void load_cached(const uint16_t *p) { v = __ldg(p); }
+    __device__ __forceinline__ float get(int) const { return bf16_to_f32(v); }
+};
+
+template <int MT, int R, int VEC>
+__global__ void __launch_bounds__(256) dotprod_kernel(const uint16_t *__restrict__ x,
+                                                      const uint16_t *__restrict__ W,
+                                                      const uint16_t *__restrict__ bias,
+                                                      uint16_t *__restrict__ out, int M, int N, int K) {
+    constexpr int U = (VEC == 8) ? 8 : 4;  // vectors per row a thread loads before computing
+    __shared__ float red[8][R * MT];
+
+    const int tid = threadIdx.x;
+    const int nt = blockDim.x;
+    const int warp = tid >> 5, lane = tid & 31, nwarps = nt >> 5;
+    const int n0 = blockIdx.x * R;
+    const int nvec = K / VEC;
+
+    const uint16_t *wrow[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int n = min(n0 + r, N - 1);  // rows past N re-read the last row and are not stored
+        wrow[r] = W + (size_t)n * K;
+    }
+
+    for (int m0 = 0; m0 < M; m0 += MT) {
+        float acc[R][MT];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
+
+        for (int v0 = tid; v0 < nvec; v0 += U * nt) {
+            Vec<VEC> wv[U][R];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int v = v0 + u * nt;
+                if (v < nvec) {
+#pragma unroll
+                    for (int r = 0; r < R; ++r) wv[u][r].load_stream(wrow[r] + (size_t)v * VEC);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int v = v0 + u * nt;
+                if (v < nvec) {
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        if (m0 + m < M) {
+                            Vec<VEC> xv;
+                            xv.load_cached(x + (size_t)(m0 + m) * K + (size_t)v * VEC);
+#pragma unroll
+                            for (int e = 0; e < VEC; ++e) {
+                                const float xe = xv.get(e);
+#pragma unroll
+                                for (int r = 0; r < R; ++r) acc[r][m] = fmaf(xe, wv[u][r].get(e), acc[r][m]);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+
+        // Block reduction: shuffle tree within each warp, then warps in order.
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                float v = acc[r][m];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                if (lane == 0) red[warp][r * MT + m] = v;
+            }
+        __syncthreads();
+        if (tid < R * MT) {
+            const int r = tid / MT, m = tid % MT;
+            float s = 0.f;
+            for (int w = 0; w < nwarps; ++w) s += red[w][tid];
+            const int n = n0 + r, mm = m0 + m;
+            if (n < N && mm < M) {
+                if (bias) s += bf16_to_f32(bias[n]);
+                out[(size_t)mm * N + n] = f32_to_bf16(s);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+typedef void (*DotFn)(const uint16_t *, const uint16_t *, const uint16_t *, uint16_t *, int, int, int);
+
+template <int MT, int R>
+static DotFn pick_vec(bool vec8) {
+    return vec8 ? dotprod_kernel<MT, R, 8> : dotprod_kernel<MT, R, 1>;
+}
+
+template <int MT>
+static DotFn pick_rows(int R, bool vec8) {
+    switch (R) {
+        case 1: return pick_vec<MT, 1>(vec8);
+        case 2: return pick_vec<MT, 2>(vec8);
+        case 4: return pick_vec<MT, 4>(vec8);
+        default: return nullptr;
+    }
+}
+
+static DotFn pick(int MT, int R, bool vec8) {
+    switch (MT) {
+        case 1: return pick_rows<1>(R, vec8);
+        case 2: return pick_rows<2>(R, vec8);
+        case 3: return pick_rows<3>(R, vec8);
+        case 4: return pick_rows<4>(R, vec8);
+        case 5: return pick_rows<5>(R, vec8);
+        case 6: return pick_rows<6>(R, vec8);
+        case 7: return pick_rows<7>(R, vec8);
+        case 8: return pick_rows<8>(R, vec8);
+        default: return nullptr;
+    }
+}
+
+int init_dotprod() { return (int)cudaSuccess; }
+
+int launch_dotprod(const LaunchArgs &a, const bf16l_plan &p) {
+    const int MT = a.M < kDotMaxTokens ? a.M : kDotMaxTokens;
+    DotFn fn = pick(MT, p.rows_per_cta, (a.K % 8) == 0);
+    if (!fn) return (int)cudaErrorInvalidValue;
+    const dim3 grid((unsigned)p.grid), block((unsigned)p.threads);
+    fn<<<grid, block, 0, (cudaStream_t)a.stream>>>(
+        static_cast<const uint16_t *>(a.x), static_cast<const uint16_t *>(a.W),
+        static_cast<const uint16_t *>(a.bias), static_cast<uint16_t *>(a.out), a.M, a.N, a.K);
+    return (int)cudaGetLastError();
+}
+
+}  // namespace bf16l

@@ -1,0 +1,67 @@
+// kernels.h — internal interface between the C ABI (api.cu), the planner
+// (plan.cpp) and the three kernels.  Host-only declarations: no CUDA headers,
+// so the planner builds and runs without a GPU.
+#pragma once
+
+#include <stdint.h>
+
+#include "bf16_linear.h"
+
+namespace bf16l {
+
+// ---- parameter limits shared by the planner and the launchers ----
+
+// Dot-product kernel: tokens handled per pass over W (one template instance
+// per count), W rows per CTA, and block sizes.
+constexpr int kDotMaxTokens = 8;
+constexpr int kDotRows[] = {1, 2, 4};
+constexpr int kDotThreads[] = {64, 128, 256};
+
+// Cluster split-K kernel: 128 W rows on the MMA M side; tokens (MMA N) padded
+// to a multiple of 16 up to 64; K split over up to 16 CTAs of one cluster.
+constexpr int kSplitRows = 128;
+constexpr int kSplitMaxTokens = 64;
+constexpr int kSplitMaxCluster = 16;
+constexpr int kSplitMaxStages = 8;
+constexpr int kSplitThreads = 128;
+
+// Tile kernel: BM x rows, BN W rows per tile, 64-wide K chunks.
+constexpr int kTileBM = 128;
+constexpr int kTileBN = 256;
+constexpr int kTileMinStages = 2;
+constexpr int kTileMaxStages = 4;
+constexpr int kTileThreads = 192;
+
+constexpr int kChunkK = 64;  // K elements per TMA box row (128 bytes, the swizzle width)
+
+// GB300 default device description (cc 10.3, 152 SMs).
+constexpr int kGb300Sms = 152;
+
+// Validate a plan against a shape; BF16L_OK or the error to return.  Fills
+// plan->grid.  Pure host logic.
+int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *plan);
+
+// Device-side launchers (defined in the .cu files).
+struct LaunchArgs {
+    const void *x;
+    const void *W;
+    const void *bias;
+    void *out;
+    int M, N, K;
+    void *stream;     // cudaStream_t
+    int num_sms;
+    int32_t *status;  // device address of the kernel status word
+};
+
+// Each returns a cudaError_t value (0 on success).
+int launch_dotprod(const LaunchArgs &a, const bf16l_plan &p);
+int launch_splitk(const LaunchArgs &a, const bf16l_plan &p);
+int launch_tile(const LaunchArgs &a, const bf16l_plan &p);
+
+// One-time per-device kernel attribute setup (dynamic shared memory limits,
+// non-portable cluster sizes).  Returns a cudaError_t value.
+int init_dotprod();
+int init_splitk();
+int init_tile();
+
+}  // namespace bf16l

@@ -1,0 +1,156 @@
+// plan.cpp — shape -> kernel dispatch (pure host code, no CUDA calls).
+//
+// Structure follows the vLLM LL-BF16 router GEMM dispatcher (vLLM PR #48774
+// page, LLBf16Gemm.dispatch / _arch_tuned_configs): a table keyed by (K, N)
+// with one entry per M, measured on the target GPU, decides; anything not in
+// the table falls back to size rules.  The page's own rule (dot product when
+// M <= 4 or K < 2048, split-K otherwise, default (split_k, num_stages) =
+// (6, 4)) was tuned on other hardware; here the table is re-measured on GB300
+// (dispatch_table.inc, written by the sweep in bench.py) and the size rules
+// are only the starting point for shapes it does not list.
+#include <stdint.h>
+
+#include "bf16_linear.h"
+#include "kernels.h"
+
+namespace bf16l {
+
+namespace {
+
+struct TableEntry {
+    int K, N, M;
+    int kernel, threads, rows_per_cta, tokens_per_cta, split_k, stages;
+};
+
+// Measured on GB300 (sm_103a, 152 SMs).  Regenerate with `python bench.py --sweep`.
+const TableEntry kTable[] = {
+#include "dispatch_table.inc"
+    {0, 0, 0, 0, 0, 0, 0, 0, 0}  // sentinel
+};
+
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+int round_up(int a, int b) { return ceil_div(a, b) * b; }
+
+bool in_list(int v, const int *list, int n) {
+    for (int i = 0; i < n; ++i)
+        if (list[i] == v) return true;
+    return false;
+}
+
+void plan_dotprod(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
+    (void)M;
+    (void)K;
+    p->kernel = BF16L_KERNEL_DOTPROD;
+    p->threads = 128;
+    p->rows_per_cta = (N < 2 * dev.num_sms) ? 1 : (N < 16 * dev.num_sms ? 2 : 4);
+}
+
+void plan_splitk(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
+    const int n_tiles = ceil_div(N, kSplitRows);
+    const int chunks = ceil_div(K, kChunkK);
+    int split = dev.num_sms / n_tiles;
+    if (split < 1) split = 1;
+    if (split > kSplitMaxCluster) split = kSplitMaxCluster;
+    if (split > chunks) split = chunks;
+    int per_cta = ceil_div(chunks, split);
+    p->kernel = BF16L_KERNEL_SPLITK;
+    p->threads = kSplitThreads;
+    p->rows_per_cta = kSplitRows;
+    p->tokens_per_cta = round_up(M, 16);
+    p->split_k = split;
+    p->stages = per_cta < kSplitMaxStages ? per_cta : kSplitMaxStages;
+}
+
+void plan_tile(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
+    (void)M;
+    (void)N;
+    (void)K;
+    (void)dev;
+    p->kernel = BF16L_KERNEL_TILE;
+    p->threads = kTileThreads;
+    p->rows_per_cta = kTileBN;
+    p->tokens_per_cta = kTileBM;
+    p->stages = kTileMaxStages;
+}
+
+}  // namespace
+
+int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
+    if (M < 0 || N <= 0 || K <= 0) return BF16L_EINVAL;
+    const int64_t n_tiles_split = (N + kSplitRows - 1) / kSplitRows;
+    switch (p->kernel) {
+        case BF16L_KERNEL_DOTPROD: {
+            if (!in_list(p->threads, kDotThreads, 3) || !in_list(p->rows_per_cta, kDotRows, 3))
+                return BF16L_EINVAL;
+            p->grid = M == 0 ? 0 : ceil_div(N, p->rows_per_cta);
+            return BF16L_OK;
+        }
+        case BF16L_KERNEL_SPLITK: {
+            if (K % 8 != 0) return BF16L_EUNSUPPORTED;  // TMA needs 16-byte row strides
+            if (M > kSplitMaxTokens) return BF16L_EUNSUPPORTED;
+            const int chunks = ceil_div(K, kChunkK);
+            if (p->threads != kSplitThreads || p->rows_per_cta != kSplitRows) return BF16L_EINVAL;
+            if (p->tokens_per_cta < 16 || p->tokens_per_cta > kSplitMaxTokens || p->tokens_per_cta % 16 != 0 ||
+                p->tokens_per_cta < M)
+                return BF16L_EINVAL;
+            if (p->split_k < 1 || p->split_k > kSplitMaxCluster || p->split_k > chunks) return BF16L_EINVAL;
+            if (p->stages < 1 || p->stages > kSplitMaxStages) return BF16L_EINVAL;
+            const int64_t grid = n_tiles_split * p->split_k;
+            if (grid > 65535LL * kSplitMaxCluster) return BF16L_EUNSUPPORTED;
+            p->grid = M == 0 ? 0 : (int)grid;
+            return BF16L_OK;
+        }
+        case BF16L_KERNEL_TILE: {
+            if (K % 8 != 0) return BF16L_EUNSUPPORTED;
+            if (p->threads != kTileThreads || p->rows_per_cta != kTileBN || p->tokens_per_cta != kTileBM)
+                return BF16L_EINVAL;
+            if (p->stages < kTileMinStages || p->stages > kTileMaxStages) return BF16L_EINVAL;
+            const int64_t tiles = (int64_t)ceil_div(M, kTileBM) * ceil_div(N, kTileBN);
+            const int64_t grid = tiles < dev.num_sms ? tiles : dev.num_sms;
+            p->grid = M == 0 ? 0 : (int)grid;
+            return BF16L_OK;
+        }
+        default:
+            return BF16L_EINVAL;
+    }
+}
+
+}  // namespace bf16l
+
+extern "C" int bf16_linear_plan(int M, int N, int K, const bf16l_device *devp, bf16l_plan *plan) {
+    using namespace bf16l;
+    if (!plan || M < 0 || N <= 0 || K <= 0) return BF16L_EINVAL;
+    const bf16l_device gb300 = {10, 3, kGb300Sms};
+    const bf16l_device &dev = devp ? *devp : gb300;
+    if (dev.cc_major != 10 || dev.cc_minor != 3) return BF16L_EARCH;
+    if (dev.num_sms <= 0) return BF16L_EINVAL;
+
+    bf16l_plan p = {};
+    bool from_table = false;
+    for (const TableEntry *e = kTable; e->K != 0; ++e) {
+        if (e->K == K && e->N == N && e->M == M) {
+            p.kernel = e->kernel;
+            p.threads = e->threads;
+            p.rows_per_cta = e->rows_per_cta;
+            p.tokens_per_cta = e->tokens_per_cta;
+            p.split_k = e->split_k;
+            p.stages = e->stages;
+            from_table = check_plan(M, N, K, dev, &p) == BF16L_OK;
+            break;
+        }
+    }
+    if (!from_table) {
+        p = bf16l_plan{};
+        if (K % 8 != 0 || M <= 4 || (M <= 16 && K < 2048))
+            plan_dotprod(M, N, K, dev, &p);
+        else if (M <= kSplitMaxTokens)
+            plan_splitk(M, N, K, dev, &p);
+        else
+            plan_tile(M, N, K, dev, &p);
+        const int st = check_plan(M, N, K, dev, &p);
+        if (st != BF16L_OK) return st;
+    }
+    *plan = p;
+    return BF16L_OK;
+}

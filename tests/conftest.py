@@ -26,3 +26,13 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def lib():
+    """The built C-ABI library (built here if stale; there is no fallback)."""
+    from moe_router_gemm_gb300 import build as _build
+    _build.build()
+    import moe_router_gemm_gb300 as m
+    m.load()
+    return m

@@ -1,0 +1,138 @@
+"""Host-side checks of the C ABI that need no GPU: exports, plan(), validation."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(HEADER_DIR):
+        if fn.endswith(".h"):
+            text = open(os.path.join(HEADER_DIR, fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"^[A-Za-z_][\w \*]*?\b(bf16_linear\w*)\s*\(", text, flags=re.M))
+    return sorted(names)
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for want in ("bf16_linear", "bf16_linear_plan", "bf16_linear_with_plan", "bf16_linear_strerror"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    so = ctypes.CDLL(lib.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(so, n)]
+    assert not missing, f"declared but not exported: {missing}"
+
+
+def test_version_and_strerror(lib):
+    assert lib.version() >= 10000
+    for st in range(0, -7, -1):
+        assert lib.strerror(st) and lib.strerror(st) != "unknown status"
+    assert lib.strerror(12345) == "unknown status"
+
+
+# ---- plan(): the dispatch rules, on fake devices (no CUDA call is made) ----
+
+def test_plan_refuses_other_architectures(lib):
+    for dev in [(9, 0, 132), (10, 0, 148), (12, 0, 84), (10, 1, 100)]:
+        with pytest.raises(lib.BF16LinearError) as e:
+            lib.plan(4, 256, 2048, device=dev)
+        assert e.value.status == -3
+
+
+def test_plan_rejects_bad_sizes(lib):
+    for s in [(-1, 4, 4), (1, 0, 4), (1, 4, 0), (1, -3, 4)]:
+        with pytest.raises(lib.BF16LinearError) as e:
+            lib.plan(*s)
+        assert e.value.status == -1
+
+
+def test_plan_size_rules(lib):
+    # tiny M -> dot product (the pages' default rule M <= 4), any K % 8 != 0 -> dot product
+    assert lib.plan(4, 256, 2048).kernel == lib.KERNEL_DOTPROD
+    assert lib.plan(40, 256, 2881).kernel == lib.KERNEL_DOTPROD
+    assert lib.plan(300, 256, 2881).kernel == lib.KERNEL_DOTPROD
+    # large M -> tile kernel
+    p = lib.plan(8192, 14336, 4096)
+    assert p.kernel == lib.KERNEL_TILE and p.grid == 152
+    p = lib.plan(8192, 14336, 4096, device=(10, 3, 100))
+    assert p.grid == 100
+
+
+def test_plan_m_zero_launches_nothing(lib):
+    assert lib.plan(0, 256, 2048).grid == 0
+
+
+def test_plan_is_valid_everywhere(lib):
+    """Every plan the dispatcher returns for the workload shapes is a valid plan."""
+    import workloads as wl
+    pts = wl.router_sweep() + wl.decode_proj() + wl.mlp_bias() + wl.prefill() + wl.router_smallest()
+    for pt in pts:
+        p = lib.plan(pt["M"], pt["N"], pt["K"])
+        assert p.grid > 0
+        if p.kernel == lib.KERNEL_SPLITK:
+            assert p.tokens_per_cta >= pt["M"] and p.tokens_per_cta % 16 == 0
+            assert 1 <= p.split_k <= 16 and p.split_k <= -(-pt["K"] // 64)
+            assert p.grid == p.split_k * -(-pt["N"] // 128)
+        if p.kernel == lib.KERNEL_DOTPROD:
+            assert p.grid == -(-pt["N"] // p.rows_per_cta)
+
+
+# ---- bf16_linear(): argument validation happens before any CUDA call ----
+
+def _raw(lib):
+    return lib.load()
+
+
+def test_validation_without_gpu(lib):
+    L = _raw(lib)
+    A = ctypes.c_void_p(0x10000)      # never dereferenced: rejected before any CUDA call
+    B = ctypes.c_void_p(0x20000000)
+    O = ctypes.c_void_p(0x40000000)
+    # sizes
+    assert L.bf16_linear(A, B, None, O, -1, 4, 8, None) == -1
+    assert L.bf16_linear(A, B, None, O, 1, 0, 8, None) == -1
+    assert L.bf16_linear(A, B, None, O, 1, 4, 0, None) == -1
+    # M == 0: nothing to do
+    assert L.bf16_linear(None, None, None, None, 0, 4, 8, None) == 0
+    # NULL required pointers
+    assert L.bf16_linear(None, B, None, O, 1, 4, 8, None) == -1
+    assert L.bf16_linear(A, None, None, O, 1, 4, 8, None) == -1
+    assert L.bf16_linear(A, B, None, None, 1, 4, 8, None) == -1
+    # misalignment
+    assert L.bf16_linear(ctypes.c_void_p(0x10008), B, None, O, 1, 4, 8, None) == -2
+    assert L.bf16_linear(A, B, ctypes.c_void_p(0x30000002), O, 1, 4, 8, None) == -2
+    # out overlapping an input
+    assert L.bf16_linear(A, B, None, ctypes.c_void_p(0x10000), 1, 4, 8, None) == -1
+
+
+def test_forced_plan_rules_without_gpu(lib):
+    L = _raw(lib)
+    A, B, O = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000000), ctypes.c_void_p(0x40000000)
+
+    def run(M, N, K, **plan):
+        p = lib.make_plan(**plan)
+        return L.bf16_linear_with_plan(A, B, None, O, M, N, K, ctypes.byref(p), None)
+
+    split = dict(kernel="splitk", threads=128, rows_per_cta=128, tokens_per_cta=16, split_k=4, stages=2)
+    assert run(8, 256, 2049, **split) == -6            # TMA kernels need K % 8 == 0
+    assert run(65, 256, 2048, **{**split, "tokens_per_cta": 64}) == -6  # split-K holds at most 64 tokens
+    assert run(20, 256, 2048, **split) == -1           # tokens_per_cta < M
+    assert run(8, 256, 2048, **{**split, "split_k": 17}) == -1
+    assert run(8, 256, 128, **{**split, "split_k": 3}) == -1  # more CTAs than 64-wide K chunks
+    assert run(8, 256, 2048, **{**split, "stages": 9}) == -1
+    assert run(8, 256, 2048, **{**split, "tokens_per_cta": 24}) == -1
+    assert run(8, 256, 2048, kernel="dotprod", threads=96, rows_per_cta=2) == -1
+    assert run(8, 256, 2048, kernel="dotprod", threads=128, rows_per_cta=3) == -1
+    assert run(8, 256, 2048, kernel="tile", threads=192, rows_per_cta=256, tokens_per_cta=128, stages=9) == -1
+    assert run(8, 256, 2049, kernel="tile", threads=192, rows_per_cta=256, tokens_per_cta=128, stages=4) == -6
+    p = lib.make_plan(kernel=7)
+    assert L.bf16_linear_with_plan(A, B, None, O, 8, 256, 2048, ctypes.byref(p), None) == -1
+    assert L.bf16_linear_with_plan(A, B, None, O, 8, 256, 2048, None, None) == -1
