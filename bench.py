@@ -1,0 +1,544 @@
+"""Benchmark of the skinny BF16 linear layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload router|smallest|decode|mlp|prefill] [--pdl]
+
+Default workload: the MoE router sweep, M = 1..16 x (K, N) in {(4096,256),
+(6144,256), (7168,256), (7168,384), (2880,128)} (80 shapes), seeded synthetic
+bf16 inputs (workloads.py).  One step runs every shape once per weight copy in
+its rotation: each shape owns R copies of W whose total exceeds 256 MB, so
+every call reads its weights from HBM (L2-cold; x, 2..230 KB, stays L2-hot
+as an activation would).  The R back-to-back calls of a shape are one CUDA
+graph; CUDA events on the launching stream bracket each graph, so a shape's
+time per call is its events' elapsed time / R.
+
+metric / value: mean microseconds per call over the 80 shapes (lower is
+better).  roofline: the dominant kernel's algorithmic bytes (2NK + 2MK + 2MN)
+per launch over its measured average launch time, against the measured HBM
+copy bandwidth.  e2e: the same calls through the public API from pinned host
+buffers, with x and W copied in and out copied back inside the timed region.
+cpu_baseline / --impl reference: the CPU oracle (tests' reference
+implementation, f64) on the same shapes, on the host's cores.
+
+Multi-GPU: the path does not shard across GPUs in this library (replicas
+only); under torchrun each rank runs the same sweep on its own GPU and rank 0
+reports the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+L2_COLD_BYTES = 256 << 20
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def algo_bytes(M, N, K, bias):
+    return 2 * N * K + 2 * M * K + 2 * M * N + (2 * N if bias else 0)
+
+
+def algo_flops(M, N, K, bias):
+    return 2 * M * N * K + (M * N if bias else 0)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def workload_points(name):
+    return {"router": wl.router_sweep, "smallest": wl.router_smallest, "decode": wl.decode_proj,
+            "mlp": wl.mlp_bias, "prefill": wl.prefill}[name]()
+
+
+def workload_desc(name):
+    return {
+        "router": "MoE router sweep: M=1..16 x (K,N) in {(4096,256),(6144,256),(7168,256),(7168,384),(2880,128)}, no bias",
+        "smallest": "router smallest case: M=4, K=2048, N=256, no bias",
+        "decode": "decode attention-input projection: M in {1,2,4,8,16,32,64}, K=7168, N=2112, no bias",
+        "mlp": "dense MLP with bias: M in {1,8,64,256}, K=4096, N=14336",
+        "prefill": "prefill: M in {2048,8192} x (K,N) in {(7168,2112),(4096,14336),(7168,7168)}, bias on/off",
+    }[name]
+
+
+def kernel_source_hash(kernel_name):
+    src = {"dotprod": "dotprod.cu", "splitk": "splitk.cu", "tile": "tile.cu"}[kernel_name]
+    h = hashlib.sha256()
+    for f in (src, "common.cuh"):
+        h.update(open(os.path.join(ROOT, "moe_router_gemm_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:12]
+
+
+def ncu_traffic(kernel_name, M, N, K):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    want = kernel_source_hash(kernel_name)
+    for line in open(p):
+        if line.startswith("#") or not line.strip():
+            continue
+        f = line.split()
+        # kernel M N K dram_bytes_per_launch source_hash
+        if len(f) >= 6 and f[0] == kernel_name and (int(f[1]), int(f[2]), int(f[3])) == (M, N, K):
+            return int(float(f[4])) if f[5] == want else None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+
+class OracleSample:
+    """A bounded sample of the workload for the CPU oracle, run on host threads.
+
+    Shapes are taken cheapest first until the estimated cost of one pass fills
+    the budget; a shape too large for the budget on its own contributes its
+    first rows only.  The oracle is called as it stands; ctypes releases the
+    GIL, so threads evaluate different shapes (or row blocks) concurrently."""
+
+    def __init__(self, points, budget_s=15.0, threads=None, rate_macs_per_s=0.5e9):
+        import oracle
+        oracle.build()
+        self.oracle = oracle
+        self.threads = threads or os.cpu_count() or 1
+        budget = budget_s * rate_macs_per_s * self.threads
+        order = sorted(range(len(points)), key=lambda i: points[i]["M"] * points[i]["N"] * points[i]["K"])
+        self.jobs = []      # (inputs, rows or None)
+        self.calls = 0.0    # fraction of full calls one pass covers
+        self.flops = 0.0
+        acc = 0.0
+        for i in order:
+            pt = points[i]
+            M, N, K = pt["M"], pt["N"], pt["K"]
+            cost = M * N * K
+            rows = None
+            if acc + cost > budget:
+                if self.jobs and acc > 0.5 * budget:
+                    break
+                nrows = max(1, int((budget - acc) // (N * K)))
+                if nrows >= M:
+                    nrows = M
+                else:
+                    rows = np.arange(nrows, dtype=np.int64)
+                cost = nrows * N * K
+            x, W, b = wl.make_inputs(M, N, K, pt["seed"], pt["bias"])
+            self.jobs.append(((wl.bits(x), wl.bits(W), wl.bits(b)), rows))
+            frac = 1.0 if rows is None else len(rows) / M
+            self.calls += frac
+            self.flops += algo_flops(M, N, K, pt["bias"]) * frac
+            acc += cost
+        self.desc = (f"{len(self.jobs)} of {len(points)} shapes"
+                     + ("" if all(r is None for _, r in self.jobs) else " (largest on leading rows only)")
+                     + f", one oracle call each, {self.threads} host threads")
+
+    def _one(self, job):
+        (x, W, b), rows = job
+        if rows is None:
+            return self.oracle.linear_bf16(x, W, b)
+        return self.oracle.linear_rows_bf16(x, W, b, rows)
+
+    def run(self, passes):
+        import concurrent.futures as cf
+        with cf.ThreadPoolExecutor(max_workers=self.threads) as ex:
+            t0 = time.perf_counter()
+            for _ in range(passes):
+                list(ex.map(self._one, self.jobs))
+            return time.perf_counter() - t0
+
+    def value(self, wall, passes, large):
+        if large:
+            return self.flops * passes / wall / 1e12
+        return wall / (self.calls * passes) * 1e6
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+class Shape:
+    def __init__(self, pt, device, lib, plan_override=None, pdl=False):
+        self.pt = pt
+        M, N, K, bias = pt["M"], pt["N"], pt["K"], pt["bias"]
+        self.M, self.N, self.K, self.bias = M, N, K, bias
+        x, W, b = wl.make_inputs(M, N, K, pt["seed"], bias)
+        self.host = (x, W, b)
+        wbytes = 2 * N * K
+        self.R = max(2, -(-L2_COLD_BYTES // wbytes)) if wbytes < L2_COLD_BYTES else 2
+        self.x = x.to(device)
+        W0 = W.to(device)
+        self.Ws = [W0] + [W0.clone() for _ in range(self.R - 1)]
+        self.b = b.to(device) if b is not None else None
+        self.out = torch.empty(M, N, dtype=torch.bfloat16, device=device)
+        self.plan = plan_override or lib.plan(M, N, K)
+        self.plan.flags = 1 if pdl else 0  # BF16L_FLAG_PDL
+        self.kernel = lib.KERNEL_NAMES[self.plan.kernel]
+        self.lib = lib
+        self.graph = None
+
+    def call(self, i):
+        self.lib.bf16_linear_with_plan(self.x, self.Ws[i % self.R], self.b, self.out, plan_=self.plan)
+
+    def capture(self, stream):
+        for i in range(min(self.R, 3)):  # initialise outside capture
+            self.call(i)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(self.R):
+                self.call(i)
+        self.graph = g
+
+
+def gpu_arm(args, points, rank, world):
+    import moe_router_gemm_gb300 as lib
+    from moe_router_gemm_gb300 import build as _build
+    _build.build()
+    device = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.Stream(device)
+
+    shapes = [Shape(pt, device, lib, pdl=args.pdl) for pt in points]
+    with torch.cuda.stream(stream):
+        for s in shapes:
+            s.capture(stream)
+    torch.cuda.synchronize()
+
+    def step(events=None):
+        for j, s in enumerate(shapes):
+            if events is not None:
+                events[j][0].record(stream)
+            s.graph.replay()
+            if events is not None:
+                events[j][1].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in shapes] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for k in range(args.steps):
+            step(ev[k])
+        t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    total_ms = t0.elapsed_time(t1)
+    per_shape_us = []
+    for j, s in enumerate(shapes):
+        ms = [ev[k][j][0].elapsed_time(ev[k][j][1]) for k in range(args.steps)]
+        per_shape_us.append(1000.0 * statistics.median(ms) / s.R)
+    launches = args.steps * sum(s.R for s in shapes)
+
+    # ---- e2e: public API from pinned host buffers, copies inside the timed region ----
+    e2e = e2e_arm(args, shapes, lib, device, stream)
+
+    return dict(shapes=shapes, per_shape_us=per_shape_us, total_ms=total_ms, launches=launches,
+                clocks=clocks, e2e=e2e)
+
+
+def eager_profile(args, points):
+    """Profiling mode (for ncu launch lists): no graphs, two rotation copies per shape."""
+    import moe_router_gemm_gb300 as lib
+    from moe_router_gemm_gb300 import build as _build
+    _build.build()
+    device = torch.device("cuda", torch.cuda.current_device())
+    shapes = [Shape(pt, device, lib, pdl=args.pdl) for pt in points]
+    for s in shapes:
+        s.R = min(s.R, 2)
+        s.Ws = s.Ws[:2]
+    torch.cuda.empty_cache()
+    for _ in range(args.warmup):
+        for s in shapes:
+            s.call(0)
+    torch.cuda.synchronize()
+    res = {}
+    for s in shapes:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for k in range(args.steps):
+            s.call(k)
+        b.record()
+        torch.cuda.synchronize()
+        res[f"M{s.M}_N{s.N}_K{s.K}"] = {"kernel": s.kernel, "eager_us_per_call": 1000 * a.elapsed_time(b) / args.steps,
+                                      "plan": s.plan.as_dict()}
+    print(json.dumps({"mode": "eager", "steps": args.steps, "shapes": res}))
+
+
+def e2e_arm(args, shapes, lib, device, stream):
+    host = []
+    for s in shapes:
+        x, W, b = s.host
+        host.append((x.pin_memory(), W.pin_memory(), b.pin_memory() if b is not None else None,
+                     torch.empty(s.M, s.N, dtype=torch.bfloat16).pin_memory()))
+    dev = [(torch.empty_like(s.x), torch.empty_like(s.Ws[0]), torch.empty_like(s.b) if s.b is not None else None,
+            torch.empty_like(s.out)) for s in shapes]
+    h2d = sum(h[0].numel() * 2 + h[1].numel() * 2 + (h[2].numel() * 2 if h[2] is not None else 0) for h in host)
+    d2h = sum(h[3].numel() * 2 for h in host)
+
+    def one_step():
+        for (hx, hW, hb, ho), (dx, dW, db, do) in zip(host, dev):
+            dx.copy_(hx, non_blocking=True)
+            dW.copy_(hW, non_blocking=True)
+            if hb is not None:
+                db.copy_(hb, non_blocking=True)
+            lib.bf16_linear(dx, dW, db, do)
+            ho.copy_(do, non_blocking=True)
+
+    steps = max(1, min(args.steps, 5))
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            one_step()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            one_step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return {"us_per_call": 1000.0 * ms / len(shapes), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="router", choices=["router", "smallest", "decode", "mlp", "prefill"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pdl", action="store_true",
+                    help="launch with programmatic dependent launch (BF16L_FLAG_PDL): back-to-back calls overlap")
+    ap.add_argument("--only", action="append", default=[],
+                    help="restrict to shapes M,N,K[,bias] (repeatable); for profiling")
+    ap.add_argument("--eager", action="store_true",
+                    help="profiling mode: each step calls every shape once per rotation copy, no graphs, "
+                         "no e2e/cpu legs; prints per-shape timings only")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3  # at least three warm-up steps
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    points = workload_points(args.workload)
+    if args.only:
+        points = []
+        for spec in args.only:
+            f = [int(v) for v in spec.split(",")]
+            M, N, K = f[:3]
+            points.append(dict(name=f"only_M{M}_N{N}_K{K}", M=M, N=N, K=K, bias=bool(f[3]) if len(f) > 3 else False,
+                               seed=7 + M + N + K))
+    peaks = load_peaks()
+    large = args.workload == "prefill"
+    metric = ("bf16 GEMM TFLOP/s (prefill, tile path)" if large else
+              "M<=16 bf16 GEMM us per call (L2-cold), mean over the router sweep")
+    unit = "TFLOP/s" if large else "us/call"
+    config = {"workload": workload_desc(args.workload), "shapes": len(points),
+              "l2": "cold: weights rotated over copies totalling >=256 MB per shape; x L2-hot",
+              "timing": "CUDA graph of R back-to-back calls per shape, CUDA events on the launching stream",
+              "pdl": bool(args.pdl)}
+
+    if args.impl == "reference":
+        if world > 1 and rank != 0:
+            return
+        smp = OracleSample(points, budget_s=args.cpu_budget / max(1, args.steps))
+        smp.run(1)  # one untimed warm-up pass
+        wall = smp.run(args.steps)
+        value = smp.value(wall, args.steps, large)
+        line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": 1, "ms_per_step": 1000.0 * wall / args.steps,
+                "higher_is_better": large, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": value, "unit": unit, "cores": smp.threads, "kind": "oracle",
+                                 "sample": smp.desc},
+                "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+        torch.cuda.set_device(local_rank)
+    else:
+        torch.cuda.set_device(0)
+
+    if args.eager:
+        eager_profile(args, points)
+        return
+    r = gpu_arm(args, points, rank, world)
+    shapes, per_us = r["shapes"], r["per_shape_us"]
+    total_ms = r["total_ms"]
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # dominant kernel: the largest share of measured time
+    share = {}
+    for s, us in zip(shapes, per_us):
+        share.setdefault(s.kernel, [0.0, 0, 0.0, []])
+        share[s.kernel][0] += us
+        share[s.kernel][1] += 1
+        share[s.kernel][2] += algo_flops(s.M, s.N, s.K, s.bias) if large else algo_bytes(s.M, s.N, s.K, s.bias)
+        share[s.kernel][3].append(s)
+    dom = max(share, key=lambda k: share[k][0])
+    dom_us, dom_n, dom_work, dom_shapes = share[dom]
+    if large:
+        achieved = dom_work / (dom_us * 1e-6) / 1e12
+        peak = peaks["bf16_tflops"]
+        bound, runit = "tensor", "TFLOP/s"
+    else:
+        achieved = dom_work / (dom_us * 1e-6) / 1e9
+        peak = peaks["hbm_gbs"]
+        bound, runit = "hbm", "GB/s"
+    # traffic: ncu DRAM bytes per launch for one representative shape of the dominant kernel
+    rep = max(dom_shapes, key=lambda s: s.M * s.N * s.K)
+    traffic = ncu_traffic(dom, rep.M, rep.N, rep.K)
+
+    calls_per_step = sum(s.R for s in shapes)
+    if large:
+        flops_step = sum(algo_flops(s.M, s.N, s.K, s.bias) * s.R for s in shapes)
+        value = flops_step * args.steps * world / (total_ms * 1e-3) / 1e12
+    else:
+        value = statistics.mean(per_us) / world if world > 1 else statistics.mean(per_us)
+    ms_per_step = total_ms / args.steps
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        smp = OracleSample(points, budget_s=args.cpu_budget)
+        wall = smp.run(1)
+        cpu = {"value": smp.value(wall, 1, large), "unit": unit, "cores": smp.threads, "kind": "oracle",
+               "sample": smp.desc}
+
+    e2e = r["e2e"]
+    if large:
+        e2e_value = sum(algo_flops(s.M, s.N, s.K, s.bias) for s in shapes) / (e2e["us_per_call"] * len(shapes) * 1e-6) / 1e12
+    else:
+        e2e_value = e2e["us_per_call"]
+
+    per_shape = {}
+    for s, us in zip(shapes, per_us):
+        key = f"K{s.K}_N{s.N}"
+        per_shape.setdefault(key, []).append(round(us, 3))
+    line = {
+        "metric": metric, "value": round(value, 4), "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": large,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config,
+        "roofline": {"bound": bound, "kernel": dom, "achieved": round(achieved, 2), "peak": peak, "unit": runit,
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "traffic_shape": f"M={rep.M} N={rep.N} K={rep.K}",
+                     "peak_source": peaks["source"]},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 4), "unit": unit, "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
+                "d2h_bytes_per_step": e2e["d2h_bytes_per_step"]},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+        "kernel_share": {k: round(v[0] / sum(x[0] for x in share.values()), 4) for k, v in share.items()},
+        "per_shape_us": per_shape,
+        "pct_hbm_roofline_per_shape": None if large else {
+            k: [round(100.0 * algo_bytes(s.M, s.N, s.K, s.bias) / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 1)
+                for s, us in zip(shapes, per_us) if f"K{s.K}_N{s.N}" == k] for k in per_shape},
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

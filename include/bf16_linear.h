@@ -73,13 +73,23 @@ typedef enum {
 typedef struct {
     int32_t kernel;        /* bf16l_kernel */
     int32_t threads;       /* threads per CTA */
-    int32_t rows_per_cta;  /* DOTPROD: W rows per CTA;  SPLITK / TILE: W rows per tile (MMA M or N) */
-    int32_t tokens_per_cta;/* SPLITK: tokens per MMA (M padded to 16);  TILE: x rows per tile */
+    int32_t rows_per_cta;  /* W rows per CTA (DOTPROD 1/2/4; SPLITK 16..256, the MMA N); TILE: W rows per tile */
+    int32_t tokens_per_cta;/* SPLITK: x rows loaded per chunk (M rounded up to 8, <= 64);  TILE: x rows per tile */
     int32_t split_k;       /* SPLITK: CTAs per cluster along K (1..16) */
     int32_t stages;        /* SPLITK / TILE: shared-memory ring depth (64-wide K chunks) */
     int32_t grid;          /* CTAs launched (informational; computed by the plan) */
-    int32_t flags;         /* reserved, 0 */
+    int32_t flags;         /* BF16L_FLAG_* bits the launch uses */
 } bf16l_plan;
+
+/*
+ * Launch flag: programmatic dependent launch.  The kernel reads W (and
+ * issues its TMA weight loads) before waiting for the preceding kernel in the
+ * stream, and reads x / writes out only after that wait; it also lets the
+ * following kernel start early.  Use only when W and bias are not written by
+ * the kernel launched just before this call on the same stream (true for
+ * weights).  Honoured by the split-K and dot-product kernels.
+ */
+#define BF16L_FLAG_PDL 1u
 
 /*
  * Describe the device a plan is made for.  bf16_linear() fills this from the
@@ -119,6 +129,13 @@ int bf16_linear_plan(int M, int N, int K, const bf16l_device *dev, bf16l_plan *p
  */
 int bf16_linear(const void *x, const void *W, const void *bias, void *out,
                 int M, int N, int K, bf16l_stream_t stream);
+
+/*
+ * bf16_linear_ex — as bf16_linear, with BF16L_FLAG_* launch flags (0 = the
+ * same as bf16_linear).  Unknown flag bits return BF16L_EINVAL.
+ */
+int bf16_linear_ex(const void *x, const void *W, const void *bias, void *out,
+                   int M, int N, int K, uint32_t flags, bf16l_stream_t stream);
 
 /*
  * bf16_linear_with_plan — as bf16_linear, but run exactly `plan` (for tests,

@@ -66,6 +66,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         vp, i32 = ctypes.c_void_p, ctypes.c_int
         lib.bf16_linear.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp]
         lib.bf16_linear.restype = i32
+        lib.bf16_linear_ex.argtypes = [vp, vp, vp, vp, i32, i32, i32, ctypes.c_uint32, vp]
+        lib.bf16_linear_ex.restype = i32
         lib.bf16_linear_with_plan.argtypes = [vp, vp, vp, vp, i32, i32, i32, ctypes.POINTER(Plan), vp]
         lib.bf16_linear_with_plan.restype = i32
         lib.bf16_linear_plan.argtypes = [i32, i32, i32, ctypes.POINTER(Device), ctypes.POINTER(Plan)]

@@ -102,9 +102,10 @@ int check_args(const void *x, const void *W, const void *bias, void *out, int M,
 }
 
 int run(const void *x, const void *W, const void *bias, void *out, int M, int N, int K, const bf16l_plan *forced,
-        bf16l_stream_t stream) {
+        uint32_t flags, bf16l_stream_t stream) {
     int st = check_args(x, W, bias, out, M, N, K);
     if (st != BF16L_OK) return st;
+    if (flags & ~BF16L_FLAG_PDL) return BF16L_EINVAL;
     if (M == 0) return BF16L_OK;
     if (forced) {
         // Check the requested plan's shape rules before touching the device.
@@ -123,6 +124,7 @@ int run(const void *x, const void *W, const void *bias, void *out, int M, int N,
         st = check_plan(M, N, K, ds->dev, &p);
     } else {
         st = bf16_linear_plan(M, N, K, &ds->dev, &p);
+        p.flags = (int32_t)flags;
     }
     if (st != BF16L_OK) return st;
 
@@ -179,13 +181,18 @@ int make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_
 // ---------------------------------------------------------------------------
 extern "C" int bf16_linear(const void *x, const void *W, const void *bias, void *out, int M, int N, int K,
                            bf16l_stream_t stream) {
-    return bf16l::run(x, W, bias, out, M, N, K, nullptr, stream);
+    return bf16l::run(x, W, bias, out, M, N, K, nullptr, 0u, stream);
+}
+
+extern "C" int bf16_linear_ex(const void *x, const void *W, const void *bias, void *out, int M, int N, int K,
+                              uint32_t flags, bf16l_stream_t stream) {
+    return bf16l::run(x, W, bias, out, M, N, K, nullptr, flags, stream);
 }
 
 extern "C" int bf16_linear_with_plan(const void *x, const void *W, const void *bias, void *out, int M, int N,
                                      int K, const bf16l_plan *plan, bf16l_stream_t stream) {
     if (!plan) return BF16L_EINVAL;
-    return bf16l::run(x, W, bias, out, M, N, K, plan, stream);
+    return bf16l::run(x, W, bias, out, M, N, K, plan, (uint32_t)plan->flags, stream);
 }
 
 extern "C" int bf16_linear_device_status(int32_t *status, int clear) {

@@ -29,7 +29,8 @@ enum WaitSite : int32_t {
     kSiteAccum = 3,      // epilogue waiting for the accumulator
     kSiteTmemEmpty = 4,  // MMA issuer waiting for the epilogue to drain TMEM
     kSiteDrain = 5,      // exit path draining copies still in flight
-    kSiteSelftest = 6    // bf16_linear_selftest_wait
+    kSiteSelftest = 6,   // bf16_linear_selftest_wait
+    kSiteRecv = 7        // split-K owner waiting for its peers' partials
 };
 
 // Default limit for one wait: 1 s of wall-clock time.
@@ -100,6 +101,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
         : "r"(bar_addr), "r"(parity)
         : "memory");
     return ok != 0;
+}
+
+// As mbar_try_wait, with acquire semantics at cluster scope (for data other
+// CTAs wrote with st.async).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, int32_t *status, int32_t site,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait_cluster(a, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait_cluster(a, parity)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            record_timeout(status, site);
+            return false;
+        }
+    }
 }
 
 // Wait until the phase with the given parity has completed, for at most
@@ -226,9 +257,10 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // 32 lanes x 32 bits, 16 consecutive columns: thread t of the warp gets lane
-// (quarter base + t), columns [col, col+16).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
+// (quarter base + t), columns [col, col+16).  The registers are not valid
+// until tmem_ld_wait16() on the same array: that wait names them as in-out
+// operands, so the compiler cannot read them before it.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
         "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -236,8 +268,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
           "=r"(r[15])
         : "r"(taddr));
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld_wait16(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -268,6 +307,33 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
     return r;
+}
+
+// Asynchronous 16-byte store into another CTA's shared memory; the bytes are
+// counted on that CTA's mbarrier (complete_tx), so the receiver can wait for
+// all of them without a cluster barrier.
+__device__ __forceinline__ void st_async_f4(uint32_t remote_addr, float a, float b, float c, float d,
+                                            uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+                 ::"r"(remote_addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
+                 : "memory");
+}
+
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// this CTA's shared memory into another CTA's shared memory; the bytes are
+// counted on the destination CTA's mbarrier.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t remote_dst, const void *local_src, uint32_t bytes,
+                                                  uint32_t remote_bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(remote_dst), "r"(smem_u32(local_src)), "r"(bytes), "r"(remote_bar)
+        : "memory");
+}
+
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy accesses (bulk copies, TMA) of the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {

@@ -6,11 +6,17 @@
 // warp-shuffle then shared-memory reduction; chosen for M <= 4 or K < 2048.
 //
 // This kernel keeps that structure and adds what GB300 needs to keep enough
-// bytes in flight at such small sizes: a CTA owns R consecutive W rows (so each
-// x vector, read from L2, is reused R times), and every thread issues all the
-// 16-byte weight loads of a batch of up to 8 vectors per row before it does any
-// arithmetic.  Tokens are processed MT at a time (MT = M for M <= 8); larger M
-// loops over W again, which only the K % 8 != 0 fallback ever does.
+// bytes in flight at such small sizes:
+//   * a CTA owns R consecutive W rows, so each x vector is reused R times;
+//   * every thread issues the 16-byte weight loads of its first batch (up to
+//     8 vectors per row) before anything else, then the CTA copies x (all MT
+//     token rows, a few KB to ~100 KB) into shared memory while those loads are
+//     in flight; the multiply-adds then read x from shared memory instead of
+//     waiting on L2 once per (vector, token);
+//   * rows whose length is not a multiple of 8 elements (K % 8 != 0, so not
+//     16-byte aligned) take a scalar path that reads x from global memory.
+// Tokens are processed MT at a time (MT = M for M <= 8); larger M loops over
+// W again, which only the K % 8 != 0 fallback ever does.
 //
 // Arithmetic: fp32 products and sums (each thread sums its k-slice in
 // ascending order, then a fixed shuffle tree and a fixed in-order sum over
@@ -19,6 +25,10 @@
 #include "kernels.h"
 
 namespace bf16l {
+
+namespace {
+
+constexpr int kXSmemMax = 160 * 1024;  // largest x slab staged in shared memory
 
 template <int VEC>
 struct Vec;
@@ -40,13 +50,16 @@ struct Vec<1> {  // one bf16 (rows not 16-byte aligned when K % 8 != 0)
     __device__ __forceinline__ float get(int) const { return bf16_to_f32(v); }
 };
 
-template <int MT, int R, int VEC>
+}  // namespace
+
+template <int MT, int R, int VEC, bool XSMEM>
 __global__ void __launch_bounds__(256) dotprod_kernel(const uint16_t *__restrict__ x,
                                                       const uint16_t *__restrict__ W,
                                                       const uint16_t *__restrict__ bias,
                                                       uint16_t *__restrict__ out, int M, int N, int K) {
     constexpr int U = (VEC == 8) ? 8 : 4;  // vectors per row a thread loads before computing
     __shared__ float red[8][R * MT];
+    extern __shared__ uint4 xs[];  // XSMEM: x[m0 + m][k] as 16-byte vectors, [MT][K / 8]
 
     const int tid = threadIdx.x;
     const int nt = blockDim.x;
@@ -68,8 +81,8 @@ __global__ void __launch_bounds__(256) dotprod_kernel(const uint16_t *__restrict
 #pragma unroll
             for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
 
-        for (int v0 = tid; v0 < nvec; v0 += U * nt) {
-            Vec<VEC> wv[U][R];
+        Vec<VEC> wv[U][R];
+        auto load_batch = [&](int v0) {
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int v = v0 + u * nt;
@@ -78,15 +91,37 @@ __global__ void __launch_bounds__(256) dotprod_kernel(const uint16_t *__restrict
                     for (int r = 0; r < R; ++r) wv[u][r].load_stream(wrow[r] + (size_t)v * VEC);
                 }
             }
+        };
+        load_batch(tid);  // first weight batch in flight before x is touched
+        if (m0 == 0) {
+            pdl_launch_dependents();  // (no-ops unless launched with programmatic serialization)
+            pdl_wait();               // x may be written by the previous kernel; out may still be read by it
+        }
+
+        if constexpr (XSMEM) {
+            // Stage the MT token rows of x in shared memory (zeros past M).
+            const uint4 *xg = reinterpret_cast<const uint4 *>(x);
+            for (int i = tid; i < MT * nvec; i += nt) {
+                const int m = i / nvec, v = i - m * nvec;
+                xs[i] = (m0 + m < M) ? __ldg(xg + (size_t)(m0 + m) * nvec + v) : make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncthreads();
+        }
+
+        for (int v0 = tid; v0 < nvec; v0 += U * nt) {
+            if (v0 != tid) load_batch(v0);
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int v = v0 + u * nt;
                 if (v < nvec) {
 #pragma unroll
                     for (int m = 0; m < MT; ++m) {
-                        if (m0 + m < M) {
+                        if (XSMEM || m0 + m < M) {
                             Vec<VEC> xv;
-                            xv.load_cached(x + (size_t)(m0 + m) * K + (size_t)v * VEC);
+                            if constexpr (XSMEM)
+                                xv.v = xs[m * nvec + v];
+                            else
+                                xv.load_cached(x + (size_t)(m0 + m) * K + (size_t)v * VEC);
 #pragma unroll
                             for (int e = 0; e < VEC; ++e) {
                                 const float xe = xv.get(e);
@@ -120,52 +155,80 @@ __global__ void __launch_bounds__(256) dotprod_kernel(const uint16_t *__restrict
                 out[(size_t)mm * N + n] = f32_to_bf16(s);
             }
         }
-        __syncthreads();
+        __syncthreads();  // red[] and xs[] are reused by the next pass
     }
 }
+
+namespace {
 
 typedef void (*DotFn)(const uint16_t *, const uint16_t *, const uint16_t *, uint16_t *, int, int, int);
 
+// kind: 0 = 16-byte vectors with x in shared memory, 1 = 16-byte vectors with
+// x from global memory, 2 = scalar (K % 8 != 0).
 template <int MT, int R>
-static DotFn pick_vec(bool vec8) {
-    return vec8 ? dotprod_kernel<MT, R, 8> : dotprod_kernel<MT, R, 1>;
+DotFn pick_kind(int kind) {
+    switch (kind) {
+        case 0: return dotprod_kernel<MT, R, 8, true>;
+        case 1: return dotprod_kernel<MT, R, 8, false>;
+        default: return dotprod_kernel<MT, R, 1, false>;
+    }
 }
 
 template <int MT>
-static DotFn pick_rows(int R, bool vec8) {
+DotFn pick_rows(int R, int kind) {
     switch (R) {
-        case 1: return pick_vec<MT, 1>(vec8);
-        case 2: return pick_vec<MT, 2>(vec8);
-        case 4: return pick_vec<MT, 4>(vec8);
+        case 1: return pick_kind<MT, 1>(kind);
+        case 2: return pick_kind<MT, 2>(kind);
+        case 4: return pick_kind<MT, 4>(kind);
         default: return nullptr;
     }
 }
 
-static DotFn pick(int MT, int R, bool vec8) {
+DotFn pick(int MT, int R, int kind) {
     switch (MT) {
-        case 1: return pick_rows<1>(R, vec8);
-        case 2: return pick_rows<2>(R, vec8);
-        case 3: return pick_rows<3>(R, vec8);
-        case 4: return pick_rows<4>(R, vec8);
-        case 5: return pick_rows<5>(R, vec8);
-        case 6: return pick_rows<6>(R, vec8);
-        case 7: return pick_rows<7>(R, vec8);
-        case 8: return pick_rows<8>(R, vec8);
+        case 1: return pick_rows<1>(R, kind);
+        case 2: return pick_rows<2>(R, kind);
+        case 3: return pick_rows<3>(R, kind);
+        case 4: return pick_rows<4>(R, kind);
+        case 5: return pick_rows<5>(R, kind);
+        case 6: return pick_rows<6>(R, kind);
+        case 7: return pick_rows<7>(R, kind);
+        case 8: return pick_rows<8>(R, kind);
         default: return nullptr;
     }
 }
 
-int init_dotprod() { return (int)cudaSuccess; }
+}  // namespace
+
+int init_dotprod() {
+    for (int MT = 1; MT <= kDotMaxTokens; ++MT)
+        for (int R : kDotRows) {
+            const int e = (int)cudaFuncSetAttribute(pick(MT, R, 0), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                    kXSmemMax);
+            if (e) return e;
+        }
+    return (int)cudaSuccess;
+}
 
 int launch_dotprod(const LaunchArgs &a, const bf16l_plan &p) {
     const int MT = a.M < kDotMaxTokens ? a.M : kDotMaxTokens;
-    DotFn fn = pick(MT, p.rows_per_cta, (a.K % 8) == 0);
+    const size_t xbytes = (size_t)MT * a.K * 2;
+    const int kind = (a.K % 8 != 0) ? 2 : (xbytes <= (size_t)kXSmemMax ? 0 : 1);
+    DotFn fn = pick(MT, p.rows_per_cta, kind);
     if (!fn) return (int)cudaErrorInvalidValue;
-    const dim3 grid((unsigned)p.grid), block((unsigned)p.threads);
-    fn<<<grid, block, 0, (cudaStream_t)a.stream>>>(
-        static_cast<const uint16_t *>(a.x), static_cast<const uint16_t *>(a.W),
-        static_cast<const uint16_t *>(a.bias), static_cast<uint16_t *>(a.out), a.M, a.N, a.K);
-    return (int)cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.grid);
+    cfg.blockDim = dim3((unsigned)p.threads);
+    cfg.dynamicSmemBytes = kind == 0 ? xbytes : 0;
+    cfg.stream = (cudaStream_t)a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = (p.flags & BF16L_FLAG_PDL) ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return (int)cudaLaunchKernelEx(&cfg, fn, static_cast<const uint16_t *>(a.x), static_cast<const uint16_t *>(a.W),
+                                   static_cast<const uint16_t *>(a.bias), static_cast<uint16_t *>(a.out), a.M, a.N,
+                                   a.K);
 }
 
 }  // namespace bf16l

@@ -17,13 +17,20 @@ constexpr int kDotMaxTokens = 8;
 constexpr int kDotRows[] = {1, 2, 4};
 constexpr int kDotThreads[] = {64, 128, 256};
 
-// Cluster split-K kernel: 128 W rows on the MMA M side; tokens (MMA N) padded
-// to a multiple of 16 up to 64; K split over up to 16 CTAs of one cluster.
-constexpr int kSplitRows = 128;
+// Cluster split-K kernel: tokens (M <= 64, padded to a multiple of 8) on the
+// MMA M side, 16..256 weight rows per CTA on the N side, K split over up to 16
+// CTAs of one cluster, up to 16 ring stages.
 constexpr int kSplitMaxTokens = 64;
 constexpr int kSplitMaxCluster = 16;
-constexpr int kSplitMaxStages = 8;
+constexpr int kSplitMaxStages = 16;
 constexpr int kSplitThreads = 128;
+// Shared-memory layout arithmetic of the split-K kernel (defined in splitk.cu).
+int split_stage_bytes(int tokens, int rows);
+int split_recv_bytes(int tokens, int rows);
+int split_smem_bytes(int tokens, int rows, int stages);
+int split_max_stages(int tokens, int rows);  // 0 when even one stage does not fit
+int split_tmem_cols(int rows);
+bool split_rows_supported(int rows);         // a kernel instance exists for this many rows
 
 // Tile kernel: BM x rows, BN W rows per tile, 64-wide K chunks.
 constexpr int kTileBM = 128;

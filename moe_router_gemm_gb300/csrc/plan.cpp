@@ -10,6 +10,8 @@
 // are only the starting point for shapes it does not list.
 #include <stdint.h>
 
+#include <initializer_list>
+
 #include "bf16_linear.h"
 #include "kernels.h"
 
@@ -47,19 +49,30 @@ void plan_dotprod(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
 }
 
 void plan_splitk(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
-    const int n_tiles = ceil_div(N, kSplitRows);
+    // Aim for about one CTA per SM: weight tiles small enough that N / rows
+    // tiles times a cluster of <= 16 reaches the SM count, then as many K
+    // splits as the SMs allow.
     const int chunks = ceil_div(K, kChunkK);
-    int split = dev.num_sms / n_tiles;
+    const int want_tiles = ceil_div(dev.num_sms, kSplitMaxCluster);
+    int rows = 16;
+    for (int r : {256, 128, 64, 32, 16})
+        if (ceil_div(N, r) >= want_tiles) {
+            rows = r;
+            break;
+        }
+    const int tiles = ceil_div(N, rows);
+    int split = dev.num_sms / tiles;
     if (split < 1) split = 1;
     if (split > kSplitMaxCluster) split = kSplitMaxCluster;
     if (split > chunks) split = chunks;
-    int per_cta = ceil_div(chunks, split);
     p->kernel = BF16L_KERNEL_SPLITK;
     p->threads = kSplitThreads;
-    p->rows_per_cta = kSplitRows;
-    p->tokens_per_cta = round_up(M, 16);
+    p->rows_per_cta = rows;
+    p->tokens_per_cta = round_up(M, 8);
     p->split_k = split;
-    p->stages = per_cta < kSplitMaxStages ? per_cta : kSplitMaxStages;
+    const int per_cta = ceil_div(chunks, split);
+    const int max_stages = split_max_stages(p->tokens_per_cta, rows);
+    p->stages = per_cta < max_stages ? per_cta : max_stages;
 }
 
 void plan_tile(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
@@ -78,7 +91,7 @@ void plan_tile(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
 
 int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
     if (M < 0 || N <= 0 || K <= 0) return BF16L_EINVAL;
-    const int64_t n_tiles_split = (N + kSplitRows - 1) / kSplitRows;
+    if ((uint32_t)p->flags & ~BF16L_FLAG_PDL) return BF16L_EINVAL;
     switch (p->kernel) {
         case BF16L_KERNEL_DOTPROD: {
             if (!in_list(p->threads, kDotThreads, 3) || !in_list(p->rows_per_cta, kDotRows, 3))
@@ -90,14 +103,15 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
             if (K % 8 != 0) return BF16L_EUNSUPPORTED;  // TMA needs 16-byte row strides
             if (M > kSplitMaxTokens) return BF16L_EUNSUPPORTED;
             const int chunks = ceil_div(K, kChunkK);
-            if (p->threads != kSplitThreads || p->rows_per_cta != kSplitRows) return BF16L_EINVAL;
-            if (p->tokens_per_cta < 16 || p->tokens_per_cta > kSplitMaxTokens || p->tokens_per_cta % 16 != 0 ||
+            if (p->threads != kSplitThreads || !split_rows_supported(p->rows_per_cta)) return BF16L_EINVAL;
+            if (p->tokens_per_cta < 8 || p->tokens_per_cta > kSplitMaxTokens || p->tokens_per_cta % 8 != 0 ||
                 p->tokens_per_cta < M)
                 return BF16L_EINVAL;
             if (p->split_k < 1 || p->split_k > kSplitMaxCluster || p->split_k > chunks) return BF16L_EINVAL;
-            if (p->stages < 1 || p->stages > kSplitMaxStages) return BF16L_EINVAL;
-            const int64_t grid = n_tiles_split * p->split_k;
-            if (grid > 65535LL * kSplitMaxCluster) return BF16L_EUNSUPPORTED;
+            if (p->stages < 1 || p->stages > split_max_stages(p->tokens_per_cta, p->rows_per_cta))
+                return BF16L_EINVAL;
+            const int64_t grid = (int64_t)ceil_div(N, p->rows_per_cta) * p->split_k;
+            if (ceil_div(N, p->rows_per_cta) > 65535) return BF16L_EUNSUPPORTED;
             p->grid = M == 0 ? 0 : (int)grid;
             return BF16L_OK;
         }
@@ -119,6 +133,7 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
 }  // namespace bf16l
 
 extern "C" int bf16_linear_plan(int M, int N, int K, const bf16l_device *devp, bf16l_plan *plan) {
+    // (flags are chosen by the caller of the launch, not by the plan)
     using namespace bf16l;
     if (!plan || M < 0 || N <= 0 || K <= 0) return BF16L_EINVAL;
     const bf16l_device gb300 = {10, 3, kGb300Sms};

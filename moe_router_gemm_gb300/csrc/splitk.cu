@@ -5,25 +5,36 @@
 // cluster (8 by default), a warp-specialised DMA/MMA pipeline, fp32 partial
 // tiles reduced across the cluster through distributed shared memory
 // (st.shared::cluster), non-.aligned cluster barriers (its review found the
-// .aligned forms hung), fp32 logits out.
+// .aligned forms hung), tile_m = 16 tokens, tile_n = 16 weight rows.
 //
-// On sm_103a this is rebuilt around tcgen05 instead of mma.sync:
-//   * swap-AB: 128 weight rows sit on the MMA M side and the (few) tokens,
-//     padded to TOK = 16..64, on the MMA N side, so one 128 x TOK x 16
-//     tcgen05.mma does the work of a whole warpgroup of m16n8k16 MMAs and the
-//     fp32 accumulator lives in TMEM (TOK columns), not in registers;
-//   * one thread issues TMA tile loads (128-byte swizzle, out-of-bounds rows
-//     and K-columns zero-filled) of W[n0:n0+128, kslice] and x[0:TOK, kslice]
-//     into a `stages`-deep ring of 64-wide K chunks, all issued at once when
-//     the slice fits, so every CTA has its whole weight slice in flight;
-//   * one thread issues the MMAs and frees each stage with tcgen05.commit;
-//   * all four warps then move the accumulator TMEM -> registers -> shared
-//     memory, and after a cluster barrier each CTA reduces a 1/S share of the
-//     tile by reading the S partials over DSMEM (ld.shared::cluster) in rank
-//     order (deterministic), adds the bias, rounds to bf16 and stores.
+// Rebuilt for sm_103a around what limits a skinny GEMM on GB300: one CTA's TMA
+// intake is only some tens of GB/s, so the weights must be spread over 100+
+// CTAs, each streaming a few tens of KB, and the prologue / epilogue chain
+// must be short.
+//   * MMA shape: tokens on the MMA M side (M = 128; only the first TOKP rows of
+//     the A tile hold x, the rest is whatever follows in shared memory and only
+//     feeds accumulator rows that are never read), BN = 16..256 weight rows on
+//     the N side.  So a CTA's weight tile can be as small as 16 rows and the
+//     grid can have hundreds of CTAs even for N = 128..384.
+//   * One thread issues TMA tile loads (128-byte swizzle; rows past N, tokens
+//     past M and K past the end are zero-filled) into a `stages`-deep ring of
+//     64-wide K chunks: the weight halves first, before anything else, then
+//     (after the programmatic-launch wait, when enabled) the x halves.
+//   * One thread issues tcgen05.mma (128 x BN x 16, fp32 accumulate in TMEM)
+//     and frees each stage with tcgen05.commit.
+//   * Exchange, push-based: the tile's M x BN partial sums are cut into
+//     float4 items (token-major); rank d of the cluster owns a contiguous 1/S
+//     of them.  Each token's thread reads its row of the accumulator from
+//     TMEM and st.async-s every item straight into its owner's receive buffer,
+//     whose mbarrier counts the bytes.  The owner sums the S partials in rank
+//     order (deterministic), adds the bias, rounds to bf16 and stores 4
+//     outputs at a time.
+//   * Programmatic dependent launch (optional): weights are read before
+//     griddepcontrol.wait, x and the output only after it, and every CTA lets
+//     the next kernel start as soon as its own weight loads are issued.
 //
-// Grid: (S, ceil(N/128)) with cluster dims (S, 1, 1); rank r of a cluster
-// takes K chunks [r*C/S, (r+1)*C/S) of the C = ceil(K/64) chunks.
+// Grid: (S, ceil(N/BN)) with cluster dims (S, 1, 1); rank r takes K chunks
+// [r*C/S, (r+1)*C/S) of the C = ceil(K/64) chunks.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -31,98 +42,142 @@ namespace bf16l {
 
 namespace {
 
-constexpr int kRows = kSplitRows;               // 128 W rows per CTA (MMA M)
-constexpr int kSmemPerSm = 233472;              // 228 KB of shared memory per SM on sm_103
-constexpr int kWTileBytes = kRows * kChunkK * 2;  // 16 KB per stage
+constexpr int kSmemPerSm = 233472;  // 228 KB of shared memory per SM on sm_103
+constexpr int kSmemPerCta = 232448; // 227 KB usable by one CTA
+constexpr int kMmaM = 128;          // MMA rows (tokens, zero- or garbage-padded)
+constexpr int kATileBytes = kMmaM * kChunkK * 2;  // the 16 KB the MMA reads as A per chunk
 
-template <int TOK>
-struct SplitCfg {
-    static constexpr int kXTileBytes = TOK * kChunkK * 2;
-    static constexpr int kStageBytes = kWTileBytes + kXTileBytes;  // multiple of 1024
-    static constexpr int kPartBytes = TOK * kRows * 4;            // fp32 partial tile [TOK][128]
-    static constexpr int kTmemCols = TOK <= 32 ? 32 : 64;
-    static constexpr uint32_t kIdesc = idesc_bf16_f32(kRows, TOK);
-    // Shared memory per CTA.  Padded so that the CTAs that fit on one SM can
-    // never ask for more than the SM's 512 TMEM columns between them (an
-    // allocation that cannot be satisfied would stall its CTA).
-    static int smem_bytes(int stages) {
-        const int ring = stages * kStageBytes;
-        int bytes = 1024 /*alignment slack*/ + (ring > kPartBytes ? ring : kPartBytes) + 256 /*barriers*/;
-        const int min_bytes = kSmemPerSm / (512 / kTmemCols);
-        return bytes > min_bytes ? bytes : min_bytes;
-    }
-};
-
-struct SplitShared {  // bookkeeping placed after the ring
+struct SplitShared {  // bookkeeping placed after the receive buffer (<= 512 bytes)
     uint64_t full[kSplitMaxStages];
     uint64_t empty[kSplitMaxStages];
     uint64_t accum;
+    uint64_t recv;
     uint32_t tmem_base;
     int32_t aborted;   // set when a wait gave up: skip the rest of the math
     int32_t issued;    // TMA chunks issued by the producer
     int32_t consumed;  // chunks whose data the MMA issuer saw arrive
 };
 
+__device__ __forceinline__ int part_begin(int d, int T, int S) { return (int)(((long long)d * T) / S); }
+
 }  // namespace
 
-template <int TOK>
+static_assert(sizeof(SplitShared) <= 512, "bookkeeping must fit its reserved space");
+
+// Host-visible layout arithmetic (shared with the planner through kernels.h).
+int split_stage_bytes(int tokens, int rows) { return (tokens + rows) * kChunkK * 2; }
+
+int split_recv_bytes(int tokens, int rows) {
+    // S partials of this CTA's share: at most S * ceil(T / S) <= T + S items of 16 bytes.
+    return (tokens * rows / 4 + kSplitMaxCluster) * 16;
+}
+
+int split_tmem_cols(int rows) { return rows <= 32 ? 32 : rows <= 64 ? 64 : rows <= 128 ? 128 : 256; }
+
+int split_ring_bytes(int tokens, int rows, int stages) {
+    // The ring, which the accumulator staging (tokens x rows fp32) reuses once the MMAs are done.
+    const int ring = stages * split_stage_bytes(tokens, rows), acc = tokens * rows * 4;
+    return ring > acc ? ring : acc;
+}
+
+int split_smem_bytes(int tokens, int rows, int stages) {
+    const int stage = split_stage_bytes(tokens, rows);
+    int body = split_ring_bytes(tokens, rows, stages) + split_recv_bytes(tokens, rows) + 512 /*bookkeeping*/;
+    // The MMA reads a full 128-row A window from the last stage's x chunk on.
+    const int window = (stages - 1) * stage + kATileBytes;
+    if (window > body) body = window;
+    int bytes = 1024 /*alignment slack*/ + body;
+    // Pad so that the CTAs that fit on one SM never ask for more than its 512
+    // TMEM columns between them (an allocation that cannot be met would stall).
+    const int cols = split_tmem_cols(rows);
+    const int min_bytes = kSmemPerSm / (512 / cols + 1) + 1;
+    return bytes > min_bytes ? bytes : min_bytes;
+}
+
+int split_max_stages(int tokens, int rows) {
+    int s = kSplitMaxStages;
+    while (s > 1 && split_smem_bytes(tokens, rows, s) > kSmemPerCta) --s;
+    return split_smem_bytes(tokens, rows, s) <= kSmemPerCta ? s : 0;
+}
+
+template <int BN>
 __global__ void __launch_bounds__(kSplitThreads, 1)
     splitk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
-                  const uint16_t *__restrict__ bias, uint16_t *__restrict__ out, int M, int N, int K, int stages,
-                  int32_t *status) {
-    using Cfg = SplitCfg<TOK>;
+                  const uint16_t *__restrict__ bias, uint16_t *__restrict__ out, int M, int N, int K, int tokp,
+                  int stages, int32_t *status) {
+    constexpr uint32_t kIdesc = idesc_bf16_f32(kMmaM, BN);
+    constexpr int kCols = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+    constexpr int kWBytes = BN * kChunkK * 2;
+
     extern __shared__ uint8_t smem_raw[];
-    // 1024-byte aligned ring (required by the 128-byte swizzle layout).
     const uint32_t raw = smem_u32(smem_raw);
-    uint8_t *ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    const int ring_bytes = stages * Cfg::kStageBytes > Cfg::kPartBytes ? stages * Cfg::kStageBytes : Cfg::kPartBytes;
-    SplitShared &sh = *reinterpret_cast<SplitShared *>(ring + ring_bytes);
+    uint8_t *ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-aligned (128-byte swizzle atoms)
+    const int xbytes = tokp * kChunkK * 2;
+    const int stage_bytes = xbytes + kWBytes;
+    const int T = M * (BN / 4);  // float4 items of the tile's partial sums
+    const int ring_bytes = stages * stage_bytes > tokp * BN * 4 ? stages * stage_bytes : tokp * BN * 4;
+    float4 *stage_out = reinterpret_cast<float4 *>(ring);  // accumulator staging, [M][BN] fp32, after the MMAs
+    float4 *recv = reinterpret_cast<float4 *>(ring + ring_bytes);
+    const int recv_bytes = (tokp * BN / 4 + kSplitMaxCluster) * 16;  // as split_recv_bytes()
+    SplitShared &sh = *reinterpret_cast<SplitShared *>(ring + ring_bytes + recv_bytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t rank = cluster_ctarank();
-    const int S = (int)gridDim.x;  // cluster spans the whole x dimension of the grid
-    const int n0 = blockIdx.y * kRows;
+    const int rank = (int)cluster_ctarank();
+    const int S = (int)gridDim.x;  // the cluster spans the whole x dimension of the grid
+    const int n0 = blockIdx.y * BN;
     const int C = (K + kChunkK - 1) / kChunkK;
     const int c_begin = (int)(((long long)rank * C) / S);
-    const int c_end = (int)(((long long)(rank + 1) * C) / S);
-    const int nchunks = c_end - c_begin;
+    const int nchunks = (int)(((long long)(rank + 1) * C) / S) - c_begin;
+    const int first = nchunks < stages ? nchunks : stages;  // chunks whose weights go out at once
 
     if (tid == 0) {
+        tma_prefetch_desc(&tm_w);
+        tma_prefetch_desc(&tm_x);
         for (int s = 0; s < stages; ++s) {
             mbar_init(&sh.full[s], 1);
             mbar_init(&sh.empty[s], 1);
         }
         mbar_init(&sh.accum, 1);
+        mbar_init(&sh.recv, 1);
         sh.aborted = 0;
         sh.issued = 0;
         sh.consumed = 0;
         fence_barrier_init();
+        // Weights do not depend on the previous kernel: put them in flight first.
+        for (int i = 0; i < first; ++i) {
+            uint8_t *st = ring + i * stage_bytes;
+            mbar_arrive_expect_tx(&sh.full[i], (uint32_t)stage_bytes);
+            tma_load_2d(st + xbytes, &tm_w, &sh.full[i], (c_begin + i) * kChunkK, n0);
+        }
     }
     if (warp == 1) {
-        tmem_alloc(&sh.tmem_base, Cfg::kTmemCols);
+        tmem_alloc(&sh.tmem_base, kCols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_launch_dependents();   // the next kernel may start its own weight loads now
+    cluster_arrive_release();  // phase 1: "my receive barrier is initialised"
     const uint32_t tmem = sh.tmem_base;
 
     if (warp == 0) {
         if (lane == 0) {  // ---- TMA producer ----
-            tma_prefetch_desc(&tm_w);
-            tma_prefetch_desc(&tm_x);
-            int i = 0;
+            pdl_wait();   // x may be written by the previous kernel
+            for (int i = 0; i < first; ++i)
+                tma_load_2d(ring + i * stage_bytes, &tm_x, &sh.full[i], (c_begin + i) * kChunkK, 0);
+            int i = first;
             for (; i < nchunks; ++i) {
                 const int s = i % stages;
-                if (i >= stages && !mbar_wait(&sh.empty[s], ((i / stages) - 1) & 1, status, kSiteEmpty)) {
+                if (!mbar_wait(&sh.empty[s], ((i / stages) - 1) & 1, status, kSiteEmpty)) {
                     atomicExch(&sh.aborted, 1);
                     break;
                 }
-                uint8_t *st = ring + s * Cfg::kStageBytes;
-                mbar_arrive_expect_tx(&sh.full[s], Cfg::kStageBytes);
+                uint8_t *st = ring + s * stage_bytes;
+                mbar_arrive_expect_tx(&sh.full[s], (uint32_t)stage_bytes);
                 const int kc = (c_begin + i) * kChunkK;
-                tma_load_2d(st, &tm_w, &sh.full[s], kc, n0);
-                tma_load_2d(st + kWTileBytes, &tm_x, &sh.full[s], kc, 0);
+                tma_load_2d(st + xbytes, &tm_w, &sh.full[s], kc, n0);
+                tma_load_2d(st, &tm_x, &sh.full[s], kc, 0);
             }
             sh.issued = i;
         }
@@ -137,12 +192,12 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint8_t *st = ring + s * Cfg::kStageBytes;
+                const uint8_t *st = ring + s * stage_bytes;
                 const uint64_t adesc = smem_desc_sw128(smem_u32(st));
-                const uint64_t bdesc = smem_desc_sw128(smem_u32(st + kWTileBytes));
+                const uint64_t bdesc = smem_desc_sw128(smem_u32(st + xbytes));
 #pragma unroll
                 for (int kk = 0; kk < kChunkK / 16; ++kk)  // 4 MMAs of K = 16 (32 bytes) each
-                    mma_bf16(tmem, adesc + 2 * kk, bdesc + 2 * kk, Cfg::kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
+                    mma_bf16(tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&sh.empty[s]);
             }
             sh.consumed = i;
@@ -154,47 +209,71 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         __syncwarp();
     }
 
-    // ---- epilogue, all four warps: TMEM -> shared partial [TOK][128] ----
-    float *part = reinterpret_cast<float *>(ring);  // overlays the (consumed) ring
+    // ---- epilogue: accumulator -> local staging [M][BN] -> one bulk copy per owner ----
     const bool ok = mbar_wait(&sh.accum, 0, status, kSiteAccum);
     tc_fence_after();
-    if (ok && !*((volatile int32_t *)&sh.aborted)) {
-        const int row = warp * 32 + lane;  // TMEM lane == W row within the tile
+    const bool have = ok && !*((volatile int32_t *)&sh.aborted);
+    if (warp * 32 < M) {  // warps whose TMEM lanes hold real tokens
+        const int t = warp * 32 + lane;  // token == TMEM lane
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 16) {
+            uint32_t r[16];
+            if (have) {
+                tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, r);
+                tmem_ld_wait16(r);
+            } else {
 #pragma unroll
-        for (int c = 0; c < TOK; c += 16) {
-            float v[16];
-            tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
-            tmem_ld_wait();
+                for (int j = 0; j < 16; ++j) r[j] = 0u;
+            }
+            if (t < M) {
+                float4 *dst = stage_out + (t * BN + c) / 4;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) part[(c + j) * kRows + row] = v[j];
+                for (int q4 = 0; q4 < 4; ++q4)
+                    dst[q4] = make_float4(__uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]),
+                                          __uint_as_float(r[4 * q4 + 2]), __uint_as_float(r[4 * q4 + 3]));
+            }
         }
+        fence_proxy_async_smem();  // the bulk copies below read the staging through the async proxy
     }
     tc_fence_before();
-    cluster_sync();  // every CTA's partial is written and visible cluster-wide
+    __syncthreads();
+    cluster_wait_acquire();  // phase 1 done: every CTA's receive barrier exists
+    if (tid < S) {  // thread d sends owner d its slice [it0(d), it1(d)) of the items
+        const int d = tid;
+        const int d0 = part_begin(d, T, S);
+        const int nd = part_begin(d + 1, T, S) - d0;
+        if (nd > 0)
+            bulk_copy_to_peer(mapa_shared(smem_u32(recv + rank * nd), (uint32_t)d), stage_out + d0,
+                              (uint32_t)(nd * 16), mapa_shared(smem_u32(&sh.recv), (uint32_t)d));
+    }
 
-    // ---- distributed reduction: this CTA owns items [r*T/S, (r+1)*T/S) of T = M*32 float4s ----
-    const bool aborted = *((volatile int32_t *)&sh.aborted) != 0;
-    if (!aborted) {
-        const int T = M * (kRows / 4);
-        const int it0 = (int)(((long long)rank * T) / S), it1 = (int)(((long long)(rank + 1) * T) / S);
-        const uint32_t part_addr = smem_u32(part);
-        for (int it = it0 + tid; it < it1; it += kSplitThreads) {
-            const int m = it / (kRows / 4), g = it % (kRows / 4);
-            const uint32_t off = (uint32_t)((m * kRows + 4 * g) * 4);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int q = 0; q < S; ++q) {
-                const float4 v = ld_dsmem_f4(mapa_shared(part_addr + off, (uint32_t)q));
+    // ---- owner: S partials of my items -> bias -> bf16 -> out ----
+    const int it0 = part_begin(rank, T, S);
+    const int mine = part_begin(rank + 1, T, S) - it0;
+    if (tid == 0) mbar_arrive_expect_tx(&sh.recv, (uint32_t)(S * mine * 16));
+    const bool got = mbar_wait_cluster(&sh.recv, 0, status, kSiteRecv);
+    // Every copy into this CTA has landed, so every peer's copy out of its own
+    // staging has been read: phase 2 lets all of them exit.
+    cluster_arrive_release();
+    pdl_wait();  // the previous kernel may still read `out`
+    if (got && !*((volatile int32_t *)&sh.aborted)) {
+        for (int j = tid; j < mine; j += kSplitThreads) {
+            float4 acc = recv[j];
+            for (int q = 1; q < S; ++q) {
+                const float4 v = recv[q * mine + j];
                 acc.x += v.x;
                 acc.y += v.y;
                 acc.z += v.z;
                 acc.w += v.w;
             }
-            const int n = n0 + 4 * g;
+            const int item = it0 + j;
+            const int m = item / (BN / 4);
+            const int n = n0 + 4 * (item % (BN / 4));
             float r4[4] = {acc.x, acc.y, acc.z, acc.w};
             if (bias) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (n + j < N) r4[j] += bf16_to_f32(bias[n + j]);
+                for (int e = 0; e < 4; ++e)
+                    if (n + e < N) r4[e] += bf16_to_f32(bias[n + e]);
             }
             const size_t o = (size_t)m * N + n;
             if (n + 3 < N && (o & 3) == 0) {
@@ -204,8 +283,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
                 *reinterpret_cast<uint2 *>(out + o) = pk;
             } else {
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (n + j < N) out[o + j] = f32_to_bf16(r4[j]);
+                for (int e = 0; e < 4; ++e)
+                    if (n + e < N) out[o + e] = f32_to_bf16(r4[e]);
             }
         }
     }
@@ -215,68 +294,72 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         for (int i = sh.consumed; i < sh.issued; ++i)
             mbar_wait(&sh.full[i % stages], (i / stages) & 1, status, kSiteDrain);
     }
-    cluster_sync();  // peers have finished reading this CTA's partial
+    cluster_wait_acquire();  // phase 2 done: no copy into or out of this CTA is pending
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, Cfg::kTmemCols);
+        tmem_dealloc(tmem, kCols);
     }
 }
 
 namespace {
 
-template <int TOK>
-int set_attrs() {
-    auto fn = splitk_kernel<TOK>;
-    int e = (int)cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      SplitCfg<TOK>::smem_bytes(kSplitMaxStages));
-    if (!e) e = (int)cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    return e;
-}
+typedef void (*SplitFn)(CUtensorMap, CUtensorMap, const uint16_t *, uint16_t *, int, int, int, int, int, int32_t *);
 
-template <int TOK>
-int launch(const LaunchArgs &a, const bf16l_plan &p) {
-    CUtensorMap tw, tx;
-    int r = make_tmap_bf16_2d(&tw, a.W, (uint64_t)a.N, (uint64_t)a.K, kRows, kChunkK, CU_TENSOR_MAP_SWIZZLE_128B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-    if (r) return (int)cudaErrorInvalidValue;
-    r = make_tmap_bf16_2d(&tx, a.x, (uint64_t)a.M, (uint64_t)a.K, TOK, kChunkK, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-    if (r) return (int)cudaErrorInvalidValue;
-
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.split_k, (unsigned)((a.N + kRows - 1) / kRows), 1);
-    cfg.blockDim = dim3(kSplitThreads, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)SplitCfg<TOK>::smem_bytes(p.stages);
-    cfg.stream = (cudaStream_t)a.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)p.split_k;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return (int)cudaLaunchKernelEx(&cfg, splitk_kernel<TOK>, tw, tx, static_cast<const uint16_t *>(a.bias),
-                                   static_cast<uint16_t *>(a.out), a.M, a.N, a.K, p.stages, a.status);
+SplitFn pick(int BN) {
+    switch (BN) {
+        case 16: return splitk_kernel<16>;
+        case 32: return splitk_kernel<32>;
+        case 48: return splitk_kernel<48>;
+        case 64: return splitk_kernel<64>;
+        case 96: return splitk_kernel<96>;
+        case 128: return splitk_kernel<128>;
+        case 192: return splitk_kernel<192>;
+        case 256: return splitk_kernel<256>;
+        default: return nullptr;
+    }
 }
 
 }  // namespace
 
+bool split_rows_supported(int rows) { return pick(rows) != nullptr; }
+
 int init_splitk() {
-    int e = set_attrs<16>();
-    if (!e) e = set_attrs<32>();
-    if (!e) e = set_attrs<48>();
-    if (!e) e = set_attrs<64>();
-    return e;
+    for (int BN : {16, 32, 48, 64, 96, 128, 192, 256}) {
+        int e = (int)cudaFuncSetAttribute(pick(BN), cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPerCta);
+        if (!e) e = (int)cudaFuncSetAttribute(pick(BN), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e) return e;
+    }
+    return 0;
 }
 
 int launch_splitk(const LaunchArgs &a, const bf16l_plan &p) {
-    switch (p.tokens_per_cta) {
-        case 16: return launch<16>(a, p);
-        case 32: return launch<32>(a, p);
-        case 48: return launch<48>(a, p);
-        case 64: return launch<64>(a, p);
-        default: return (int)cudaErrorInvalidValue;
-    }
+    SplitFn fn = pick(p.rows_per_cta);
+    if (!fn) return (int)cudaErrorInvalidValue;
+    CUtensorMap tw, tx;
+    int r = make_tmap_bf16_2d(&tw, a.W, (uint64_t)a.N, (uint64_t)a.K, (uint32_t)p.rows_per_cta, kChunkK,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    if (r) return (int)cudaErrorInvalidValue;
+    r = make_tmap_bf16_2d(&tx, a.x, (uint64_t)a.M, (uint64_t)a.K, (uint32_t)p.tokens_per_cta, kChunkK,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    if (r) return (int)cudaErrorInvalidValue;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.split_k, (unsigned)((a.N + p.rows_per_cta - 1) / p.rows_per_cta), 1);
+    cfg.blockDim = dim3(kSplitThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)split_smem_bytes(p.tokens_per_cta, p.rows_per_cta, p.stages);
+    cfg.stream = (cudaStream_t)a.stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.split_k;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = (p.flags & BF16L_FLAG_PDL) ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return (int)cudaLaunchKernelEx(&cfg, fn, tw, tx, static_cast<const uint16_t *>(a.bias),
+                                   static_cast<uint16_t *>(a.out), a.M, a.N, a.K, p.tokens_per_cta, p.stages,
+                                   a.status);
 }
 
 }  // namespace bf16l

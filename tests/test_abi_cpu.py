@@ -78,9 +78,9 @@ def test_plan_is_valid_everywhere(lib):
         p = lib.plan(pt["M"], pt["N"], pt["K"])
         assert p.grid > 0
         if p.kernel == lib.KERNEL_SPLITK:
-            assert p.tokens_per_cta >= pt["M"] and p.tokens_per_cta % 16 == 0
+            assert p.tokens_per_cta >= pt["M"] and p.tokens_per_cta % 8 == 0
             assert 1 <= p.split_k <= 16 and p.split_k <= -(-pt["K"] // 64)
-            assert p.grid == p.split_k * -(-pt["N"] // 128)
+            assert p.grid == p.split_k * -(-pt["N"] // p.rows_per_cta)
         if p.kernel == lib.KERNEL_DOTPROD:
             assert p.grid == -(-pt["N"] // p.rows_per_cta)
 
@@ -121,14 +121,17 @@ def test_forced_plan_rules_without_gpu(lib):
         p = lib.make_plan(**plan)
         return L.bf16_linear_with_plan(A, B, None, O, M, N, K, ctypes.byref(p), None)
 
-    split = dict(kernel="splitk", threads=128, rows_per_cta=128, tokens_per_cta=16, split_k=4, stages=2)
+    split = dict(kernel="splitk", threads=128, rows_per_cta=32, tokens_per_cta=16, split_k=4, stages=2)
     assert run(8, 256, 2049, **split) == -6            # TMA kernels need K % 8 == 0
     assert run(65, 256, 2048, **{**split, "tokens_per_cta": 64}) == -6  # split-K holds at most 64 tokens
     assert run(20, 256, 2048, **split) == -1           # tokens_per_cta < M
     assert run(8, 256, 2048, **{**split, "split_k": 17}) == -1
     assert run(8, 256, 128, **{**split, "split_k": 3}) == -1  # more CTAs than 64-wide K chunks
-    assert run(8, 256, 2048, **{**split, "stages": 9}) == -1
-    assert run(8, 256, 2048, **{**split, "tokens_per_cta": 24}) == -1
+    assert run(8, 256, 2048, **{**split, "stages": 17}) == -1
+    assert run(8, 256, 2048, **{**split, "tokens_per_cta": 12}) == -1   # not a multiple of 8
+    assert run(8, 256, 2048, **{**split, "rows_per_cta": 24}) == -1     # no kernel for 24 rows
+    assert run(8, 256, 2048, **{**split, "rows_per_cta": 512}) == -1
+    assert run(8, 256, 2048, **{**split, "flags": 2}) == -1             # unknown launch flag
     assert run(8, 256, 2048, kernel="dotprod", threads=96, rows_per_cta=2) == -1
     assert run(8, 256, 2048, kernel="dotprod", threads=128, rows_per_cta=3) == -1
     assert run(8, 256, 2048, kernel="tile", threads=192, rows_per_cta=256, tokens_per_cta=128, stages=9) == -1

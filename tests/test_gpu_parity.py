@@ -50,9 +50,9 @@ def _check(lib, M, N, K, seed=0, bias=False, plan=None, what=""):
     return got, want
 
 
-def splitk_plan(lib, M, split, stages, tokens=None):
-    return lib.make_plan("splitk", threads=128, rows_per_cta=128,
-                         tokens_per_cta=tokens or max(16, -(-M // 16) * 16), split_k=split, stages=stages)
+def splitk_plan(lib, M, split, stages, rows=32, tokens=None):
+    return lib.make_plan("splitk", threads=128, rows_per_cta=rows,
+                         tokens_per_cta=tokens or max(8, -(-M // 8) * 8), split_k=split, stages=stages)
 
 
 def dot_plan(lib, R, threads=128):
@@ -142,33 +142,60 @@ def test_dotprod_block_sizes(lib, threads):
 
 
 SPLIT_CASES = [
-    # M, N, K, split, stages
-    (5, 256, 4096, 8, 5),
-    (16, 256, 7168, 16, 7),
-    (16, 384, 7168, 7, 5),
-    (9, 128, 2880, 8, 2),       # K = 2880: 45 chunks over 8 CTAs (uneven split)
-    (12, 256, 6144, 6, 4),      # the pages' default (split_k, num_stages) = (6, 4)
-    (1, 200, 64, 1, 1),         # one chunk, one CTA, ragged N
-    (3, 130, 136, 3, 1),        # K tail inside the last chunk, ring reuse
-    (32, 2112, 7168, 8, 8),     # N tail (2112 = 16.5 x 128)
-    (64, 2112, 7168, 8, 3),     # full 64 tokens, ring wraps several times
-    (48, 300, 520, 2, 2),
-    (17, 129, 1032, 5, 2),      # ragged everything
-    (8, 14336, 4096, 2, 4),
+    # M, N, K, rows (MMA N), split, stages
+    (5, 256, 4096, 32, 8, 5),
+    (16, 256, 7168, 16, 9, 13),
+    (16, 384, 7168, 32, 12, 10),
+    (9, 128, 2880, 16, 8, 2),       # K = 2880: 45 chunks over 8 CTAs (uneven split), ring reuse
+    (12, 256, 6144, 64, 6, 4),      # the pages' default (split_k, num_stages) = (6, 4)
+    (1, 200, 64, 16, 1, 1),         # one chunk, one CTA, ragged N
+    (3, 130, 136, 48, 1, 1),        # K tail inside the last chunk, one stage reused 3 times
+    (32, 2112, 7168, 128, 8, 8),    # N tail (2112 = 16.5 x 128)
+    (64, 2112, 7168, 128, 8, 3),    # 64 tokens, ring wraps several times
+    (48, 300, 520, 96, 2, 2),
+    (17, 129, 1032, 192, 5, 2),     # ragged everything
+    (8, 14336, 4096, 256, 2, 4),
+    (64, 1000, 1024, 256, 1, 2),
+    (2, 64, 7168, 16, 16, 7),       # 16-CTA cluster, M = 2
 ]
 
 
 @pytest.mark.parametrize("case", SPLIT_CASES, ids=lambda c: "x".join(map(str, c)))
 def test_splitk_forced(lib, case):
-    M, N, K, split, stages = case
+    M, N, K, rows, split, stages = case
     for bias in (False, True):
-        _check(lib, M, N, K, seed=M + N + K + split, bias=bias, plan=splitk_plan(lib, M, split, stages))
+        _check(lib, M, N, K, seed=M + N + K + split, bias=bias, plan=splitk_plan(lib, M, split, stages, rows=rows))
 
 
-@pytest.mark.parametrize("tokens", [16, 32, 48, 64])
+@pytest.mark.parametrize("tokens", [8, 16, 24, 40, 64])
 def test_splitk_token_padding(lib, tokens):
-    """Fewer tokens than the MMA width: padded rows are zero-filled and never stored."""
-    _check(lib, 3, 256, 2048, seed=tokens, plan=splitk_plan(lib, 3, 4, 4, tokens=tokens))
+    """Fewer tokens than the loaded x rows: padded rows are zero-filled and never stored."""
+    _check(lib, 3, 256, 2048, seed=tokens, plan=splitk_plan(lib, 3, 4, 4, rows=32, tokens=tokens))
+
+
+@pytest.mark.parametrize("rows", [16, 32, 48, 64, 96, 128, 192, 256])
+def test_splitk_every_tile_width(lib, rows):
+    _check(lib, 11, 520, 1536, seed=rows, bias=True, plan=splitk_plan(lib, 11, 3, 3, rows=rows))
+
+
+def test_pdl_launch_matches(lib):
+    """Programmatic dependent launch changes scheduling only, never the result."""
+    import ctypes
+    for (M, N, K) in [(16, 256, 7168), (2, 384, 7168), (64, 2112, 7168)]:
+        x, W, b = _inputs(M, N, K, 21, True)
+        xd, Wd, bd = x.to(DEV), W.to(DEV), b.to(DEV)
+        plain = tensor_bits(lib.bf16_linear(xd, Wd, bd))
+        outs = []
+        for _ in range(3):
+            o = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+            st = lib.load().bf16_linear_ex(ctypes.c_void_p(xd.data_ptr()), ctypes.c_void_p(Wd.data_ptr()),
+                                           ctypes.c_void_p(bd.data_ptr()), ctypes.c_void_p(o.data_ptr()),
+                                           M, N, K, 1, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+            assert st == 0
+            outs.append(o)
+        torch.cuda.synchronize()
+        for o in outs:
+            assert np.array_equal(tensor_bits(o), plain)
 
 
 # ---------------------------------------------------------------------------
@@ -178,7 +205,7 @@ def test_splitk_token_padding(lib, tokens):
 def _plans_for(lib, M):
     plans = [None, dot_plan(lib, 2)]
     if M <= 64:
-        plans.append(splitk_plan(lib, M, 4, 2))
+        plans.append(splitk_plan(lib, M, 4, 2, rows=32))
     return plans
 
 
