@@ -69,6 +69,8 @@ def load_peaks():
 
 
 def workload_points(name):
+    if name == "all":
+        return wl.router_smallest() + wl.router_sweep() + wl.decode_proj() + wl.mlp_bias()
     return {"router": wl.router_sweep, "smallest": wl.router_smallest, "decode": wl.decode_proj,
             "mlp": wl.mlp_bias, "prefill": wl.prefill}[name]()
 
@@ -80,6 +82,7 @@ def workload_desc(name):
         "decode": "decode attention-input projection: M in {1,2,4,8,16,32,64}, K=7168, N=2112, no bias",
         "mlp": "dense MLP with bias: M in {1,8,64,256}, K=4096, N=14336",
         "prefill": "prefill: M in {2048,8192} x (K,N) in {(7168,2112),(4096,14336),(7168,7168)}, bias on/off",
+        "all": "every skinny workload shape (router, decode, MLP)",
     }[name]
 
 
@@ -317,11 +320,35 @@ def gpu_arm(args, points, rank, world):
         per_shape_us.append(1000.0 * statistics.median(ms) / s.R)
     launches = args.steps * sum(s.R for s in shapes)
 
+    # ---- the same shapes launched with programmatic dependent launch (BF16L_FLAG_PDL) ----
+    pdl_us = None
+    if not args.pdl and not args.no_pdl_variant:
+        for s_ in shapes:
+            s_.plan.flags = 1
+        with torch.cuda.stream(stream):
+            for s_ in shapes:
+                s_.capture(stream)
+        torch.cuda.synchronize()
+        pdl_ms = [[] for _ in shapes]
+        with torch.cuda.stream(stream):
+            for k in range(max(3, args.steps // 2)):
+                for j, s_ in enumerate(shapes):
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    s_.graph.replay()
+                    b.record(stream)
+                    pdl_ms[j].append((a, b))
+        torch.cuda.synchronize()
+        pdl_us = [1000.0 * statistics.median([a.elapsed_time(b) for a, b in pdl_ms[j]]) / s_.R
+                  for j, s_ in enumerate(shapes)]
+        for s_ in shapes:
+            s_.plan.flags = 0
+
     # ---- e2e: public API from pinned host buffers, copies inside the timed region ----
     e2e = e2e_arm(args, shapes, lib, device, stream)
 
     return dict(shapes=shapes, per_shape_us=per_shape_us, total_ms=total_ms, launches=launches,
-                clocks=clocks, e2e=e2e)
+                clocks=clocks, e2e=e2e, pdl_us=pdl_us)
 
 
 def eager_profile(args, points):
@@ -350,6 +377,100 @@ def eager_profile(args, points):
         res[f"M{s.M}_N{s.N}_K{s.K}"] = {"kernel": s.kernel, "eager_us_per_call": 1000 * a.elapsed_time(b) / args.steps,
                                       "plan": s.plan.as_dict()}
     print(json.dumps({"mode": "eager", "steps": args.steps, "shapes": res}))
+
+
+def candidate_plans(lib, M, N, K):
+    """Every plan worth timing for one shape (the tuning space of the sweep)."""
+    cands = []
+    if M <= 16:
+        for R in (1, 2, 4):
+            for threads in (128, 256):
+                cands.append(lib.make_plan("dotprod", threads=threads, rows_per_cta=R))
+    if K % 8 == 0 and M <= 64:
+        chunks = -(-K // 64)
+        tokens = max(8, -(-M // 8) * 8)
+        for rows in (16, 32, 64, 128, 256):
+            if rows > max(16, 2 * N):
+                continue
+            for split in (1, 2, 4, 6, 8, 12, 16):
+                if split > chunks:
+                    continue
+                tiles = -(-N // rows)
+                if tiles * split < 16 or tiles * split > 4 * 152:
+                    continue
+                per = -(-chunks // split)
+                p = lib.make_plan("splitk", threads=128, rows_per_cta=rows, tokens_per_cta=tokens,
+                                  split_k=split, stages=1)
+                # deepest ring that fits (the planner's rule), found by trying
+                for st in (16, 14, 12, 10, 8, 7, 6, 5, 4, 3, 2, 1):
+                    p.stages = min(st, per)
+                    try:
+                        lib.plan_check(M, N, K, p)
+                        break
+                    except Exception:
+                        continue
+                cands.append(p)
+    if K % 8 == 0 and M > 32:
+        for st in (4, 3):
+            cands.append(lib.make_plan("tile", threads=192, rows_per_cta=256, tokens_per_cta=128, stages=st))
+    return cands
+
+
+def sweep(args, points):
+    """Time every candidate plan of every shape (L2-cold graphs) and write the dispatch table."""
+    import moe_router_gemm_gb300 as lib
+    from moe_router_gemm_gb300 import build as _build
+    _build.build()
+    device = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.Stream(device)
+    results = []
+    out_dir = os.path.join(ROOT, "gpurun_out") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ROOT
+    for pt in points:
+        base = Shape(pt, device, lib)
+        R = min(base.R, 64)  # 64 rotated copies keep every call L2-cold for these sizes
+        rows = []
+        for p in candidate_plans(lib, pt["M"], pt["N"], pt["K"]):
+            base.plan = p
+            try:
+                with torch.cuda.stream(stream):
+                    for i in range(2):
+                        base.call(i)
+                    torch.cuda.synchronize()
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=stream):
+                        for i in range(R):
+                            base.call(i)
+                    g.replay()
+                    torch.cuda.synchronize()
+                    best = 1e9
+                    for _ in range(3):
+                        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        a.record(stream)
+                        g.replay()
+                        b.record(stream)
+                        torch.cuda.synchronize()
+                        best = min(best, 1000.0 * a.elapsed_time(b) / R)
+                rows.append((best, p.as_dict()))
+            except Exception as e:  # an unusable candidate is skipped, not fatal
+                rows.append((float("inf"), dict(p.as_dict(), error=str(e)[:80])))
+        rows.sort(key=lambda r: r[0])
+        default = lib.plan(pt["M"], pt["N"], pt["K"]).as_dict()
+        results.append({"M": pt["M"], "N": pt["N"], "K": pt["K"], "best_us": rows[0][0], "best": rows[0][1],
+                        "default": default, "top": [(round(t, 3), d) for t, d in rows[:5]]})
+        print(json.dumps({"shape": [pt["M"], pt["N"], pt["K"]], "best_us": round(rows[0][0], 3),
+                          "best": rows[0][1]}), flush=True)
+        del base
+        torch.cuda.empty_cache()
+    with open(os.path.join(out_dir, "sweep_results.json"), "w") as f:
+        json.dump(results, f, indent=1)
+    lines = ["// Measured GB300 dispatch entries (python bench.py --sweep): fastest plan per shape, L2-cold.",
+             "// {K, N, M, kernel, threads, rows_per_cta, tokens_per_cta, split_k, stages},"]
+    for r in sorted(results, key=lambda r: (r["K"], r["N"], r["M"])):
+        b = r["best"]
+        lines.append(f"{{{r['K']}, {r['N']}, {r['M']}, {b['kernel']}, {b['threads']}, {b['rows_per_cta']}, "
+                     f"{b['tokens_per_cta']}, {b['split_k']}, {b['stages']}}},  // {r['best_us']:.3f} us")
+    with open(os.path.join(out_dir, "dispatch_table.inc"), "w") as f:
+        f.write("\n".join(lines) + "\n")
 
 
 def e2e_arm(args, shapes, lib, device, stream):
@@ -398,13 +519,18 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="router", choices=["router", "smallest", "decode", "mlp", "prefill"])
+    ap.add_argument("--workload", default="router", choices=["router", "smallest", "decode", "mlp", "prefill", "all"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pdl", action="store_true",
                     help="launch with programmatic dependent launch (BF16L_FLAG_PDL): back-to-back calls overlap")
+    ap.add_argument("--no-pdl-variant", action="store_true",
+                    help="skip the extra pass that re-times every shape with programmatic dependent launch")
     ap.add_argument("--only", action="append", default=[],
                     help="restrict to shapes M,N,K[,bias] (repeatable); for profiling")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every candidate plan of the workload's shapes and write dispatch_table.inc "
+                         "(to gpurun_out/ when that folder exists)")
     ap.add_argument("--eager", action="store_true",
                     help="profiling mode: each step calls every shape once per rotation copy, no graphs, "
                          "no e2e/cpu legs; prints per-shape timings only")
@@ -458,6 +584,9 @@ def main():
 
     if args.eager:
         eager_profile(args, points)
+        return
+    if args.sweep:
+        sweep(args, points)
         return
     r = gpu_arm(args, points, rank, world)
     shapes, per_us = r["shapes"], r["per_shape_us"]
@@ -529,6 +658,13 @@ def main():
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
         "kernel_share": {k: round(v[0] / sum(x[0] for x in share.values()), 4) for k, v in share.items()},
+        "pdl_variant": None if r["pdl_us"] is None else {
+            "note": "same shapes and rotation, launched with BF16L_FLAG_PDL (weights fetched before the "
+                    "grid-dependency wait, so back-to-back calls overlap); timed after the main region",
+            "value": round(statistics.mean(r["pdl_us"]), 4) if not large else None,
+            "unit": unit,
+            "per_shape_us": {k: [round(u, 3) for s_, u in zip(shapes, r["pdl_us"]) if f"K{s_.K}_N{s_.N}" == k]
+                             for k in per_shape}},
         "per_shape_us": per_shape,
         "pct_hbm_roofline_per_shape": None if large else {
             k: [round(100.0 * algo_bytes(s.M, s.N, s.K, s.bias) / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 1)

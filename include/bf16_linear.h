@@ -119,6 +119,15 @@ typedef struct {
 int bf16_linear_plan(int M, int N, int K, const bf16l_device *dev, bf16l_plan *plan);
 
 /*
+ * bf16_linear_plan_check — validate an explicit plan for (M, N, K) on `dev`
+ * (NULL = GB300) and fill plan->grid.  Pure host code.  Returns BF16L_OK,
+ * BF16L_EINVAL (a parameter outside the kernel's limits, or a shared-memory
+ * ring that does not fit), BF16L_EUNSUPPORTED (the kernel cannot run this
+ * shape, e.g. K % 8 != 0 for the TMA kernels) or BF16L_EARCH.
+ */
+int bf16_linear_plan_check(int M, int N, int K, const bf16l_device *dev, bf16l_plan *plan);
+
+/*
  * bf16_linear — out = x @ W^T (+ bias), bf16 out, on `stream`.
  *
  * x: device bf16 [M][K]; W: device bf16 [N][K]; bias: device bf16 [N] or NULL;

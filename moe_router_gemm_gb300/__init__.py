@@ -8,4 +8,4 @@ dispatcher.  This package is its thin Python binding; build the library with
 """
 from ._binding import (BF16LinearError, Device, KERNEL_DOTPROD, KERNEL_NAMES, KERNEL_SPLITK,  # noqa: F401
                        KERNEL_TILE, LIB_PATH, Plan, bf16_linear, bf16_linear_with_plan, device_status,
-                       load, make_plan, plan, selftest_wait, strerror, version)
+                       load, make_plan, plan, plan_check, selftest_wait, strerror, version)

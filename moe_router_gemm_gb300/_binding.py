@@ -72,6 +72,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.bf16_linear_with_plan.restype = i32
         lib.bf16_linear_plan.argtypes = [i32, i32, i32, ctypes.POINTER(Device), ctypes.POINTER(Plan)]
         lib.bf16_linear_plan.restype = i32
+        lib.bf16_linear_plan_check.argtypes = [i32, i32, i32, ctypes.POINTER(Device), ctypes.POINTER(Plan)]
+        lib.bf16_linear_plan_check.restype = i32
         lib.bf16_linear_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32), i32]
         lib.bf16_linear_device_status.restype = i32
         lib.bf16_linear_selftest_wait.argtypes = [ctypes.c_uint32, vp]
@@ -106,6 +108,16 @@ def plan(M: int, N: int, K: int, device: tuple[int, int, int] | None = None) -> 
                                  ctypes.byref(p))
     if st != OK:
         _raise(st, f"bf16_linear_plan({M},{N},{K})")
+    return p
+
+
+def plan_check(M: int, N: int, K: int, p: Plan, device: tuple[int, int, int] | None = None) -> Plan:
+    """Validate an explicit plan for (M, N, K); fills p.grid, raises BF16LinearError if unusable."""
+    dev = Device(*device) if device is not None else None
+    st = load().bf16_linear_plan_check(int(M), int(N), int(K), ctypes.byref(dev) if dev is not None else None,
+                                       ctypes.byref(p))
+    if st != OK:
+        _raise(st, f"bf16_linear_plan_check({M},{N},{K}, {p})")
     return p
 
 

@@ -30,7 +30,8 @@ enum WaitSite : int32_t {
     kSiteTmemEmpty = 4,  // MMA issuer waiting for the epilogue to drain TMEM
     kSiteDrain = 5,      // exit path draining copies still in flight
     kSiteSelftest = 6,   // bf16_linear_selftest_wait
-    kSiteRecv = 7        // split-K owner waiting for its peers' partials
+    kSiteRecv = 7,       // split-K owner waiting for its peers' partials
+    kSiteStage = 8       // dot-product CTA waiting for its copy of x
 };
 
 // Default limit for one wait: 1 s of wall-clock time.
@@ -177,6 +178,14 @@ __device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *m
         : "memory");
 }
 
+// Untiled bulk copy global -> this CTA's shared memory (both addresses 16-byte
+// aligned, bytes a multiple of 16), completion counted on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -296,6 +305,10 @@ __device__ __forceinline__ void cluster_arrive_release() {
 }
 __device__ __forceinline__ void cluster_wait_acquire() {
     asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+// Arrive without ordering memory (for phases that publish nothing).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_sync() {
     cluster_arrive_release();

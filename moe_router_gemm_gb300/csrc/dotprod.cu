@@ -9,10 +9,11 @@
 // bytes in flight at such small sizes:
 //   * a CTA owns R consecutive W rows, so each x vector is reused R times;
 //   * every thread issues the 16-byte weight loads of its first batch (up to
-//     8 vectors per row) before anything else, then the CTA copies x (all MT
-//     token rows, a few KB to ~100 KB) into shared memory while those loads are
-//     in flight; the multiply-adds then read x from shared memory instead of
-//     waiting on L2 once per (vector, token);
+//     8 vectors per row) before anything else, while one thread copies x (all
+//     MT token rows, a few KB to ~100 KB) into shared memory with one bulk
+//     copy per row (a single L2 round trip, counted on an mbarrier); the
+//     multiply-adds then read x from shared memory instead of waiting on L2
+//     once per (vector, token);
 //   * rows whose length is not a multiple of 8 elements (K % 8 != 0, so not
 //     16-byte aligned) take a scalar path that reads x from global memory.
 // Tokens are processed MT at a time (MT = M for M <= 8); larger M loops over
@@ -56,9 +57,11 @@ template <int MT, int R, int VEC, bool XSMEM>
 __global__ void __launch_bounds__(256) dotprod_kernel(const uint16_t *__restrict__ x,
                                                       const uint16_t *__restrict__ W,
                                                       const uint16_t *__restrict__ bias,
-                                                      uint16_t *__restrict__ out, int M, int N, int K) {
+                                                      uint16_t *__restrict__ out, int M, int N, int K,
+                                                      int32_t *status) {
     constexpr int U = (VEC == 8) ? 8 : 4;  // vectors per row a thread loads before computing
     __shared__ float red[8][R * MT];
+    __shared__ __align__(8) uint64_t xbar;
     extern __shared__ uint4 xs[];  // XSMEM: x[m0 + m][k] as 16-byte vectors, [MT][K / 8]
 
     const int tid = threadIdx.x;
@@ -74,7 +77,15 @@ __global__ void __launch_bounds__(256) dotprod_kernel(const uint16_t *__restrict
         wrow[r] = W + (size_t)n * K;
     }
 
-    for (int m0 = 0; m0 < M; m0 += MT) {
+    if constexpr (XSMEM) {
+        if (tid == 0) {
+            mbar_init(&xbar, 1);
+            fence_barrier_init();
+        }
+        __syncthreads();
+    }
+
+    for (int m0 = 0, pass = 0; m0 < M; m0 += MT, ++pass) {
         float acc[R][MT];
 #pragma unroll
         for (int r = 0; r < R; ++r)
@@ -99,13 +110,16 @@ __global__ void __launch_bounds__(256) dotprod_kernel(const uint16_t *__restrict
         }
 
         if constexpr (XSMEM) {
-            // Stage the MT token rows of x in shared memory (zeros past M).
-            const uint4 *xg = reinterpret_cast<const uint4 *>(x);
-            for (int i = tid; i < MT * nvec; i += nt) {
-                const int m = i / nvec, v = i - m * nvec;
-                xs[i] = (m0 + m < M) ? __ldg(xg + (size_t)(m0 + m) * nvec + v) : make_uint4(0u, 0u, 0u, 0u);
+            // Stage the token rows of this pass in shared memory: one bulk copy
+            // per row.  Rows past M are left stale: they only feed accumulators
+            // that are never stored.
+            if (tid == 0) {
+                const int rows = (M - m0) < MT ? (M - m0) : MT;
+                mbar_arrive_expect_tx(&xbar, (uint32_t)(rows * K * 2));
+                for (int r = 0; r < rows; ++r)
+                    bulk_load(xs + (size_t)r * nvec, x + (size_t)(m0 + r) * K, (uint32_t)(K * 2), &xbar);
             }
-            __syncthreads();
+            mbar_wait(&xbar, (uint32_t)(pass & 1), status, kSiteStage);
         }
 
         for (int v0 = tid; v0 < nvec; v0 += U * nt) {
@@ -161,7 +175,7 @@ __global__ void __launch_bounds__(256) dotprod_kernel(const uint16_t *__restrict
 
 namespace {
 
-typedef void (*DotFn)(const uint16_t *, const uint16_t *, const uint16_t *, uint16_t *, int, int, int);
+typedef void (*DotFn)(const uint16_t *, const uint16_t *, const uint16_t *, uint16_t *, int, int, int, int32_t *);
 
 // kind: 0 = 16-byte vectors with x in shared memory, 1 = 16-byte vectors with
 // x from global memory, 2 = scalar (K % 8 != 0).
@@ -228,7 +242,7 @@ int launch_dotprod(const LaunchArgs &a, const bf16l_plan &p) {
     cfg.numAttrs = 1;
     return (int)cudaLaunchKernelEx(&cfg, fn, static_cast<const uint16_t *>(a.x), static_cast<const uint16_t *>(a.W),
                                    static_cast<const uint16_t *>(a.bias), static_cast<uint16_t *>(a.out), a.M, a.N,
-                                   a.K);
+                                   a.K, a.status);
 }
 
 }  // namespace bf16l

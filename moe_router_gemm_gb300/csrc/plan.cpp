@@ -41,29 +41,30 @@ bool in_list(int v, const int *list, int n) {
 }
 
 void plan_dotprod(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
-    (void)M;
     (void)K;
+    // GB300 sweep: one W row per CTA for a single token on small N, two rows
+    // otherwise (each x vector then serves two rows), four on very large N.
     p->kernel = BF16L_KERNEL_DOTPROD;
-    p->threads = 128;
-    p->rows_per_cta = (N < 2 * dev.num_sms) ? 1 : (N < 16 * dev.num_sms ? 2 : 4);
+    p->threads = (N >= 16 * dev.num_sms) ? 128 : 256;
+    p->rows_per_cta = (M == 1 && N < 8 * dev.num_sms) ? 1 : (N < 64 * dev.num_sms ? 2 : 4);
 }
 
 void plan_splitk(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
-    // Aim for about one CTA per SM: weight tiles small enough that N / rows
-    // tiles times a cluster of <= 16 reaches the SM count, then as many K
-    // splits as the SMs allow.
+    // GB300 sweep: 64 weight rows x a 16-CTA cluster for router-sized N; for
+    // large N, 256 rows and as many K splits as give about half a CTA per SM
+    // (each CTA then streams a deep ring).
     const int chunks = ceil_div(K, kChunkK);
-    const int want_tiles = ceil_div(dev.num_sms, kSplitMaxCluster);
-    int rows = 16;
-    for (int r : {256, 128, 64, 32, 16})
-        if (ceil_div(N, r) >= want_tiles) {
-            rows = r;
-            break;
-        }
-    const int tiles = ceil_div(N, rows);
-    int split = dev.num_sms / tiles;
-    if (split < 1) split = 1;
-    if (split > kSplitMaxCluster) split = kSplitMaxCluster;
+    int rows, split;
+    if (N <= 512) {
+        rows = 64;
+        split = kSplitMaxCluster;
+    } else {
+        rows = 256;
+        const int tiles = ceil_div(N, rows);
+        split = ceil_div(dev.num_sms / 2, tiles);
+        if (split < 1) split = 1;
+        if (split > 8) split = 8;
+    }
     if (split > chunks) split = chunks;
     p->kernel = BF16L_KERNEL_SPLITK;
     p->threads = kSplitThreads;
@@ -157,7 +158,9 @@ extern "C" int bf16_linear_plan(int M, int N, int K, const bf16l_device *devp, b
     }
     if (!from_table) {
         p = bf16l_plan{};
-        if (K % 8 != 0 || M <= 4 || (M <= 16 && K < 2048))
+        // The pages' rule was M <= 4 or K < 2048 for the dot product; on GB300
+        // the dot product stays ahead up to M = 8 (one pass over W).
+        if (K % 8 != 0 || M <= kDotMaxTokens || (M <= 16 && K < 2048))
             plan_dotprod(M, N, K, dev, &p);
         else if (M <= kSplitMaxTokens)
             plan_splitk(M, N, K, dev, &p);
@@ -168,4 +171,14 @@ extern "C" int bf16_linear_plan(int M, int N, int K, const bf16l_device *devp, b
     }
     *plan = p;
     return BF16L_OK;
+}
+
+extern "C" int bf16_linear_plan_check(int M, int N, int K, const bf16l_device *devp, bf16l_plan *plan) {
+    using namespace bf16l;
+    if (!plan) return BF16L_EINVAL;
+    const bf16l_device gb300 = {10, 3, kGb300Sms};
+    const bf16l_device &dev = devp ? *devp : gb300;
+    if (dev.cc_major != 10 || dev.cc_minor != 3) return BF16L_EARCH;
+    if (dev.num_sms <= 0) return BF16L_EINVAL;
+    return check_plan(M, N, K, dev, plan);
 }

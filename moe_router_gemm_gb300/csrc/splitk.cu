@@ -11,11 +11,12 @@
 // intake is only some tens of GB/s, so the weights must be spread over 100+
 // CTAs, each streaming a few tens of KB, and the prologue / epilogue chain
 // must be short.
-//   * MMA shape: tokens on the MMA M side (M = 128; only the first TOKP rows of
+//   * MMA shape: tokens on the MMA M side (M = 64; only the first TOKP rows of
 //     the A tile hold x, the rest is whatever follows in shared memory and only
 //     feeds accumulator rows that are never read), BN = 16..256 weight rows on
 //     the N side.  So a CTA's weight tile can be as small as 16 rows and the
-//     grid can have hundreds of CTAs even for N = 128..384.
+//     grid can have hundreds of CTAs even for N = 128..384.  With M = 64 the
+//     accumulator row of token t sits in TMEM lane 32*(t/16) + t%16.
 //   * One thread issues TMA tile loads (128-byte swizzle; rows past N, tokens
 //     past M and K past the end are zero-filled) into a `stages`-deep ring of
 //     64-wide K chunks: the weight halves first, before anything else, then
@@ -44,8 +45,8 @@ namespace {
 
 constexpr int kSmemPerSm = 233472;  // 228 KB of shared memory per SM on sm_103
 constexpr int kSmemPerCta = 232448; // 227 KB usable by one CTA
-constexpr int kMmaM = 128;          // MMA rows (tokens, zero- or garbage-padded)
-constexpr int kATileBytes = kMmaM * kChunkK * 2;  // the 16 KB the MMA reads as A per chunk
+constexpr int kMmaM = 64;           // MMA rows (tokens, zero- or garbage-padded)
+constexpr int kATileBytes = kMmaM * kChunkK * 2;  // the 8 KB the MMA reads as A per chunk
 
 struct SplitShared {  // bookkeeping placed after the receive buffer (<= 512 bytes)
     uint64_t full[kSplitMaxStages];
@@ -83,7 +84,7 @@ int split_ring_bytes(int tokens, int rows, int stages) {
 int split_smem_bytes(int tokens, int rows, int stages) {
     const int stage = split_stage_bytes(tokens, rows);
     int body = split_ring_bytes(tokens, rows, stages) + split_recv_bytes(tokens, rows) + 512 /*bookkeeping*/;
-    // The MMA reads a full 128-row A window from the last stage's x chunk on.
+    // The MMA reads a full 64-row A window from the last stage's x chunk on.
     const int window = (stages - 1) * stage + kATileBytes;
     if (window > body) body = window;
     int bytes = 1024 /*alignment slack*/ + body;
@@ -149,6 +150,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
             mbar_arrive_expect_tx(&sh.full[i], (uint32_t)stage_bytes);
             tma_load_2d(st + xbytes, &tm_w, &sh.full[i], (c_begin + i) * kChunkK, n0);
         }
+        pdl_launch_dependents();  // the next kernel may start its own weight loads now
+        pdl_wait();               // x may be written by the previous kernel
+        for (int i = 0; i < first; ++i)
+            tma_load_2d(ring + i * stage_bytes, &tm_x, &sh.full[i], (c_begin + i) * kChunkK, 0);
     }
     if (warp == 1) {
         tmem_alloc(&sh.tmem_base, kCols);
@@ -157,15 +162,12 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    pdl_launch_dependents();   // the next kernel may start its own weight loads now
-    cluster_arrive_release();  // phase 1: "my receive barrier is initialised"
+    pdl_launch_dependents();
+    cluster_arrive_relaxed();  // phase 1: "my receive barrier is initialised" (init fence above)
     const uint32_t tmem = sh.tmem_base;
 
     if (warp == 0) {
-        if (lane == 0) {  // ---- TMA producer ----
-            pdl_wait();   // x may be written by the previous kernel
-            for (int i = 0; i < first; ++i)
-                tma_load_2d(ring + i * stage_bytes, &tm_x, &sh.full[i], (c_begin + i) * kChunkK, 0);
+        if (lane == 0) {  // ---- TMA producer: ring refills beyond the first `stages` chunks ----
             int i = first;
             for (; i < nchunks; ++i) {
                 const int s = i % stages;
@@ -210,11 +212,12 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     }
 
     // ---- epilogue: accumulator -> local staging [M][BN] -> one bulk copy per owner ----
+    cluster_wait_acquire();  // phase 1 done (long since): every CTA's receive barrier exists
     const bool ok = mbar_wait(&sh.accum, 0, status, kSiteAccum);
     tc_fence_after();
     const bool have = ok && !*((volatile int32_t *)&sh.aborted);
-    if (warp * 32 < M) {  // warps whose TMEM lanes hold real tokens
-        const int t = warp * 32 + lane;  // token == TMEM lane
+    if (warp * 16 < M) {  // warp w holds tokens 16w..16w+15 in its lanes 0..15
+        const int t = warp * 16 + lane;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 16) {
             uint32_t r[16];
@@ -225,7 +228,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 16; ++j) r[j] = 0u;
             }
-            if (t < M) {
+            if (lane < 16 && t < M) {
                 float4 *dst = stage_out + (t * BN + c) / 4;
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4)
@@ -237,7 +240,6 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    cluster_wait_acquire();  // phase 1 done: every CTA's receive barrier exists
     if (tid < S) {  // thread d sends owner d its slice [it0(d), it1(d)) of the items
         const int d = tid;
         const int d0 = part_begin(d, T, S);
@@ -254,7 +256,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     const bool got = mbar_wait_cluster(&sh.recv, 0, status, kSiteRecv);
     // Every copy into this CTA has landed, so every peer's copy out of its own
     // staging has been read: phase 2 lets all of them exit.
-    cluster_arrive_release();
+    cluster_arrive_relaxed();
     pdl_wait();  // the previous kernel may still read `out`
     if (got && !*((volatile int32_t *)&sh.aborted)) {
         for (int j = tid; j < mine; j += kSplitThreads) {

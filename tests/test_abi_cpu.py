@@ -139,3 +139,17 @@ def test_forced_plan_rules_without_gpu(lib):
     p = lib.make_plan(kernel=7)
     assert L.bf16_linear_with_plan(A, B, None, O, 8, 256, 2048, ctypes.byref(p), None) == -1
     assert L.bf16_linear_with_plan(A, B, None, O, 8, 256, 2048, None, None) == -1
+
+
+def test_plan_check_accepts_and_rejects(lib):
+    p = lib.make_plan("splitk", threads=128, rows_per_cta=64, tokens_per_cta=16, split_k=16, stages=7)
+    assert lib.plan_check(16, 256, 7168, p).grid == 64
+    with pytest.raises(lib.BF16LinearError):
+        lib.plan_check(16, 256, 7168, lib.make_plan("splitk", threads=128, rows_per_cta=64, tokens_per_cta=16,
+                                                    split_k=16, stages=40))
+    with pytest.raises(lib.BF16LinearError):
+        lib.plan_check(16, 256, 7168, p, device=(9, 0, 132))
+    # every plan the dispatcher makes passes its own check
+    for (M, N, K) in [(1, 256, 2048), (16, 384, 7168), (64, 2112, 7168), (300, 1000, 520), (5, 7, 9)]:
+        q = lib.plan(M, N, K)
+        assert lib.plan_check(M, N, K, q).grid == q.grid
