@@ -59,6 +59,19 @@ def algo_flops(M, N, K, bias):
     return 2 * M * N * K + (M * N if bias else 0)
 
 
+def max_over_ranks(value: float, device="cpu") -> float:
+    """The slowest rank's time (every rank gets it).  Works on any torch.distributed backend."""
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_value(per_rank_us_per_call: float, world: int) -> float:
+    """Whole-job us per call when `world` replicas each ran the same calls in the same
+    (max-over-ranks) time: the job completed world times as many calls."""
+    return per_rank_us_per_call / world
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -94,20 +107,28 @@ def kernel_source_hash(kernel_name):
     return h.hexdigest()[:12]
 
 
-def ncu_traffic(kernel_name, M, N, K):
-    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel source."""
+def ncu_traffic(kernel_name, shapes):
+    """Mean DRAM bytes per launch over `shapes` (M, N, K) from the committed ncu summary
+    (profiles/dram_traffic.txt), or None if a shape is missing or the kernel source
+    changed since the counters were taken."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(p):
         return None
     want = kernel_source_hash(kernel_name)
+    table = {}
     for line in open(p):
         if line.startswith("#") or not line.strip():
             continue
         f = line.split()
         # kernel M N K dram_bytes_per_launch source_hash
-        if len(f) >= 6 and f[0] == kernel_name and (int(f[1]), int(f[2]), int(f[3])) == (M, N, K):
-            return int(float(f[4])) if f[5] == want else None
-    return None
+        if len(f) >= 6 and f[0] == kernel_name:
+            table[(int(f[1]), int(f[2]), int(f[3]))] = (float(f[4]), f[5])
+    vals = []
+    for shp in shapes:
+        if shp not in table or table[shp][1] != want:
+            return None
+        vals.append(table[shp][0])
+    return int(sum(vals) / len(vals)) if vals else None
 
 
 class ClockSampler:
@@ -592,9 +613,7 @@ def main():
     shapes, per_us = r["shapes"], r["per_shape_us"]
     total_ms = r["total_ms"]
     if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, device="cuda")
 
     # dominant kernel: the largest share of measured time
     share = {}
@@ -614,16 +633,16 @@ def main():
         achieved = dom_work / (dom_us * 1e-6) / 1e9
         peak = peaks["hbm_gbs"]
         bound, runit = "hbm", "GB/s"
-    # traffic: ncu DRAM bytes per launch for one representative shape of the dominant kernel
-    rep = max(dom_shapes, key=lambda s: s.M * s.N * s.K)
-    traffic = ncu_traffic(dom, rep.M, rep.N, rep.K)
+    # traffic: ncu DRAM bytes per launch, averaged over the dominant kernel's shapes (as `achieved` is)
+    traffic = ncu_traffic(dom, [(s.M, s.N, s.K) for s in dom_shapes])
+    algo_per_launch = dom_work / dom_n
 
     calls_per_step = sum(s.R for s in shapes)
     if large:
         flops_step = sum(algo_flops(s.M, s.N, s.K, s.bias) * s.R for s in shapes)
         value = flops_step * args.steps * world / (total_ms * 1e-3) / 1e12
     else:
-        value = statistics.mean(per_us) / world if world > 1 else statistics.mean(per_us)
+        value = replica_value(statistics.mean(per_us), world)
     ms_per_step = total_ms / args.steps
 
     cpu = None
@@ -650,7 +669,8 @@ def main():
         "config": config,
         "roofline": {"bound": bound, "kernel": dom, "achieved": round(achieved, 2), "peak": peak, "unit": runit,
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "traffic_shape": f"M={rep.M} N={rep.N} K={rep.K}",
+                     "algorithmic_per_launch": round(algo_per_launch) if not large else None,
+                     "averaged_over": f"{dom_n} shapes run by the {dom} kernel",
                      "peak_source": peaks["source"]},
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 4), "unit": unit, "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
