@@ -17,7 +17,7 @@
  *    stream reaches it).
  *  - Layouts are dense row-major with no padding: x[M][K], W[N][K] (the
  *    nn.Linear weight layout), out[M][N], bias[N].  Elements are IEEE bfloat16
- *    (the upper 16 bits of a binary32), except out of bf16_linear_f32out.
+ *    (the upper 16 bits of a binary32), except out of bf16_linear_f32out (fp32).
  *  - Pointers must be 16-byte aligned (the vLLM PR #42562 review lowered the
  *    assumed alignment of these kernels to 16 bytes).  out must not overlap
  *    x, W or bias.
@@ -145,6 +145,22 @@ int bf16_linear(const void *x, const void *W, const void *bias, void *out,
  */
 int bf16_linear_ex(const void *x, const void *W, const void *bias, void *out,
                    int M, int N, int K, uint32_t flags, bf16l_stream_t stream);
+
+/*
+ * bf16_linear_f32out — the router-logits variant: the same product and bias,
+ * but out is fp32 [M][N] (each output is the fp32 accumulation plus the bias,
+ * not rounded to bf16).  The vLLM PR #42562 page's split-K router kernel
+ * writes fp32 (LLBf16SplitK, out_dtype=cutlass.Float32) so that top-k expert
+ * selection sees unrounded logits.  Same plans, kernels, arguments, flags and
+ * errors as bf16_linear_ex; out must be 16-byte aligned and not overlap the
+ * inputs.
+ */
+int bf16_linear_f32out(const void *x, const void *W, const void *bias, float *out,
+                       int M, int N, int K, uint32_t flags, bf16l_stream_t stream);
+
+/* bf16_linear_f32out with an explicit plan (no fallback, as bf16_linear_with_plan). */
+int bf16_linear_f32out_with_plan(const void *x, const void *W, const void *bias, float *out,
+                                 int M, int N, int K, const bf16l_plan *plan, bf16l_stream_t stream);
 
 /*
  * bf16_linear_with_plan — as bf16_linear, but run exactly `plan` (for tests,

@@ -17,6 +17,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libbf16_linear.so")
 
 OK, EINVAL, EALIGN, EARCH, ELAUNCH, ETIMEOUT, EUNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
+FLAG_PDL = 1
 KERNEL_DOTPROD, KERNEL_SPLITK, KERNEL_TILE = 0, 1, 2
 KERNEL_NAMES = {KERNEL_DOTPROD: "dotprod", KERNEL_SPLITK: "splitk", KERNEL_TILE: "tile"}
 
@@ -68,6 +69,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.bf16_linear.restype = i32
         lib.bf16_linear_ex.argtypes = [vp, vp, vp, vp, i32, i32, i32, ctypes.c_uint32, vp]
         lib.bf16_linear_ex.restype = i32
+        lib.bf16_linear_f32out.argtypes = [vp, vp, vp, vp, i32, i32, i32, ctypes.c_uint32, vp]
+        lib.bf16_linear_f32out.restype = i32
+        lib.bf16_linear_f32out_with_plan.argtypes = [vp, vp, vp, vp, i32, i32, i32, ctypes.POINTER(Plan), vp]
+        lib.bf16_linear_f32out_with_plan.restype = i32
         lib.bf16_linear_with_plan.argtypes = [vp, vp, vp, vp, i32, i32, i32, ctypes.POINTER(Plan), vp]
         lib.bf16_linear_with_plan.restype = i32
         lib.bf16_linear_plan.argtypes = [i32, i32, i32, ctypes.POINTER(Device), ctypes.POINTER(Plan)]
@@ -136,7 +141,7 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
 
-def _check(x, W, bias, out):
+def _check(x, W, bias, out, out_dtype=None):
     import torch
     if x.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
         raise TypeError(f"x and W must be torch.bfloat16 (got {x.dtype}, {W.dtype})")
@@ -151,10 +156,11 @@ def _check(x, W, bias, out):
     for name, t in (("x", x), ("W", W), ("bias", bias)):
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    odt = out_dtype or torch.bfloat16
     if out is None:
-        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
-    elif out.dtype != torch.bfloat16 or tuple(out.shape) != (M, N) or not out.is_contiguous() or not out.is_cuda:
-        raise ValueError("out must be a contiguous CUDA bf16 tensor of shape [M, N]")
+        out = torch.empty((M, N), dtype=odt, device=x.device)
+    elif out.dtype != odt or tuple(out.shape) != (M, N) or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError(f"out must be a contiguous CUDA {odt} tensor of shape [M, N]")
     devs = {t.device for t in (x, W, bias, out) if t is not None}
     if len(devs) != 1:
         raise ValueError(f"all tensors must be on one device, got {devs}")
@@ -191,6 +197,34 @@ def bf16_linear_with_plan(x, W, bias=None, out=None, plan_: Plan | None = None, 
                                           ctypes.byref(plan_), _stream_handle(stream, x.device))
     if st != OK:
         _raise(st, f"bf16_linear_with_plan(M={M}, N={N}, K={K}, {plan_})")
+    return out
+
+
+def bf16_linear_f32out(x, W, bias=None, out=None, stream=None, flags: int = 0, plan_: Plan | None = None):
+    """fp32 out[M,N] = x @ W^T (+ bias): the router-logits variant (no rounding to bf16)."""
+    import torch
+    M, N, K, out = _check(x, W, bias, out, out_dtype=torch.float32)
+    with torch.cuda.device(x.device):
+        if plan_ is None:
+            st = load().bf16_linear_f32out(_ptr(x), _ptr(W), _ptr(bias), _ptr(out), M, N, K, int(flags),
+                                           _stream_handle(stream, x.device))
+        else:
+            st = load().bf16_linear_f32out_with_plan(_ptr(x), _ptr(W), _ptr(bias), _ptr(out), M, N, K,
+                                                     ctypes.byref(plan_), _stream_handle(stream, x.device))
+    if st != OK:
+        _raise(st, f"bf16_linear_f32out(M={M}, N={N}, K={K})")
+    return out
+
+
+def bf16_linear_ex(x, W, bias=None, out=None, flags: int = 0, stream=None):
+    """bf16_linear with BF16L_FLAG_* launch flags (1 = programmatic dependent launch)."""
+    import torch
+    M, N, K, out = _check(x, W, bias, out)
+    with torch.cuda.device(x.device):
+        st = load().bf16_linear_ex(_ptr(x), _ptr(W), _ptr(bias), _ptr(out), M, N, K, int(flags),
+                                   _stream_handle(stream, x.device))
+    if st != OK:
+        _raise(st, f"bf16_linear_ex(M={M}, N={N}, K={K})")
     return out
 
 

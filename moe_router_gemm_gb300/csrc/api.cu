@@ -55,6 +55,7 @@ void init_device(DeviceState &s) {
         e = (int)cudaGetSymbolAddress(&p, g_status);
         s.status = static_cast<int32_t *>(p);
         if (!e) e = init_dotprod();
+        if (!e) e = init_dotprod_f32();
         if (!e) e = init_splitk();
         if (!e) e = init_tile();
     }
@@ -90,20 +91,20 @@ bool overlaps(const void *a, uint64_t abytes, const void *b, uint64_t bbytes) {
 }
 
 // Size and pointer checks that need no GPU.  BF16L_OK means "go on".
-int check_args(const void *x, const void *W, const void *bias, void *out, int M, int N, int K) {
+int check_args(const void *x, const void *W, const void *bias, void *out, int M, int N, int K, int out_elem) {
     if (M < 0 || N <= 0 || K <= 0) return BF16L_EINVAL;
     if (M == 0) return BF16L_OK;
     if (!x || !W || !out) return BF16L_EINVAL;
     if (misaligned(x) || misaligned(W) || misaligned(out) || (bias && misaligned(bias))) return BF16L_EALIGN;
     const uint64_t xb = 2ull * (uint64_t)M * (uint64_t)K, wb = 2ull * (uint64_t)N * (uint64_t)K;
-    const uint64_t ob = 2ull * (uint64_t)M * (uint64_t)N, bb = bias ? 2ull * (uint64_t)N : 0;
+    const uint64_t ob = (uint64_t)out_elem * (uint64_t)M * (uint64_t)N, bb = bias ? 2ull * (uint64_t)N : 0;
     if (overlaps(out, ob, x, xb) || overlaps(out, ob, W, wb) || overlaps(out, ob, bias, bb)) return BF16L_EINVAL;
     return BF16L_OK;
 }
 
 int run(const void *x, const void *W, const void *bias, void *out, int M, int N, int K, const bf16l_plan *forced,
-        uint32_t flags, bf16l_stream_t stream) {
-    int st = check_args(x, W, bias, out, M, N, K);
+        uint32_t flags, bf16l_stream_t stream, int out_f32 = 0) {
+    int st = check_args(x, W, bias, out, M, N, K, out_f32 ? 4 : 2);
     if (st != BF16L_OK) return st;
     if (flags & ~BF16L_FLAG_PDL) return BF16L_EINVAL;
     if (M == 0) return BF16L_OK;
@@ -128,7 +129,7 @@ int run(const void *x, const void *W, const void *bias, void *out, int M, int N,
     }
     if (st != BF16L_OK) return st;
 
-    LaunchArgs a = {x, W, bias, out, M, N, K, stream, ds->dev.num_sms, ds->status};
+    LaunchArgs a = {x, W, bias, out, M, N, K, stream, ds->dev.num_sms, ds->status, out_f32};
     int e = 0;
     switch (p.kernel) {
         case BF16L_KERNEL_DOTPROD: e = launch_dotprod(a, p); break;
@@ -187,6 +188,17 @@ extern "C" int bf16_linear(const void *x, const void *W, const void *bias, void 
 extern "C" int bf16_linear_ex(const void *x, const void *W, const void *bias, void *out, int M, int N, int K,
                               uint32_t flags, bf16l_stream_t stream) {
     return bf16l::run(x, W, bias, out, M, N, K, nullptr, flags, stream);
+}
+
+extern "C" int bf16_linear_f32out(const void *x, const void *W, const void *bias, float *out, int M, int N, int K,
+                                  uint32_t flags, bf16l_stream_t stream) {
+    return bf16l::run(x, W, bias, out, M, N, K, nullptr, flags, stream, 1);
+}
+
+extern "C" int bf16_linear_f32out_with_plan(const void *x, const void *W, const void *bias, float *out, int M, int N,
+                                            int K, const bf16l_plan *plan, bf16l_stream_t stream) {
+    if (!plan) return BF16L_EINVAL;
+    return bf16l::run(x, W, bias, out, M, N, K, plan, (uint32_t)plan->flags, stream, 1);
 }
 
 extern "C" int bf16_linear_with_plan(const void *x, const void *W, const void *bias, void *out, int M, int N,

@@ -67,6 +67,43 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
     return *reinterpret_cast<uint16_t *>(&b);
 }
 
+// Output element stores for the two output types: bf16 (RNE) and fp32 (the
+// router-logits variant).  `four` needs 4-element alignment of the index;
+// `eight` needs 8-element alignment.
+template <typename OutT>
+struct OutStore;
+
+template <>
+struct OutStore<uint16_t> {
+    static __device__ __forceinline__ void one(uint16_t *p, float v) { *p = f32_to_bf16(v); }
+    static __device__ __forceinline__ void four(uint16_t *p, float a, float b, float c, float d) {
+        uint2 pk;
+        pk.x = pack_bf16x2(a, b);
+        pk.y = pack_bf16x2(c, d);
+        *reinterpret_cast<uint2 *>(p) = pk;
+    }
+    static __device__ __forceinline__ void eight(uint16_t *p, const float *v) {
+        uint4 pk;
+        pk.x = pack_bf16x2(v[0], v[1]);
+        pk.y = pack_bf16x2(v[2], v[3]);
+        pk.z = pack_bf16x2(v[4], v[5]);
+        pk.w = pack_bf16x2(v[6], v[7]);
+        *reinterpret_cast<uint4 *>(p) = pk;
+    }
+};
+
+template <>
+struct OutStore<float> {
+    static __device__ __forceinline__ void one(float *p, float v) { *p = v; }
+    static __device__ __forceinline__ void four(float *p, float a, float b, float c, float d) {
+        *reinterpret_cast<float4 *>(p) = make_float4(a, b, c, d);
+    }
+    static __device__ __forceinline__ void eight(float *p, const float *v) {
+        reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+        reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+};
+
 // ---------------------------------------------------------------------------
 // Shared-memory addresses and mbarriers.
 // ---------------------------------------------------------------------------

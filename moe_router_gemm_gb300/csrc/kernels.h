@@ -58,6 +58,7 @@ struct LaunchArgs {
     void *stream;     // cudaStream_t
     int num_sms;
     int32_t *status;  // device address of the kernel status word
+    int out_f32;      // 1: out is fp32 [M][N] (router logits); 0: bf16
 };
 
 // Each returns a cudaError_t value (0 on success).
@@ -68,6 +69,8 @@ int launch_tile(const LaunchArgs &a, const bf16l_plan &p);
 // One-time per-device kernel attribute setup (dynamic shared memory limits,
 // non-portable cluster sizes).  Returns a cudaError_t value.
 int init_dotprod();
+int init_dotprod_f32();
+int launch_dotprod_f32(const LaunchArgs &a, const bf16l_plan &p);
 int init_splitk();
 int init_tile();
 

@@ -73,7 +73,15 @@ int split_recv_bytes(int tokens, int rows) {
     return (tokens * rows / 4 + kSplitMaxCluster) * 16;
 }
 
-int split_tmem_cols(int rows) { return rows <= 32 ? 32 : rows <= 64 ? 64 : rows <= 128 ? 128 : 256; }
+// Independent accumulators per CTA: consecutive MMAs of a chunk rotate over
+// them, so a short MMA does not wait for the previous one to finish adding
+// into the same TMEM tile.  Summed in fixed order in the epilogue.
+__host__ __device__ constexpr int split_acc_count(int rows) { return rows <= 64 ? 4 : rows <= 128 ? 2 : 1; }
+
+int split_tmem_cols(int rows) {
+    const int need = split_acc_count(rows) * rows;
+    return need <= 32 ? 32 : need <= 64 ? 64 : need <= 128 ? 128 : 256;
+}
 
 int split_ring_bytes(int tokens, int rows, int stages) {
     // The ring, which the accumulator staging (tokens x rows fp32) reuses once the MMAs are done.
@@ -101,13 +109,14 @@ int split_max_stages(int tokens, int rows) {
     return split_smem_bytes(tokens, rows, s) <= kSmemPerCta ? s : 0;
 }
 
-template <int BN>
+template <int BN, typename OutT>
 __global__ void __launch_bounds__(kSplitThreads, 1)
     splitk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
-                  const uint16_t *__restrict__ bias, uint16_t *__restrict__ out, int M, int N, int K, int tokp,
+                  const uint16_t *__restrict__ bias, OutT *__restrict__ out, int M, int N, int K, int tokp,
                   int stages, int32_t *status) {
     constexpr uint32_t kIdesc = idesc_bf16_f32(kMmaM, BN);
-    constexpr int kCols = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+    constexpr int kAcc = split_acc_count(BN);
+    constexpr int kCols = kAcc * BN <= 32 ? 32 : kAcc * BN <= 64 ? 64 : kAcc * BN <= 128 ? 128 : 256;
     constexpr int kWBytes = BN * kChunkK * 2;
 
     extern __shared__ uint8_t smem_raw[];
@@ -199,7 +208,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
                 const uint64_t bdesc = smem_desc_sw128(smem_u32(st + xbytes));
 #pragma unroll
                 for (int kk = 0; kk < kChunkK / 16; ++kk)  // 4 MMAs of K = 16 (32 bytes) each
-                    mma_bf16(tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
+                    mma_bf16(tmem + (uint32_t)((kk % kAcc) * BN), adesc + 2 * kk, bdesc + 2 * kk, kIdesc,
+                             (i > 0 || kk >= kAcc) ? 1u : 0u);
                 mma_commit(&sh.empty[s]);
             }
             sh.consumed = i;
@@ -222,8 +232,17 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         for (int c = 0; c < BN; c += 16) {
             uint32_t r[16];
             if (have) {
-                tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, r);
+                const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c;
+                tmem_ld16(lane_base, r);
                 tmem_ld_wait16(r);
+#pragma unroll
+                for (int a = 1; a < kAcc; ++a) {  // fixed order: accumulator 0, 1, ...
+                    uint32_t r2[16];
+                    tmem_ld16(lane_base + (uint32_t)(a * BN), r2);
+                    tmem_ld_wait16(r2);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
+                }
             } else {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) r[j] = 0u;
@@ -279,14 +298,11 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
             }
             const size_t o = (size_t)m * N + n;
             if (n + 3 < N && (o & 3) == 0) {
-                uint2 pk;
-                pk.x = pack_bf16x2(r4[0], r4[1]);
-                pk.y = pack_bf16x2(r4[2], r4[3]);
-                *reinterpret_cast<uint2 *>(out + o) = pk;
+                OutStore<OutT>::four(out + o, r4[0], r4[1], r4[2], r4[3]);
             } else {
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    if (n + e < N) out[o + e] = f32_to_bf16(r4[e]);
+                    if (n + e < N) OutStore<OutT>::one(out + o + e, r4[e]);
             }
         }
     }
@@ -305,37 +321,37 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 
 namespace {
 
-typedef void (*SplitFn)(CUtensorMap, CUtensorMap, const uint16_t *, uint16_t *, int, int, int, int, int, int32_t *);
+template <typename OutT>
+using SplitFn = void (*)(CUtensorMap, CUtensorMap, const uint16_t *, OutT *, int, int, int, int, int, int32_t *);
 
-SplitFn pick(int BN) {
+template <typename OutT>
+SplitFn<OutT> pick(int BN) {
     switch (BN) {
-        case 16: return splitk_kernel<16>;
-        case 32: return splitk_kernel<32>;
-        case 48: return splitk_kernel<48>;
-        case 64: return splitk_kernel<64>;
-        case 96: return splitk_kernel<96>;
-        case 128: return splitk_kernel<128>;
-        case 192: return splitk_kernel<192>;
-        case 256: return splitk_kernel<256>;
+        case 16: return splitk_kernel<16, OutT>;
+        case 32: return splitk_kernel<32, OutT>;
+        case 48: return splitk_kernel<48, OutT>;
+        case 64: return splitk_kernel<64, OutT>;
+        case 96: return splitk_kernel<96, OutT>;
+        case 128: return splitk_kernel<128, OutT>;
+        case 192: return splitk_kernel<192, OutT>;
+        case 256: return splitk_kernel<256, OutT>;
         default: return nullptr;
     }
 }
 
-}  // namespace
-
-bool split_rows_supported(int rows) { return pick(rows) != nullptr; }
-
-int init_splitk() {
+template <typename OutT>
+int set_split_attrs() {
     for (int BN : {16, 32, 48, 64, 96, 128, 192, 256}) {
-        int e = (int)cudaFuncSetAttribute(pick(BN), cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPerCta);
-        if (!e) e = (int)cudaFuncSetAttribute(pick(BN), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        int e = (int)cudaFuncSetAttribute(pick<OutT>(BN), cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPerCta);
+        if (!e) e = (int)cudaFuncSetAttribute(pick<OutT>(BN), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e) return e;
     }
     return 0;
 }
 
-int launch_splitk(const LaunchArgs &a, const bf16l_plan &p) {
-    SplitFn fn = pick(p.rows_per_cta);
+template <typename OutT>
+int launch_split_t(const LaunchArgs &a, const bf16l_plan &p) {
+    SplitFn<OutT> fn = pick<OutT>(p.rows_per_cta);
     if (!fn) return (int)cudaErrorInvalidValue;
     CUtensorMap tw, tx;
     int r = make_tmap_bf16_2d(&tw, a.W, (uint64_t)a.N, (uint64_t)a.K, (uint32_t)p.rows_per_cta, kChunkK,
@@ -360,8 +376,22 @@ int launch_splitk(const LaunchArgs &a, const bf16l_plan &p) {
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     return (int)cudaLaunchKernelEx(&cfg, fn, tw, tx, static_cast<const uint16_t *>(a.bias),
-                                   static_cast<uint16_t *>(a.out), a.M, a.N, a.K, p.tokens_per_cta, p.stages,
+                                   static_cast<OutT *>(a.out), a.M, a.N, a.K, p.tokens_per_cta, p.stages,
                                    a.status);
+}
+
+}  // namespace
+
+bool split_rows_supported(int rows) { return pick<uint16_t>(rows) != nullptr; }
+
+int init_splitk() {
+    int e = set_split_attrs<uint16_t>();
+    if (!e) e = set_split_attrs<float>();
+    return e;
+}
+
+int launch_splitk(const LaunchArgs &a, const bf16l_plan &p) {
+    return a.out_f32 ? launch_split_t<float>(a, p) : launch_split_t<uint16_t>(a, p);
 }
 
 }  // namespace bf16l

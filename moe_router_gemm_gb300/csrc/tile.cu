@@ -63,9 +63,10 @@ __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int
 
 }  // namespace
 
+template <typename OutT>
 __global__ void __launch_bounds__(kTileThreads, 1)
     tile_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                const uint16_t *__restrict__ bias, uint16_t *__restrict__ out, int M, int N, int K, int stages,
+                const uint16_t *__restrict__ bias, OutT *__restrict__ out, int M, int N, int K, int stages,
                 int32_t *status) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -205,21 +206,14 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                             for (int j = 0; j < 32; ++j)
                                 if (n + j < N) v[j] += bf16_to_f32(bias[n + j]);
                         }
-                        uint16_t *o = out + (size_t)m * N + n;
+                        OutT *o = out + (size_t)m * N + n;
                         if (vec_ok && n + 32 <= N) {
 #pragma unroll
-                            for (int j = 0; j < 32; j += 8) {
-                                uint4 pk;
-                                pk.x = pack_bf16x2(v[j], v[j + 1]);
-                                pk.y = pack_bf16x2(v[j + 2], v[j + 3]);
-                                pk.z = pack_bf16x2(v[j + 4], v[j + 5]);
-                                pk.w = pack_bf16x2(v[j + 6], v[j + 7]);
-                                *reinterpret_cast<uint4 *>(o + j) = pk;
-                            }
+                            for (int j = 0; j < 32; j += 8) OutStore<OutT>::eight(o + j, v + j);
                         } else {
 #pragma unroll
                             for (int j = 0; j < 32; ++j)
-                                if (n + j < N) o[j] = f32_to_bf16(v[j]);
+                                if (n + j < N) OutStore<OutT>::one(o + j, v[j]);
                         }
                     }
                 }
@@ -247,11 +241,16 @@ __global__ void __launch_bounds__(kTileThreads, 1)
 int tile_smem_bytes(int stages) { return 1024 + stages * kStageBytes + 256; }
 
 int init_tile() {
-    return (int)cudaFuncSetAttribute(tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     tile_smem_bytes(kTileMaxStages));
+    int e = (int)cudaFuncSetAttribute(tile_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      tile_smem_bytes(kTileMaxStages));
+    if (!e)
+        e = (int)cudaFuncSetAttribute(tile_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      tile_smem_bytes(kTileMaxStages));
+    return e;
 }
 
-int launch_tile(const LaunchArgs &a, const bf16l_plan &p) {
+template <typename OutT>
+static int launch_tile_t(const LaunchArgs &a, const bf16l_plan &p) {
     CUtensorMap tx, tw;
     int r = make_tmap_bf16_2d(&tx, a.x, (uint64_t)a.M, (uint64_t)a.K, kBM, kChunkK, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
@@ -269,8 +268,12 @@ int launch_tile(const LaunchArgs &a, const bf16l_plan &p) {
     attr[0].val.programmaticStreamSerializationAllowed = (p.flags & BF16L_FLAG_PDL) ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return (int)cudaLaunchKernelEx(&cfg, tile_kernel, tx, tw, static_cast<const uint16_t *>(a.bias),
-                                   static_cast<uint16_t *>(a.out), a.M, a.N, a.K, p.stages, a.status);
+    return (int)cudaLaunchKernelEx(&cfg, tile_kernel<OutT>, tx, tw, static_cast<const uint16_t *>(a.bias),
+                                   static_cast<OutT *>(a.out), a.M, a.N, a.K, p.stages, a.status);
+}
+
+int launch_tile(const LaunchArgs &a, const bf16l_plan &p) {
+    return a.out_f32 ? launch_tile_t<float>(a, p) : launch_tile_t<uint16_t>(a, p);
 }
 
 }  // namespace bf16l
