@@ -26,7 +26,9 @@
  *    summation order depends on the kernel the plan picks; for a fixed plan the
  *    result is bitwise deterministic from run to run.
  *  - Nothing allocates device memory, nothing synchronises the stream, and the
- *    calls are safe to make from several host threads at once.  A call may be
+ *    calls are safe to make from several host threads at once.  (Plans that
+ *    need scratch memory run only when the caller passes a workspace to
+ *    bf16_linear_run.)  A call may be
  *    captured in a CUDA graph once the device has been initialised by one
  *    earlier non-captured call on it (initialisation sets kernel attributes).
  *  - Device: compute capability 10.3 (GB300) only; any other device returns
@@ -37,6 +39,7 @@
 #ifndef BF16_LINEAR_H
 #define BF16_LINEAR_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -61,7 +64,9 @@ typedef enum {
     BF16L_KERNEL_DOTPROD = 0, /* CUDA-core dot product, 128-bit weight loads, one CTA per slice of W rows */
     BF16L_KERNEL_SPLITK = 1,  /* TMA -> tcgen05 (weights on the MMA M side), K split over a thread-block
                                  cluster, fp32 partials reduced through distributed shared memory */
-    BF16L_KERNEL_TILE = 2     /* persistent warp-specialised TMA -> tcgen05 -> TMEM tile GEMM */
+    BF16L_KERNEL_TILE = 2,    /* persistent warp-specialised TMA -> tcgen05 -> TMEM tile GEMM */
+    BF16L_KERNEL_SPLITK_WS = 3 /* the split-K kernel without a cluster: K split over up to 64 CTAs, fp32
+                                  partials reduced through a caller-provided workspace (see bf16_linear_run) */
 } bf16l_kernel;
 
 /*
@@ -75,7 +80,7 @@ typedef struct {
     int32_t threads;       /* threads per CTA */
     int32_t rows_per_cta;  /* W rows per CTA (DOTPROD 1/2/4; SPLITK 16..256, the MMA N); TILE: W rows per tile */
     int32_t tokens_per_cta;/* SPLITK: x rows loaded per chunk (M rounded up to 8, <= 64);  TILE: x rows per tile */
-    int32_t split_k;       /* SPLITK: CTAs per cluster along K (1..16) */
+    int32_t split_k;       /* SPLITK: CTAs per cluster along K (1..16); SPLITK_WS: CTAs along K (1..64) */
     int32_t stages;        /* SPLITK / TILE: shared-memory ring depth (64-wide K chunks) */
     int32_t grid;          /* CTAs launched (informational; computed by the plan) */
     int32_t flags;         /* BF16L_FLAG_* bits the launch uses */
@@ -190,6 +195,51 @@ int bf16_linear_device_status(int32_t *status, int clear);
  * BF16L_ELAUNCH.
  */
 int bf16_linear_selftest_wait(uint32_t limit_us, bf16l_stream_t stream);
+
+/*
+ * The general entry point.  Every other launch entry point is a special case
+ * of this one.
+ *
+ * workspace: device scratch for plans that need it (kernel
+ * BF16L_KERNEL_SPLITK_WS), or NULL.  It must be 256-byte aligned, zero-filled
+ * before its first use (one cudaMemset), and not shared by calls that can run
+ * at the same time on different streams.  Consecutive calls on one stream may
+ * share one, with or without BF16L_FLAG_PDL (a kernel touches the workspace
+ * only after its grid-dependency wait).  Every completed call leaves the
+ * workspace's counters zero again, so no clearing is needed between calls.  With plan == NULL the dispatcher may pick
+ * a workspace plan only when workspace_bytes is large enough for it
+ * (bf16_linear_workspace_size); otherwise it picks the best plan that needs
+ * none.  With an explicit workspace plan and too small a workspace the call
+ * returns BF16L_EINVAL.
+ */
+typedef struct {
+    const void *x;            /* bf16 [M][K] */
+    const void *W;            /* bf16 [N][K] */
+    const void *bias;         /* bf16 [N] or NULL */
+    void *out;                /* bf16 [M][N], or fp32 [M][N] when out_f32 */
+    int32_t M, N, K;
+    int32_t out_f32;          /* 0: bf16 out; 1: fp32 out (router logits) */
+    uint32_t flags;           /* BF16L_FLAG_* (ignored when plan != NULL: plan->flags is used) */
+    const bf16l_plan *plan;   /* NULL: the dispatcher chooses */
+    void *workspace;          /* see above; may be NULL */
+    size_t workspace_bytes;
+    bf16l_stream_t stream;
+} bf16l_call;
+
+int bf16_linear_run(const bf16l_call *call);
+
+/*
+ * Bytes of workspace a call needs: for `plan` when given, else for the plan
+ * the dispatcher picks for (M, N, K) on a GB300 when any workspace is
+ * allowed.  0 when the plan needs none.  Pure host code.
+ */
+size_t bf16_linear_workspace_size(int M, int N, int K, const bf16l_plan *plan);
+
+/*
+ * The dispatcher's choice when `workspace_bytes` of workspace are available
+ * (bf16_linear_plan is this with workspace_bytes == 0).  Pure host code.
+ */
+int bf16_linear_plan_ws(int M, int N, int K, const bf16l_device *dev, size_t workspace_bytes, bf16l_plan *plan);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *bf16_linear_strerror(int status);

@@ -18,8 +18,9 @@ LIB_PATH = os.path.join(PKG, "libbf16_linear.so")
 
 OK, EINVAL, EALIGN, EARCH, ELAUNCH, ETIMEOUT, EUNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
 FLAG_PDL = 1
-KERNEL_DOTPROD, KERNEL_SPLITK, KERNEL_TILE = 0, 1, 2
-KERNEL_NAMES = {KERNEL_DOTPROD: "dotprod", KERNEL_SPLITK: "splitk", KERNEL_TILE: "tile"}
+KERNEL_DOTPROD, KERNEL_SPLITK, KERNEL_TILE, KERNEL_SPLITK_WS = 0, 1, 2, 3
+KERNEL_NAMES = {KERNEL_DOTPROD: "dotprod", KERNEL_SPLITK: "splitk", KERNEL_TILE: "tile",
+                KERNEL_SPLITK_WS: "splitk_ws"}
 
 
 class Plan(ctypes.Structure):
@@ -41,6 +42,14 @@ class Plan(ctypes.Structure):
 class Device(ctypes.Structure):
     """Mirror of bf16l_device."""
     _fields_ = [("cc_major", ctypes.c_int32), ("cc_minor", ctypes.c_int32), ("num_sms", ctypes.c_int32)]
+
+
+class Call(ctypes.Structure):
+    """Mirror of bf16l_call (the argument block of bf16_linear_run)."""
+    _fields_ = [("x", ctypes.c_void_p), ("W", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("out", ctypes.c_void_p),
+                ("M", ctypes.c_int32), ("N", ctypes.c_int32), ("K", ctypes.c_int32), ("out_f32", ctypes.c_int32),
+                ("flags", ctypes.c_uint32), ("plan", ctypes.POINTER(Plan)), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t), ("stream", ctypes.c_void_p)]
 
 
 class BF16LinearError(RuntimeError):
@@ -79,6 +88,13 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.bf16_linear_plan.restype = i32
         lib.bf16_linear_plan_check.argtypes = [i32, i32, i32, ctypes.POINTER(Device), ctypes.POINTER(Plan)]
         lib.bf16_linear_plan_check.restype = i32
+        lib.bf16_linear_run.argtypes = [ctypes.POINTER(Call)]
+        lib.bf16_linear_run.restype = i32
+        lib.bf16_linear_workspace_size.argtypes = [i32, i32, i32, ctypes.POINTER(Plan)]
+        lib.bf16_linear_workspace_size.restype = ctypes.c_size_t
+        lib.bf16_linear_plan_ws.argtypes = [i32, i32, i32, ctypes.POINTER(Device), ctypes.c_size_t,
+                                            ctypes.POINTER(Plan)]
+        lib.bf16_linear_plan_ws.restype = i32
         lib.bf16_linear_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32), i32]
         lib.bf16_linear_device_status.restype = i32
         lib.bf16_linear_selftest_wait.argtypes = [ctypes.c_uint32, vp]
@@ -124,6 +140,22 @@ def plan_check(M: int, N: int, K: int, p: Plan, device: tuple[int, int, int] | N
     if st != OK:
         _raise(st, f"bf16_linear_plan_check({M},{N},{K}, {p})")
     return p
+
+
+def plan_ws(M: int, N: int, K: int, workspace_bytes: int, device: tuple[int, int, int] | None = None) -> Plan:
+    """The dispatcher's choice when `workspace_bytes` of workspace are available."""
+    p = Plan()
+    dev = Device(*device) if device is not None else None
+    st = load().bf16_linear_plan_ws(int(M), int(N), int(K), ctypes.byref(dev) if dev is not None else None,
+                                    int(workspace_bytes), ctypes.byref(p))
+    if st != OK:
+        _raise(st, f"bf16_linear_plan_ws({M},{N},{K})")
+    return p
+
+
+def workspace_size(M: int, N: int, K: int, p: Plan | None = None) -> int:
+    """Workspace bytes a call needs (for plan p, else for the dispatcher's choice with workspace allowed)."""
+    return int(load().bf16_linear_workspace_size(int(M), int(N), int(K), ctypes.byref(p) if p is not None else None))
 
 
 def make_plan(kernel: int | str, **fields) -> Plan:
@@ -186,18 +218,42 @@ def bf16_linear(x, W, bias=None, out=None, stream=None):
     return out
 
 
-def bf16_linear_with_plan(x, W, bias=None, out=None, plan_: Plan | None = None, stream=None):
-    """Run exactly `plan_` (no fallback: an unusable plan raises)."""
+def run(x, W, bias=None, out=None, *, out_f32=False, flags=0, plan_: Plan | None = None, workspace=None,
+        stream=None):
+    """The general entry point (bf16_linear_run): optional explicit plan and workspace tensor."""
     import torch
+    M, N, K, out = _check(x, W, bias, out, out_dtype=torch.float32 if out_f32 else torch.bfloat16)
+    c = Call()
+    c.x, c.W, c.bias, c.out = x.data_ptr(), W.data_ptr(), (bias.data_ptr() if bias is not None else None), \
+        out.data_ptr()
+    c.M, c.N, c.K = M, N, K
+    c.out_f32 = 1 if out_f32 else 0
+    c.flags = int(flags)
+    c.plan = ctypes.pointer(plan_) if plan_ is not None else None
+    if workspace is not None:
+        if not workspace.is_cuda or workspace.device != x.device or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor on the inputs' device")
+        c.workspace = workspace.data_ptr()
+        c.workspace_bytes = workspace.numel() * workspace.element_size()
+    with torch.cuda.device(x.device):
+        c.stream = _stream_handle(stream, x.device).value
+        st = load().bf16_linear_run(ctypes.byref(c))
+    if st != OK:
+        _raise(st, f"bf16_linear_run(M={M}, N={N}, K={K}, plan={plan_})")
+    return out
+
+
+def bf16_linear_with_plan(x, W, bias=None, out=None, plan_: Plan | None = None, stream=None, workspace=None):
+    """Run exactly `plan_` (no fallback: an unusable plan raises)."""
     if plan_ is None:
         raise ValueError("plan_ is required")
-    M, N, K, out = _check(x, W, bias, out)
-    with torch.cuda.device(x.device):
-        st = load().bf16_linear_with_plan(_ptr(x), _ptr(W), _ptr(bias), _ptr(out), M, N, K,
-                                          ctypes.byref(plan_), _stream_handle(stream, x.device))
-    if st != OK:
-        _raise(st, f"bf16_linear_with_plan(M={M}, N={N}, K={K}, {plan_})")
-    return out
+    return run(x, W, bias, out, plan_=plan_, workspace=workspace, stream=stream)
+
+
+def new_workspace(nbytes: int, device=None):
+    """A zero-filled workspace tensor of at least nbytes (256-byte aligned by the caching allocator)."""
+    import torch
+    return torch.zeros(max(256, int(nbytes)), dtype=torch.uint8, device=device or "cuda")
 
 
 def bf16_linear_f32out(x, W, bias=None, out=None, stream=None, flags: int = 0, plan_: Plan | None = None):

@@ -102,18 +102,21 @@ int check_args(const void *x, const void *W, const void *bias, void *out, int M,
     return BF16L_OK;
 }
 
-int run(const void *x, const void *W, const void *bias, void *out, int M, int N, int K, const bf16l_plan *forced,
-        uint32_t flags, bf16l_stream_t stream, int out_f32 = 0) {
-    int st = check_args(x, W, bias, out, M, N, K, out_f32 ? 4 : 2);
+int run(const bf16l_call &c) {
+    const bf16l_plan *forced = c.plan;
+    const uint32_t flags = forced ? (uint32_t)forced->flags : c.flags;
+    int st = check_args(c.x, c.W, c.bias, c.out, c.M, c.N, c.K, c.out_f32 ? 4 : 2);
     if (st != BF16L_OK) return st;
     if (flags & ~BF16L_FLAG_PDL) return BF16L_EINVAL;
-    if (M == 0) return BF16L_OK;
+    if (c.workspace && (reinterpret_cast<uintptr_t>(c.workspace) & 255u)) return BF16L_EALIGN;
+    if (c.M == 0) return BF16L_OK;
     if (forced) {
         // Check the requested plan's shape rules before touching the device.
         bf16l_plan tmp = *forced;
         const bf16l_device any = {10, 3, kGb300Sms};
-        st = check_plan(M, N, K, any, &tmp);
+        st = check_plan(c.M, c.N, c.K, any, &tmp);
         if (st != BF16L_OK) return st;
+        if (split_ws_bytes(c.M, c.N, tmp) > (c.workspace ? c.workspace_bytes : 0)) return BF16L_EINVAL;
     }
     DeviceState *ds = nullptr;
     st = current_device(&ds);
@@ -122,18 +125,20 @@ int run(const void *x, const void *W, const void *bias, void *out, int M, int N,
     bf16l_plan p;
     if (forced) {
         p = *forced;
-        st = check_plan(M, N, K, ds->dev, &p);
+        st = check_plan(c.M, c.N, c.K, ds->dev, &p);
     } else {
-        st = bf16_linear_plan(M, N, K, &ds->dev, &p);
+        st = bf16_linear_plan_ws(c.M, c.N, c.K, &ds->dev, c.workspace ? c.workspace_bytes : 0, &p);
         p.flags = (int32_t)flags;
     }
     if (st != BF16L_OK) return st;
 
-    LaunchArgs a = {x, W, bias, out, M, N, K, stream, ds->dev.num_sms, ds->status, out_f32};
+    LaunchArgs a = {c.x,      c.W,          c.bias, c.out, c.M, c.N, c.K, c.stream, ds->dev.num_sms, ds->status,
+                    c.out_f32, c.workspace, c.workspace ? c.workspace_bytes : 0};
     int e = 0;
     switch (p.kernel) {
         case BF16L_KERNEL_DOTPROD: e = launch_dotprod(a, p); break;
-        case BF16L_KERNEL_SPLITK: e = launch_splitk(a, p); break;
+        case BF16L_KERNEL_SPLITK:
+        case BF16L_KERNEL_SPLITK_WS: e = launch_splitk(a, p); break;
         case BF16L_KERNEL_TILE: e = launch_tile(a, p); break;
         default: return BF16L_EINVAL;
     }
@@ -142,6 +147,23 @@ int run(const void *x, const void *W, const void *bias, void *out, int M, int N,
         return BF16L_ELAUNCH;
     }
     return BF16L_OK;
+}
+
+int run(const void *x, const void *W, const void *bias, void *out, int M, int N, int K, const bf16l_plan *forced,
+        uint32_t flags, bf16l_stream_t stream, int out_f32 = 0) {
+    bf16l_call c = {};
+    c.x = x;
+    c.W = W;
+    c.bias = bias;
+    c.out = out;
+    c.M = M;
+    c.N = N;
+    c.K = K;
+    c.out_f32 = out_f32;
+    c.flags = flags;
+    c.plan = forced;
+    c.stream = stream;
+    return run(c);
 }
 
 // One thread waits on an mbarrier that nothing arrives on, for limit_ns.
@@ -205,6 +227,11 @@ extern "C" int bf16_linear_with_plan(const void *x, const void *W, const void *b
                                      int K, const bf16l_plan *plan, bf16l_stream_t stream) {
     if (!plan) return BF16L_EINVAL;
     return bf16l::run(x, W, bias, out, M, N, K, plan, (uint32_t)plan->flags, stream);
+}
+
+extern "C" int bf16_linear_run(const bf16l_call *call) {
+    if (!call) return BF16L_EINVAL;
+    return bf16l::run(*call);
 }
 
 extern "C" int bf16_linear_device_status(int32_t *status, int clear) {

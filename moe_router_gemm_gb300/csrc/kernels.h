@@ -3,6 +3,7 @@
 // so the planner builds and runs without a GPU.
 #pragma once
 
+#include <stddef.h>
 #include <stdint.h>
 
 #include "bf16_linear.h"
@@ -31,6 +32,11 @@ int split_smem_bytes(int tokens, int rows, int stages);
 int split_max_stages(int tokens, int rows);  // 0 when even one stage does not fit
 int split_tmem_cols(int rows);
 bool split_rows_supported(int rows);         // a kernel instance exists for this many rows
+constexpr int kSplitWsMaxSplit = 64;         // K splits of the cluster-free (workspace) variant
+// Workspace layout of the cluster-free split-K: per-tile arrival counters
+// (rounded up to 256 bytes), then the fp32 partial tiles [tiles][S][M][rows].
+size_t split_ws_counter_bytes(int tiles);
+size_t split_ws_bytes(int M, int N, const bf16l_plan &p);
 
 // Tile kernel: BM x rows, BN W rows per tile, 64-wide K chunks.
 constexpr int kTileBM = 128;
@@ -59,6 +65,8 @@ struct LaunchArgs {
     int num_sms;
     int32_t *status;  // device address of the kernel status word
     int out_f32;      // 1: out is fp32 [M][N] (router logits); 0: bf16
+    void *workspace;  // caller's scratch for workspace plans (zeroed once before first use), or null
+    size_t workspace_bytes;
 };
 
 // Each returns a cudaError_t value (0 on success).

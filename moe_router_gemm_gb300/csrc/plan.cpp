@@ -100,7 +100,9 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
             p->grid = M == 0 ? 0 : ceil_div(N, p->rows_per_cta);
             return BF16L_OK;
         }
-        case BF16L_KERNEL_SPLITK: {
+        case BF16L_KERNEL_SPLITK:
+        case BF16L_KERNEL_SPLITK_WS: {
+            const int max_split = p->kernel == BF16L_KERNEL_SPLITK ? kSplitMaxCluster : kSplitWsMaxSplit;
             if (K % 8 != 0) return BF16L_EUNSUPPORTED;  // TMA needs 16-byte row strides
             if (M > kSplitMaxTokens) return BF16L_EUNSUPPORTED;
             const int chunks = ceil_div(K, kChunkK);
@@ -108,7 +110,7 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
             if (p->tokens_per_cta < 8 || p->tokens_per_cta > kSplitMaxTokens || p->tokens_per_cta % 8 != 0 ||
                 p->tokens_per_cta < M)
                 return BF16L_EINVAL;
-            if (p->split_k < 1 || p->split_k > kSplitMaxCluster || p->split_k > chunks) return BF16L_EINVAL;
+            if (p->split_k < 1 || p->split_k > max_split || p->split_k > chunks) return BF16L_EINVAL;
             if (p->stages < 1 || p->stages > split_max_stages(p->tokens_per_cta, p->rows_per_cta))
                 return BF16L_EINVAL;
             const int64_t grid = (int64_t)ceil_div(N, p->rows_per_cta) * p->split_k;
@@ -133,8 +135,8 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
 
 }  // namespace bf16l
 
-extern "C" int bf16_linear_plan(int M, int N, int K, const bf16l_device *devp, bf16l_plan *plan) {
-    // (flags are chosen by the caller of the launch, not by the plan)
+extern "C" int bf16_linear_plan_ws(int M, int N, int K, const bf16l_device *devp, size_t workspace_bytes,
+                                   bf16l_plan *plan) {
     using namespace bf16l;
     if (!plan || M < 0 || N <= 0 || K <= 0) return BF16L_EINVAL;
     const bf16l_device gb300 = {10, 3, kGb300Sms};
@@ -142,19 +144,20 @@ extern "C" int bf16_linear_plan(int M, int N, int K, const bf16l_device *devp, b
     if (dev.cc_major != 10 || dev.cc_minor != 3) return BF16L_EARCH;
     if (dev.num_sms <= 0) return BF16L_EINVAL;
 
+    // The table lists, per shape, the fastest plan first; when that one needs
+    // a workspace it is followed by the fastest plan that needs none.
     bf16l_plan p = {};
     bool from_table = false;
-    for (const TableEntry *e = kTable; e->K != 0; ++e) {
-        if (e->K == K && e->N == N && e->M == M) {
-            p.kernel = e->kernel;
-            p.threads = e->threads;
-            p.rows_per_cta = e->rows_per_cta;
-            p.tokens_per_cta = e->tokens_per_cta;
-            p.split_k = e->split_k;
-            p.stages = e->stages;
-            from_table = check_plan(M, N, K, dev, &p) == BF16L_OK;
-            break;
-        }
+    for (const TableEntry *e = kTable; e->K != 0 && !from_table; ++e) {
+        if (e->K != K || e->N != N || e->M != M) continue;
+        p = bf16l_plan{};
+        p.kernel = e->kernel;
+        p.threads = e->threads;
+        p.rows_per_cta = e->rows_per_cta;
+        p.tokens_per_cta = e->tokens_per_cta;
+        p.split_k = e->split_k;
+        p.stages = e->stages;
+        from_table = check_plan(M, N, K, dev, &p) == BF16L_OK && split_ws_bytes(M, N, p) <= workspace_bytes;
     }
     if (!from_table) {
         p = bf16l_plan{};
@@ -171,6 +174,19 @@ extern "C" int bf16_linear_plan(int M, int N, int K, const bf16l_device *devp, b
     }
     *plan = p;
     return BF16L_OK;
+}
+
+extern "C" int bf16_linear_plan(int M, int N, int K, const bf16l_device *devp, bf16l_plan *plan) {
+    return bf16_linear_plan_ws(M, N, K, devp, 0, plan);
+}
+
+extern "C" size_t bf16_linear_workspace_size(int M, int N, int K, const bf16l_plan *plan) {
+    using namespace bf16l;
+    if (M < 0 || N <= 0 || K <= 0) return 0;
+    if (plan) return split_ws_bytes(M, N, *plan);
+    bf16l_plan p;
+    if (bf16_linear_plan_ws(M, N, K, nullptr, (size_t)-1, &p) != BF16L_OK) return 0;
+    return split_ws_bytes(M, N, p);
 }
 
 extern "C" int bf16_linear_plan_check(int M, int N, int K, const bf16l_device *devp, bf16l_plan *plan) {

@@ -57,6 +57,7 @@ struct SplitShared {  // bookkeeping placed after the receive buffer (<= 512 byt
     int32_t aborted;   // set when a wait gave up: skip the rest of the math
     int32_t issued;    // TMA chunks issued by the producer
     int32_t consumed;  // chunks whose data the MMA issuer saw arrive
+    int32_t last;      // (workspace mode) this CTA arrived last for its tile
 };
 
 __device__ __forceinline__ int part_begin(int d, int T, int S) { return (int)(((long long)d * T) / S); }
@@ -109,11 +110,15 @@ int split_max_stages(int tokens, int rows) {
     return split_smem_bytes(tokens, rows, s) <= kSmemPerCta ? s : 0;
 }
 
-template <int BN, typename OutT>
+// kClus: the S CTAs that share a tile form a thread-block cluster and reduce
+// through distributed shared memory.  !kClus: no cluster; every CTA writes its
+// fp32 partial tile to the workspace `ws` and bumps the tile's counter; the
+// last CTA to arrive sums the S partials in rank order and resets the counter.
+template <int BN, typename OutT, bool kClus>
 __global__ void __launch_bounds__(kSplitThreads, 1)
     splitk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                   const uint16_t *__restrict__ bias, OutT *__restrict__ out, int M, int N, int K, int tokp,
-                  int stages, int32_t *status) {
+                  int stages, int32_t *status, float *__restrict__ ws, uint32_t *__restrict__ counters) {
     constexpr uint32_t kIdesc = idesc_bf16_f32(kMmaM, BN);
     constexpr int kAcc = split_acc_count(BN);
     constexpr int kCols = kAcc * BN <= 32 ? 32 : kAcc * BN <= 64 ? 64 : kAcc * BN <= 128 ? 128 : 256;
@@ -132,8 +137,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     SplitShared &sh = *reinterpret_cast<SplitShared *>(ring + ring_bytes + recv_bytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int rank = (int)cluster_ctarank();
-    const int S = (int)gridDim.x;  // the cluster spans the whole x dimension of the grid
+    const int rank = kClus ? (int)cluster_ctarank() : (int)blockIdx.x;
+    const int S = (int)gridDim.x;  // the K split spans the whole x dimension of the grid
     const int n0 = blockIdx.y * BN;
     const int C = (K + kChunkK - 1) / kChunkK;
     const int c_begin = (int)(((long long)rank * C) / S);
@@ -172,7 +177,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     __syncthreads();
     tc_fence_after();
     pdl_launch_dependents();
-    cluster_arrive_relaxed();  // phase 1: "my receive barrier is initialised" (init fence above)
+    if constexpr (kClus) cluster_arrive_relaxed();  // phase 1: "my receive barrier is initialised"
     const uint32_t tmem = sh.tmem_base;
 
     if (warp == 0) {
@@ -221,6 +226,84 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         __syncwarp();
     }
 
+    if constexpr (!kClus) {
+        // ---- epilogue without a cluster: partial tile -> workspace; the last CTA reduces ----
+        const bool ok = mbar_wait(&sh.accum, 0, status, kSiteAccum);
+        tc_fence_after();
+        const bool have = ok && !*((volatile int32_t *)&sh.aborted);
+        pdl_wait();  // the workspace and `out` may still be in use by the previous kernel
+        float4 *part = reinterpret_cast<float4 *>(ws) + (size_t)(blockIdx.y * S + rank) * T;
+        if (warp * 16 < M) {  // warp w holds tokens 16w..16w+15 in its lanes 0..15
+            const int t = warp * 16 + lane;
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 16) {
+                uint32_t r[16];
+                if (have) {
+                    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c;
+                    tmem_ld16(lane_base, r);
+                    tmem_ld_wait16(r);
+#pragma unroll
+                    for (int a = 1; a < kAcc; ++a) {
+                        uint32_t r2[16];
+                        tmem_ld16(lane_base + (uint32_t)(a * BN), r2);
+                        tmem_ld_wait16(r2);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) r[j] = 0u;
+                }
+                if (lane < 16 && t < M) {
+                    float4 *dst = part + (t * BN + c) / 4;
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        __stcg(dst + q4, make_float4(__uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]),
+                                                     __uint_as_float(r[4 * q4 + 2]), __uint_as_float(r[4 * q4 + 3])));
+                }
+            }
+            __threadfence();  // this CTA's partial is visible GPU-wide before the counter moves
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            const uint32_t prev = atomicAdd(&counters[blockIdx.y], 1u);
+            *reinterpret_cast<volatile int32_t *>(&sh.last) = (prev == (uint32_t)(S - 1)) ? 1 : 0;
+            __threadfence();
+        }
+        __syncthreads();
+        if (*reinterpret_cast<volatile int32_t *>(&sh.last)) {
+            const float4 *pt = reinterpret_cast<const float4 *>(ws) + (size_t)blockIdx.y * S * T;
+            for (int j = tid; j < T; j += kSplitThreads) {
+                float4 acc = __ldcg(pt + j);
+                for (int q = 1; q < S; ++q) {  // rank order: deterministic
+                    const float4 v = __ldcg(pt + (size_t)q * T + j);
+                    acc.x += v.x;
+                    acc.y += v.y;
+                    acc.z += v.z;
+                    acc.w += v.w;
+                }
+                const int m = j / (BN / 4);
+                const int n = n0 + 4 * (j % (BN / 4));
+                float r4[4] = {acc.x, acc.y, acc.z, acc.w};
+                if (bias) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (n + e < N) r4[e] += bf16_to_f32(bias[n + e]);
+                }
+                const size_t o = (size_t)m * N + n;
+                if (n + 3 < N && (o & 3) == 0) {
+                    OutStore<OutT>::four(out + o, r4[0], r4[1], r4[2], r4[3]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (n + e < N) OutStore<OutT>::one(out + o + e, r4[e]);
+                }
+            }
+            if (tid == 0) counters[blockIdx.y] = 0u;  // ready for the next call
+        }
+    } else {
     // ---- epilogue: accumulator -> local staging [M][BN] -> one bulk copy per owner ----
     cluster_wait_acquire();  // phase 1 done (long since): every CTA's receive barrier exists
     const bool ok = mbar_wait(&sh.accum, 0, status, kSiteAccum);
@@ -307,12 +390,14 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         }
     }
 
+    }  // kClus
+
     // Drain TMA copies that were issued but never consumed (only after a timeout).
     if (tid == 0) {
         for (int i = sh.consumed; i < sh.issued; ++i)
             mbar_wait(&sh.full[i % stages], (i / stages) & 1, status, kSiteDrain);
     }
-    cluster_wait_acquire();  // phase 2 done: no copy into or out of this CTA is pending
+    if constexpr (kClus) cluster_wait_acquire();  // phase 2 done: no copy into or out of this CTA is pending
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kCols);
@@ -321,37 +406,39 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 
 namespace {
 
-template <typename OutT>
-using SplitFn = void (*)(CUtensorMap, CUtensorMap, const uint16_t *, OutT *, int, int, int, int, int, int32_t *);
+template <typename OutT, bool kClus>
+using SplitFn = void (*)(CUtensorMap, CUtensorMap, const uint16_t *, OutT *, int, int, int, int, int, int32_t *,
+                         float *, uint32_t *);
 
-template <typename OutT>
-SplitFn<OutT> pick(int BN) {
+template <typename OutT, bool kClus>
+SplitFn<OutT, kClus> pick(int BN) {
     switch (BN) {
-        case 16: return splitk_kernel<16, OutT>;
-        case 32: return splitk_kernel<32, OutT>;
-        case 48: return splitk_kernel<48, OutT>;
-        case 64: return splitk_kernel<64, OutT>;
-        case 96: return splitk_kernel<96, OutT>;
-        case 128: return splitk_kernel<128, OutT>;
-        case 192: return splitk_kernel<192, OutT>;
-        case 256: return splitk_kernel<256, OutT>;
+        case 16: return splitk_kernel<16, OutT, kClus>;
+        case 32: return splitk_kernel<32, OutT, kClus>;
+        case 48: return splitk_kernel<48, OutT, kClus>;
+        case 64: return splitk_kernel<64, OutT, kClus>;
+        case 96: return splitk_kernel<96, OutT, kClus>;
+        case 128: return splitk_kernel<128, OutT, kClus>;
+        case 192: return splitk_kernel<192, OutT, kClus>;
+        case 256: return splitk_kernel<256, OutT, kClus>;
         default: return nullptr;
     }
 }
 
-template <typename OutT>
+template <typename OutT, bool kClus>
 int set_split_attrs() {
     for (int BN : {16, 32, 48, 64, 96, 128, 192, 256}) {
-        int e = (int)cudaFuncSetAttribute(pick<OutT>(BN), cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPerCta);
-        if (!e) e = (int)cudaFuncSetAttribute(pick<OutT>(BN), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        auto fn = pick<OutT, kClus>(BN);
+        int e = (int)cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPerCta);
+        if (!e && kClus) e = (int)cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e) return e;
     }
     return 0;
 }
 
-template <typename OutT>
+template <typename OutT, bool kClus>
 int launch_split_t(const LaunchArgs &a, const bf16l_plan &p) {
-    SplitFn<OutT> fn = pick<OutT>(p.rows_per_cta);
+    SplitFn<OutT, kClus> fn = pick<OutT, kClus>(p.rows_per_cta);
     if (!fn) return (int)cudaErrorInvalidValue;
     CUtensorMap tw, tx;
     int r = make_tmap_bf16_2d(&tw, a.W, (uint64_t)a.N, (uint64_t)a.K, (uint32_t)p.rows_per_cta, kChunkK,
@@ -361,37 +448,62 @@ int launch_split_t(const LaunchArgs &a, const bf16l_plan &p) {
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (r) return (int)cudaErrorInvalidValue;
 
+    const int tiles = (a.N + p.rows_per_cta - 1) / p.rows_per_cta;
+    uint32_t *counters = nullptr;
+    float *parts = nullptr;
+    if (!kClus) {
+        if (!a.workspace || a.workspace_bytes < split_ws_bytes(a.M, a.N, p)) return (int)cudaErrorInvalidValue;
+        counters = static_cast<uint32_t *>(a.workspace);
+        parts = reinterpret_cast<float *>(static_cast<uint8_t *>(a.workspace) + split_ws_counter_bytes(tiles));
+    }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.split_k, (unsigned)((a.N + p.rows_per_cta - 1) / p.rows_per_cta), 1);
+    cfg.gridDim = dim3((unsigned)p.split_k, (unsigned)tiles, 1);
     cfg.blockDim = dim3(kSplitThreads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)split_smem_bytes(p.tokens_per_cta, p.rows_per_cta, p.stages);
     cfg.stream = (cudaStream_t)a.stream;
     cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)p.split_k;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = (p.flags & BF16L_FLAG_PDL) ? 1 : 0;
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = (p.flags & BF16L_FLAG_PDL) ? 1 : 0;
+    ++na;
+    if (kClus) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)p.split_k;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = na;
     return (int)cudaLaunchKernelEx(&cfg, fn, tw, tx, static_cast<const uint16_t *>(a.bias),
                                    static_cast<OutT *>(a.out), a.M, a.N, a.K, p.tokens_per_cta, p.stages,
-                                   a.status);
+                                   a.status, parts, counters);
 }
 
 }  // namespace
 
-bool split_rows_supported(int rows) { return pick<uint16_t>(rows) != nullptr; }
+size_t split_ws_counter_bytes(int tiles) { return ((size_t)tiles * 4 + 255) / 256 * 256; }
+
+size_t split_ws_bytes(int M, int N, const bf16l_plan &p) {
+    if (p.kernel != BF16L_KERNEL_SPLITK_WS || p.rows_per_cta <= 0) return 0;
+    const int tiles = (N + p.rows_per_cta - 1) / p.rows_per_cta;
+    return split_ws_counter_bytes(tiles) + (size_t)tiles * p.split_k * M * p.rows_per_cta * 4;
+}
+
+bool split_rows_supported(int rows) { return pick<uint16_t, true>(rows) != nullptr; }
 
 int init_splitk() {
-    int e = set_split_attrs<uint16_t>();
-    if (!e) e = set_split_attrs<float>();
+    int e = set_split_attrs<uint16_t, true>();
+    if (!e) e = set_split_attrs<float, true>();
+    if (!e) e = set_split_attrs<uint16_t, false>();
+    if (!e) e = set_split_attrs<float, false>();
     return e;
 }
 
 int launch_splitk(const LaunchArgs &a, const bf16l_plan &p) {
-    return a.out_f32 ? launch_split_t<float>(a, p) : launch_split_t<uint16_t>(a, p);
+    const bool clus = p.kernel == BF16L_KERNEL_SPLITK;
+    if (a.out_f32) return clus ? launch_split_t<float, true>(a, p) : launch_split_t<float, false>(a, p);
+    return clus ? launch_split_t<uint16_t, true>(a, p) : launch_split_t<uint16_t, false>(a, p);
 }
 
 }  // namespace bf16l

@@ -153,3 +153,25 @@ def test_plan_check_accepts_and_rejects(lib):
     for (M, N, K) in [(1, 256, 2048), (16, 384, 7168), (64, 2112, 7168), (300, 1000, 520), (5, 7, 9)]:
         q = lib.plan(M, N, K)
         assert lib.plan_check(M, N, K, q).grid == q.grid
+
+
+def test_workspace_plans_on_cpu(lib):
+    import ctypes
+    p = lib.make_plan("splitk_ws", threads=128, rows_per_cta=64, tokens_per_cta=16, split_k=64, stages=2)
+    assert lib.plan_check(16, 256, 7168, p).grid == 64 * 4
+    with pytest.raises(lib.BF16LinearError):
+        lib.plan_check(16, 256, 7168, lib.make_plan("splitk_ws", threads=128, rows_per_cta=64, tokens_per_cta=16,
+                                                    split_k=65, stages=2))
+    # counters (4 tiles, rounded up to 256 bytes) + partials [tiles][S][M][rows] fp32
+    assert lib.workspace_size(16, 256, 7168, p) == 256 + 4 * 64 * 16 * 64 * 4
+    assert lib.workspace_size(16, 256, 7168, lib.make_plan("dotprod", threads=128, rows_per_cta=2)) == 0
+    # the dispatcher never needs a workspace it was not given
+    assert lib.workspace_size(16, 256, 7168, lib.plan(16, 256, 7168)) == 0
+    # a misaligned workspace is rejected before any CUDA call
+    L = lib.load()
+    c = lib.Call()
+    c.x, c.W, c.out = 0x10000, 0x20000000, 0x40000000
+    c.M, c.N, c.K = 16, 256, 7168
+    c.workspace, c.workspace_bytes = 0x50000010, 1 << 20
+    assert L.bf16_linear_run(ctypes.byref(c)) == -2
+    assert L.bf16_linear_run(None) == -1
