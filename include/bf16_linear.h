@@ -56,7 +56,8 @@ typedef enum {
     BF16L_EARCH = -3,        /* current device is not compute capability 10.3 */
     BF16L_ELAUNCH = -4,      /* the CUDA launch (or device query) failed; see bf16_linear_cuda_error */
     BF16L_ETIMEOUT = -5,     /* a kernel's bounded wait gave up (read via bf16_linear_device_status) */
-    BF16L_EUNSUPPORTED = -6  /* the requested kernel does not support this shape (e.g. K % 8 != 0 for a TMA kernel) */
+    BF16L_EUNSUPPORTED = -6, /* the requested kernel does not support this shape (e.g. K % 8 != 0 for a TMA kernel) */
+    BF16L_ENOSCRATCH = -7    /* bf16_linear_noalloc: the shape needs more scratch than its fixed array holds */
 } bf16l_status;
 
 /* Kernels behind the dispatcher. */
@@ -240,6 +241,33 @@ size_t bf16_linear_workspace_size(int M, int N, int K, const bf16l_plan *plan);
  * (bf16_linear_plan is this with workspace_bytes == 0).  Pure host code.
  */
 int bf16_linear_plan_ws(int M, int N, int K, const bf16l_device *dev, size_t workspace_bytes, bf16l_plan *plan);
+
+/*
+ * bf16_linear_noalloc — the same operation for callers that cannot allocate
+ * device memory.  (No counterpart on the pages: it exists for callers such as
+ * a plug-in that receives its input and output buffers from a host program
+ * owning all device memory, and so has no way to obtain a workspace.)
+ *
+ * It runs the cluster-free split-K kernel (BF16L_KERNEL_SPLITK_WS) with its
+ * scratch in a fixed array of bf16_linear_noalloc_scratch_bytes() (4 MiB)
+ * that is part of the library's device image: every GPU that loads the
+ * library holds it until the process exits.  Nothing is allocated or freed.
+ * x, W, bias, out: as bf16_linear (bf16 out).  Requires M <= 64 and
+ * K % 8 == 0 (else BF16L_EUNSUPPORTED); the plan takes fewer K splits until
+ * its scratch fits, and a shape that does not fit even unsplit (about
+ * M * N * 4 bytes > 4 MiB) returns BF16L_ENOSCRATCH.
+ *
+ * The first call on a device looks up the array's device address once (with
+ * that device current); make that first call before any stream capture.
+ * Each call clears the array's counters on `stream` before its launch.  All
+ * calls share the one array, so calls that can overlap on the GPU (different
+ * streams, or PDL) race and give wrong results; issue them on one stream.
+ */
+int bf16_linear_noalloc(const void *x, const void *W, const void *bias, void *out,
+                        int M, int N, int K, bf16l_stream_t stream);
+
+/* Size in bytes of the fixed scratch array behind bf16_linear_noalloc. */
+size_t bf16_linear_noalloc_scratch_bytes(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *bf16_linear_strerror(int status);

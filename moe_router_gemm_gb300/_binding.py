@@ -16,7 +16,7 @@ import threading
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libbf16_linear.so")
 
-OK, EINVAL, EALIGN, EARCH, ELAUNCH, ETIMEOUT, EUNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
+OK, EINVAL, EALIGN, EARCH, ELAUNCH, ETIMEOUT, EUNSUPPORTED, ENOSCRATCH = 0, -1, -2, -3, -4, -5, -6, -7
 FLAG_PDL = 1
 KERNEL_DOTPROD, KERNEL_SPLITK, KERNEL_TILE, KERNEL_SPLITK_WS = 0, 1, 2, 3
 KERNEL_NAMES = {KERNEL_DOTPROD: "dotprod", KERNEL_SPLITK: "splitk", KERNEL_TILE: "tile",
@@ -95,6 +95,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.bf16_linear_plan_ws.argtypes = [i32, i32, i32, ctypes.POINTER(Device), ctypes.c_size_t,
                                             ctypes.POINTER(Plan)]
         lib.bf16_linear_plan_ws.restype = i32
+        lib.bf16_linear_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp]
+        lib.bf16_linear_noalloc.restype = i32
+        lib.bf16_linear_noalloc_scratch_bytes.argtypes = []
+        lib.bf16_linear_noalloc_scratch_bytes.restype = ctypes.c_size_t
         lib.bf16_linear_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32), i32]
         lib.bf16_linear_device_status.restype = i32
         lib.bf16_linear_selftest_wait.argtypes = [ctypes.c_uint32, vp]
@@ -281,6 +285,24 @@ def bf16_linear_ex(x, W, bias=None, out=None, flags: int = 0, stream=None):
                                    _stream_handle(stream, x.device))
     if st != OK:
         _raise(st, f"bf16_linear_ex(M={M}, N={N}, K={K})")
+    return out
+
+
+def bf16_linear_noalloc(x, W, bias=None, out=None, stream=None):
+    """bf16 out = x @ W^T (+ bias) for callers that cannot allocate device memory.
+
+    Runs the workspace split-K kernel with its scratch in the library's fixed
+    device array (see bf16_linear.h); the library allocates nothing.  Pass
+    `out` to avoid the allocation this wrapper would otherwise make for it.
+    Calls share the array: keep them on one stream.
+    """
+    import torch
+    M, N, K, out = _check(x, W, bias, out)
+    with torch.cuda.device(x.device):
+        st = load().bf16_linear_noalloc(_ptr(x), _ptr(W), _ptr(bias), _ptr(out), M, N, K,
+                                        _stream_handle(stream, x.device))
+    if st != OK:
+        _raise(st, f"bf16_linear_noalloc(M={M}, N={N}, K={K})")
     return out
 
 

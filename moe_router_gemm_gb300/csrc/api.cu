@@ -277,6 +277,7 @@ extern "C" const char *bf16_linear_strerror(int status) {
         case BF16L_ELAUNCH: return "CUDA launch or device query failed";
         case BF16L_ETIMEOUT: return "a kernel wait timed out";
         case BF16L_EUNSUPPORTED: return "the requested kernel does not support this shape";
+        case BF16L_ENOSCRATCH: return "the shape needs more scratch than the fixed no-allocation array holds";
         default: return "unknown status";
     }
 }
