@@ -455,6 +455,17 @@ def candidate_plans(lib, M, N, K):
                     except Exception:
                         continue
                 cands.append(p)
+    if K % 8 == 0 and M <= 4 and K <= 8192:
+        for rg in (1, 2, 4):
+            if rg == 4 and M > 3:
+                continue
+            for st in (4, 6, 8, 12, 16):
+                p = lib.make_plan("stream", threads=288, rows_per_cta=rg, stages=st)
+                try:
+                    lib.plan_check(M, N, K, p)
+                except Exception:
+                    continue
+                cands.append(p)
     if K % 8 == 0 and M > 32:
         for st in (4, 3):
             cands.append(lib.make_plan("tile", threads=192, rows_per_cta=256, tokens_per_cta=128, stages=st))

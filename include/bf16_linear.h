@@ -66,8 +66,10 @@ typedef enum {
     BF16L_KERNEL_SPLITK = 1,  /* TMA -> tcgen05 (weights on the MMA M side), K split over a thread-block
                                  cluster, fp32 partials reduced through distributed shared memory */
     BF16L_KERNEL_TILE = 2,    /* persistent warp-specialised TMA -> tcgen05 -> TMEM tile GEMM */
-    BF16L_KERNEL_SPLITK_WS = 3 /* the split-K kernel without a cluster: K split over up to 64 CTAs, fp32
-                                  partials reduced through a caller-provided workspace (see bf16_linear_run) */
+    BF16L_KERNEL_SPLITK_WS = 3, /* the split-K kernel without a cluster: K split over up to 64 CTAs, fp32
+                                   partials reduced through a caller-provided workspace (see bf16_linear_run) */
+    BF16L_KERNEL_STREAM = 4    /* persistent CUDA-core kernel for M <= 4 and K <= 8192: one CTA per SM streams
+                                  a contiguous row range through a bulk-copy ring (large N: decode, MLP) */
 } bf16l_kernel;
 
 /*
@@ -79,7 +81,8 @@ typedef enum {
 typedef struct {
     int32_t kernel;        /* bf16l_kernel */
     int32_t threads;       /* threads per CTA */
-    int32_t rows_per_cta;  /* W rows per CTA (DOTPROD 1/2/4; SPLITK 16..256, the MMA N); TILE: W rows per tile */
+    int32_t rows_per_cta;  /* W rows per CTA (DOTPROD 1/2/4; SPLITK 16..256, the MMA N); TILE: W rows per tile;
+                              STREAM: W rows per ring stage (1, 2, or 4 when M <= 3) */
     int32_t tokens_per_cta;/* SPLITK: x rows loaded per chunk (M rounded up to 8, <= 64);  TILE: x rows per tile */
     int32_t split_k;       /* SPLITK: CTAs per cluster along K (1..16); SPLITK_WS: CTAs along K (1..64) */
     int32_t stages;        /* SPLITK / TILE: shared-memory ring depth (64-wide K chunks) */

@@ -38,6 +38,16 @@ constexpr int kSplitWsMaxSplit = 64;         // K splits of the cluster-free (wo
 size_t split_ws_counter_bytes(int tiles);
 size_t split_ws_bytes(int M, int N, const bf16l_plan &p);
 
+// Streaming kernel: M <= 4 tokens, K <= 8192 (x slice held in registers),
+// 1, 2 or 4 W rows per ring stage (4 only for M <= 3), one CTA per SM.
+constexpr int kStreamMaxTokens = 4;
+constexpr int kStreamMaxStages = 16;
+constexpr int kStreamMaxRows = 4;
+constexpr int kStreamMaxK = 8192;
+constexpr int kStreamThreads = 288;
+int stream_smem_bytes(int K, int rows, int stages);
+int init_stream();
+
 // Tile kernel: BM x rows, BN W rows per tile, 64-wide K chunks.
 constexpr int kTileBM = 128;
 constexpr int kTileBN = 256;
@@ -73,6 +83,7 @@ struct LaunchArgs {
 int launch_dotprod(const LaunchArgs &a, const bf16l_plan &p);
 int launch_splitk(const LaunchArgs &a, const bf16l_plan &p);
 int launch_tile(const LaunchArgs &a, const bf16l_plan &p);
+int launch_stream(const LaunchArgs &a, const bf16l_plan &p);
 
 // One-time per-device kernel attribute setup (dynamic shared memory limits,
 // non-portable cluster sizes).  Returns a cudaError_t value.

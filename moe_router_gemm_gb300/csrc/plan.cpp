@@ -118,6 +118,18 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
             p->grid = M == 0 ? 0 : (int)grid;
             return BF16L_OK;
         }
+        case BF16L_KERNEL_STREAM: {
+            if (K % 8 != 0 || K > kStreamMaxK || M > kStreamMaxTokens) return BF16L_EUNSUPPORTED;
+            if (p->threads != kStreamThreads ||
+                (p->rows_per_cta != 1 && p->rows_per_cta != 2 && p->rows_per_cta != 4) ||
+                (p->rows_per_cta == 4 && M > 3))
+                return BF16L_EINVAL;
+            if (p->stages < 1 || p->stages > kStreamMaxStages ||
+                stream_smem_bytes(K, p->rows_per_cta, p->stages) > 232448)
+                return BF16L_EINVAL;
+            p->grid = M == 0 ? 0 : (N < dev.num_sms ? N : dev.num_sms);
+            return BF16L_OK;
+        }
         case BF16L_KERNEL_TILE: {
             if (K % 8 != 0) return BF16L_EUNSUPPORTED;
             if (p->threads != kTileThreads || p->rows_per_cta != kTileBN || p->tokens_per_cta != kTileBM)
