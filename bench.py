@@ -100,9 +100,10 @@ def workload_desc(name):
 
 
 def kernel_source_hash(kernel_name):
-    src = {"dotprod": "dotprod.cu", "splitk": "splitk.cu", "tile": "tile.cu"}[kernel_name]
+    src = {"dotprod": ("dotprod.cuh", "dotprod.cu"), "splitk": ("splitk.cu",), "splitk_ws": ("splitk.cu",),
+           "tile": ("tile.cu",), "stream": ("stream.cu",)}[kernel_name]
     h = hashlib.sha256()
-    for f in (src, "common.cuh"):
+    for f in src + ("common.cuh", "kernels.h"):
         h.update(open(os.path.join(ROOT, "moe_router_gemm_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:12]
 
@@ -282,14 +283,17 @@ class Shape:
     def call(self, i):
         self.lib.run(self.x, self.Ws[i % self.R], self.b, self.out, plan_=self.plan, workspace=self.ws)
 
-    def capture(self, stream):
+    def capture(self, stream, warm=False):
+        """One graph of R back-to-back calls: on the R weight copies in turn (L2-cold),
+        or all on copy 0 (L2-warm: after the first call the weight is L2-resident
+        wherever it fits)."""
         for i in range(min(self.R, 3)):  # initialise outside capture
             self.call(i)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(self.R):
-                self.call(i)
+                self.call(0 if warm else i)
         self.graph = g
 
 
@@ -368,11 +372,34 @@ def gpu_arm(args, points, rank, world):
         for s_ in shapes:
             s_.plan.flags = 0
 
+    # ---- L2-warm: the same calls, every one on the same weight copy ----
+    warm_us = None
+    if not args.no_pdl_variant:
+        for s_ in shapes:
+            s_.plan.flags = 1 if args.pdl else 0
+        with torch.cuda.stream(stream):
+            for s_ in shapes:
+                s_.capture(stream, warm=True)
+                s_.graph.replay()  # brings the weight into L2
+        torch.cuda.synchronize()
+        warm_ms = [[] for _ in shapes]
+        with torch.cuda.stream(stream):
+            for k in range(max(3, args.steps // 2)):
+                for j, s_ in enumerate(shapes):
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    s_.graph.replay()
+                    b.record(stream)
+                    warm_ms[j].append((a, b))
+        torch.cuda.synchronize()
+        warm_us = [1000.0 * statistics.median([a.elapsed_time(b) for a, b in warm_ms[j]]) / s_.R
+                   for j, s_ in enumerate(shapes)]
+
     # ---- e2e: public API from pinned host buffers, copies inside the timed region ----
     e2e = e2e_arm(args, shapes, lib, device, stream)
 
     return dict(shapes=shapes, per_shape_us=per_shape_us, total_ms=total_ms, launches=launches,
-                clocks=clocks, e2e=e2e, pdl_us=pdl_us)
+                clocks=clocks, e2e=e2e, pdl_us=pdl_us, warm_us=warm_us)
 
 
 def eager_profile(args, points):
@@ -407,9 +434,12 @@ def candidate_plans(lib, M, N, K):
     """Every plan worth timing for one shape (the tuning space of the sweep)."""
     cands = []
     if M <= 16:
-        for R in (1, 2, 4):
-            for threads in (128, 256):
-                cands.append(lib.make_plan("dotprod", threads=threads, rows_per_cta=R))
+        # token groups: 0 = one CTA loops over groups of 8; t > 0 = ceil(M / t) CTAs per row slice
+        groups = [0] + sorted({-(-M // g) for g in (2, 3, 4) if -(-M // g) < M and -(-M // g) <= 8})
+        for t in groups:
+            for R in (1, 2, 4):
+                for threads in (128, 256):
+                    cands.append(lib.make_plan("dotprod", threads=threads, rows_per_cta=R, tokens_per_cta=t))
     if K % 8 == 0 and M <= 64:
         chunks = -(-K // 64)
         tokens = max(8, -(-M // 8) * 8)
@@ -589,7 +619,8 @@ def main():
     ap.add_argument("--pdl", action="store_true",
                     help="launch with programmatic dependent launch (BF16L_FLAG_PDL): back-to-back calls overlap")
     ap.add_argument("--no-pdl-variant", action="store_true",
-                    help="skip the extra pass that re-times every shape with programmatic dependent launch")
+                    help="skip the extra passes that re-time every shape with programmatic dependent launch "
+                         "and L2-warm")
     ap.add_argument("--only", action="append", default=[],
                     help="restrict to shapes M,N,K[,bias] (repeatable); for profiling")
     ap.add_argument("--sweep", action="store_true",
@@ -728,6 +759,18 @@ def main():
             "unit": unit,
             "per_shape_us": {k: [round(u, 3) for s_, u in zip(shapes, r["pdl_us"]) if f"K{s_.K}_N{s_.N}" == k]
                              for k in per_shape}},
+        "l2_warm": None if r["warm_us"] is None else {
+            "note": "same calls, every one on the same weight copy (L2-resident after the first where it fits "
+                    "in L2); effective GB/s = algorithmic bytes / time, against the HBM copy peak",
+            "value": round(statistics.mean(r["warm_us"]), 4) if not large else round(
+                sum(algo_flops(s.M, s.N, s.K, s.bias) for s in shapes)
+                / (sum(r["warm_us"]) * 1e-6) / 1e12, 2),
+            "unit": unit,
+            "per_shape_us": {k: [round(u, 3) for s_, u in zip(shapes, r["warm_us"]) if f"K{s_.K}_N{s_.N}" == k]
+                             for k in per_shape},
+            "pct_hbm_roofline_per_shape": None if large else {
+                k: [round(100.0 * algo_bytes(s.M, s.N, s.K, s.bias) / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 1)
+                    for s, us in zip(shapes, r["warm_us"]) if f"K{s.K}_N{s.N}" == k] for k in per_shape}},
         "per_shape_us": per_shape,
         "pct_hbm_roofline_per_shape": None if large else {
             k: [round(100.0 * algo_bytes(s.M, s.N, s.K, s.bias) / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 1)

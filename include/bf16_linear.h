@@ -83,7 +83,9 @@ typedef struct {
     int32_t threads;       /* threads per CTA */
     int32_t rows_per_cta;  /* W rows per CTA (DOTPROD 1/2/4; SPLITK 16..256, the MMA N); TILE: W rows per tile;
                               STREAM: W rows per ring stage (1, 2, or 4 when M <= 3) */
-    int32_t tokens_per_cta;/* SPLITK: x rows loaded per chunk (M rounded up to 8, <= 64);  TILE: x rows per tile */
+    int32_t tokens_per_cta;/* SPLITK: x rows loaded per chunk (M rounded up to 8, <= 64);  TILE: x rows per tile;
+                              DOTPROD: tokens per CTA, 1..8 (0 = min(M, 8)); ceil(M / tokens) CTAs then share each
+                              row slice, one token group each, instead of one CTA looping over the groups */
     int32_t split_k;       /* SPLITK: CTAs per cluster along K (1..16); SPLITK_WS: CTAs along K (1..64) */
     int32_t stages;        /* SPLITK / TILE: shared-memory ring depth (64-wide K chunks) */
     int32_t grid;          /* CTAs launched (informational; computed by the plan) */

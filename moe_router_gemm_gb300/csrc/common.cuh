@@ -61,6 +61,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// acc += x.lo * w.lo, then acc += x.hi * w.hi, for two packed bf16 pairs, with
+// the fp32-accumulating mixed-precision fma (sm_100+).  A product of two bf16
+// values is exact in fp32, so each step equals fmaf(float(x), float(w), acc)
+// bit for bit; only the widening instructions go away.
+__device__ __forceinline__ float fma2_bf16(uint32_t x2, uint32_t w2, float acc) {
+    asm("{\n\t.reg .b16 xl, xh, wl, wh;\n\t"
+        "mov.b32 {xl, xh}, %1;\n\t"
+        "mov.b32 {wl, wh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, xl, wl, %0;\n\t"
+        "fma.rn.f32.bf16 %0, xh, wh, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(x2), "r"(w2));
+    return acc;
+}
 __device__ __forceinline__ float bf16_to_f32(uint16_t v) { return __uint_as_float((uint32_t)v << 16); }
 __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
     __nv_bfloat16 b = __float2bfloat16_rn(f);

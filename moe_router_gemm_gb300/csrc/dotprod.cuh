@@ -18,10 +18,16 @@
 //     once per (vector, token);
 //   * rows whose length is not a multiple of 8 elements (K % 8 != 0, so not
 //     16-byte aligned) take a scalar path that reads x from global memory.
-// Tokens are processed MT at a time (MT = M for M <= 8); larger M loops over
-// W again, which only the K % 8 != 0 fallback ever does.
+// Tokens are processed MT at a time.  With gridDim.y == 1 a CTA loops over the
+// token groups, streaming its rows again for each; with gridDim.y = G token
+// groups, CTA (b, y) takes groups y, y + G, ... of the same rows, so groups run
+// side by side and the weight bytes of the later readers come from L2.
 //
-// Arithmetic: fp32 products and sums (each thread sums its k-slice in
+// Arithmetic: the products go through the mixed-precision fma
+// (fma.rn.f32.bf16: bf16 x bf16 + fp32 -> fp32), so neither operand is widened
+// by a separate instruction; the product of two bf16 values is exact in fp32,
+// so this is fmaf(float(x), float(w), acc) bit for bit.
+// fp32 products and sums (each thread sums its k-slice in
 // ascending order, then a fixed shuffle tree and a fixed in-order sum over
 // warps), bias added in fp32, one RNE rounding to bf16.  Deterministic.
 #pragma once
@@ -89,7 +95,7 @@ __global__ void __launch_bounds__(256) dotprod_kernel(const uint16_t *__restrict
         __syncthreads();
     }
 
-    for (int m0 = 0, pass = 0; m0 < M; m0 += MT, ++pass) {
+    for (int m0 = (int)blockIdx.y * MT, pass = 0; m0 < M; m0 += MT * (int)gridDim.y, ++pass) {
         float acc[R][MT];
 #pragma unroll
         for (int r = 0; r < R; ++r)
@@ -108,7 +114,7 @@ __global__ void __launch_bounds__(256) dotprod_kernel(const uint16_t *__restrict
             }
         };
         load_batch(tid);  // first weight batch in flight before x is touched
-        if (m0 == 0) {
+        if (pass == 0) {
             pdl_launch_dependents();  // (no-ops unless launched with programmatic serialization)
             pdl_wait();               // x may be written by the previous kernel; out may still be read by it
         }
@@ -140,11 +146,23 @@ __global__ void __launch_bounds__(256) dotprod_kernel(const uint16_t *__restrict
                                 xv.v = xs[m * nvec + v];
                             else
                                 xv.load_cached(x + (size_t)(m0 + m) * K + (size_t)v * VEC);
+                            if constexpr (VEC == 8) {  // bf16 x bf16 + fp32 in one instruction per product
 #pragma unroll
-                            for (int e = 0; e < VEC; ++e) {
-                                const float xe = xv.get(e);
+                                for (int r = 0; r < R; ++r) {
+                                    float a_ = acc[r][m];
+                                    a_ = fma2_bf16(xv.v.x, wv[u][r].v.x, a_);
+                                    a_ = fma2_bf16(xv.v.y, wv[u][r].v.y, a_);
+                                    a_ = fma2_bf16(xv.v.z, wv[u][r].v.z, a_);
+                                    a_ = fma2_bf16(xv.v.w, wv[u][r].v.w, a_);
+                                    acc[r][m] = a_;
+                                }
+                            } else {
 #pragma unroll
-                                for (int r = 0; r < R; ++r) acc[r][m] = fmaf(xe, wv[u][r].get(e), acc[r][m]);
+                                for (int e = 0; e < VEC; ++e) {
+                                    const float xe = xv.get(e);
+#pragma unroll
+                                    for (int r = 0; r < R; ++r) acc[r][m] = fmaf(xe, wv[u][r].get(e), acc[r][m]);
+                                }
                             }
                         }
                     }
@@ -231,13 +249,15 @@ int init_dotprod_t() {
 
 template <typename OutT>
 int launch_dotprod_t(const LaunchArgs &a, const bf16l_plan &p) {
-    const int MT = a.M < kDotMaxTokens ? a.M : kDotMaxTokens;
+    const int t = p.tokens_per_cta > 0 ? p.tokens_per_cta : kDotMaxTokens;
+    const int MT = a.M < t ? a.M : t;
     const size_t xbytes = (size_t)MT * a.K * 2;
     const int kind = (a.K % 8 != 0) ? 2 : (xbytes <= (size_t)kXSmemMax ? 0 : 1);
     DotFn<OutT> fn = pick<OutT>(MT, p.rows_per_cta, kind);
     if (!fn) return (int)cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.grid);
+    cfg.gridDim = dim3((unsigned)((a.N + p.rows_per_cta - 1) / p.rows_per_cta),
+                       (unsigned)dot_token_groups(a.M, p.tokens_per_cta));
     cfg.blockDim = dim3((unsigned)p.threads);
     cfg.dynamicSmemBytes = kind == 0 ? xbytes : 0;
     cfg.stream = (cudaStream_t)a.stream;

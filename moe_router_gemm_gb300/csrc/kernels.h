@@ -17,6 +17,13 @@ namespace bf16l {
 constexpr int kDotMaxTokens = 8;
 constexpr int kDotRows[] = {1, 2, 4};
 constexpr int kDotThreads[] = {64, 128, 256};
+// CTAs along y of a dot-product launch: one per token group of `tokens`
+// (0 = a single CTA row that loops over groups of kDotMaxTokens).
+inline int dot_token_groups(int M, int tokens) {
+    if (tokens <= 0 || M <= 0) return 1;
+    const int mt = M < tokens ? M : tokens;
+    return (M + mt - 1) / mt;
+}
 
 // Cluster split-K kernel: tokens (M <= 64, padded to a multiple of 8) on the
 // MMA M side, 16..256 weight rows per CTA on the N side, K split over up to 16

@@ -97,7 +97,8 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
         case BF16L_KERNEL_DOTPROD: {
             if (!in_list(p->threads, kDotThreads, 3) || !in_list(p->rows_per_cta, kDotRows, 3))
                 return BF16L_EINVAL;
-            p->grid = M == 0 ? 0 : ceil_div(N, p->rows_per_cta);
+            if (p->tokens_per_cta < 0 || p->tokens_per_cta > kDotMaxTokens) return BF16L_EINVAL;
+            p->grid = M == 0 ? 0 : ceil_div(N, p->rows_per_cta) * dot_token_groups(M, p->tokens_per_cta);
             return BF16L_OK;
         }
         case BF16L_KERNEL_SPLITK:

@@ -128,20 +128,14 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 for (int r = 0; r < RG; ++r) {
                     if (r >= rows) break;
                     const uint4 w = wst[(size_t)r * nvec + v];
-                    const float wf[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                                         bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
 #pragma unroll
-                    for (int m = 0; m < MT; ++m) {
+                    for (int m = 0; m < MT; ++m) {  // mixed-precision fma: exact products, fp32 sums
                         const uint4 xx = xv[i][m];
                         float a = acc[r][m];
-                        a = fmaf(bf16_lo(xx.x), wf[0], a);
-                        a = fmaf(bf16_hi(xx.x), wf[1], a);
-                        a = fmaf(bf16_lo(xx.y), wf[2], a);
-                        a = fmaf(bf16_hi(xx.y), wf[3], a);
-                        a = fmaf(bf16_lo(xx.z), wf[4], a);
-                        a = fmaf(bf16_hi(xx.z), wf[5], a);
-                        a = fmaf(bf16_lo(xx.w), wf[6], a);
-                        a = fmaf(bf16_hi(xx.w), wf[7], a);
+                        a = fma2_bf16(xx.x, w.x, a);
+                        a = fma2_bf16(xx.y, w.y, a);
+                        a = fma2_bf16(xx.z, w.z, a);
+                        a = fma2_bf16(xx.w, w.w, a);
                         acc[r][m] = a;
                     }
                 }

@@ -155,6 +155,21 @@ def test_plan_check_accepts_and_rejects(lib):
         assert lib.plan_check(M, N, K, q).grid == q.grid
 
 
+def test_dotprod_token_groups_on_cpu(lib):
+    # ceil(N / R) row slices x ceil(M / t) token groups
+    assert lib.plan_check(16, 256, 7168, lib.make_plan("dotprod", threads=128, rows_per_cta=2,
+                                                       tokens_per_cta=8)).grid == 128 * 2
+    assert lib.plan_check(13, 256, 7168, lib.make_plan("dotprod", threads=128, rows_per_cta=1,
+                                                       tokens_per_cta=4)).grid == 256 * 4
+    assert lib.plan_check(3, 256, 7168, lib.make_plan("dotprod", threads=128, rows_per_cta=1,
+                                                      tokens_per_cta=8)).grid == 256
+    # 0 = one CTA row looping over groups of 8
+    assert lib.plan_check(16, 256, 7168, lib.make_plan("dotprod", threads=128, rows_per_cta=2)).grid == 128
+    for bad in (-1, 9):
+        with pytest.raises(lib.BF16LinearError):
+            lib.plan_check(16, 256, 7168, lib.make_plan("dotprod", threads=128, rows_per_cta=2, tokens_per_cta=bad))
+
+
 def test_workspace_plans_on_cpu(lib):
     import ctypes
     p = lib.make_plan("splitk_ws", threads=128, rows_per_cta=64, tokens_per_cta=16, split_k=64, stages=2)

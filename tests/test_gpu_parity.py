@@ -136,6 +136,25 @@ def test_dotprod_forced(lib, shape, R):
         _check(lib, M, N, K, seed=M * 7 + N + K, bias=bias, plan=dot_plan(lib, R, threads=128 if K > 64 else 64))
 
 
+@pytest.mark.parametrize("case", [(9, 256, 4096, 5, 2), (16, 384, 7168, 8, 2), (13, 40, 2880, 4, 1),
+                                  (16, 256, 6144, 3, 4), (6, 128, 2880, 2, 1), (11, 33, 1032, 7, 2),
+                                  (5, 17, 101, 2, 1), (12, 300, 7168, 6, 4)],
+                         ids=lambda c: "x".join(map(str, c)))
+def test_dotprod_token_groups(lib, case):
+    """Token groups side by side (grid.y = ceil(M / t)), including a ragged last group
+    and the scalar K % 8 != 0 form."""
+    M, N, K, t, R = case
+    plan = lib.make_plan("dotprod", threads=128, rows_per_cta=R, tokens_per_cta=t)
+    for bias in (False, True):
+        got, _ = _check(lib, M, N, K, seed=M + N + K + t, bias=bias, plan=plan)
+    # Each (row, token) output is summed in the same order whatever the grouping
+    # (per-thread k-slices, shuffle tree, warps in order), so the bits must match
+    # a single CTA row looping over groups of 8.
+    x, W, b = _inputs(M, N, K, 3, True)
+    loop = _run(lib, x, W, b, lib.make_plan("dotprod", threads=128, rows_per_cta=R, tokens_per_cta=0))
+    assert np.array_equal(loop, _run(lib, x, W, b, plan))
+
+
 @pytest.mark.parametrize("threads", [64, 256])
 def test_dotprod_block_sizes(lib, threads):
     _check(lib, 4, 384, 7168, seed=5, plan=dot_plan(lib, 2, threads))
