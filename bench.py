@@ -101,7 +101,7 @@ def workload_desc(name):
 
 def kernel_source_hash(kernel_name):
     src = {"dotprod": ("dotprod.cuh", "dotprod.cu"), "splitk": ("splitk.cu",), "splitk_ws": ("splitk.cu",),
-           "tile": ("tile.cu",), "stream": ("stream.cu",)}[kernel_name]
+           "tile": ("tile.cu",), "stream": ("stream.cu",), "tile2": ("tile2.cu",)}[kernel_name]
     h = hashlib.sha256()
     for f in src + ("common.cuh", "kernels.h"):
         h.update(open(os.path.join(ROOT, "moe_router_gemm_gb300", "csrc", f), "rb").read())
@@ -304,7 +304,7 @@ def gpu_arm(args, points, rank, world):
     device = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.Stream(device)
 
-    shapes = [Shape(pt, device, lib, pdl=args.pdl) for pt in points]
+    shapes = [Shape(pt, device, lib, plan_override=forced_plan(lib, args.plan), pdl=args.pdl) for pt in points]
     with torch.cuda.stream(stream):
         for s in shapes:
             s.capture(stream)
@@ -402,13 +402,22 @@ def gpu_arm(args, points, rank, world):
                 clocks=clocks, e2e=e2e, pdl_us=pdl_us, warm_us=warm_us)
 
 
+def forced_plan(lib, spec):
+    """The plan given by --plan (kernel name, threads, rows, tokens, split, stages), or None."""
+    if not spec:
+        return None
+    f = spec.split(",")
+    names = ("threads", "rows_per_cta", "tokens_per_cta", "split_k", "stages")
+    return lib.make_plan(f[0], **{k: int(v) for k, v in zip(names, f[1:])})
+
+
 def eager_profile(args, points):
     """Profiling mode (for ncu launch lists): no graphs, two rotation copies per shape."""
     import moe_router_gemm_gb300 as lib
     from moe_router_gemm_gb300 import build as _build
     _build.build()
     device = torch.device("cuda", torch.cuda.current_device())
-    shapes = [Shape(pt, device, lib, pdl=args.pdl) for pt in points]
+    shapes = [Shape(pt, device, lib, plan_override=forced_plan(lib, args.plan), pdl=args.pdl) for pt in points]
     for s in shapes:
         s.R = min(s.R, 2)
         s.Ws = s.Ws[:2]
@@ -496,6 +505,9 @@ def candidate_plans(lib, M, N, K):
                 except Exception:
                     continue
                 cands.append(p)
+    if K % 8 == 0 and M > 64:
+        for st in (6, 5, 4):
+            cands.append(lib.make_plan("tile2", threads=192, rows_per_cta=256, tokens_per_cta=256, stages=st))
     if K % 8 == 0 and M > 32:
         for st in (4, 3):
             cands.append(lib.make_plan("tile", threads=192, rows_per_cta=256, tokens_per_cta=128, stages=st))
@@ -621,6 +633,9 @@ def main():
     ap.add_argument("--no-pdl-variant", action="store_true",
                     help="skip the extra passes that re-time every shape with programmatic dependent launch "
                          "and L2-warm")
+    ap.add_argument("--plan", default=None,
+                    help="force one plan on every shape: kernel,threads,rows_per_cta,tokens_per_cta,split_k,stages "
+                         "(kernel by name, e.g. tile2,192,256,256,0,6); for profiling one kernel")
     ap.add_argument("--only", action="append", default=[],
                     help="restrict to shapes M,N,K[,bias] (repeatable); for profiling")
     ap.add_argument("--sweep", action="store_true",

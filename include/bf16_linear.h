@@ -68,8 +68,10 @@ typedef enum {
     BF16L_KERNEL_TILE = 2,    /* persistent warp-specialised TMA -> tcgen05 -> TMEM tile GEMM */
     BF16L_KERNEL_SPLITK_WS = 3, /* the split-K kernel without a cluster: K split over up to 64 CTAs, fp32
                                    partials reduced through a caller-provided workspace (see bf16_linear_run) */
-    BF16L_KERNEL_STREAM = 4    /* persistent CUDA-core kernel for M <= 4 and K <= 8192: one CTA per SM streams
+    BF16L_KERNEL_STREAM = 4,   /* persistent CUDA-core kernel for M <= 4 and K <= 8192: one CTA per SM streams
                                   a contiguous row range through a bulk-copy ring (large N: decode, MLP) */
+    BF16L_KERNEL_TILE2 = 5     /* persistent tcgen05 tile GEMM on CTA pairs (cta_group::2, clusters of 2):
+                                  256 x 256 tiles, each CTA stages half of each operand; large M */
 } bf16l_kernel;
 
 /*
@@ -187,6 +189,11 @@ int bf16_linear_with_plan(const void *x, const void *W, const void *bias, void *
  * bf16_linear_device_status — read (and optionally clear) the current device's
  * kernel status word.  0 means no kernel gave up; otherwise the first failing
  * wait's code (BF16L_ETIMEOUT in the low byte, the wait site above it).
+ * Sites: 1 MMA waiting for a stage, 2 producer waiting for a free stage,
+ * 3 epilogue waiting for the accumulator, 4 MMA waiting for the epilogue,
+ * 5 exit drain, 6 self-test, 7 split-K owner waiting for partials, 8 dot
+ * product waiting for x, 9 the two CTAs of a pair (BF16L_KERNEL_TILE2) got
+ * different TMEM addresses and gave up before any MMA.
  * Synchronises the device (reads device memory).  Returns BF16L_OK or
  * BF16L_ELAUNCH.
  */

@@ -59,6 +59,7 @@ void init_device(DeviceState &s) {
         if (!e) e = init_splitk();
         if (!e) e = init_tile();
         if (!e) e = init_stream();
+        if (!e) e = init_tile2();
     }
     s.err = e;
 }
@@ -142,6 +143,7 @@ int run(const bf16l_call &c) {
         case BF16L_KERNEL_SPLITK_WS: e = launch_splitk(a, p); break;
         case BF16L_KERNEL_TILE: e = launch_tile(a, p); break;
         case BF16L_KERNEL_STREAM: e = launch_stream(a, p); break;
+        case BF16L_KERNEL_TILE2: e = launch_tile2(a, p); break;
         default: return BF16L_EINVAL;
     }
     if (e) {

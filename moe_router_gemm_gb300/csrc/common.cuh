@@ -31,7 +31,8 @@ enum WaitSite : int32_t {
     kSiteDrain = 5,      // exit path draining copies still in flight
     kSiteSelftest = 6,   // bf16_linear_selftest_wait
     kSiteRecv = 7,       // split-K owner waiting for its peers' partials
-    kSiteStage = 8       // dot-product CTA waiting for its copy of x
+    kSiteStage = 8,      // dot-product CTA waiting for its copy of x
+    kSitePairTmem = 9    // the two CTAs of a pair got different TMEM addresses (gave up before any MMA)
 };
 
 // Default limit for one wait: 1 s of wall-clock time.
@@ -338,6 +339,60 @@ __device__ __forceinline__ void tmem_ld_wait16(uint32_t (&r)[16]) {
                    "+r"(r[14]), "+r"(r[15])
                  :
                  : "memory");
+}
+
+// ---- CTA pairs (cta_group::2): two CTAs of a cluster share one MMA ----
+// Both CTAs of the pair allocate together: one warp in each (the same warp
+// index) executes the alloc, and each CTA's TMEM gets the columns at the
+// address written to its own shared memory.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Pair MMA, issued by one thread of the even CTA: D (rows split 128/128 over
+// the two CTAs' TMEM) (+)= A (each CTA's own 128 rows) x B^T (each CTA holds
+// half of the N rows), operands at the same shared-memory offsets in both CTAs.
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on the mbarrier at this shared-memory offset in every CTA of `mask`
+// once the pair MMAs issued so far by this thread have completed.
+__device__ __forceinline__ void mma_commit_pair(uint64_t *bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        ::"r"(smem_u32(bar)), "h"(mask)
+        : "memory");
+}
+
+// TMA tile load into this CTA's shared memory whose completion is counted on
+// an mbarrier that may sit in the peer CTA of the pair (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map, uint32_t bar_cluster,
+                                                 int32_t c0, int32_t c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%3, %4}], [%2];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+// Arrive (release, cluster scope) on an mbarrier in another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
 // ---------------------------------------------------------------------------

@@ -62,6 +62,13 @@ constexpr int kTileMinStages = 2;
 constexpr int kTileMaxStages = 4;
 constexpr int kTileThreads = 192;
 
+// Pair tile kernel (cta_group::2): 256 x rows x 256 W rows per cluster of 2,
+// 32 KB ring stages per CTA.
+constexpr int kTile2MinStages = 2;
+constexpr int kTile2MaxStages = 6;
+int tile2_smem_bytes(int stages);
+int init_tile2();
+
 constexpr int kChunkK = 64;  // K elements per TMA box row (128 bytes, the swizzle width)
 
 // GB300 default device description (cc 10.3, 152 SMs).
@@ -91,6 +98,7 @@ int launch_dotprod(const LaunchArgs &a, const bf16l_plan &p);
 int launch_splitk(const LaunchArgs &a, const bf16l_plan &p);
 int launch_tile(const LaunchArgs &a, const bf16l_plan &p);
 int launch_stream(const LaunchArgs &a, const bf16l_plan &p);
+int launch_tile2(const LaunchArgs &a, const bf16l_plan &p);
 
 // One-time per-device kernel attribute setup (dynamic shared memory limits,
 // non-portable cluster sizes).  Returns a cudaError_t value.

@@ -56,7 +56,8 @@ def test_plan_rejects_bad_sizes(lib):
 
 def test_plan_size_rules(lib):
     # tiny M -> dot product (the pages' default rule M <= 4), any K % 8 != 0 -> dot product
-    assert lib.plan(4, 256, 2048).kernel == lib.KERNEL_DOTPROD
+    # (K = 3000 has no measured table entry, so the size rules decide)
+    assert lib.plan(4, 256, 3000).kernel == lib.KERNEL_DOTPROD
     assert lib.plan(40, 256, 2881).kernel == lib.KERNEL_DOTPROD
     assert lib.plan(300, 256, 2881).kernel == lib.KERNEL_DOTPROD
     # large M -> tile kernel
@@ -82,7 +83,9 @@ def test_plan_is_valid_everywhere(lib):
             assert 1 <= p.split_k <= 16 and p.split_k <= -(-pt["K"] // 64)
             assert p.grid == p.split_k * -(-pt["N"] // p.rows_per_cta)
         if p.kernel == lib.KERNEL_DOTPROD:
-            assert p.grid == -(-pt["N"] // p.rows_per_cta)
+            t = p.tokens_per_cta
+            groups = 1 if t == 0 else -(-pt["M"] // min(t, pt["M"]))
+            assert 0 <= t <= 8 and p.grid == -(-pt["N"] // p.rows_per_cta) * groups
 
 
 # ---- bf16_linear(): argument validation happens before any CUDA call ----
@@ -168,6 +171,20 @@ def test_dotprod_token_groups_on_cpu(lib):
     for bad in (-1, 9):
         with pytest.raises(lib.BF16LinearError):
             lib.plan_check(16, 256, 7168, lib.make_plan("dotprod", threads=128, rows_per_cta=2, tokens_per_cta=bad))
+
+
+def test_pair_tile_plans_on_cpu(lib):
+    p = lib.make_plan("tile2", threads=192, rows_per_cta=256, tokens_per_cta=256, stages=6)
+    # 8 x 28 pair tiles of 256 x 256; 76 clusters of 2 on 152 SMs
+    assert lib.plan_check(2048, 7168, 7168, p).grid == 152
+    assert lib.plan_check(256, 256, 64, p).grid == 2
+    assert lib.plan_check(300, 300, 64, p).grid == 2 * 2 * 2
+    for bad in (dict(stages=7), dict(stages=1), dict(rows_per_cta=128), dict(tokens_per_cta=128), dict(threads=128)):
+        q = lib.make_plan("tile2", **dict(dict(threads=192, rows_per_cta=256, tokens_per_cta=256, stages=4), **bad))
+        with pytest.raises(lib.BF16LinearError):
+            lib.plan_check(2048, 7168, 7168, q)
+    with pytest.raises(lib.BF16LinearError):
+        lib.plan_check(2048, 7168, 7161, p)  # TMA needs K % 8 == 0
 
 
 def test_workspace_plans_on_cpu(lib):
