@@ -60,6 +60,7 @@ void init_device(DeviceState &s) {
         if (!e) e = init_tile();
         if (!e) e = init_stream();
         if (!e) e = init_tile2();
+        if (!e) e = init_warprow();
     }
     s.err = e;
 }
@@ -144,6 +145,7 @@ int run(const bf16l_call &c) {
         case BF16L_KERNEL_TILE: e = launch_tile(a, p); break;
         case BF16L_KERNEL_STREAM: e = launch_stream(a, p); break;
         case BF16L_KERNEL_TILE2: e = launch_tile2(a, p); break;
+        case BF16L_KERNEL_WARPROW: e = launch_warprow(a, p); break;
         default: return BF16L_EINVAL;
     }
     if (e) {

@@ -62,6 +62,13 @@ constexpr int kTileMinStages = 2;
 constexpr int kTileMaxStages = 4;
 constexpr int kTileThreads = 192;
 
+// Warp-per-row kernel: M <= 8 tokens staged in shared memory (M*K*2 bytes),
+// 256/512/1024 threads, 1/2/4 warps per row, a few CTAs per SM.
+constexpr int kWarpRowMaxTokens = 8;
+constexpr int kWarpRowMaxSmem = 200 * 1024;
+int warprow_smem_bytes(int M, int K);
+int init_warprow();
+
 // Pair tile kernel (cta_group::2): 256 x rows x 256 W rows per cluster of 2,
 // 32 KB ring stages per CTA.
 constexpr int kTile2MinStages = 2;
@@ -99,6 +106,7 @@ int launch_splitk(const LaunchArgs &a, const bf16l_plan &p);
 int launch_tile(const LaunchArgs &a, const bf16l_plan &p);
 int launch_stream(const LaunchArgs &a, const bf16l_plan &p);
 int launch_tile2(const LaunchArgs &a, const bf16l_plan &p);
+int launch_warprow(const LaunchArgs &a, const bf16l_plan &p);
 
 // One-time per-device kernel attribute setup (dynamic shared memory limits,
 // non-portable cluster sizes).  Returns a cudaError_t value.

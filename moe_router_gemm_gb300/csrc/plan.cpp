@@ -141,6 +141,20 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
             p->grid = M == 0 ? 0 : (int)grid;
             return BF16L_OK;
         }
+        case BF16L_KERNEL_WARPROW: {
+            if (K % 8 != 0 || M > kWarpRowMaxTokens || warprow_smem_bytes(M, K) > kWarpRowMaxSmem)
+                return BF16L_EUNSUPPORTED;
+            const int t = p->threads, wpr = p->rows_per_cta, cps = p->stages;
+            if ((t != 256 && t != 512 && t != 1024) || (wpr != 1 && wpr != 2 && wpr != 4)) return BF16L_EINVAL;
+            // a named barrier per row group (ids 1..15) when warps share a row
+            if (wpr > 1 && (t / 32) / wpr > 15) return BF16L_EINVAL;
+            if (cps < 1 || cps > 4 || t * cps > 2048 ||
+                cps * (warprow_smem_bytes(M, K) + 2048) > 232448)
+                return BF16L_EINVAL;
+            const int64_t ctas = (int64_t)dev.num_sms * cps;
+            p->grid = M == 0 ? 0 : (int)(ctas < N ? ctas : N);
+            return BF16L_OK;
+        }
         case BF16L_KERNEL_TILE2: {
             // A pair tile is 256 x rows x 256 W rows; threads and tile sizes are fixed.
             if (K % 8 != 0) return BF16L_EUNSUPPORTED;

@@ -187,6 +187,21 @@ def test_pair_tile_plans_on_cpu(lib):
         lib.plan_check(2048, 7168, 7161, p)  # TMA needs K % 8 == 0
 
 
+def test_warprow_plans_on_cpu(lib):
+    mk = lambda t, w, c: lib.make_plan("warprow", threads=t, rows_per_cta=w, stages=c)
+    assert lib.plan_check(1, 2112, 7168, mk(512, 2, 2)).grid == 304
+    assert lib.plan_check(1, 100, 7168, mk(512, 2, 2)).grid == 100  # never more CTAs than rows
+    for bad in (mk(128, 1, 1), mk(512, 3, 1), mk(1024, 1, 3), mk(512, 1, 5), mk(256, 1, 0)):
+        with pytest.raises(lib.BF16LinearError):
+            lib.plan_check(4, 2112, 7168, bad)
+    with pytest.raises(lib.BF16LinearError):
+        lib.plan_check(9, 2112, 7168, mk(512, 1, 1))   # at most 8 tokens
+    with pytest.raises(lib.BF16LinearError):
+        lib.plan_check(4, 2112, 7170, mk(512, 1, 1))   # 16-byte vectors need K % 8 == 0
+    with pytest.raises(lib.BF16LinearError):
+        lib.plan_check(8, 64, 16384, mk(512, 1, 1))    # x does not fit in shared memory
+
+
 def test_workspace_plans_on_cpu(lib):
     import ctypes
     p = lib.make_plan("splitk_ws", threads=128, rows_per_cta=64, tokens_per_cta=16, split_k=64, stages=2)
