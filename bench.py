@@ -101,7 +101,8 @@ def workload_desc(name):
 
 def kernel_source_hash(kernel_name):
     src = {"dotprod": ("dotprod.cuh", "dotprod.cu"), "splitk": ("splitk.cu",), "splitk_ws": ("splitk.cu",),
-           "tile": ("tile.cu",), "stream": ("stream.cu",), "tile2": ("tile2.cu",), "warprow": ("warprow.cu",)}[kernel_name]
+           "tile": ("tile.cu",), "stream": ("stream.cu",), "tile2": ("tile2.cu",), "warprow": ("warprow.cu",),
+           "warpmma": ("warpmma.cu",)}[kernel_name]
     h = hashlib.sha256()
     for f in src + ("common.cuh", "kernels.h"):
         h.update(open(os.path.join(ROOT, "moe_router_gemm_gb300", "csrc", f), "rb").read())
@@ -509,6 +510,15 @@ def candidate_plans(lib, M, N, K):
         for t, w, c in ((512, 1, 2), (512, 2, 2), (512, 4, 2), (1024, 1, 1), (1024, 2, 1), (1024, 4, 1),
                         (256, 1, 4), (256, 2, 4)):
             p = lib.make_plan("warprow", threads=t, rows_per_cta=w, stages=c)
+            try:
+                lib.plan_check(M, N, K, p)
+            except Exception:
+                continue
+            cands.append(p)
+    if K % 8 == 0 and M <= 16 and M * K * 2 <= 200 * 1024:
+        for t, w, c in ((512, 1, 2), (512, 2, 2), (512, 4, 2), (512, 8, 2), (1024, 1, 1), (1024, 4, 1),
+                        (1024, 8, 1), (1024, 16, 1), (256, 1, 4), (256, 2, 4), (256, 8, 4)):
+            p = lib.make_plan("warpmma", threads=t, rows_per_cta=w, stages=c)
             try:
                 lib.plan_check(M, N, K, p)
             except Exception:

@@ -72,8 +72,10 @@ typedef enum {
                                   a contiguous row range through a bulk-copy ring (large N: decode, MLP) */
     BF16L_KERNEL_TILE2 = 5,    /* persistent tcgen05 tile GEMM on CTA pairs (cta_group::2, clusters of 2):
                                   256 x 256 tiles, each CTA stages half of each operand; large M */
-    BF16L_KERNEL_WARPROW = 6   /* persistent CUDA-core kernel for M <= 8 and many rows: a group of 1, 2 or 4
+    BF16L_KERNEL_WARPROW = 6,  /* persistent CUDA-core kernel for M <= 8 and many rows: a group of 1, 2 or 4
                                   warps computes one W row at a time from 16-byte loads, x in shared memory */
+    BF16L_KERNEL_WARPMMA = 7   /* persistent kernel for M <= 16 and many rows: 16-byte weight loads feed the
+                                  warp-level tensor-core MMA (m16n8k16) directly; 8 W rows per group of warps */
 } bf16l_kernel;
 
 /*
@@ -87,12 +89,14 @@ typedef struct {
     int32_t threads;       /* threads per CTA */
     int32_t rows_per_cta;  /* W rows per CTA (DOTPROD 1/2/4; SPLITK 16..256, the MMA N); TILE: W rows per tile;
                               STREAM: W rows per ring stage (1, 2, or 4 when M <= 3);
-                              WARPROW: warps that share one row (1, 2 or 4) */
+                              WARPROW: warps that share one row (1, 2 or 4);
+                              WARPMMA: warps that share one group of 8 rows (1, 2, 4, 8 or 16) */
     int32_t tokens_per_cta;/* SPLITK: x rows loaded per chunk (M rounded up to 8, <= 64);  TILE: x rows per tile;
                               DOTPROD: tokens per CTA, 1..8 (0 = min(M, 8)); ceil(M / tokens) CTAs then share each
                               row slice, one token group each, instead of one CTA looping over the groups */
     int32_t split_k;       /* SPLITK: CTAs per cluster along K (1..16); SPLITK_WS: CTAs along K (1..64) */
-    int32_t stages;        /* SPLITK / TILE: shared-memory ring depth (64-wide K chunks); WARPROW: CTAs per SM */
+    int32_t stages;        /* SPLITK / TILE: shared-memory ring depth (64-wide K chunks);
+                              WARPROW / WARPMMA: CTAs per SM */
     int32_t grid;          /* CTAs launched (informational; computed by the plan) */
     int32_t flags;         /* BF16L_FLAG_* bits the launch uses */
 } bf16l_plan;

@@ -61,6 +61,7 @@ void init_device(DeviceState &s) {
         if (!e) e = init_stream();
         if (!e) e = init_tile2();
         if (!e) e = init_warprow();
+        if (!e) e = init_warpmma();
     }
     s.err = e;
 }
@@ -146,6 +147,7 @@ int run(const bf16l_call &c) {
         case BF16L_KERNEL_STREAM: e = launch_stream(a, p); break;
         case BF16L_KERNEL_TILE2: e = launch_tile2(a, p); break;
         case BF16L_KERNEL_WARPROW: e = launch_warprow(a, p); break;
+        case BF16L_KERNEL_WARPMMA: e = launch_warpmma(a, p); break;
         default: return BF16L_EINVAL;
     }
     if (e) {

@@ -69,6 +69,13 @@ constexpr int kWarpRowMaxSmem = 200 * 1024;
 int warprow_smem_bytes(int M, int K);
 int init_warprow();
 
+// Warp-level tensor-core kernel: M <= 16 tokens staged in shared memory,
+// 8 W rows per group of 1..16 warps.
+constexpr int kWarpMmaMaxTokens = 16;
+constexpr int kWarpMmaMaxSmem = 200 * 1024;
+int warpmma_smem_bytes(int M, int K);
+int init_warpmma();
+
 // Pair tile kernel (cta_group::2): 256 x rows x 256 W rows per cluster of 2,
 // 32 KB ring stages per CTA.
 constexpr int kTile2MinStages = 2;
@@ -107,6 +114,7 @@ int launch_tile(const LaunchArgs &a, const bf16l_plan &p);
 int launch_stream(const LaunchArgs &a, const bf16l_plan &p);
 int launch_tile2(const LaunchArgs &a, const bf16l_plan &p);
 int launch_warprow(const LaunchArgs &a, const bf16l_plan &p);
+int launch_warpmma(const LaunchArgs &a, const bf16l_plan &p);
 
 // One-time per-device kernel attribute setup (dynamic shared memory limits,
 // non-portable cluster sizes).  Returns a cudaError_t value.

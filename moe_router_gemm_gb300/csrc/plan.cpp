@@ -155,6 +155,22 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
             p->grid = M == 0 ? 0 : (int)(ctas < N ? ctas : N);
             return BF16L_OK;
         }
+        case BF16L_KERNEL_WARPMMA: {
+            if (K % 8 != 0 || M > kWarpMmaMaxTokens || warpmma_smem_bytes(M, K) > kWarpMmaMaxSmem)
+                return BF16L_EUNSUPPORTED;
+            const int t = p->threads, wpr = p->rows_per_cta, cps = p->stages;
+            if ((t != 256 && t != 512 && t != 1024) ||
+                (wpr != 1 && wpr != 2 && wpr != 4 && wpr != 8 && wpr != 16) || (t / 32) % wpr != 0)
+                return BF16L_EINVAL;
+            if (wpr > 1 && (t / 32) / wpr > 15) return BF16L_EINVAL;  // named barriers 1..15
+            const int static_smem = (wpr > 1 ? 32 * 32 * 4 * 4 : 512) + 1024;
+            if (cps < 1 || cps > 4 || t * cps > 1024 ||
+                cps * (warpmma_smem_bytes(M, K) + static_smem) > 232448)
+                return BF16L_EINVAL;
+            const int64_t ctas = (int64_t)dev.num_sms * cps, groups = ceil_div(N, 8);
+            p->grid = M == 0 ? 0 : (int)(ctas < groups ? ctas : groups);
+            return BF16L_OK;
+        }
         case BF16L_KERNEL_TILE2: {
             // A pair tile is 256 x rows x 256 W rows; threads and tile sizes are fixed.
             if (K % 8 != 0) return BF16L_EUNSUPPORTED;

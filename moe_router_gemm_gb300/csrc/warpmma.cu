@@ -1,0 +1,234 @@
+// warpmma.cu — persistent warp-level tensor-core kernel for M <= 16 tokens and
+// many W rows (decode projections, MLP weights).
+//
+// The warp-per-row kernel (warprow.cu) streams W at close to the copy
+// bandwidth, but its CUDA-core arithmetic (one fma per weight and token) costs
+// as much as the streaming once M reaches 4: a 30 MB weight (15 M elements)
+// times 8 tokens is 120 M fmas, about 3 us of issue on all 152 SMs.
+// This kernel keeps the same data movement — 16-byte weight loads straight into
+// registers from a full SM of warps, the fastest way found to stream such
+// weights here — and hands the arithmetic to the tensor cores with the
+// warp-level mma.sync.m16n8k16 (bf16 x bf16 -> fp32), whose B operand is the
+// very registers the loads filled.  (tcgen05.mma reads B only from shared
+// memory: using it would mean staging W through shared memory, with 2-D TMA
+// boxes that stream these weights measurably slower than 16-byte loads.)
+//
+//   * a group of WPR warps owns 8 consecutive W rows (the MMA N) at a time;
+//     each warp of the group takes a fixed K slice of whole 32-wide blocks;
+//   * per 32-wide K block, lane (g = lane / 4, t = lane % 4) loads the 16 bytes
+//     W[n0 + g][kb + 8t, kb + 8t + 8) and the same 16 bytes of x tokens g and
+//     g + 8 from shared memory.  The MMA's k index runs over a permutation of
+//     the block's 32 positions, the same for A and B, in two m16n8k16 steps;
+//   * tokens sit on the MMA M side (rows 0..15; rows past M are zero);
+//   * D lane (g, t) ends with out[token g (and g + 8)][rows n0 + 2t, n0 + 2t + 1];
+//     with WPR > 1 the group's warps are summed in order through shared memory;
+//   * x staged once per CTA by bulk copies (M * K * 2 bytes); the first weight
+//     batch is issued before the programmatic-launch wait.
+// The tensor core's internal summation order is fixed, so a plan is bitwise
+// reproducible.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bf16l {
+
+namespace {
+
+constexpr int kWmMaxWarps = 32;
+
+// D (16x8 fp32) += A (16x16 bf16, row-major) * B (16x8 bf16, column-major).
+// Fragments: lane (g, t): A {a0: row g, k 2t..2t+1; a1: row g+8, k 2t..; a2: row g,
+// k 2t+8..; a3: row g+8, k 2t+8..}; B {b0: k 2t..2t+1, col g; b1: k 2t+8.., col g};
+// D {d0: row g, col 2t; d1: row g, col 2t+1; d2, d3: row g+8}.
+__device__ __forceinline__ void mma_m16n8k16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+}  // namespace
+
+int warpmma_smem_bytes(int M, int K) { return M * K * 2; }
+
+// NT: block size the instance is compiled for (512 or 1024; a 256-thread block
+// runs the 512 instance); all keep 1024 threads per SM resident.  HI: M > 8
+// (tokens 8..15 in the MMA's upper rows).
+template <int WPR, int NT, bool HI, typename OutT>
+__global__ void __launch_bounds__(NT, 1024 / NT)
+    warpmma_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ W, const uint16_t *__restrict__ bias,
+                   OutT *__restrict__ out, int M, int N, int K, int32_t *status) {
+    constexpr int U = 8;                           // 32-wide K blocks per lane per batch
+    extern __shared__ uint4 xs[];                  // x[m][k] as 16-byte vectors, [M][K / 8]
+    __shared__ float part[WPR > 1 ? kWmMaxWarps : 1][32][4];  // WPR > 1: every lane's four sums
+    __shared__ __align__(8) uint64_t xbar;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int nw = (int)blockDim.x >> 5;
+    const int groups = nw / WPR;
+    const int grp = warp / WPR, gw = warp - grp * WPR;
+    const int nvec = K >> 3;
+    // this warp's K slice in 16-byte vectors, whole 32-wide blocks (4 vectors)
+    const int nblk = (nvec + 3) >> 2;
+    const int per = (nblk + WPR - 1) / WPR;
+    const int vb0 = 4 * gw * per;
+    const int vb1 = min(nvec, 4 * (gw + 1) * per);
+    // CTA b owns the 8-row groups [RG*b/G, RG*(b+1)/G)
+    const int RG = (N + 7) >> 3;
+    const int G = (int)gridDim.x, b = (int)blockIdx.x;
+    const int q0 = (int)(((long long)RG * b) / G), q1 = (int)(((long long)RG * (b + 1)) / G);
+    const bool tok_lo = g < M, tok_hi = HI && (g + 8 < M);
+
+    if (tid == 0) {
+        mbar_init(&xbar, 1);
+        fence_barrier_init();
+    }
+
+    uint4 wv[U];
+    auto load_batch = [&](int n0, int vb) {  // the batch of blocks starting at vector vb
+        const int row = n0 + g;
+        const uint4 *wr = reinterpret_cast<const uint4 *>(W + (size_t)(row < N ? row : N - 1) * K);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int vv = vb + 4 * u + t;
+            wv[u] = (vv < vb1 && row < N) ? ldg_stream_v4(wr + vv) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+    int q = q0 + grp;
+    if (q < q1) load_batch(8 * q, vb0);
+
+    pdl_launch_dependents();
+    pdl_wait();  // x may be written, and out still read, by the previous kernel
+    __syncthreads();
+    if (tid == 0 && q1 > q0) {
+        mbar_arrive_expect_tx(&xbar, (uint32_t)(M * K * 2));
+        for (int m = 0; m < M; ++m) bulk_load(xs + (size_t)m * nvec, x + (size_t)m * K, (uint32_t)(K * 2), &xbar);
+    }
+    const bool staged = q1 > q0 ? mbar_wait(&xbar, 0, status, kSiteStage) : true;
+    if (!__syncthreads_and(staged)) return;  // the whole CTA leaves together (only after a timeout)
+
+    const uint4 *xlo = xs + (size_t)(tok_lo ? g : 0) * nvec;
+    const uint4 *xhi = xs + (size_t)(tok_hi ? g + 8 : 0) * nvec;
+    for (bool first = true; q < q1; q += groups, first = false) {
+        const int n0 = 8 * q;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int vb = vb0; vb < vb1; vb += 4 * U) {  // warp-uniform trip count: mma.sync is warp-wide
+            if (!(first && vb == vb0)) load_batch(n0, vb);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int vv = vb + 4 * u + t;
+                const bool in = vv < vb1;
+                const uint4 lo = (tok_lo && in) ? xlo[vv] : make_uint4(0u, 0u, 0u, 0u);
+                uint4 hi = make_uint4(0u, 0u, 0u, 0u);
+                if constexpr (HI) {
+                    if (tok_hi && in) hi = xhi[vv];
+                }
+                // this lane's block positions 8t..8t+7: step 0 takes +0..3, step 1 takes +4..7
+                mma_m16n8k16(d, lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
+                mma_m16n8k16(d, lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
+            }
+        }
+        if constexpr (WPR > 1) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) part[warp][lane][j] = d[j];
+            asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(WPR * 32) : "memory");
+            if (gw == 0) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float s = 0.f;
+                    for (int w = 0; w < WPR; ++w) s += part[grp * WPR + w][lane][j];
+                    d[j] = s;
+                }
+            }
+        }
+        if (WPR == 1 || gw == 0) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int m = g + (j >> 1) * 8, n = n0 + 2 * t + (j & 1);
+                if (m < M && n < N) {
+                    float s = d[j];
+                    if (bias) s += bf16_to_f32(bias[n]);
+                    OutStore<OutT>::one(out + (size_t)m * N + n, s);
+                }
+            }
+        }
+        if constexpr (WPR > 1) asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(WPR * 32) : "memory");
+    }
+}
+
+namespace {
+
+template <typename OutT>
+using WmFn = void (*)(const uint16_t *, const uint16_t *, const uint16_t *, OutT *, int, int, int, int32_t *);
+
+template <int WPR, bool HI, typename OutT>
+WmFn<OutT> pick_nt(int threads) {
+    return threads > 512 ? warpmma_kernel<WPR, 1024, HI, OutT> : warpmma_kernel<WPR, 512, HI, OutT>;
+}
+
+template <bool HI, typename OutT>
+WmFn<OutT> pick_wpr(int wpr, int threads) {
+    switch (wpr) {
+        case 1: return pick_nt<1, HI, OutT>(threads);
+        case 2: return pick_nt<2, HI, OutT>(threads);
+        case 4: return pick_nt<4, HI, OutT>(threads);
+        case 8: return pick_nt<8, HI, OutT>(threads);
+        case 16: return pick_nt<16, HI, OutT>(threads);
+        default: return nullptr;
+    }
+}
+
+template <typename OutT>
+WmFn<OutT> pick_wm(int M, int wpr, int threads) {
+    return M > 8 ? pick_wpr<true, OutT>(wpr, threads) : pick_wpr<false, OutT>(wpr, threads);
+}
+
+template <typename OutT>
+int set_wm_attrs() {
+    for (int M : {8, 16})
+        for (int wpr : {1, 2, 4, 8, 16})
+            for (int t : {512, 1024}) {
+                const int e = (int)cudaFuncSetAttribute(pick_wm<OutT>(M, wpr, t),
+                                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                        kWarpMmaMaxSmem);
+                if (e) return e;
+            }
+    return 0;
+}
+
+template <typename OutT>
+int launch_wm_t(const LaunchArgs &a, const bf16l_plan &p) {
+    WmFn<OutT> fn = pick_wm<OutT>(a.M, p.rows_per_cta, p.threads);
+    if (!fn) return (int)cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.grid);
+    cfg.blockDim = dim3((unsigned)p.threads);
+    cfg.dynamicSmemBytes = (size_t)warpmma_smem_bytes(a.M, a.K);
+    cfg.stream = (cudaStream_t)a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = (p.flags & BF16L_FLAG_PDL) ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return (int)cudaLaunchKernelEx(&cfg, fn, static_cast<const uint16_t *>(a.x), static_cast<const uint16_t *>(a.W),
+                                   static_cast<const uint16_t *>(a.bias), static_cast<OutT *>(a.out), a.M, a.N, a.K,
+                                   a.status);
+}
+
+}  // namespace
+
+int init_warpmma() {
+    int e = set_wm_attrs<uint16_t>();
+    if (!e) e = set_wm_attrs<float>();
+    return e;
+}
+
+int launch_warpmma(const LaunchArgs &a, const bf16l_plan &p) {
+    return a.out_f32 ? launch_wm_t<float>(a, p) : launch_wm_t<uint16_t>(a, p);
+}
+
+}  // namespace bf16l

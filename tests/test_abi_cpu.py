@@ -202,6 +202,19 @@ def test_warprow_plans_on_cpu(lib):
         lib.plan_check(8, 64, 16384, mk(512, 1, 1))    # x does not fit in shared memory
 
 
+def test_warpmma_plans_on_cpu(lib):
+    mk = lambda t, w, c: lib.make_plan("warpmma", threads=t, rows_per_cta=w, stages=c)
+    assert lib.plan_check(16, 14336, 4096, mk(1024, 4, 1)).grid == 152
+    assert lib.plan_check(4, 2112, 7168, mk(512, 4, 2)).grid == 264  # 264 groups of 8 rows < 304 CTAs
+    for bad in (mk(512, 3, 1), mk(256, 16, 1), mk(1024, 2, 1), mk(1024, 1, 2), mk(512, 1, 0), mk(128, 1, 1)):
+        with pytest.raises(lib.BF16LinearError):
+            lib.plan_check(4, 2112, 7168, bad)
+    with pytest.raises(lib.BF16LinearError):
+        lib.plan_check(17, 2112, 4096, mk(512, 1, 1))   # at most 16 tokens
+    with pytest.raises(lib.BF16LinearError):
+        lib.plan_check(16, 2112, 7168, mk(512, 1, 1))   # x (229 KB) does not fit in shared memory
+
+
 def test_workspace_plans_on_cpu(lib):
     import ctypes
     p = lib.make_plan("splitk_ws", threads=128, rows_per_cta=64, tokens_per_cta=16, split_k=64, stages=2)
