@@ -102,7 +102,7 @@ def workload_desc(name):
 def kernel_source_hash(kernel_name):
     src = {"dotprod": ("dotprod.cuh", "dotprod.cu"), "splitk": ("splitk.cu",), "splitk_ws": ("splitk.cu",),
            "tile": ("tile.cu",), "stream": ("stream.cu",), "tile2": ("tile2.cu",), "warprow": ("warprow.cu",),
-           "warpmma": ("warpmma.cu",)}[kernel_name]
+           "warpmma": ("warpmma.cu",), "dotmma": ("dotmma.cu",)}[kernel_name]
     h = hashlib.sha256()
     for f in src + ("common.cuh", "kernels.h"):
         h.update(open(os.path.join(ROOT, "moe_router_gemm_gb300", "csrc", f), "rb").read())
@@ -524,6 +524,15 @@ def candidate_plans(lib, M, N, K):
             except Exception:
                 continue
             cands.append(p)
+    if K % 8 == 0 and M <= 16 and N <= 1024:
+        for S in (1, 2, 4, 8):
+            for t in (128, 256):
+                p = lib.make_plan("dotmma", threads=t, rows_per_cta=8, split_k=S)
+                try:
+                    lib.plan_check(M, N, K, p)
+                except Exception:
+                    continue
+                cands.append(p)
     if K % 8 == 0 and M > 64:
         for st in (6, 5, 4):
             cands.append(lib.make_plan("tile2", threads=192, rows_per_cta=256, tokens_per_cta=256, stages=st))

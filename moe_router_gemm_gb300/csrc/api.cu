@@ -62,6 +62,7 @@ void init_device(DeviceState &s) {
         if (!e) e = init_tile2();
         if (!e) e = init_warprow();
         if (!e) e = init_warpmma();
+        if (!e) e = init_dotmma();
     }
     s.err = e;
 }
@@ -148,6 +149,7 @@ int run(const bf16l_call &c) {
         case BF16L_KERNEL_TILE2: e = launch_tile2(a, p); break;
         case BF16L_KERNEL_WARPROW: e = launch_warprow(a, p); break;
         case BF16L_KERNEL_WARPMMA: e = launch_warpmma(a, p); break;
+        case BF16L_KERNEL_DOTMMA: e = launch_dotmma(a, p); break;
         default: return BF16L_EINVAL;
     }
     if (e) {

@@ -1,0 +1,242 @@
+// dotmma.cu — router-sized N with up to 16 tokens: 8 W rows per CTA, K split
+// over a cluster of S CTAs, warp-level tensor-core MMAs fed by 16-byte loads.
+//
+// Prior art: the cluster split-K router kernel on the vLLM PR #42562 page
+// ("实现拆解" items 2-3): K split over the CTAs of a cluster, fp32 partials
+// summed by one CTA through distributed shared memory, for 4 < M <= 64.
+//
+// For M = 9..16 on router weights (N = 128..384 rows, 1-6 MB) the dot-product
+// kernel does M fmas per weight element on CUDA cores and the tcgen05 split-K
+// kernel pays TMEM allocation, tensor-map fetches and a 64-row MMA for <= 16
+// tokens.  This kernel keeps the split-K shape and takes the arithmetic from the
+// warp-MMA kernel: lane (g, t) of a warp loads the 16 bytes
+// W[n0 + g][kb + 8t, +8) of each 32-wide K block — its B fragment for two
+// mma.sync.m16n8k16 steps under a permutation of the block's k positions — and
+// the same 16 bytes of tokens g and g + 8 from shared memory as its A fragment.
+//   * grid (S, ceil(N / 8)); CTA (r, q) owns rows 8q..8q+7 and the r-th of S
+//     equal runs of 32-wide K blocks; its warps split that run;
+//   * x: each CTA stages only its K slice of the M token rows (bulk copies);
+//     the weight loads of the first batch go out before that and before the
+//     programmatic-launch wait;
+//   * warps' partial tiles summed in warp order in shared memory; ranks 1..S-1
+//     send theirs (a 16 x 8 fp32 tile, 512 bytes) to rank 0 with st.async, counted on
+//     rank 0's mbarrier; rank 0 sums in rank order, adds bias, rounds, stores.
+// Two cluster barrier phases (non-.aligned): "receive barrier initialised"
+// (arrived at start, waited before sending) and "all received" (before exit).
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bf16l {
+
+namespace {
+
+constexpr int kDmWarps = 8;  // at most 256 threads
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// K blocks (of 4 16-byte vectors = 32 elements) of CTA rank r out of S.
+__host__ __device__ inline int dm_blk(int nblk, int r, int S) { return (int)(((long long)nblk * r) / S); }
+
+}  // namespace
+
+// Dynamic shared memory: x slice [M][vectors of the largest slice] as 16-byte vectors.
+int dotmma_smem_bytes(int M, int K, int S) {
+    const int nvec = K / 8, nblk = (nvec + 3) / 4;
+    int most = 0;
+    for (int r = 0; r < S; ++r) {
+        const int v0 = 4 * dm_blk(nblk, r, S);
+        const int v1 = 4 * dm_blk(nblk, r + 1, S) < nvec ? 4 * dm_blk(nblk, r + 1, S) : nvec;
+        if (v1 - v0 > most) most = v1 - v0;
+    }
+    return M * most * 16;
+}
+
+template <bool HI, typename OutT>
+__global__ void __launch_bounds__(kDmWarps * 32)
+    dotmma_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ W, const uint16_t *__restrict__ bias,
+                  OutT *__restrict__ out, int M, int N, int K, int S, int32_t *status) {
+    constexpr int U = 8;  // 32-wide K blocks per lane per batch
+    extern __shared__ uint4 xs[];
+    __shared__ float4 part[kDmWarps][32];  // per warp, lane (g, t): tokens g, g+8 x rows 2t, 2t+1
+    __shared__ float4 recv[kDotMmaMaxCluster][32];
+    __shared__ __align__(8) uint64_t xbar, rbar;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int nw = (int)blockDim.x >> 5;
+    const int rank = S > 1 ? (int)cluster_ctarank() : 0;
+    const int n0 = 8 * (int)blockIdx.y;
+    const int nvec = K >> 3, nblk = (nvec + 3) >> 2;
+    // this CTA's vectors [cv0, cv1) and this warp's blocks
+    const int cb0 = dm_blk(nblk, rank, S), cb1 = dm_blk(nblk, rank + 1, S);
+    const int cv0 = 4 * cb0, cv1 = min(nvec, 4 * cb1);
+    const int wb0 = cb0 + (int)(((long long)(cb1 - cb0) * warp) / nw);
+    const int wb1 = cb0 + (int)(((long long)(cb1 - cb0) * (warp + 1)) / nw);
+    const int wv0 = 4 * wb0, wv1 = min(cv1, 4 * wb1);
+    const int sv = cv1 - cv0;  // vectors in this CTA's x slice
+    const bool tok_lo = g < M, tok_hi = HI && (g + 8 < M);
+    const int row = n0 + g;
+    const uint4 *wr = reinterpret_cast<const uint4 *>(W + (size_t)(row < N ? row : N - 1) * K);
+
+    if (tid == 0) {
+        mbar_init(&xbar, 1);
+        mbar_init(&rbar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (S > 1) cluster_arrive_relaxed();  // phase 1: "my receive barrier is initialised"
+
+    uint4 wv[U];
+    auto load_batch = [&](int vb) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int vv = vb + 4 * u + t;
+            wv[u] = (vv < wv1 && row < N) ? ldg_stream_v4(wr + vv) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+    load_batch(wv0);  // in flight before anything waits
+
+    pdl_launch_dependents();
+    pdl_wait();  // x may be written, and out still read, by the previous kernel
+    if (tid == 0 && sv > 0) {
+        mbar_arrive_expect_tx(&xbar, (uint32_t)(M * sv * 16));
+        for (int m = 0; m < M; ++m)
+            bulk_load(xs + (size_t)m * sv, x + (size_t)m * K + (size_t)cv0 * 8, (uint32_t)(sv * 16), &xbar);
+    }
+    const bool staged = sv > 0 ? mbar_wait(&xbar, 0, status, kSiteStage) : true;
+    const bool ok = __syncthreads_and(staged) != 0;
+
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    if (ok) {
+        const uint4 *xlo = xs + (size_t)(tok_lo ? g : 0) * sv;  // indexed by vector - cv0
+        const uint4 *xhi = xs + (size_t)(tok_hi ? g + 8 : 0) * sv;
+        for (int vb = wv0; vb < wv1; vb += 4 * U) {  // warp-uniform trip count: mma.sync is warp-wide
+            if (vb != wv0) load_batch(vb);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int vv = vb + 4 * u + t;
+                const bool in = vv < wv1;
+                const uint4 lo = (tok_lo && in) ? xlo[vv - cv0] : make_uint4(0u, 0u, 0u, 0u);
+                uint4 hi = make_uint4(0u, 0u, 0u, 0u);
+                if constexpr (HI) {
+                    if (tok_hi && in) hi = xhi[vv - cv0];
+                }
+                mma16816(d, lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
+                mma16816(d, lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
+            }
+        }
+    }
+    part[warp][lane] = make_float4(d[0], d[1], d[2], d[3]);
+    __syncthreads();
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (warp == 0) {
+        for (int w = 0; w < nw; ++w) {  // warps in order
+            const float4 p = part[w][lane];
+            s.x += p.x;
+            s.y += p.y;
+            s.z += p.z;
+            s.w += p.w;
+        }
+    }
+
+    bool have = ok;
+    if (S > 1) {
+        cluster_wait_acquire();  // phase 1 done: rank 0's receive barrier exists
+        if (rank != 0) {
+            if (warp == 0)
+                st_async_f4(mapa_shared(smem_u32(&recv[rank][lane]), 0), s.x, s.y, s.z, s.w,
+                            mapa_shared(smem_u32(&rbar), 0));
+        } else {
+            if (tid == 0) mbar_arrive_expect_tx(&rbar, (uint32_t)((S - 1) * 32 * 16));
+            if (warp == 0) {
+                have = mbar_wait_cluster(&rbar, 0, status, kSiteRecv) && have;
+                for (int r = 1; r < S; ++r) {  // ranks in order
+                    const float4 p = recv[r][lane];
+                    s.x += p.x;
+                    s.y += p.y;
+                    s.z += p.z;
+                    s.w += p.w;
+                }
+            }
+        }
+        cluster_arrive_relaxed();  // phase 2: everything this CTA sends or receives has landed (rank 0)
+    }
+    if (rank == 0 && warp == 0 && have) {
+        const float v[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int m = g + (j >> 1) * 8, n = n0 + 2 * t + (j & 1);
+            if (m < M && n < N) {
+                float r = v[j];
+                if (bias) r += bf16_to_f32(bias[n]);
+                OutStore<OutT>::one(out + (size_t)m * N + n, r);
+            }
+        }
+    }
+    if (S > 1) cluster_wait_acquire();  // phase 2 done: rank 0 holds every partial; all may exit
+}
+
+namespace {
+
+template <typename OutT>
+using DmFn = void (*)(const uint16_t *, const uint16_t *, const uint16_t *, OutT *, int, int, int, int, int32_t *);
+
+template <typename OutT>
+DmFn<OutT> pick_dm(int M) {
+    return M > 8 ? dotmma_kernel<true, OutT> : dotmma_kernel<false, OutT>;
+}
+
+template <typename OutT>
+int set_dm_attrs() {
+    for (int M : {8, 16}) {
+        int e = (int)cudaFuncSetAttribute(pick_dm<OutT>(M), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          kDotMmaMaxSmem);
+        if (e) return e;
+    }
+    return 0;
+}
+
+template <typename OutT>
+int launch_dm_t(const LaunchArgs &a, const bf16l_plan &p) {
+    const int S = p.split_k;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)S, (unsigned)((a.N + 7) / 8));
+    cfg.blockDim = dim3((unsigned)p.threads);
+    cfg.dynamicSmemBytes = (size_t)dotmma_smem_bytes(a.M, a.K, S);
+    cfg.stream = (cudaStream_t)a.stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = (p.flags & BF16L_FLAG_PDL) ? 1 : 0;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)S;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = S > 1 ? 2 : 1;
+    return (int)cudaLaunchKernelEx(&cfg, pick_dm<OutT>(a.M), static_cast<const uint16_t *>(a.x),
+                                   static_cast<const uint16_t *>(a.W), static_cast<const uint16_t *>(a.bias),
+                                   static_cast<OutT *>(a.out), a.M, a.N, a.K, S, a.status);
+}
+
+}  // namespace
+
+int init_dotmma() {
+    int e = set_dm_attrs<uint16_t>();
+    if (!e) e = set_dm_attrs<float>();
+    return e;
+}
+
+int launch_dotmma(const LaunchArgs &a, const bf16l_plan &p) {
+    return a.out_f32 ? launch_dm_t<float>(a, p) : launch_dm_t<uint16_t>(a, p);
+}
+
+}  // namespace bf16l

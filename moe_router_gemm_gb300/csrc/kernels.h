@@ -76,6 +76,14 @@ constexpr int kWarpMmaMaxSmem = 200 * 1024;
 int warpmma_smem_bytes(int M, int K);
 int init_warpmma();
 
+// Router split-K on warp-level MMAs: 8 W rows per CTA, K over a cluster of
+// 1, 2, 4 or 8 CTAs, M <= 16, each CTA stages its K slice of x.
+constexpr int kDotMmaMaxTokens = 16;
+constexpr int kDotMmaMaxCluster = 8;
+constexpr int kDotMmaMaxSmem = 200 * 1024;
+int dotmma_smem_bytes(int M, int K, int S);
+int init_dotmma();
+
 // Pair tile kernel (cta_group::2): 256 x rows x 256 W rows per cluster of 2,
 // 32 KB ring stages per CTA.
 constexpr int kTile2MinStages = 2;
@@ -115,6 +123,7 @@ int launch_stream(const LaunchArgs &a, const bf16l_plan &p);
 int launch_tile2(const LaunchArgs &a, const bf16l_plan &p);
 int launch_warprow(const LaunchArgs &a, const bf16l_plan &p);
 int launch_warpmma(const LaunchArgs &a, const bf16l_plan &p);
+int launch_dotmma(const LaunchArgs &a, const bf16l_plan &p);
 
 // One-time per-device kernel attribute setup (dynamic shared memory limits,
 // non-portable cluster sizes).  Returns a cudaError_t value.

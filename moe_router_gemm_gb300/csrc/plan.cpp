@@ -171,6 +171,16 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
             p->grid = M == 0 ? 0 : (int)(ctas < groups ? ctas : groups);
             return BF16L_OK;
         }
+        case BF16L_KERNEL_DOTMMA: {
+            if (K % 8 != 0 || M > kDotMmaMaxTokens) return BF16L_EUNSUPPORTED;
+            const int S = p->split_k;
+            if ((p->threads != 128 && p->threads != 256) || p->rows_per_cta != 8 ||
+                (S != 1 && S != 2 && S != 4 && S != 8) || S > ceil_div(K / 8, 4))
+                return BF16L_EINVAL;
+            if (dotmma_smem_bytes(M, K, S) > kDotMmaMaxSmem) return BF16L_EUNSUPPORTED;
+            p->grid = M == 0 ? 0 : S * ceil_div(N, 8);
+            return BF16L_OK;
+        }
         case BF16L_KERNEL_TILE2: {
             // A pair tile is 256 x rows x 256 W rows; threads and tile sizes are fixed.
             if (K % 8 != 0) return BF16L_EUNSUPPORTED;

@@ -215,6 +215,21 @@ def test_warpmma_plans_on_cpu(lib):
         lib.plan_check(16, 2112, 7168, mk(512, 1, 1))   # x (229 KB) does not fit in shared memory
 
 
+def test_dotmma_plans_on_cpu(lib):
+    mk = lambda t, S: lib.make_plan("dotmma", threads=t, rows_per_cta=8, split_k=S)
+    assert lib.plan_check(16, 384, 7168, mk(256, 4)).grid == 4 * 48
+    assert lib.plan_check(3, 7, 4096, mk(128, 8)).grid == 8
+    for bad in (mk(512, 4), mk(256, 3), mk(256, 16), lib.make_plan("dotmma", threads=256, rows_per_cta=16, split_k=2)):
+        with pytest.raises(lib.BF16LinearError):
+            lib.plan_check(16, 384, 7168, bad)
+    with pytest.raises(lib.BF16LinearError):
+        lib.plan_check(16, 384, 7168, mk(256, 1))   # x (229 KB) does not fit one CTA
+    with pytest.raises(lib.BF16LinearError):
+        lib.plan_check(17, 384, 4096, mk(256, 4))   # at most 16 tokens
+    with pytest.raises(lib.BF16LinearError):
+        lib.plan_check(4, 384, 40, mk(256, 4))      # two 32-wide K blocks cannot feed 4 CTAs
+
+
 def test_workspace_plans_on_cpu(lib):
     import ctypes
     p = lib.make_plan("splitk_ws", threads=128, rows_per_cta=64, tokens_per_cta=16, split_k=64, stages=2)

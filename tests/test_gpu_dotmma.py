@@ -1,0 +1,104 @@
+"""GPU parity of the router split-K kernel on warp-level MMAs (BF16L_KERNEL_DOTMMA).
+
+CTA (r, q) of a cluster of S computes rows 8q..8q+7 over the r-th K run with
+mma.sync fed by 16-byte loads; rank 0 sums the S partial tiles received over
+DSMEM.  The cases cover S = 1, 2, 4, 8 and both block sizes, M = 1..16 (tokens
+8..15 in the MMA's upper rows), N not a multiple of 8, K tails inside a 32-wide
+block, K runs too short to give every warp a block, bias on and off, the router
+shapes, and the fp32 epilogue (which must round to the bf16 result of the same
+plan bit for bit).  Results for one plan are bitwise reproducible.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from tolerance import check_close, tensor_bits
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+SHAPES = [(16, 384, 7168), (9, 256, 4096), (13, 128, 2880), (4, 300, 1032), (1, 7, 136), (16, 20, 40),
+          (11, 257, 6144)]
+
+
+def _smem(M, K, S):
+    nvec = K // 8
+    nblk = -(-nvec // 4)
+    most = max(min(nvec, 4 * (nblk * (r + 1) // S)) - 4 * (nblk * r // S) for r in range(S))
+    return M * most * 16
+
+
+def _plan(lib, S, threads=256):
+    return lib.make_plan("dotmma", threads=threads, rows_per_cta=8, split_k=S)
+
+
+def _run(lib, x, W, b, plan, f32=False):
+    xd, Wd = x.to(DEV), W.to(DEV)
+    bd = b.to(DEV) if b is not None else None
+    out = (lib.bf16_linear_f32out(xd, Wd, bd, plan_=plan) if f32
+           else lib.bf16_linear_with_plan(xd, Wd, bd, plan_=plan))
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("threads", [128, 256])
+@pytest.mark.parametrize("S", [1, 2, 4, 8])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_dotmma_forced(lib, shape, S, threads):
+    M, N, K = shape
+    p = _plan(lib, S, threads)
+    if S > -(-(K // 8) // 4) or _smem(M, K, S) > 200 * 1024:  # too few K blocks, or x slice too big
+        with pytest.raises(lib.BF16LinearError):
+            lib.plan_check(M, N, K, p)
+        return
+    for bias in (False, True):
+        x, W, b = wl.make_inputs(M, N, K, M + N + K + S, bias)
+        got = tensor_bits(_run(lib, x, W, b, p))
+        want = oracle.linear_bf16(wl.bits(x), wl.bits(W), wl.bits(b))
+        check_close(got, want, f"dotmma M={M} N={N} K={K} S={S} threads={threads} bias={bias}")
+
+
+@pytest.mark.parametrize("M", range(1, 17))
+def test_dotmma_router_tokens(lib, M):
+    x, W, b = wl.make_inputs(M, 256, 7168, 100 + M, False)
+    got = tensor_bits(_run(lib, x, W, b, _plan(lib, 4)))
+    check_close(got, oracle.linear_bf16(wl.bits(x), wl.bits(W), None), f"dotmma router M={M}")
+
+
+def test_dotmma_deterministic_and_f32(lib):
+    M, N, K = 14, 384, 7168
+    x, W, b = wl.make_inputs(M, N, K, 2, True)
+    p = _plan(lib, 8)
+    a = tensor_bits(_run(lib, x, W, b, p))
+    assert np.array_equal(a, tensor_bits(_run(lib, x, W, b, p)))
+    f = _run(lib, x, W, b, p, f32=True)
+    assert np.array_equal(tensor_bits(f.to(torch.bfloat16)), a)
+    assert lib.device_status() == 0
+
+
+def test_dotmma_exact_cases(lib):
+    M, N, K = 16, 260, 2048
+    _, W, b = wl.make_inputs(M, N, K, 3, True)
+    ks = np.random.default_rng(5).integers(0, K, M)
+    x = torch.zeros(M, K, dtype=torch.bfloat16)
+    x[torch.arange(M), torch.from_numpy(ks)] = 1.0
+    p = _plan(lib, 4)
+    assert torch.equal(_run(lib, x, W, None, p).cpu(), W[:, torch.from_numpy(ks)].T.contiguous())
+    assert torch.equal(_run(lib, torch.zeros_like(x), W, b, p).cpu(), b.expand(M, N))
+    ones = _run(lib, torch.ones(M, K, dtype=torch.bfloat16), torch.ones(N, K, dtype=torch.bfloat16), None, p)
+    assert (ones.cpu().float() == float(K)).all()
+
+
+def test_dotmma_pdl_matches(lib):
+    M, N, K = 12, 256, 6144
+    x, W, b = wl.make_inputs(M, N, K, 9, False)
+    p = _plan(lib, 4)
+    ref = tensor_bits(_run(lib, x, W, None, p))
+    p.flags = lib.FLAG_PDL
+    xd, Wd = x.to(DEV), W.to(DEV)
+    outs = [lib.bf16_linear_with_plan(xd, Wd, None, plan_=p) for _ in range(3)]
+    torch.cuda.synchronize()
+    for o in outs:
+        assert np.array_equal(tensor_bits(o), ref)
