@@ -28,6 +28,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import itertools
 import json
 import os
 import statistics
@@ -525,9 +526,9 @@ def candidate_plans(lib, M, N, K):
                 continue
             cands.append(p)
     if K % 8 == 0 and M <= 16 and N <= 1024:
-        for S in (1, 2, 4, 8):
-            for t in (128, 256):
-                p = lib.make_plan("dotmma", threads=t, rows_per_cta=8, split_k=S)
+        for S, t, xr in itertools.product((2, 4, 8, 16), (128, 256), (0, 1)):
+            if True:
+                p = lib.make_plan("dotmma", threads=t, rows_per_cta=8, split_k=S, stages=xr)
                 try:
                     lib.plan_check(M, N, K, p)
                 except Exception:

@@ -76,7 +76,7 @@ typedef enum {
                                   warps computes one W row at a time from 16-byte loads, x in shared memory */
     BF16L_KERNEL_WARPMMA = 7,  /* persistent kernel for M <= 16 and many rows: 16-byte weight loads feed the
                                   warp-level tensor-core MMA (m16n8k16) directly; 8 W rows per group of warps */
-    BF16L_KERNEL_DOTMMA = 8    /* router-sized N, M <= 16: 8 W rows per CTA, K split over a cluster of 1..8 CTAs,
+    BF16L_KERNEL_DOTMMA = 8    /* router-sized N, M <= 16: 8 W rows per CTA, K split over a cluster of 1..16 CTAs,
                                   16-byte loads feed m16n8k16 MMAs, partials summed by rank 0 over DSMEM */
 } bf16l_kernel;
 
@@ -97,9 +97,10 @@ typedef struct {
                               DOTPROD: tokens per CTA, 1..8 (0 = min(M, 8)); ceil(M / tokens) CTAs then share each
                               row slice, one token group each, instead of one CTA looping over the groups */
     int32_t split_k;       /* SPLITK: CTAs per cluster along K (1..16); SPLITK_WS: CTAs along K (1..64);
-                              DOTMMA: CTAs per cluster along K (1, 2, 4 or 8) */
+                              DOTMMA: CTAs per cluster along K (1, 2, 4, 8 or 16) */
     int32_t stages;        /* SPLITK / TILE: shared-memory ring depth (64-wide K chunks);
-                              WARPROW / WARPMMA: CTAs per SM */
+                              WARPROW / WARPMMA: CTAs per SM; DOTMMA: 1 = x fragments loaded from global
+                              memory into registers, 0 = each CTA's x slice staged in shared memory */
     int32_t grid;          /* CTAs launched (informational; computed by the plan) */
     int32_t flags;         /* BF16L_FLAG_* bits the launch uses */
 } bf16l_plan;

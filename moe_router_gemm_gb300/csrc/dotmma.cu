@@ -15,7 +15,8 @@
 // the same 16 bytes of tokens g and g + 8 from shared memory as its A fragment.
 //   * grid (S, ceil(N / 8)); CTA (r, q) owns rows 8q..8q+7 and the r-th of S
 //     equal runs of 32-wide K blocks; its warps split that run;
-//   * x: each CTA stages only its K slice of the M token rows (bulk copies);
+//   * x: each CTA stages only its K slice of the M token rows (bulk copies),
+//     or (XR) each lane loads its x fragments from L2 next to its weights;
 //     the weight loads of the first batch go out before that and before the
 //     programmatic-launch wait;
 //   * warps' partial tiles summed in warp order in shared memory; ranks 1..S-1
@@ -60,7 +61,10 @@ int dotmma_smem_bytes(int M, int K, int S) {
     return M * most * 16;
 }
 
-template <bool HI, typename OutT>
+// HI: M > 8 (tokens 8..15 on the MMA's upper rows).  XR: x fragments loaded
+// from global memory (L2) straight into registers next to the weights, instead
+// of a bulk copy of the CTA's x slice into shared memory.
+template <bool HI, bool XR, typename OutT>
 __global__ void __launch_bounds__(kDmWarps * 32)
     dotmma_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ W, const uint16_t *__restrict__ bias,
                   OutT *__restrict__ out, int M, int N, int K, int S, int32_t *status) {
@@ -107,28 +111,48 @@ __global__ void __launch_bounds__(kDmWarps * 32)
 
     pdl_launch_dependents();
     pdl_wait();  // x may be written, and out still read, by the previous kernel
-    if (tid == 0 && sv > 0) {
-        mbar_arrive_expect_tx(&xbar, (uint32_t)(M * sv * 16));
-        for (int m = 0; m < M; ++m)
-            bulk_load(xs + (size_t)m * sv, x + (size_t)m * K + (size_t)cv0 * 8, (uint32_t)(sv * 16), &xbar);
+    bool ok = true;
+    if constexpr (!XR) {
+        if (tid == 0 && sv > 0) {
+            mbar_arrive_expect_tx(&xbar, (uint32_t)(M * sv * 16));
+            for (int m = 0; m < M; ++m)
+                bulk_load(xs + (size_t)m * sv, x + (size_t)m * K + (size_t)cv0 * 8, (uint32_t)(sv * 16), &xbar);
+        }
+        const bool staged = sv > 0 ? mbar_wait(&xbar, 0, status, kSiteStage) : true;
+        ok = __syncthreads_and(staged) != 0;
     }
-    const bool staged = sv > 0 ? mbar_wait(&xbar, 0, status, kSiteStage) : true;
-    const bool ok = __syncthreads_and(staged) != 0;
 
     float d[4] = {0.f, 0.f, 0.f, 0.f};
     if (ok) {
         const uint4 *xlo = xs + (size_t)(tok_lo ? g : 0) * sv;  // indexed by vector - cv0
         const uint4 *xhi = xs + (size_t)(tok_hi ? g + 8 : 0) * sv;
+        const uint4 *glo = reinterpret_cast<const uint4 *>(x + (size_t)(tok_lo ? g : 0) * K);
+        const uint4 *ghi = reinterpret_cast<const uint4 *>(x + (size_t)(tok_hi ? g + 8 : 0) * K);
         for (int vb = wv0; vb < wv1; vb += 4 * U) {  // warp-uniform trip count: mma.sync is warp-wide
             if (vb != wv0) load_batch(vb);
+            uint4 xl[U], xh[U];
+            if constexpr (XR) {  // this batch's x fragments, in flight together
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int vv = vb + 4 * u + t;
+                    const bool in = vv < wv1;
+                    xl[u] = (tok_lo && in) ? __ldg(glo + vv) : make_uint4(0u, 0u, 0u, 0u);
+                    xh[u] = (HI && tok_hi && in) ? __ldg(ghi + vv) : make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int vv = vb + 4 * u + t;
                 const bool in = vv < wv1;
-                const uint4 lo = (tok_lo && in) ? xlo[vv - cv0] : make_uint4(0u, 0u, 0u, 0u);
-                uint4 hi = make_uint4(0u, 0u, 0u, 0u);
-                if constexpr (HI) {
-                    if (tok_hi && in) hi = xhi[vv - cv0];
+                uint4 lo, hi = make_uint4(0u, 0u, 0u, 0u);
+                if constexpr (XR) {
+                    lo = xl[u];
+                    hi = xh[u];
+                } else {
+                    lo = (tok_lo && in) ? xlo[vv - cv0] : make_uint4(0u, 0u, 0u, 0u);
+                    if constexpr (HI) {
+                        if (tok_hi && in) hi = xhi[vv - cv0];
+                    }
                 }
                 mma16816(d, lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
                 mma16816(d, lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
@@ -191,17 +215,20 @@ template <typename OutT>
 using DmFn = void (*)(const uint16_t *, const uint16_t *, const uint16_t *, OutT *, int, int, int, int, int32_t *);
 
 template <typename OutT>
-DmFn<OutT> pick_dm(int M) {
-    return M > 8 ? dotmma_kernel<true, OutT> : dotmma_kernel<false, OutT>;
+DmFn<OutT> pick_dm(int M, bool xr) {
+    if (xr) return M > 8 ? dotmma_kernel<true, true, OutT> : dotmma_kernel<false, true, OutT>;
+    return M > 8 ? dotmma_kernel<true, false, OutT> : dotmma_kernel<false, false, OutT>;
 }
 
 template <typename OutT>
 int set_dm_attrs() {
-    for (int M : {8, 16}) {
-        int e = (int)cudaFuncSetAttribute(pick_dm<OutT>(M), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          kDotMmaMaxSmem);
-        if (e) return e;
-    }
+    for (int M : {8, 16})
+        for (bool xr : {false, true}) {
+            int e = (int)cudaFuncSetAttribute(pick_dm<OutT>(M, xr), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              kDotMmaMaxSmem);
+            if (!e) e = (int)cudaFuncSetAttribute(pick_dm<OutT>(M, xr), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e) return e;
+        }
     return 0;
 }
 
@@ -211,7 +238,8 @@ int launch_dm_t(const LaunchArgs &a, const bf16l_plan &p) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)S, (unsigned)((a.N + 7) / 8));
     cfg.blockDim = dim3((unsigned)p.threads);
-    cfg.dynamicSmemBytes = (size_t)dotmma_smem_bytes(a.M, a.K, S);
+    const bool xr = p.stages == 1;
+    cfg.dynamicSmemBytes = xr ? 0 : (size_t)dotmma_smem_bytes(a.M, a.K, S);
     cfg.stream = (cudaStream_t)a.stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -222,7 +250,7 @@ int launch_dm_t(const LaunchArgs &a, const bf16l_plan &p) {
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = S > 1 ? 2 : 1;
-    return (int)cudaLaunchKernelEx(&cfg, pick_dm<OutT>(a.M), static_cast<const uint16_t *>(a.x),
+    return (int)cudaLaunchKernelEx(&cfg, pick_dm<OutT>(a.M, xr), static_cast<const uint16_t *>(a.x),
                                    static_cast<const uint16_t *>(a.W), static_cast<const uint16_t *>(a.bias),
                                    static_cast<OutT *>(a.out), a.M, a.N, a.K, S, a.status);
 }

@@ -79,7 +79,7 @@ int init_warpmma();
 // Router split-K on warp-level MMAs: 8 W rows per CTA, K over a cluster of
 // 1, 2, 4 or 8 CTAs, M <= 16, each CTA stages its K slice of x.
 constexpr int kDotMmaMaxTokens = 16;
-constexpr int kDotMmaMaxCluster = 8;
+constexpr int kDotMmaMaxCluster = 16;
 constexpr int kDotMmaMaxSmem = 200 * 1024;
 int dotmma_smem_bytes(int M, int K, int S);
 int init_dotmma();

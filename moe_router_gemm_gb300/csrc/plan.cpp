@@ -175,9 +175,11 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
             if (K % 8 != 0 || M > kDotMmaMaxTokens) return BF16L_EUNSUPPORTED;
             const int S = p->split_k;
             if ((p->threads != 128 && p->threads != 256) || p->rows_per_cta != 8 ||
-                (S != 1 && S != 2 && S != 4 && S != 8) || S > ceil_div(K / 8, 4))
+                (S != 1 && S != 2 && S != 4 && S != 8 && S != 16) || S > ceil_div(K / 8, 4) ||
+                (p->stages != 0 && p->stages != 1))
                 return BF16L_EINVAL;
-            if (dotmma_smem_bytes(M, K, S) > kDotMmaMaxSmem) return BF16L_EUNSUPPORTED;
+            // stages 1: x straight from global memory; 0: the CTA's x slice staged in shared memory
+            if (p->stages == 0 && dotmma_smem_bytes(M, K, S) > kDotMmaMaxSmem) return BF16L_EUNSUPPORTED;
             p->grid = M == 0 ? 0 : S * ceil_div(N, 8);
             return BF16L_OK;
         }

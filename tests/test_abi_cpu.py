@@ -219,11 +219,15 @@ def test_dotmma_plans_on_cpu(lib):
     mk = lambda t, S: lib.make_plan("dotmma", threads=t, rows_per_cta=8, split_k=S)
     assert lib.plan_check(16, 384, 7168, mk(256, 4)).grid == 4 * 48
     assert lib.plan_check(3, 7, 4096, mk(128, 8)).grid == 8
-    for bad in (mk(512, 4), mk(256, 3), mk(256, 16), lib.make_plan("dotmma", threads=256, rows_per_cta=16, split_k=2)):
+    assert lib.plan_check(16, 384, 7168, mk(256, 16)).grid == 16 * 48
+    for bad in (mk(512, 4), mk(256, 3), mk(256, 32), lib.make_plan("dotmma", threads=256, rows_per_cta=16, split_k=2),
+                lib.make_plan("dotmma", threads=256, rows_per_cta=8, split_k=4, stages=2)):
         with pytest.raises(lib.BF16LinearError):
             lib.plan_check(16, 384, 7168, bad)
     with pytest.raises(lib.BF16LinearError):
-        lib.plan_check(16, 384, 7168, mk(256, 1))   # x (229 KB) does not fit one CTA
+        lib.plan_check(16, 384, 7168, mk(256, 1))   # x (229 KB) does not fit one CTA's shared memory
+    xr = lib.make_plan("dotmma", threads=256, rows_per_cta=8, split_k=1, stages=1)
+    assert lib.plan_check(16, 384, 7168, xr).grid == 48  # ... but x straight from L2 needs none
     with pytest.raises(lib.BF16LinearError):
         lib.plan_check(17, 384, 4096, mk(256, 4))   # at most 16 tokens
     with pytest.raises(lib.BF16LinearError):

@@ -30,8 +30,8 @@ def _smem(M, K, S):
     return M * most * 16
 
 
-def _plan(lib, S, threads=256):
-    return lib.make_plan("dotmma", threads=threads, rows_per_cta=8, split_k=S)
+def _plan(lib, S, threads=256, xr=0):
+    return lib.make_plan("dotmma", threads=threads, rows_per_cta=8, split_k=S, stages=xr)
 
 
 def _run(lib, x, W, b, plan, f32=False):
@@ -43,13 +43,15 @@ def _run(lib, x, W, b, plan, f32=False):
     return out
 
 
+@pytest.mark.parametrize("xr", [0, 1], ids=["xsmem", "xreg"])
 @pytest.mark.parametrize("threads", [128, 256])
-@pytest.mark.parametrize("S", [1, 2, 4, 8])
+@pytest.mark.parametrize("S", [1, 2, 4, 8, 16])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_dotmma_forced(lib, shape, S, threads):
+def test_dotmma_forced(lib, shape, S, threads, xr):
     M, N, K = shape
-    p = _plan(lib, S, threads)
-    if S > -(-(K // 8) // 4) or _smem(M, K, S) > 200 * 1024:  # too few K blocks, or x slice too big
+    p = _plan(lib, S, threads, xr)
+    # too few K blocks for the cluster, or (x in shared memory) the x slice does not fit
+    if S > -(-(K // 8) // 4) or (not xr and _smem(M, K, S) > 200 * 1024):
         with pytest.raises(lib.BF16LinearError):
             lib.plan_check(M, N, K, p)
         return
@@ -63,8 +65,18 @@ def test_dotmma_forced(lib, shape, S, threads):
 @pytest.mark.parametrize("M", range(1, 17))
 def test_dotmma_router_tokens(lib, M):
     x, W, b = wl.make_inputs(M, 256, 7168, 100 + M, False)
-    got = tensor_bits(_run(lib, x, W, b, _plan(lib, 4)))
-    check_close(got, oracle.linear_bf16(wl.bits(x), wl.bits(W), None), f"dotmma router M={M}")
+    want = oracle.linear_bf16(wl.bits(x), wl.bits(W), None)
+    for xr in (0, 1):
+        got = tensor_bits(_run(lib, x, W, b, _plan(lib, 4, 256, xr)))
+        check_close(got, want, f"dotmma router M={M} xr={xr}")
+
+
+def test_dotmma_x_paths_agree(lib):
+    # x from shared memory or from registers: the same fragments, the same MMAs, the same bits
+    for (M, N, K, S) in [(16, 384, 7168, 4), (5, 130, 2880, 2), (12, 256, 4096, 16)]:
+        x, W, b = wl.make_inputs(M, N, K, 7, True)
+        a = tensor_bits(_run(lib, x, W, b, _plan(lib, S, 128, 0)))
+        assert np.array_equal(a, tensor_bits(_run(lib, x, W, b, _plan(lib, S, 128, 1))))
 
 
 def test_dotmma_deterministic_and_f32(lib):
