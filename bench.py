@@ -525,6 +525,9 @@ def candidate_plans(lib, M, N, K):
             except Exception:
                 continue
             cands.append(p)
+    if K % 8 == 0 and M <= 16 and N > 1024:  # x fragments from L2 (any K)
+        for t, w, c in ((512, 4, 1), (512, 8, 1), (512, 16, 1), (256, 4, 2), (256, 8, 2)):
+            cands.append(lib.make_plan("warpmma", threads=t, rows_per_cta=w, stages=c, split_k=1))
     if K % 8 == 0 and M <= 16 and N <= 1024:
         for S, t, xr in itertools.product((2, 4, 8, 16), (128, 256), (0, 1)):
             if True:

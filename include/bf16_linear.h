@@ -97,7 +97,9 @@ typedef struct {
                               DOTPROD: tokens per CTA, 1..8 (0 = min(M, 8)); ceil(M / tokens) CTAs then share each
                               row slice, one token group each, instead of one CTA looping over the groups */
     int32_t split_k;       /* SPLITK: CTAs per cluster along K (1..16); SPLITK_WS: CTAs along K (1..64);
-                              DOTMMA: CTAs per cluster along K (1, 2, 4, 8 or 16) */
+                              DOTMMA: CTAs per cluster along K (1, 2, 4, 8 or 16);
+                              WARPMMA: 1 = x fragments loaded from global memory into registers (512 threads per
+                              SM at most), 0 = x staged in shared memory */
     int32_t stages;        /* SPLITK / TILE: shared-memory ring depth (64-wide K chunks);
                               WARPROW / WARPMMA: CTAs per SM; DOTMMA: 1 = x fragments loaded from global
                               memory into registers, 0 = each CTA's x slice staged in shared memory */

@@ -156,16 +156,19 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
             return BF16L_OK;
         }
         case BF16L_KERNEL_WARPMMA: {
-            if (K % 8 != 0 || M > kWarpMmaMaxTokens || warpmma_smem_bytes(M, K) > kWarpMmaMaxSmem)
+            // split_k 1: x fragments from L2 into registers (no shared-memory x, at most 512 threads per SM)
+            const bool xr = p->split_k == 1;
+            if (K % 8 != 0 || M > kWarpMmaMaxTokens || (!xr && warpmma_smem_bytes(M, K) > kWarpMmaMaxSmem))
                 return BF16L_EUNSUPPORTED;
             const int t = p->threads, wpr = p->rows_per_cta, cps = p->stages;
             if ((t != 256 && t != 512 && t != 1024) ||
-                (wpr != 1 && wpr != 2 && wpr != 4 && wpr != 8 && wpr != 16) || (t / 32) % wpr != 0)
+                (wpr != 1 && wpr != 2 && wpr != 4 && wpr != 8 && wpr != 16) || (t / 32) % wpr != 0 ||
+                (p->split_k != 0 && p->split_k != 1))
                 return BF16L_EINVAL;
             if (wpr > 1 && (t / 32) / wpr > 15) return BF16L_EINVAL;  // named barriers 1..15
             const int static_smem = (wpr > 1 ? 32 * 32 * 4 * 4 : 512) + 1024;
-            if (cps < 1 || cps > 4 || t * cps > 1024 ||
-                cps * (warpmma_smem_bytes(M, K) + static_smem) > 232448)
+            if (cps < 1 || cps > 4 || t * cps > (xr ? 512 : 1024) ||
+                cps * ((xr ? 0 : warpmma_smem_bytes(M, K)) + static_smem) > 232448)
                 return BF16L_EINVAL;
             const int64_t ctas = (int64_t)dev.num_sms * cps, groups = ceil_div(N, 8);
             p->grid = M == 0 ? 0 : (int)(ctas < groups ? ctas : groups);

@@ -56,9 +56,12 @@ int warpmma_smem_bytes(int M, int K) { return M * K * 2; }
 
 // NT: block size the instance is compiled for (512 or 1024; a 256-thread block
 // runs the 512 instance); all keep 1024 threads per SM resident.  HI: M > 8
-// (tokens 8..15 in the MMA's upper rows).
-template <int WPR, int NT, bool HI, typename OutT>
-__global__ void __launch_bounds__(NT, 1024 / NT)
+// (tokens 8..15 in the MMA's upper rows).  XR: x fragments loaded from L2 into
+// registers with each weight batch instead of staged in shared memory (for x
+// too large to stage, e.g. 16 tokens of K = 7168); 512 threads per SM then, as
+// the batch of x fragments takes another 64 registers a thread.
+template <int WPR, int NT, bool HI, bool XR, typename OutT>
+__global__ void __launch_bounds__(NT, XR ? 1 : 1024 / NT)
     warpmma_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ W, const uint16_t *__restrict__ bias,
                    OutT *__restrict__ out, int M, int N, int K, int32_t *status) {
     constexpr int U = 8;                           // 32-wide K blocks per lane per batch
@@ -104,28 +107,48 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
     pdl_launch_dependents();
     pdl_wait();  // x may be written, and out still read, by the previous kernel
     __syncthreads();
-    if (tid == 0 && q1 > q0) {
-        mbar_arrive_expect_tx(&xbar, (uint32_t)(M * K * 2));
-        for (int m = 0; m < M; ++m) bulk_load(xs + (size_t)m * nvec, x + (size_t)m * K, (uint32_t)(K * 2), &xbar);
+    if constexpr (!XR) {
+        if (tid == 0 && q1 > q0) {
+            mbar_arrive_expect_tx(&xbar, (uint32_t)(M * K * 2));
+            for (int m = 0; m < M; ++m)
+                bulk_load(xs + (size_t)m * nvec, x + (size_t)m * K, (uint32_t)(K * 2), &xbar);
+        }
+        const bool staged = q1 > q0 ? mbar_wait(&xbar, 0, status, kSiteStage) : true;
+        if (!__syncthreads_and(staged)) return;  // the whole CTA leaves together (only after a timeout)
     }
-    const bool staged = q1 > q0 ? mbar_wait(&xbar, 0, status, kSiteStage) : true;
-    if (!__syncthreads_and(staged)) return;  // the whole CTA leaves together (only after a timeout)
 
     const uint4 *xlo = xs + (size_t)(tok_lo ? g : 0) * nvec;
     const uint4 *xhi = xs + (size_t)(tok_hi ? g + 8 : 0) * nvec;
+    const uint4 *glo = reinterpret_cast<const uint4 *>(x + (size_t)(tok_lo ? g : 0) * K);
+    const uint4 *ghi = reinterpret_cast<const uint4 *>(x + (size_t)(tok_hi ? g + 8 : 0) * K);
     for (bool first = true; q < q1; q += groups, first = false) {
         const int n0 = 8 * q;
         float d[4] = {0.f, 0.f, 0.f, 0.f};
         for (int vb = vb0; vb < vb1; vb += 4 * U) {  // warp-uniform trip count: mma.sync is warp-wide
             if (!(first && vb == vb0)) load_batch(n0, vb);
+            uint4 xl[XR ? U : 1], xh[XR ? U : 1];
+            if constexpr (XR) {  // this batch's x fragments, in flight with the weights
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int vv = vb + 4 * u + t;
+                    const bool in = vv < vb1;
+                    xl[u] = (tok_lo && in) ? __ldg(glo + vv) : make_uint4(0u, 0u, 0u, 0u);
+                    xh[u] = (HI && tok_hi && in) ? __ldg(ghi + vv) : make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int vv = vb + 4 * u + t;
                 const bool in = vv < vb1;
-                const uint4 lo = (tok_lo && in) ? xlo[vv] : make_uint4(0u, 0u, 0u, 0u);
-                uint4 hi = make_uint4(0u, 0u, 0u, 0u);
-                if constexpr (HI) {
-                    if (tok_hi && in) hi = xhi[vv];
+                uint4 lo, hi = make_uint4(0u, 0u, 0u, 0u);
+                if constexpr (XR) {
+                    lo = xl[u];
+                    hi = xh[u];
+                } else {
+                    lo = (tok_lo && in) ? xlo[vv] : make_uint4(0u, 0u, 0u, 0u);
+                    if constexpr (HI) {
+                        if (tok_hi && in) hi = xhi[vv];
+                    }
                 }
                 // this lane's block positions 8t..8t+7: step 0 takes +0..3, step 1 takes +4..7
                 mma_m16n8k16(d, lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
@@ -165,26 +188,28 @@ namespace {
 template <typename OutT>
 using WmFn = void (*)(const uint16_t *, const uint16_t *, const uint16_t *, OutT *, int, int, int, int32_t *);
 
-template <int WPR, bool HI, typename OutT>
+template <int WPR, bool HI, bool XR, typename OutT>
 WmFn<OutT> pick_nt(int threads) {
-    return threads > 512 ? warpmma_kernel<WPR, 1024, HI, OutT> : warpmma_kernel<WPR, 512, HI, OutT>;
+    if constexpr (XR) return warpmma_kernel<WPR, 512, HI, true, OutT>;  // at most 512 threads
+    return threads > 512 ? warpmma_kernel<WPR, 1024, HI, false, OutT> : warpmma_kernel<WPR, 512, HI, false, OutT>;
 }
 
-template <bool HI, typename OutT>
+template <bool HI, bool XR, typename OutT>
 WmFn<OutT> pick_wpr(int wpr, int threads) {
     switch (wpr) {
-        case 1: return pick_nt<1, HI, OutT>(threads);
-        case 2: return pick_nt<2, HI, OutT>(threads);
-        case 4: return pick_nt<4, HI, OutT>(threads);
-        case 8: return pick_nt<8, HI, OutT>(threads);
-        case 16: return pick_nt<16, HI, OutT>(threads);
+        case 1: return pick_nt<1, HI, XR, OutT>(threads);
+        case 2: return pick_nt<2, HI, XR, OutT>(threads);
+        case 4: return pick_nt<4, HI, XR, OutT>(threads);
+        case 8: return pick_nt<8, HI, XR, OutT>(threads);
+        case 16: return pick_nt<16, HI, XR, OutT>(threads);
         default: return nullptr;
     }
 }
 
 template <typename OutT>
-WmFn<OutT> pick_wm(int M, int wpr, int threads) {
-    return M > 8 ? pick_wpr<true, OutT>(wpr, threads) : pick_wpr<false, OutT>(wpr, threads);
+WmFn<OutT> pick_wm(int M, int wpr, int threads, bool xr) {
+    if (xr) return M > 8 ? pick_wpr<true, true, OutT>(wpr, threads) : pick_wpr<false, true, OutT>(wpr, threads);
+    return M > 8 ? pick_wpr<true, false, OutT>(wpr, threads) : pick_wpr<false, false, OutT>(wpr, threads);
 }
 
 template <typename OutT>
@@ -192,7 +217,7 @@ int set_wm_attrs() {
     for (int M : {8, 16})
         for (int wpr : {1, 2, 4, 8, 16})
             for (int t : {512, 1024}) {
-                const int e = (int)cudaFuncSetAttribute(pick_wm<OutT>(M, wpr, t),
+                const int e = (int)cudaFuncSetAttribute(pick_wm<OutT>(M, wpr, t, false),
                                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                         kWarpMmaMaxSmem);
                 if (e) return e;
@@ -202,12 +227,13 @@ int set_wm_attrs() {
 
 template <typename OutT>
 int launch_wm_t(const LaunchArgs &a, const bf16l_plan &p) {
-    WmFn<OutT> fn = pick_wm<OutT>(a.M, p.rows_per_cta, p.threads);
+    const bool xr = p.split_k == 1;
+    WmFn<OutT> fn = pick_wm<OutT>(a.M, p.rows_per_cta, p.threads, xr);
     if (!fn) return (int)cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid);
     cfg.blockDim = dim3((unsigned)p.threads);
-    cfg.dynamicSmemBytes = (size_t)warpmma_smem_bytes(a.M, a.K);
+    cfg.dynamicSmemBytes = xr ? 0 : (size_t)warpmma_smem_bytes(a.M, a.K);
     cfg.stream = (cudaStream_t)a.stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

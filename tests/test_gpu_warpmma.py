@@ -25,8 +25,8 @@ SHAPES = [(1, 300, 1032), (3, 517, 2880), (8, 64, 4096), (5, 1000, 136), (2, 5, 
           (12, 96, 2056), (9, 1, 40)]
 
 
-def _plan(lib, threads=512, wpr=1, cps=1):
-    return lib.make_plan("warpmma", threads=threads, rows_per_cta=wpr, stages=cps)
+def _plan(lib, threads=512, wpr=1, cps=1, xr=0):
+    return lib.make_plan("warpmma", threads=threads, rows_per_cta=wpr, stages=cps, split_k=xr)
 
 
 def _fits(M, K, cfg):
@@ -61,6 +61,34 @@ def test_warpmma_forced(lib, shape, cfg):
         return
     for bias in (False, True):
         _check(lib, M, N, K, seed=M + N + K, bias=bias, plan=_plan(lib, *cfg))
+
+
+XR_CFGS = [(512, 1, 1), (512, 4, 1), (512, 16, 1), (256, 2, 2), (256, 8, 2)]
+
+
+@pytest.mark.parametrize("cfg", XR_CFGS, ids=lambda c: "xreg_t%d_wpr%d_cps%d" % c)
+@pytest.mark.parametrize("shape", SHAPES + [(16, 333, 7168)], ids=lambda s: "x".join(map(str, s)))
+def test_warpmma_x_from_l2(lib, shape, cfg):
+    """x fragments loaded from L2 with each weight batch (no shared-memory x): any K, M <= 16."""
+    M, N, K = shape
+    for bias in (False, True):
+        _check(lib, M, N, K, seed=M + N + K + 1, bias=bias, plan=_plan(lib, *cfg, xr=1))
+
+
+def test_warpmma_x_paths_agree(lib):
+    # the same fragments reach the same MMAs from shared memory or from L2: the same bits
+    x, W, b = wl.make_inputs(12, 2112, 4096, 4, True)
+    a = tensor_bits(_run(lib, x, W, b, _plan(lib, 512, 4, 1, 0)))
+    assert np.array_equal(a, tensor_bits(_run(lib, x, W, b, _plan(lib, 512, 4, 1, 1))))
+
+
+@pytest.mark.parametrize("M", [9, 16])
+def test_warpmma_decode_16_tokens(lib, M):
+    # 9..16 tokens of K = 7168 (> 115 KB) can still fit, 16 do not: the L2 path takes any
+    if M * 7168 * 2 > 200 * 1024:
+        with pytest.raises(lib.BF16LinearError):
+            lib.plan_check(M, 2112, 7168, _plan(lib, 512, 4, 1, 0))
+    _check(lib, M, 2112, 7168, seed=77, bias=False, plan=_plan(lib, 512, 4, 1, 1))
 
 
 @pytest.mark.parametrize("M", [1, 2, 4, 8])
