@@ -103,7 +103,8 @@ def workload_desc(name):
 def kernel_source_hash(kernel_name):
     src = {"dotprod": ("dotprod.cuh", "dotprod.cu"), "splitk": ("splitk.cu",), "splitk_ws": ("splitk.cu",),
            "tile": ("tile.cu",), "stream": ("stream.cu",), "tile2": ("tile2.cu",), "warprow": ("warprow.cu",),
-           "warpmma": ("warpmma.cu",), "dotmma": ("dotmma.cu",)}[kernel_name]
+           "warpmma": ("warpmma.cu",), "dotmma": ("dotmma.cu",),
+           "dotmma_ws": ("dotmma.cu",)}[kernel_name]
     h = hashlib.sha256()
     for f in src + ("common.cuh", "kernels.h"):
         h.update(open(os.path.join(ROOT, "moe_router_gemm_gb300", "csrc", f), "rb").read())
@@ -441,6 +442,9 @@ def eager_profile(args, points):
     print(json.dumps({"mode": "eager", "steps": args.steps, "shapes": res}))
 
 
+WS_KERNELS = (3, 9)  # the cluster-free split-K forms, which need a caller workspace
+
+
 def candidate_plans(lib, M, N, K):
     """Every plan worth timing for one shape (the tuning space of the sweep)."""
     cands = []
@@ -529,6 +533,13 @@ def candidate_plans(lib, M, N, K):
         for t, w, c in ((512, 4, 1), (512, 8, 1), (512, 16, 1), (256, 4, 2), (256, 8, 2)):
             cands.append(lib.make_plan("warpmma", threads=t, rows_per_cta=w, stages=c, split_k=1))
     if K % 8 == 0 and M <= 16 and N <= 1024:
+        for S, t, xr in itertools.product((8, 16, 32), (128, 256), (0, 1)):
+            p = lib.make_plan("dotmma_ws", threads=t, rows_per_cta=8, split_k=S, stages=xr)
+            try:
+                lib.plan_check(M, N, K, p)
+            except Exception:
+                continue
+            cands.append(p)
         for S, t, xr in itertools.product((2, 4, 8, 16), (128, 256), (0, 1)):
             if True:
                 p = lib.make_plan("dotmma", threads=t, rows_per_cta=8, split_k=S, stages=xr)
@@ -587,7 +598,7 @@ def sweep(args, points):
             except Exception as e:  # an unusable candidate is skipped, not fatal
                 rows.append((float("inf"), dict(p.as_dict(), error=str(e)[:80])))
         rows.sort(key=lambda r: r[0])
-        best_plain = next((r for r in rows if r[1].get("kernel") != 3), rows[0])
+        best_plain = next((r for r in rows if r[1].get("kernel") not in WS_KERNELS), rows[0])
         default = lib.plan(pt["M"], pt["N"], pt["K"]).as_dict()
         results.append({"M": pt["M"], "N": pt["N"], "K": pt["K"], "best_us": rows[0][0], "best": rows[0][1],
                         "best_plain_us": best_plain[0], "best_plain": best_plain[1],
@@ -602,7 +613,7 @@ def sweep(args, points):
              "// {K, N, M, kernel, threads, rows_per_cta, tokens_per_cta, split_k, stages},"]
     for r in sorted(results, key=lambda r: (r["K"], r["N"], r["M"])):
         entries = [(r["best"], r["best_us"])]
-        if r["best"].get("kernel") == 3:  # needs a workspace: follow it with the best plan that needs none
+        if r["best"].get("kernel") in WS_KERNELS:  # needs a workspace: follow it with the best plan that needs none
             entries.append((r["best_plain"], r["best_plain_us"]))
         for b, us in entries:
             lines.append(f"{{{r['K']}, {r['N']}, {r['M']}, {b['kernel']}, {b['threads']}, {b['rows_per_cta']}, "

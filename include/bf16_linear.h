@@ -76,8 +76,10 @@ typedef enum {
                                   warps computes one W row at a time from 16-byte loads, x in shared memory */
     BF16L_KERNEL_WARPMMA = 7,  /* persistent kernel for M <= 16 and many rows: 16-byte weight loads feed the
                                   warp-level tensor-core MMA (m16n8k16) directly; 8 W rows per group of warps */
-    BF16L_KERNEL_DOTMMA = 8    /* router-sized N, M <= 16: 8 W rows per CTA, K split over a cluster of 1..16 CTAs,
+    BF16L_KERNEL_DOTMMA = 8,   /* router-sized N, M <= 16: 8 W rows per CTA, K split over a cluster of 1..16 CTAs,
                                   16-byte loads feed m16n8k16 MMAs, partials summed by rank 0 over DSMEM */
+    BF16L_KERNEL_DOTMMA_WS = 9 /* the same without a cluster: K split over 2..64 CTAs whose partial tiles meet in
+                                  a caller-provided workspace (see bf16_linear_run); the last CTA reduces */
 } bf16l_kernel;
 
 /*
@@ -98,6 +100,7 @@ typedef struct {
                               row slice, one token group each, instead of one CTA looping over the groups */
     int32_t split_k;       /* SPLITK: CTAs per cluster along K (1..16); SPLITK_WS: CTAs along K (1..64);
                               DOTMMA: CTAs per cluster along K (1, 2, 4, 8 or 16);
+                              DOTMMA_WS: CTAs along K (a power of two, 2..64);
                               WARPMMA: 1 = x fragments loaded from global memory into registers (512 threads per
                               SM at most), 0 = x staged in shared memory */
     int32_t stages;        /* SPLITK / TILE: shared-memory ring depth (64-wide K chunks);

@@ -8,7 +8,7 @@ dispatcher.  This package is its thin Python binding; build the library with
 """
 from ._binding import (BF16LinearError, Call, Device, KERNEL_DOTPROD, KERNEL_NAMES, KERNEL_SPLITK,  # noqa: F401
                        KERNEL_SPLITK_WS, KERNEL_STREAM, KERNEL_TILE2, KERNEL_WARPROW,
-                       KERNEL_WARPMMA, KERNEL_DOTMMA, new_workspace, plan_ws, run, workspace_size,
+                       KERNEL_WARPMMA, KERNEL_DOTMMA, KERNEL_DOTMMA_WS, new_workspace, plan_ws, run, workspace_size,
                        KERNEL_TILE, LIB_PATH, FLAG_PDL, Plan, bf16_linear, bf16_linear_ex, bf16_linear_f32out,
                        bf16_linear_noalloc,
                        bf16_linear_with_plan, device_status,

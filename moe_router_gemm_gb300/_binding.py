@@ -19,10 +19,11 @@ LIB_PATH = os.path.join(PKG, "libbf16_linear.so")
 OK, EINVAL, EALIGN, EARCH, ELAUNCH, ETIMEOUT, EUNSUPPORTED, ENOSCRATCH = 0, -1, -2, -3, -4, -5, -6, -7
 FLAG_PDL = 1
 (KERNEL_DOTPROD, KERNEL_SPLITK, KERNEL_TILE, KERNEL_SPLITK_WS, KERNEL_STREAM, KERNEL_TILE2, KERNEL_WARPROW,
- KERNEL_WARPMMA, KERNEL_DOTMMA) = range(9)
+ KERNEL_WARPMMA, KERNEL_DOTMMA, KERNEL_DOTMMA_WS) = range(10)
 KERNEL_NAMES = {KERNEL_DOTPROD: "dotprod", KERNEL_SPLITK: "splitk", KERNEL_TILE: "tile",
                 KERNEL_SPLITK_WS: "splitk_ws", KERNEL_STREAM: "stream", KERNEL_TILE2: "tile2",
-                KERNEL_WARPROW: "warprow", KERNEL_WARPMMA: "warpmma", KERNEL_DOTMMA: "dotmma"}
+                KERNEL_WARPROW: "warprow", KERNEL_WARPMMA: "warpmma", KERNEL_DOTMMA: "dotmma",
+                KERNEL_DOTMMA_WS: "dotmma_ws"}
 
 
 class Plan(ctypes.Structure):

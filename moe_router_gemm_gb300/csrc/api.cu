@@ -121,7 +121,7 @@ int run(const bf16l_call &c) {
         const bf16l_device any = {10, 3, kGb300Sms};
         st = check_plan(c.M, c.N, c.K, any, &tmp);
         if (st != BF16L_OK) return st;
-        if (split_ws_bytes(c.M, c.N, tmp) > (c.workspace ? c.workspace_bytes : 0)) return BF16L_EINVAL;
+        if (plan_ws_bytes(c.M, c.N, tmp) > (c.workspace ? c.workspace_bytes : 0)) return BF16L_EINVAL;
     }
     DeviceState *ds = nullptr;
     st = current_device(&ds);
@@ -149,7 +149,8 @@ int run(const bf16l_call &c) {
         case BF16L_KERNEL_TILE2: e = launch_tile2(a, p); break;
         case BF16L_KERNEL_WARPROW: e = launch_warprow(a, p); break;
         case BF16L_KERNEL_WARPMMA: e = launch_warpmma(a, p); break;
-        case BF16L_KERNEL_DOTMMA: e = launch_dotmma(a, p); break;
+        case BF16L_KERNEL_DOTMMA:
+        case BF16L_KERNEL_DOTMMA_WS: e = launch_dotmma(a, p); break;
         default: return BF16L_EINVAL;
     }
     if (e) {

@@ -24,6 +24,10 @@
 //     rank 0's mbarrier; rank 0 sums in rank order, adds bias, rounds, stores.
 // Two cluster barrier phases (non-.aligned): "receive barrier initialised"
 // (arrived at start, waited before sending) and "all received" (before exit).
+// Cluster-free form (WS, BF16L_KERNEL_DOTMMA_WS): the S CTAs of a row group
+// are independent; each writes its tile to a caller workspace, fences and takes
+// a ticket from the group's counter; the last to arrive sums the S tiles in
+// rank order, stores, and resets the counter for the next call.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -49,6 +53,15 @@ __host__ __device__ inline int dm_blk(int nblk, int r, int S) { return (int)(((l
 
 }  // namespace
 
+// Workspace of the cluster-free form: per-group arrival counters (rounded up
+// to 256 bytes), then the tiles [groups][S][32 lanes] of float4.
+size_t dotmma_ws_counter_bytes(int groups) { return ((size_t)groups * 4 + 255) / 256 * 256; }
+size_t dotmma_ws_bytes(int N, const bf16l_plan &p) {
+    if (p.kernel != BF16L_KERNEL_DOTMMA_WS || p.split_k <= 0) return 0;
+    const int groups = (N + 7) / 8;
+    return dotmma_ws_counter_bytes(groups) + (size_t)groups * p.split_k * 32 * 16;
+}
+
 // Dynamic shared memory: x slice [M][vectors of the largest slice] as 16-byte vectors.
 int dotmma_smem_bytes(int M, int K, int S) {
     const int nvec = K / 8, nblk = (nvec + 3) / 4;
@@ -64,10 +77,11 @@ int dotmma_smem_bytes(int M, int K, int S) {
 // HI: M > 8 (tokens 8..15 on the MMA's upper rows).  XR: x fragments loaded
 // from global memory (L2) straight into registers next to the weights, instead
 // of a bulk copy of the CTA's x slice into shared memory.
-template <bool HI, bool XR, typename OutT>
+template <bool HI, bool XR, bool WS, typename OutT>
 __global__ void __launch_bounds__(kDmWarps * 32)
     dotmma_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ W, const uint16_t *__restrict__ bias,
-                  OutT *__restrict__ out, int M, int N, int K, int S, int32_t *status) {
+                  OutT *__restrict__ out, int M, int N, int K, int S, int32_t *status, uint32_t *counters,
+                  float4 *tiles) {
     constexpr int U = 8;  // 32-wide K blocks per lane per batch
     extern __shared__ uint4 xs[];
     __shared__ float4 part[kDmWarps][32];  // per warp, lane (g, t): tokens g, g+8 x rows 2t, 2t+1
@@ -77,7 +91,8 @@ __global__ void __launch_bounds__(kDmWarps * 32)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
     const int nw = (int)blockDim.x >> 5;
-    const int rank = S > 1 ? (int)cluster_ctarank() : 0;
+    const bool clus = !WS && S > 1;
+    const int rank = WS ? (int)blockIdx.x : (S > 1 ? (int)cluster_ctarank() : 0);
     const int n0 = 8 * (int)blockIdx.y;
     const int nvec = K >> 3, nblk = (nvec + 3) >> 2;
     // this CTA's vectors [cv0, cv1) and this warp's blocks
@@ -97,7 +112,7 @@ __global__ void __launch_bounds__(kDmWarps * 32)
         fence_barrier_init();
     }
     __syncthreads();
-    if (S > 1) cluster_arrive_relaxed();  // phase 1: "my receive barrier is initialised"
+    if (clus) cluster_arrive_relaxed();  // phase 1: "my receive barrier is initialised"
 
     uint4 wv[U];
     auto load_batch = [&](int vb) {
@@ -173,7 +188,32 @@ __global__ void __launch_bounds__(kDmWarps * 32)
     }
 
     bool have = ok;
-    if (S > 1) {
+    bool store = rank == 0;
+    if constexpr (WS) {
+        // ---- cluster-free: tile to the workspace, ticket, the last CTA reduces ----
+        __shared__ uint32_t ticket;
+        const int q = (int)blockIdx.y;
+        if (warp == 0) {
+            __stcg(&tiles[((size_t)q * S + rank) * 32 + lane], s);
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) ticket = atomicAdd(&counters[q], 1u);
+        }
+        __syncthreads();
+        store = ticket == (uint32_t)(S - 1);
+        if (store && warp == 0) {
+            __threadfence();
+            s = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int r = 0; r < S; ++r) {  // ranks in order
+                const float4 p = __ldcg(&tiles[((size_t)q * S + r) * 32 + lane]);
+                s.x += p.x;
+                s.y += p.y;
+                s.z += p.z;
+                s.w += p.w;
+            }
+            if (lane == 0) counters[q] = 0u;  // ready for the next call
+        }
+    } else if (S > 1) {
         cluster_wait_acquire();  // phase 1 done: rank 0's receive barrier exists
         if (rank != 0) {
             if (warp == 0)
@@ -194,7 +234,7 @@ __global__ void __launch_bounds__(kDmWarps * 32)
         }
         cluster_arrive_relaxed();  // phase 2: everything this CTA sends or receives has landed (rank 0)
     }
-    if (rank == 0 && warp == 0 && have) {
+    if (store && warp == 0 && have) {
         const float v[4] = {s.x, s.y, s.z, s.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -206,35 +246,53 @@ __global__ void __launch_bounds__(kDmWarps * 32)
             }
         }
     }
-    if (S > 1) cluster_wait_acquire();  // phase 2 done: rank 0 holds every partial; all may exit
+    if (clus) cluster_wait_acquire();  // phase 2 done: rank 0 holds every partial; all may exit
 }
 
 namespace {
 
 template <typename OutT>
-using DmFn = void (*)(const uint16_t *, const uint16_t *, const uint16_t *, OutT *, int, int, int, int, int32_t *);
+using DmFn = void (*)(const uint16_t *, const uint16_t *, const uint16_t *, OutT *, int, int, int, int, int32_t *,
+                      uint32_t *, float4 *);
+
+template <bool WS, typename OutT>
+DmFn<OutT> pick_dm_ws(int M, bool xr) {
+    if (xr) return M > 8 ? dotmma_kernel<true, true, WS, OutT> : dotmma_kernel<false, true, WS, OutT>;
+    return M > 8 ? dotmma_kernel<true, false, WS, OutT> : dotmma_kernel<false, false, WS, OutT>;
+}
 
 template <typename OutT>
-DmFn<OutT> pick_dm(int M, bool xr) {
-    if (xr) return M > 8 ? dotmma_kernel<true, true, OutT> : dotmma_kernel<false, true, OutT>;
-    return M > 8 ? dotmma_kernel<true, false, OutT> : dotmma_kernel<false, false, OutT>;
+DmFn<OutT> pick_dm(int M, bool xr, bool ws) {
+    return ws ? pick_dm_ws<true, OutT>(M, xr) : pick_dm_ws<false, OutT>(M, xr);
 }
 
 template <typename OutT>
 int set_dm_attrs() {
     for (int M : {8, 16})
-        for (bool xr : {false, true}) {
-            int e = (int)cudaFuncSetAttribute(pick_dm<OutT>(M, xr), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              kDotMmaMaxSmem);
-            if (!e) e = (int)cudaFuncSetAttribute(pick_dm<OutT>(M, xr), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-            if (e) return e;
-        }
+        for (bool xr : {false, true})
+            for (bool ws : {false, true}) {
+                int e = (int)cudaFuncSetAttribute(pick_dm<OutT>(M, xr, ws),
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kDotMmaMaxSmem);
+                if (!e && !ws)
+                    e = (int)cudaFuncSetAttribute(pick_dm<OutT>(M, xr, ws),
+                                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                if (e) return e;
+            }
     return 0;
 }
 
 template <typename OutT>
 int launch_dm_t(const LaunchArgs &a, const bf16l_plan &p) {
     const int S = p.split_k;
+    const bool ws = p.kernel == BF16L_KERNEL_DOTMMA_WS;
+    uint32_t *counters = nullptr;
+    float4 *tiles = nullptr;
+    if (ws) {
+        const int groups = (a.N + 7) / 8;
+        if (!a.workspace || a.workspace_bytes < dotmma_ws_bytes(a.N, p)) return (int)cudaErrorInvalidValue;
+        counters = static_cast<uint32_t *>(a.workspace);
+        tiles = reinterpret_cast<float4 *>(static_cast<uint8_t *>(a.workspace) + dotmma_ws_counter_bytes(groups));
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)S, (unsigned)((a.N + 7) / 8));
     cfg.blockDim = dim3((unsigned)p.threads);
@@ -249,10 +307,10 @@ int launch_dm_t(const LaunchArgs &a, const bf16l_plan &p) {
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = S > 1 ? 2 : 1;
-    return (int)cudaLaunchKernelEx(&cfg, pick_dm<OutT>(a.M, xr), static_cast<const uint16_t *>(a.x),
+    cfg.numAttrs = (S > 1 && !ws) ? 2 : 1;
+    return (int)cudaLaunchKernelEx(&cfg, pick_dm<OutT>(a.M, xr, ws), static_cast<const uint16_t *>(a.x),
                                    static_cast<const uint16_t *>(a.W), static_cast<const uint16_t *>(a.bias),
-                                   static_cast<OutT *>(a.out), a.M, a.N, a.K, S, a.status);
+                                   static_cast<OutT *>(a.out), a.M, a.N, a.K, S, a.status, counters, tiles);
 }
 
 }  // namespace

@@ -82,6 +82,11 @@ constexpr int kDotMmaMaxTokens = 16;
 constexpr int kDotMmaMaxCluster = 16;
 constexpr int kDotMmaMaxSmem = 200 * 1024;
 int dotmma_smem_bytes(int M, int K, int S);
+constexpr int kDotMmaWsMaxSplit = 64;  // K splits of the cluster-free (workspace) form
+size_t dotmma_ws_counter_bytes(int groups);
+size_t dotmma_ws_bytes(int N, const bf16l_plan &p);
+// Workspace bytes a plan needs (0 for every kernel but the two cluster-free forms).
+inline size_t plan_ws_bytes(int M, int N, const bf16l_plan &p) { return split_ws_bytes(M, N, p) + dotmma_ws_bytes(N, p); }
 int init_dotmma();
 
 // Pair tile kernel (cta_group::2): 256 x rows x 256 W rows per cluster of 2,

@@ -174,12 +174,16 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
             p->grid = M == 0 ? 0 : (int)(ctas < groups ? ctas : groups);
             return BF16L_OK;
         }
-        case BF16L_KERNEL_DOTMMA: {
+        case BF16L_KERNEL_DOTMMA:
+        case BF16L_KERNEL_DOTMMA_WS: {
             if (K % 8 != 0 || M > kDotMmaMaxTokens) return BF16L_EUNSUPPORTED;
             const int S = p->split_k;
-            if ((p->threads != 128 && p->threads != 256) || p->rows_per_cta != 8 ||
-                (S != 1 && S != 2 && S != 4 && S != 8 && S != 16) || S > ceil_div(K / 8, 4) ||
-                (p->stages != 0 && p->stages != 1))
+            // clusters: 1..16 CTAs along K; the workspace form: any power of two up to 64
+            const bool s_ok = p->kernel == BF16L_KERNEL_DOTMMA
+                                  ? (S == 1 || S == 2 || S == 4 || S == 8 || S == 16)
+                                  : (S >= 2 && S <= kDotMmaWsMaxSplit && (S & (S - 1)) == 0);
+            if ((p->threads != 128 && p->threads != 256) || p->rows_per_cta != 8 || !s_ok ||
+                S > ceil_div(K / 8, 4) || (p->stages != 0 && p->stages != 1))
                 return BF16L_EINVAL;
             // stages 1: x straight from global memory; 0: the CTA's x slice staged in shared memory
             if (p->stages == 0 && dotmma_smem_bytes(M, K, S) > kDotMmaMaxSmem) return BF16L_EUNSUPPORTED;
@@ -226,7 +230,7 @@ extern "C" int bf16_linear_plan_ws(int M, int N, int K, const bf16l_device *devp
         p.tokens_per_cta = e->tokens_per_cta;
         p.split_k = e->split_k;
         p.stages = e->stages;
-        from_table = check_plan(M, N, K, dev, &p) == BF16L_OK && split_ws_bytes(M, N, p) <= workspace_bytes;
+        from_table = check_plan(M, N, K, dev, &p) == BF16L_OK && plan_ws_bytes(M, N, p) <= workspace_bytes;
     }
     if (!from_table) {
         p = bf16l_plan{};
@@ -252,10 +256,10 @@ extern "C" int bf16_linear_plan(int M, int N, int K, const bf16l_device *devp, b
 extern "C" size_t bf16_linear_workspace_size(int M, int N, int K, const bf16l_plan *plan) {
     using namespace bf16l;
     if (M < 0 || N <= 0 || K <= 0) return 0;
-    if (plan) return split_ws_bytes(M, N, *plan);
+    if (plan) return plan_ws_bytes(M, N, *plan);
     bf16l_plan p;
     if (bf16_linear_plan_ws(M, N, K, nullptr, (size_t)-1, &p) != BF16L_OK) return 0;
-    return split_ws_bytes(M, N, p);
+    return plan_ws_bytes(M, N, p);
 }
 
 extern "C" int bf16_linear_plan_check(int M, int N, int K, const bf16l_device *devp, bf16l_plan *plan) {

@@ -79,6 +79,49 @@ def test_dotmma_x_paths_agree(lib):
         assert np.array_equal(a, tensor_bits(_run(lib, x, W, b, _plan(lib, S, 128, 1))))
 
 
+def _ws_run(lib, x, W, b, plan, f32=False):
+    xd, Wd = x.to(DEV), W.to(DEV)
+    bd = b.to(DEV) if b is not None else None
+    ws = lib.new_workspace(lib.workspace_size(x.shape[0], W.shape[0], W.shape[1], plan), DEV)
+    out = torch.empty(x.shape[0], W.shape[0], dtype=torch.float32 if f32 else torch.bfloat16, device=DEV)
+    outs = []
+    for _ in range(2):  # the counters reset themselves: a second call on the same workspace must agree
+        lib.run(xd, Wd, bd, out, plan_=plan, workspace=ws)
+        torch.cuda.synchronize()
+        outs.append(out.clone())
+    assert torch.equal(outs[0], outs[1])
+    return outs[0]
+
+
+@pytest.mark.parametrize("xr", [0, 1], ids=["xsmem", "xreg"])
+@pytest.mark.parametrize("S", [2, 8, 32, 64])
+@pytest.mark.parametrize("shape", [(16, 384, 7168), (9, 256, 4096), (4, 300, 2056), (13, 7, 4096)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_dotmma_workspace_form(lib, shape, S, xr):
+    M, N, K = shape
+    p = lib.make_plan("dotmma_ws", threads=128, rows_per_cta=8, split_k=S, stages=xr)
+    if not xr and _smem(M, K, S) > 200 * 1024:
+        with pytest.raises(lib.BF16LinearError):
+            lib.plan_check(M, N, K, p)
+        return
+    x, W, b = wl.make_inputs(M, N, K, S + M, True)
+    got = tensor_bits(_ws_run(lib, x, W, b, p))
+    check_close(got, oracle.linear_bf16(wl.bits(x), wl.bits(W), wl.bits(b)), f"dotmma_ws M={M} N={N} K={K} S={S}")
+    # the same partial tiles summed in the same rank order as the cluster form with the same split
+    if S <= 16:
+        c = _plan(lib, S, 128, xr)
+        assert np.array_equal(got, tensor_bits(_run(lib, x, W, b, c)))
+
+
+def test_dotmma_workspace_needs_workspace(lib):
+    p = lib.make_plan("dotmma_ws", threads=128, rows_per_cta=8, split_k=8)
+    assert lib.workspace_size(16, 384, 7168, p) == 256 + 48 * 8 * 512
+    x = torch.zeros(16, 7168, dtype=torch.bfloat16, device=DEV)
+    W = torch.zeros(384, 7168, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(lib.BF16LinearError):
+        lib.bf16_linear_with_plan(x, W, None, plan_=p)  # no workspace given
+
+
 def test_dotmma_deterministic_and_f32(lib):
     M, N, K = 14, 384, 7168
     x, W, b = wl.make_inputs(M, N, K, 2, True)
