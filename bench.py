@@ -458,10 +458,10 @@ def candidate_plans(lib, M, N, K):
     if K % 8 == 0 and M <= 64:
         chunks = -(-K // 64)
         tokens = max(8, -(-M // 8) * 8)
-        for rows in (16, 32, 64, 128, 256):
+        for rows in (16, 32, 48, 64, 96, 128, 192, 256):
             if rows > max(16, 2 * N):
                 continue
-            for split in (1, 2, 4, 6, 8, 12, 16):
+            for split in (1, 2, 3, 4, 6, 8, 12, 16):
                 if split > chunks:
                     continue
                 tiles = -(-N // rows)
