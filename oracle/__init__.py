@@ -19,6 +19,12 @@ closed form; power-of-two scaling; linearity of the unrounded sum; bias
 exactness; exact-rational brute force on tiny shapes; numpy's f64 matmul.
 
 Arrays cross the boundary as numpy uint16 bit patterns (bf16) in C order.
+
+Per-tensor FP8 (oracle.c, second part; the sglang PR #28333 page): e4m3
+decoding from the format definition, the static quantisation of the page's
+kernel (binary32 reciprocal and product, clamp to +-448, round to nearest
+even), and the FP8 linear (exact f64 sum of e4m3 products, times both scales,
+plus bias, one rounding to bf16).  e4m3 codes cross the boundary as uint8.
 """
 from __future__ import annotations
 
@@ -35,6 +41,7 @@ _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
 
+_u8p = np.ctypeslib.ndpointer(dtype=np.uint8, flags="C_CONTIGUOUS")
 _u16p = np.ctypeslib.ndpointer(dtype=np.uint16, flags="C_CONTIGUOUS")
 _u32p = np.ctypeslib.ndpointer(dtype=np.uint32, flags="C_CONTIGUOUS")
 _f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
@@ -81,8 +88,17 @@ class Oracle:
                                                 _i64p, _i64, _u16p]
         lib.oracle_linear_rows_f64.argtypes = [_u16p, _u16p, opt, _i64, _i64, _i64,
                                                _i64p, _i64, _f64p]
+        lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_to_f64.restype = ctypes.c_double
+        lib.oracle_rne_e4m3.argtypes = [ctypes.c_double]
+        lib.oracle_rne_e4m3.restype = ctypes.c_uint8
+        lib.oracle_quant_fp8.argtypes = [_u16p, _i64, ctypes.c_float, _u8p]
+        lib.oracle_linear_fp8.argtypes = [_u8p, _u8p, ctypes.c_float, ctypes.c_float, opt, _i64, _i64, _i64, _u16p]
+        lib.oracle_linear_fp8_f64.argtypes = [_u8p, _u8p, ctypes.c_float, ctypes.c_float, opt, _i64, _i64, _i64,
+                                              _f64p]
         for fn in ("oracle_linear_f64", "oracle_linear_bf16", "oracle_linear_f32",
-                   "oracle_linear_rows_bf16", "oracle_linear_rows_f64"):
+                   "oracle_linear_rows_bf16", "oracle_linear_rows_f64", "oracle_quant_fp8",
+                   "oracle_linear_fp8", "oracle_linear_fp8_f64"):
             getattr(lib, fn).restype = None
         self.lib = lib
         self.path = lib_path
@@ -143,6 +159,54 @@ class Oracle:
         b = np.asarray(bits, dtype=np.uint16).ravel()
         f = self.lib.oracle_bf16_to_f64
         return np.array([f(int(h)) for h in b], dtype=np.float64)
+
+    # ---- per-tensor FP8 (e4m3 codes as numpy uint8) ----
+
+    def e4m3_to_f64(self, codes) -> np.ndarray:
+        """Exact value of each e4m3 code (NaN for 0x7F / 0xFF)."""
+        c = np.asarray(codes, dtype=np.uint8).ravel()
+        f = self.lib.oracle_e4m3_to_f64
+        return np.array([f(int(v)) for v in c], dtype=np.float64)
+
+    def rne_e4m3(self, values) -> np.ndarray:
+        """Round each value (|v| <= 448) to the nearest e4m3 code, ties to even."""
+        v = np.asarray(values, dtype=np.float64).ravel()
+        f = self.lib.oracle_rne_e4m3
+        return np.array([f(float(a)) for a in v], dtype=np.uint8)
+
+    def quant_fp8(self, x, scale: float) -> np.ndarray:
+        """Static per-tensor quantisation of bf16 bits x to e4m3 codes (same shape)."""
+        x = np.ascontiguousarray(x, dtype=np.uint16)
+        q = np.empty(x.shape, dtype=np.uint8)
+        self.lib.oracle_quant_fp8(x.ravel(), x.size, float(scale), q.reshape(-1))
+        return q
+
+    def _fp8_prep(self, xq, wq, bias):
+        xq = np.ascontiguousarray(xq, dtype=np.uint8)
+        wq = np.ascontiguousarray(wq, dtype=np.uint8)
+        if xq.ndim != 2 or wq.ndim != 2 or xq.shape[1] != wq.shape[1]:
+            raise ValueError(f"shapes xq{xq.shape} wq{wq.shape}: need xq[M,K], wq[N,K]")
+        M, K = xq.shape
+        N = wq.shape[0]
+        if bias is not None:
+            bias = np.ascontiguousarray(bias, dtype=np.uint16)
+            if bias.shape != (N,):
+                raise ValueError(f"bias shape {bias.shape}: need ({N},)")
+        return xq, wq, bias, M, N, K
+
+    def linear_fp8(self, xq, wq, sx: float, sw: float, bias=None) -> np.ndarray:
+        """bf16 bits of the FP8 linear: RNE_bf16(sx * sw * sum_k e4m3(xq) e4m3(wq) + bias)."""
+        xq, wq, bias, M, N, K = self._fp8_prep(xq, wq, bias)
+        out = np.empty((M, N), dtype=np.uint16)
+        self.lib.oracle_linear_fp8(xq, wq, float(sx), float(sw), _bias_ptr(bias), M, N, K, out)
+        return out
+
+    def linear_fp8_f64(self, xq, wq, sx: float, sw: float, bias=None) -> np.ndarray:
+        """The unrounded FP8 result (f64)."""
+        xq, wq, bias, M, N, K = self._fp8_prep(xq, wq, bias)
+        out = np.empty((M, N), dtype=np.float64)
+        self.lib.oracle_linear_fp8_f64(xq, wq, float(sx), float(sw), _bias_ptr(bias), M, N, K, out)
+        return out
 
 
 def _prep(x, W, bias):
@@ -213,3 +277,23 @@ def rne_f32(values):
 
 def bf16_to_f64(bits):
     return default().bf16_to_f64(bits)
+
+
+def e4m3_to_f64(codes):
+    return default().e4m3_to_f64(codes)
+
+
+def rne_e4m3(values):
+    return default().rne_e4m3(values)
+
+
+def quant_fp8(x, scale):
+    return default().quant_fp8(x, scale)
+
+
+def linear_fp8(xq, wq, sx, sw, bias=None):
+    return default().linear_fp8(xq, wq, sx, sw, bias)
+
+
+def linear_fp8_f64(xq, wq, sx, sw, bias=None):
+    return default().linear_fp8_f64(xq, wq, sx, sw, bias)

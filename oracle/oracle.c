@@ -161,3 +161,127 @@ void oracle_linear_rows_f64(const uint16_t *x, const uint16_t *W, const uint16_t
             acc[r * N + n] = dot_row(x + m * K, W + n * K, bias, n, K);
     }
 }
+
+/*
+ * ---------------------------------------------------------------------------
+ * Per-tensor FP8 linear (the scope's FP8 row).
+ *
+ * Source: the sglang PR #28333 page, section "关键源码片段":
+ *  - apply_fp8_linear_bmm_flashinfer (fp8_utils.py) quantises the input with
+ *    a given per-tensor scale (static_quant_fp8), multiplies the e4m3 operands
+ *    with per-tensor scales x_scale and weight_scale (bmm_fp8, output in the
+ *    input dtype), then adds bias;
+ *  - the static quantisation kernel (fp8_kernel.py, _static_quant_fp8) forms
+ *    y_s_inv = 1 / y_s and stores clamp(y * y_s_inv, fp8_min, fp8_max)
+ *    converted to the e4m3 type, with y and y_s read as fp32.
+ * Readings (also in the design notes): the product and the reciprocal round
+ * to binary32 as in the kernel; the conversion to e4m3 is round-to-nearest
+ * even (the clamp keeps it in range); the scaled sum and the bias meet before
+ * one rounding to bf16, as for the bf16 linear (the page adds bias after a
+ * bf16 result: one more rounding, inside the tolerance).
+ *
+ * e4m3 (the "fn" variant: no infinities), code c:
+ *   s = c >> 7, E = (c >> 3) & 15, m = c & 7
+ *   E == 0                 : (-1)^s * (m / 8) * 2^-6        (subnormal)
+ *   E == 15 and m == 7     : NaN
+ *   otherwise              : (-1)^s * (1 + m / 8) * 2^(E - 7)
+ * Largest finite value 448 = 1.75 * 2^8.
+ * ---------------------------------------------------------------------------
+ */
+static double e4m3_to_f64(uint8_t c)
+{
+    const int s = c >> 7, E = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (E == 15 && m == 7) {
+        uint64_t qnan = 0x7FF8000000000000ULL;
+        memcpy(&v, &qnan, sizeof v);
+        return v;
+    }
+    if (E == 0)
+        v = (double)m / 8.0 * 0.015625;                  /* 2^-6 */
+    else {
+        v = 1.0 + (double)m / 8.0;
+        for (int i = 7; i < E; ++i) v *= 2.0;             /* scale by 2^(E-7) exactly */
+        for (int i = E; i < 7; ++i) v *= 0.5;
+    }
+    return s ? -v : v;
+}
+
+/*
+ * Round a finite value with |v| <= 448 to the nearest e4m3 code, ties to an
+ * even significand; 3 trailing significand bits, exponent bias 7, smallest
+ * normal 2^-6, subnormal unit 2^-9.  Written on the f64 bit pattern like
+ * rne_narrow, with e4m3's own top binade (exponent field 15 is finite).
+ */
+static uint8_t rne_e4m3(double v)
+{
+    uint64_t b;
+    memcpy(&b, &v, sizeof b);
+    const uint8_t sign = (uint8_t)((b >> 63) << 7);
+    const int e = (int)((b >> 52) & 0x7FF);
+    if (e == 0) return sign;                              /* zero (or far below 2^-10) */
+    const uint64_t S = (1ULL << 52) | (b & ((1ULL << 52) - 1));
+    const int E = e - 1023;
+    const int emin = -6, mbits = 3;
+    const int q = (E >= emin ? E : emin) - mbits;         /* exponent of one unit in the last place */
+    const int shift = q - (E - 52);
+    if (shift > 54) return sign;                          /* below a quarter of the smallest subnormal */
+    uint64_t kept = S >> shift;
+    const uint64_t rem = S & ((1ULL << shift) - 1);
+    const uint64_t half = 1ULL << (shift - 1);
+    if (rem > half || (rem == half && (kept & 1))) kept++;
+    if (E >= emin)                                        /* kept in [8, 16]; a carry bumps the exponent */
+        return (uint8_t)(sign | (((E + 7 - 1) << mbits) + (int)kept));
+    return (uint8_t)(sign | (int)kept);                   /* subnormal (kept == 8 is the smallest normal) */
+}
+
+double oracle_e4m3_to_f64(uint8_t c) { return e4m3_to_f64(c); }
+uint8_t oracle_rne_e4m3(double v) { return rne_e4m3(v); }
+
+/* Static per-tensor quantisation of n bf16 values with the given scale. */
+void oracle_quant_fp8(const uint16_t *x, int64_t n, float scale, uint8_t *q)
+{
+    const float inv = 1.0f / scale;                       /* binary32 reciprocal */
+    for (int64_t i = 0; i < n; ++i) {
+        float y = (float)bf16_to_f64(x[i]) * inv;          /* binary32 product */
+        if (y > 448.0f) y = 448.0f;
+        if (y < -448.0f) y = -448.0f;
+        q[i] = rne_e4m3((double)y);
+    }
+}
+
+/*
+ * One FP8 output element, unrounded: the exact f64 sum of the e4m3 products
+ * (each product has at most 8 significant bits between 2^-18 and 2^18, so
+ * sums of up to 2^13 of them are exact in f64), times the two scales, plus
+ * bias.
+ */
+static double dot_row_fp8(const uint8_t *xrow, const uint8_t *wrow, double sxw, const uint16_t *bias,
+                          int64_t n, int64_t K)
+{
+    double acc = 0.0;
+    for (int64_t k = 0; k < K; ++k)
+        acc += e4m3_to_f64(xrow[k]) * e4m3_to_f64(wrow[k]);
+    acc *= sxw;
+    if (bias)
+        acc += bf16_to_f64(bias[n]);
+    return acc;
+}
+
+void oracle_linear_fp8_f64(const uint8_t *xq, const uint8_t *wq, float sx, float sw, const uint16_t *bias,
+                           int64_t M, int64_t N, int64_t K, double *acc)
+{
+    const double sxw = (double)sx * (double)sw;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            acc[m * N + n] = dot_row_fp8(xq + m * K, wq + n * K, sxw, bias, n, K);
+}
+
+void oracle_linear_fp8(const uint8_t *xq, const uint8_t *wq, float sx, float sw, const uint16_t *bias,
+                       int64_t M, int64_t N, int64_t K, uint16_t *out)
+{
+    const double sxw = (double)sx * (double)sw;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            out[m * N + n] = oracle_rne_bf16(dot_row_fp8(xq + m * K, wq + n * K, sxw, bias, n, K));
+}
