@@ -297,6 +297,40 @@ int bf16_linear_noalloc(const void *x, const void *W, const void *bias, void *ou
 /* Size in bytes of the fixed scratch array behind bf16_linear_noalloc. */
 size_t bf16_linear_noalloc_scratch_bytes(void);
 
+/*
+ * ---- Per-tensor FP8 (e4m3) ----
+ *
+ * Source: the sglang PR #28333 page, "关键源码片段": apply_fp8_linear_bmm_flashinfer
+ * quantises the input with a given per-tensor scale (static_quant_fp8), multiplies
+ * the e4m3 operands with per-tensor x_scale and weight_scale (bmm_fp8) and adds
+ * bias; the quantisation kernel forms 1 / scale and stores clamp(y * (1 / scale),
+ * -448, 448) as e4m3.
+ *
+ * bf16_quant_fp8 — static quantisation of n bf16 values x to e4m3 codes xq:
+ *   xq[i] = e4m3_rne(clamp(float(x[i]) * (1.0f / *scale), -448, 448)),
+ *   the reciprocal and the product in binary32.  scale: device pointer to one
+ *   fp32 (read on the device, after the programmatic-launch wait when `flags`
+ *   has BF16L_FLAG_PDL).  x 2-byte aligned (16-byte alignment of x and xq takes
+ *   the vector path), xq must not overlap x.  Asynchronous; BF16L_EINVAL for a
+ *   negative n, NULL pointers or unknown flags; BF16L_EALIGN.
+ *
+ * bf16_linear_fp8 — out[M,N] (bf16) =
+ *   bf16_rne(*scale_x * *scale_w * sum_k e4m3(xq[m,k]) e4m3(wq[n,k]) (+ bias[n]))
+ *   with fp32 accumulation; bias (bf16, may be NULL) enters before the one
+ *   rounding.  xq[M,K] and wq[N,K] are row-major e4m3 codes (one byte each),
+ *   K % 16 == 0 (16-byte rows, else BF16L_EUNSUPPORTED); all data pointers
+ *   16-byte aligned (BF16L_EALIGN); scale_x, scale_w device pointers to one fp32
+ *   each.  Any M (groups of 16 tokens); launches one kernel (warp-level e4m3
+ *   MMAs, K split over a cluster), allocates nothing.
+ *
+ * bf16_linear_fp8_split — the K split bf16_linear_fp8 uses for a shape on a
+ *   device with num_sms SMs (pure host logic; for tests and tuning).
+ */
+int bf16_quant_fp8(const void *x, const float *scale, void *xq, int64_t n, uint32_t flags, bf16l_stream_t stream);
+int bf16_linear_fp8(const void *xq, const void *wq, const float *scale_x, const float *scale_w, const void *bias,
+                    void *out, int M, int N, int K, uint32_t flags, bf16l_stream_t stream);
+int bf16_linear_fp8_split(int M, int N, int K, int num_sms);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *bf16_linear_strerror(int status);
 

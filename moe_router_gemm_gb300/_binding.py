@@ -100,6 +100,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.bf16_linear_plan_ws.restype = i32
         lib.bf16_linear_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp]
         lib.bf16_linear_noalloc.restype = i32
+        lib.bf16_quant_fp8.argtypes = [vp, vp, vp, ctypes.c_int64, ctypes.c_uint32, vp]
+        lib.bf16_quant_fp8.restype = i32
+        lib.bf16_linear_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, ctypes.c_uint32, vp]
+        lib.bf16_linear_fp8.restype = i32
+        lib.bf16_linear_fp8_split.argtypes = [i32, i32, i32, i32]
+        lib.bf16_linear_fp8_split.restype = i32
         lib.bf16_linear_noalloc_scratch_bytes.argtypes = []
         lib.bf16_linear_noalloc_scratch_bytes.restype = ctypes.c_size_t
         lib.bf16_linear_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32), i32]
@@ -307,6 +313,60 @@ def bf16_linear_noalloc(x, W, bias=None, out=None, stream=None):
     if st != OK:
         _raise(st, f"bf16_linear_noalloc(M={M}, N={N}, K={K})")
     return out
+
+
+def quant_fp8(x, scale, out=None, flags: int = 0, stream=None):
+    """Static per-tensor quantisation (bf16_quant_fp8): bf16 x -> e4m3 codes (torch.uint8, same shape).
+
+    `scale` is a one-element fp32 CUDA tensor (read on the device)."""
+    import torch
+    if x.dtype != torch.bfloat16:
+        raise TypeError(f"x must be torch.bfloat16 (got {x.dtype})")
+    if scale.dtype != torch.float32 or scale.numel() != 1 or not scale.is_cuda:
+        raise ValueError("scale must be a one-element float32 CUDA tensor")
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor")
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    elif out.dtype != torch.uint8 or out.shape != x.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous uint8 tensor shaped like x")
+    with torch.cuda.device(x.device):
+        st = load().bf16_quant_fp8(_ptr(x), _ptr(scale), _ptr(out), x.numel(), int(flags),
+                                   _stream_handle(stream, x.device))
+    if st != OK:
+        _raise(st, f"bf16_quant_fp8(n={x.numel()})")
+    return out
+
+
+def bf16_linear_fp8(xq, wq, scale_x, scale_w, bias=None, out=None, flags: int = 0, stream=None):
+    """Per-tensor FP8 linear (bf16_linear_fp8): e4m3 codes xq[M,K], wq[N,K] (torch.uint8),
+    one-element fp32 CUDA scale tensors, optional bf16 bias[N]; bf16 out[M,N]."""
+    import torch
+    for name, t in (("xq", xq), ("wq", wq)):
+        if t.dtype != torch.uint8 or t.dim() != 2 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 2-D uint8 (e4m3 code) CUDA tensor")
+    for name, t in (("scale_x", scale_x), ("scale_w", scale_w)):
+        if t.dtype != torch.float32 or t.numel() != 1 or not t.is_cuda:
+            raise ValueError(f"{name} must be a one-element float32 CUDA tensor")
+    M, K = xq.shape
+    N = wq.shape[0]
+    if wq.shape[1] != K:
+        raise ValueError(f"need xq[M,K] and wq[N,K], got {tuple(xq.shape)} and {tuple(wq.shape)}")
+    if bias is not None and (bias.dtype != torch.bfloat16 or tuple(bias.shape) != (N,) or not bias.is_cuda):
+        raise ValueError(f"bias must be a bf16 CUDA tensor of shape ({N},)")
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=xq.device)
+    with torch.cuda.device(xq.device):
+        st = load().bf16_linear_fp8(_ptr(xq), _ptr(wq), _ptr(scale_x), _ptr(scale_w), _ptr(bias), _ptr(out),
+                                    M, N, K, int(flags), _stream_handle(stream, xq.device))
+    if st != OK:
+        _raise(st, f"bf16_linear_fp8(M={M}, N={N}, K={K})")
+    return out
+
+
+def fp8_split(M: int, N: int, K: int, num_sms: int = 152) -> int:
+    """The K split bf16_linear_fp8 uses for a shape (host logic, no GPU)."""
+    return int(load().bf16_linear_fp8_split(M, N, K, num_sms))
 
 
 def device_status(clear: bool = False) -> int:

@@ -245,6 +245,67 @@ extern "C" int bf16_linear_run(const bf16l_call *call) {
     return bf16l::run(*call);
 }
 
+// ---- per-tensor FP8 ----
+
+extern "C" int bf16_linear_fp8_split(int M, int N, int K, int num_sms) {
+    // K splits of the FP8 kernel: the smallest power of two that gives about two
+    // CTAs per SM, at most 16 (one cluster) and at most one 64-code block each.
+    if (M <= 0 || N <= 0 || K <= 0 || num_sms <= 0) return 1;
+    const long long base = (long long)((N + 7) / 8) * ((M + 15) / 16);
+    const int nblk = (K / 16 + 3) / 4;
+    int S = 1;
+    while (S < 16 && 2 * S <= nblk && base * S < 2LL * num_sms) S *= 2;
+    return S;
+}
+
+extern "C" int bf16_linear_fp8(const void *xq, const void *wq, const float *scale_x, const float *scale_w,
+                               const void *bias, void *out, int M, int N, int K, uint32_t flags,
+                               bf16l_stream_t stream) {
+    using namespace bf16l;
+    if (M < 0 || N <= 0 || K <= 0) return BF16L_EINVAL;
+    if (flags & ~BF16L_FLAG_PDL) return BF16L_EINVAL;
+    if (M == 0) return BF16L_OK;
+    if (!xq || !wq || !out || !scale_x || !scale_w) return BF16L_EINVAL;
+    if (misaligned(xq) || misaligned(wq) || misaligned(out) || (bias && misaligned(bias)) ||
+        (reinterpret_cast<uintptr_t>(scale_x) & 3u) || (reinterpret_cast<uintptr_t>(scale_w) & 3u))
+        return BF16L_EALIGN;
+    if (K % 16 != 0) return BF16L_EUNSUPPORTED;  // 16-byte rows of e4m3 codes
+    const uint64_t ob = 2ull * (uint64_t)M * (uint64_t)N;
+    if (overlaps(out, ob, xq, (uint64_t)M * K) || overlaps(out, ob, wq, (uint64_t)N * K) ||
+        overlaps(out, ob, bias, bias ? 2ull * N : 0))
+        return BF16L_EINVAL;
+    DeviceState *ds = nullptr;
+    const int st = current_device(&ds);
+    if (st != BF16L_OK) return st;
+    const int S = bf16_linear_fp8_split(M, N, K, ds->dev.num_sms);
+    const int e = launch_dotmma_fp8(xq, wq, scale_x, scale_w, bias, out, M, N, K, S, 128, flags, stream,
+                                    ds->status);
+    if (e) {
+        note(e);
+        return BF16L_ELAUNCH;
+    }
+    return BF16L_OK;
+}
+
+extern "C" int bf16_quant_fp8(const void *x, const float *scale, void *xq, int64_t n, uint32_t flags,
+                              bf16l_stream_t stream) {
+    using namespace bf16l;
+    if (n < 0 || (flags & ~BF16L_FLAG_PDL)) return BF16L_EINVAL;
+    if (n == 0) return BF16L_OK;
+    if (!x || !scale || !xq) return BF16L_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(x) & 1u) || (reinterpret_cast<uintptr_t>(scale) & 3u)) return BF16L_EALIGN;
+    if (overlaps(xq, (uint64_t)n, x, 2ull * (uint64_t)n)) return BF16L_EINVAL;
+    DeviceState *ds = nullptr;
+    const int st = current_device(&ds);
+    if (st != BF16L_OK) return st;
+    const int e = launch_quant_fp8(x, scale, xq, (long long)n, ds->dev.num_sms, flags, stream);
+    if (e) {
+        note(e);
+        return BF16L_ELAUNCH;
+    }
+    return BF16L_OK;
+}
+
 extern "C" int bf16_linear_device_status(int32_t *status, int clear) {
     using namespace bf16l;
     if (!status) return BF16L_EINVAL;

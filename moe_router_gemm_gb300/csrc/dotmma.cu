@@ -48,6 +48,17 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// The e4m3 form: each 32-bit register holds 4 codes, so one instruction takes
+// 32 k positions (m16n8k32); the fragments sit in the same registers as above.
+__device__ __forceinline__ void mma16832_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // K blocks (of 4 16-byte vectors = 32 elements) of CTA rank r out of S.
 __host__ __device__ inline int dm_blk(int nblk, int r, int S) { return (int)(((long long)nblk * r) / S); }
 
@@ -62,7 +73,8 @@ size_t dotmma_ws_bytes(int N, const bf16l_plan &p) {
     return dotmma_ws_counter_bytes(groups) + (size_t)groups * p.split_k * 32 * 16;
 }
 
-// Dynamic shared memory: x slice [M][vectors of the largest slice] as 16-byte vectors.
+// Dynamic shared memory: x slice [M][vectors of the largest slice] as 16-byte
+// vectors (K in bf16 elements; an e4m3 row of K codes is K / 2 of them).
 int dotmma_smem_bytes(int M, int K, int S) {
     const int nvec = K / 8, nblk = (nvec + 3) / 4;
     int most = 0;
@@ -76,13 +88,16 @@ int dotmma_smem_bytes(int M, int K, int S) {
 
 // HI: M > 8 (tokens 8..15 on the MMA's upper rows).  XR: x fragments loaded
 // from global memory (L2) straight into registers next to the weights, instead
-// of a bulk copy of the CTA's x slice into shared memory.
-template <bool HI, bool XR, bool WS, typename OutT>
+// of a bulk copy of the CTA's x slice into shared memory.  F8: x and W are e4m3
+// codes (per-tensor FP8; the sum is scaled by *scale_x * *scale_w before bias).
+// Rows of x and W are RB bytes (K * 2 for bf16, K for e4m3).  grid.z: groups of
+// 16 tokens (CTA z takes tokens 16z..16z+15).
+template <bool HI, bool XR, bool WS, bool F8, typename OutT>
 __global__ void __launch_bounds__(kDmWarps * 32)
-    dotmma_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ W, const uint16_t *__restrict__ bias,
-                  OutT *__restrict__ out, int M, int N, int K, int S, int32_t *status, uint32_t *counters,
-                  float4 *tiles) {
-    constexpr int U = 8;  // 32-wide K blocks per lane per batch
+    dotmma_kernel(const uint8_t *__restrict__ x, const uint8_t *__restrict__ W, const uint16_t *__restrict__ bias,
+                  OutT *__restrict__ out, int M, int N, int RB, int S, int32_t *status, uint32_t *counters,
+                  float4 *tiles, const float *__restrict__ scale_x, const float *__restrict__ scale_w) {
+    constexpr int U = 8;  // K blocks (4 x 16 bytes across the lane quad) per lane per batch
     extern __shared__ uint4 xs[];
     __shared__ float4 part[kDmWarps][32];  // per warp, lane (g, t): tokens g, g+8 x rows 2t, 2t+1
     __shared__ float4 recv[kDotMmaMaxCluster][32];
@@ -91,10 +106,16 @@ __global__ void __launch_bounds__(kDmWarps * 32)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
     const int nw = (int)blockDim.x >> 5;
+    {  // this CTA's group of 16 tokens
+        const int m0 = 16 * (int)blockIdx.z;
+        x += (size_t)m0 * RB;
+        out += (size_t)m0 * N;
+        M = (M - m0) < 16 ? (M - m0) : 16;
+    }
     const bool clus = !WS && S > 1;
     const int rank = WS ? (int)blockIdx.x : (S > 1 ? (int)cluster_ctarank() : 0);
     const int n0 = 8 * (int)blockIdx.y;
-    const int nvec = K >> 3, nblk = (nvec + 3) >> 2;
+    const int nvec = RB >> 4, nblk = (nvec + 3) >> 2;
     // this CTA's vectors [cv0, cv1) and this warp's blocks
     const int cb0 = dm_blk(nblk, rank, S), cb1 = dm_blk(nblk, rank + 1, S);
     const int cv0 = 4 * cb0, cv1 = min(nvec, 4 * cb1);
@@ -104,7 +125,7 @@ __global__ void __launch_bounds__(kDmWarps * 32)
     const int sv = cv1 - cv0;  // vectors in this CTA's x slice
     const bool tok_lo = g < M, tok_hi = HI && (g + 8 < M);
     const int row = n0 + g;
-    const uint4 *wr = reinterpret_cast<const uint4 *>(W + (size_t)(row < N ? row : N - 1) * K);
+    const uint4 *wr = reinterpret_cast<const uint4 *>(W + (size_t)(row < N ? row : N - 1) * RB);
 
     if (tid == 0) {
         mbar_init(&xbar, 1);
@@ -131,7 +152,7 @@ __global__ void __launch_bounds__(kDmWarps * 32)
         if (tid == 0 && sv > 0) {
             mbar_arrive_expect_tx(&xbar, (uint32_t)(M * sv * 16));
             for (int m = 0; m < M; ++m)
-                bulk_load(xs + (size_t)m * sv, x + (size_t)m * K + (size_t)cv0 * 8, (uint32_t)(sv * 16), &xbar);
+                bulk_load(xs + (size_t)m * sv, x + (size_t)m * RB + (size_t)cv0 * 16, (uint32_t)(sv * 16), &xbar);
         }
         const bool staged = sv > 0 ? mbar_wait(&xbar, 0, status, kSiteStage) : true;
         ok = __syncthreads_and(staged) != 0;
@@ -141,8 +162,8 @@ __global__ void __launch_bounds__(kDmWarps * 32)
     if (ok) {
         const uint4 *xlo = xs + (size_t)(tok_lo ? g : 0) * sv;  // indexed by vector - cv0
         const uint4 *xhi = xs + (size_t)(tok_hi ? g + 8 : 0) * sv;
-        const uint4 *glo = reinterpret_cast<const uint4 *>(x + (size_t)(tok_lo ? g : 0) * K);
-        const uint4 *ghi = reinterpret_cast<const uint4 *>(x + (size_t)(tok_hi ? g + 8 : 0) * K);
+        const uint4 *glo = reinterpret_cast<const uint4 *>(x + (size_t)(tok_lo ? g : 0) * RB);
+        const uint4 *ghi = reinterpret_cast<const uint4 *>(x + (size_t)(tok_hi ? g + 8 : 0) * RB);
         for (int vb = wv0; vb < wv1; vb += 4 * U) {  // warp-uniform trip count: mma.sync is warp-wide
             if (vb != wv0) load_batch(vb);
             uint4 xl[U], xh[U];
@@ -169,8 +190,13 @@ __global__ void __launch_bounds__(kDmWarps * 32)
                         if (tok_hi && in) hi = xhi[vv - cv0];
                     }
                 }
-                mma16816(d, lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
-                mma16816(d, lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
+                if constexpr (F8) {
+                    mma16832_e4m3(d, lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
+                    mma16832_e4m3(d, lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
+                } else {
+                    mma16816(d, lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
+                    mma16816(d, lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
+                }
             }
         }
     }
@@ -235,7 +261,12 @@ __global__ void __launch_bounds__(kDmWarps * 32)
         cluster_arrive_relaxed();  // phase 2: everything this CTA sends or receives has landed (rank 0)
     }
     if (store && warp == 0 && have) {
-        const float v[4] = {s.x, s.y, s.z, s.w};
+        float v[4] = {s.x, s.y, s.z, s.w};
+        if constexpr (F8) {  // per-tensor scales (read after the grid-dependency wait)
+            const float sxw = __ldg(scale_x) * __ldg(scale_w);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] *= sxw;
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int m = g + (j >> 1) * 8, n = n0 + 2 * t + (j & 1);
@@ -252,18 +283,23 @@ __global__ void __launch_bounds__(kDmWarps * 32)
 namespace {
 
 template <typename OutT>
-using DmFn = void (*)(const uint16_t *, const uint16_t *, const uint16_t *, OutT *, int, int, int, int, int32_t *,
-                      uint32_t *, float4 *);
+using DmFn = void (*)(const uint8_t *, const uint8_t *, const uint16_t *, OutT *, int, int, int, int, int32_t *,
+                      uint32_t *, float4 *, const float *, const float *);
 
 template <bool WS, typename OutT>
 DmFn<OutT> pick_dm_ws(int M, bool xr) {
-    if (xr) return M > 8 ? dotmma_kernel<true, true, WS, OutT> : dotmma_kernel<false, true, WS, OutT>;
-    return M > 8 ? dotmma_kernel<true, false, WS, OutT> : dotmma_kernel<false, false, WS, OutT>;
+    if (xr) return M > 8 ? dotmma_kernel<true, true, WS, false, OutT> : dotmma_kernel<false, true, WS, false, OutT>;
+    return M > 8 ? dotmma_kernel<true, false, WS, false, OutT> : dotmma_kernel<false, false, WS, false, OutT>;
 }
 
 template <typename OutT>
 DmFn<OutT> pick_dm(int M, bool xr, bool ws) {
     return ws ? pick_dm_ws<true, OutT>(M, xr) : pick_dm_ws<false, OutT>(M, xr);
+}
+
+// e4m3 operands: x fragments from L2, clusters along K, bf16 out.
+DmFn<uint16_t> pick_dm_f8(int M) {
+    return M > 8 ? dotmma_kernel<true, true, false, true, uint16_t> : dotmma_kernel<false, true, false, true, uint16_t>;
 }
 
 template <typename OutT>
@@ -282,6 +318,29 @@ int set_dm_attrs() {
 }
 
 template <typename OutT>
+int launch_dm_common(DmFn<OutT> fn, const void *x, const void *W, const void *bias, OutT *out, int M, int N, int RB,
+                     int S, int threads, size_t smem, bool cluster, uint32_t flags, void *stream, int32_t *status,
+                     uint32_t *counters, float4 *tiles, const float *sx, const float *sw) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)S, (unsigned)((N + 7) / 8), (unsigned)((M + 15) / 16));
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = (flags & BF16L_FLAG_PDL) ? 1 : 0;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)S;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = cluster ? 2 : 1;
+    return (int)cudaLaunchKernelEx(&cfg, fn, static_cast<const uint8_t *>(x), static_cast<const uint8_t *>(W),
+                                   static_cast<const uint16_t *>(bias), out, M, N, RB, S, status, counters, tiles,
+                                   sx, sw);
+}
+
+template <typename OutT>
 int launch_dm_t(const LaunchArgs &a, const bf16l_plan &p) {
     const int S = p.split_k;
     const bool ws = p.kernel == BF16L_KERNEL_DOTMMA_WS;
@@ -293,24 +352,11 @@ int launch_dm_t(const LaunchArgs &a, const bf16l_plan &p) {
         counters = static_cast<uint32_t *>(a.workspace);
         tiles = reinterpret_cast<float4 *>(static_cast<uint8_t *>(a.workspace) + dotmma_ws_counter_bytes(groups));
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)S, (unsigned)((a.N + 7) / 8));
-    cfg.blockDim = dim3((unsigned)p.threads);
     const bool xr = p.stages == 1;
-    cfg.dynamicSmemBytes = xr ? 0 : (size_t)dotmma_smem_bytes(a.M, a.K, S);
-    cfg.stream = (cudaStream_t)a.stream;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = (p.flags & BF16L_FLAG_PDL) ? 1 : 0;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = (unsigned)S;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = (S > 1 && !ws) ? 2 : 1;
-    return (int)cudaLaunchKernelEx(&cfg, pick_dm<OutT>(a.M, xr, ws), static_cast<const uint16_t *>(a.x),
-                                   static_cast<const uint16_t *>(a.W), static_cast<const uint16_t *>(a.bias),
-                                   static_cast<OutT *>(a.out), a.M, a.N, a.K, S, a.status, counters, tiles);
+    const size_t smem = xr ? 0 : (size_t)dotmma_smem_bytes(a.M, a.K, S);
+    return launch_dm_common(pick_dm<OutT>(a.M, xr, ws), a.x, a.W, a.bias, static_cast<OutT *>(a.out), a.M, a.N,
+                            a.K * 2, S, p.threads, smem, S > 1 && !ws, (uint32_t)p.flags, a.stream, a.status,
+                            counters, tiles, nullptr, nullptr);
 }
 
 }  // namespace
@@ -318,11 +364,19 @@ int launch_dm_t(const LaunchArgs &a, const bf16l_plan &p) {
 int init_dotmma() {
     int e = set_dm_attrs<uint16_t>();
     if (!e) e = set_dm_attrs<float>();
+    for (int M : {8, 16})
+        if (!e) e = (int)cudaFuncSetAttribute(pick_dm_f8(M), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     return e;
 }
 
 int launch_dotmma(const LaunchArgs &a, const bf16l_plan &p) {
     return a.out_f32 ? launch_dm_t<float>(a, p) : launch_dm_t<uint16_t>(a, p);
+}
+
+int launch_dotmma_fp8(const void *xq, const void *wq, const float *sx, const float *sw, const void *bias, void *out,
+                      int M, int N, int K, int S, int threads, uint32_t flags, void *stream, int32_t *status) {
+    return launch_dm_common(pick_dm_f8(M), xq, wq, bias, static_cast<uint16_t *>(out), M, N, K, S, threads, 0,
+                            S > 1, flags, stream, status, nullptr, nullptr, sx, sw);
 }
 
 }  // namespace bf16l

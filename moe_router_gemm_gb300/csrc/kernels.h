@@ -129,6 +129,13 @@ int launch_tile2(const LaunchArgs &a, const bf16l_plan &p);
 int launch_warprow(const LaunchArgs &a, const bf16l_plan &p);
 int launch_warpmma(const LaunchArgs &a, const bf16l_plan &p);
 int launch_dotmma(const LaunchArgs &a, const bf16l_plan &p);
+// Per-tensor FP8: the router MMA split-K kernel with e4m3 operands (K in bytes
+// = codes; grid.z covers any M in groups of 16 tokens), and the static
+// quantisation of bf16 values with a per-tensor scale.
+int launch_dotmma_fp8(const void *xq, const void *wq, const float *sx, const float *sw, const void *bias, void *out,
+                      int M, int N, int K, int S, int threads, uint32_t flags, void *stream, int32_t *status);
+int launch_quant_fp8(const void *x, const float *scale, void *q, long long n, int num_sms, uint32_t flags,
+                     void *stream);
 
 // One-time per-device kernel attribute setup (dynamic shared memory limits,
 // non-portable cluster sizes).  Returns a cudaError_t value.

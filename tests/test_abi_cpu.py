@@ -116,6 +116,31 @@ def test_validation_without_gpu(lib):
     assert L.bf16_linear(A, B, None, ctypes.c_void_p(0x10000), 1, 4, 8, None) == -1
 
 
+def test_fp8_validation_and_split_without_gpu(lib):
+    L = _raw(lib)
+    A, B, O = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000000), ctypes.c_void_p(0x40000000)
+    S1, S2 = ctypes.c_void_p(0x50000000), ctypes.c_void_p(0x50000010)
+    f = L.bf16_linear_fp8
+    assert f(A, B, S1, S2, None, O, 0, 8, 64, 0, None) == 0            # M == 0: nothing to do
+    assert f(A, B, S1, S2, None, O, -1, 8, 64, 0, None) == -1
+    assert f(A, B, None, S2, None, O, 4, 8, 64, 0, None) == -1          # scales required
+    assert f(A, B, S1, S2, None, O, 4, 8, 64, 2, None) == -1            # unknown flag
+    assert f(ctypes.c_void_p(0x10008), B, S1, S2, None, O, 4, 8, 64, 0, None) == -2
+    assert f(A, B, ctypes.c_void_p(0x50000002), S2, None, O, 4, 8, 64, 0, None) == -2
+    assert f(A, B, S1, S2, None, O, 4, 8, 40, 0, None) == -6            # K % 16 != 0
+    assert f(A, B, S1, S2, None, ctypes.c_void_p(0x10000), 4, 8, 64, 0, None) == -1  # out overlaps xq
+    q = L.bf16_quant_fp8
+    assert q(A, S1, O, 0, 0, None) == 0
+    assert q(A, S1, O, -5, 0, None) == -1
+    assert q(ctypes.c_void_p(0x10001), S1, O, 8, 0, None) == -2
+    assert q(A, S1, ctypes.c_void_p(0x10004), 8, 0, None) == -1          # codes over their own input
+    # K split: about two CTAs per SM, a power of two, at most 16 and one 64-code block each
+    assert lib.fp8_split(16, 384, 7168) == 8       # 48 row groups x 8 >= 304
+    assert lib.fp8_split(1, 14336, 4096) == 1      # 1792 row groups already
+    assert lib.fp8_split(4, 8, 64) == 1            # a single 64-code block
+    assert lib.fp8_split(4, 8, 4096, num_sms=1000) == 16
+
+
 def test_forced_plan_rules_without_gpu(lib):
     L = _raw(lib)
     A, B, O = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000000), ctypes.c_void_p(0x40000000)
