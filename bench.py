@@ -658,6 +658,74 @@ def e2e_arm(args, shapes, lib, device, stream):
     return {"us_per_call": 1000.0 * ms / len(shapes), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
+def fp8_arm(args, points):
+    """Per-tensor FP8 linear (bf16_linear_fp8) on the same shapes, L2-cold, beside the bf16 call.
+
+    Weights are e4m3 codes (quantised once, on the device, with the library's own
+    static quantisation) rotated over copies totalling >= 256 MB; one CUDA graph of
+    R back-to-back calls per shape; algorithmic bytes NK + MK + 2MN (+2N bias)."""
+    import moe_router_gemm_gb300 as lib
+    from moe_router_gemm_gb300 import build as _build
+    _build.build()
+    device = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.Stream(device)
+    peaks = load_peaks()
+    res = {}
+    for pt in points:
+        M, N, K, bias = pt["M"], pt["N"], pt["K"], pt["bias"]
+        if K % 16:
+            continue
+        x, W, b = wl.make_inputs(M, N, K, pt["seed"], bias)
+        sx = torch.tensor([float(x.float().abs().max()) / 448.0], dtype=torch.float32, device=device)
+        sw = torch.tensor([float(W.float().abs().max()) / 448.0], dtype=torch.float32, device=device)
+        xq = lib.quant_fp8(x.to(device), sx)
+        w0 = lib.quant_fp8(W.to(device), sw)
+        R = max(2, -(-L2_COLD_BYTES // (N * K)))
+        Ws = [w0] + [w0.clone() for _ in range(R - 1)]
+        bd = b.to(device) if b is not None else None
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=device)
+        def timed(plan):
+            with torch.cuda.stream(stream):
+                for i in range(2):
+                    lib.bf16_linear_fp8(xq, Ws[i % R], sx, sw, bd, out=out, stream=stream, plan_=plan)
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for i in range(R):
+                        lib.bf16_linear_fp8(xq, Ws[i], sx, sw, bd, out=out, stream=stream, plan_=plan)
+                g.replay()
+                torch.cuda.synchronize()
+                ms = []
+                for _ in range(max(3, args.steps)):
+                    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    g.replay()
+                    e.record(stream)
+                    torch.cuda.synchronize()
+                    ms.append(a.elapsed_time(e))
+            return 1000.0 * statistics.median(ms) / R
+
+        us = timed(None)
+        nbytes = N * K + M * K + 2 * M * N + (2 * N if bias else 0)
+        key = f"M{M}_N{N}_K{K}"
+        res[key] = {"us": round(us, 3), "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
+                    "pct_hbm_roofline": round(100.0 * nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 1),
+                    "split_k": lib.fp8_split(M, N, K, torch.cuda.get_device_properties(device).multi_processor_count)}
+        if args.sweep_fp8:  # every (split, threads) the explicit-plan entry accepts
+            tried = []
+            for S, t in itertools.product((1, 2, 4, 8, 16), (128, 256)):
+                if S > (K // 16 + 3) // 4:
+                    continue
+                tried.append((round(timed(lib.make_plan("dotmma", threads=t, rows_per_cta=8, split_k=S)), 3), S, t))
+            res[key]["sweep"] = sorted(tried)[:4]
+        del Ws
+        torch.cuda.empty_cache()
+    mean = statistics.mean(v["us"] for v in res.values()) if res else None
+    print(json.dumps({"mode": "fp8", "metric": "per-tensor FP8 linear us per call (L2-cold)",
+                      "mean_us": None if mean is None else round(mean, 4), "unit": "us/call",
+                      "workload": workload_desc(args.workload), "shapes": res}))
+
+
 # ---------------------------------------------------------------------------
 # main
 # ---------------------------------------------------------------------------
@@ -671,6 +739,9 @@ def main():
     ap.add_argument("--workload", default="router", choices=["router", "smallest", "decode", "mlp", "prefill", "all"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep-fp8", action="store_true", help="with --fp8: also time every (split, threads)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time the per-tensor FP8 linear (bf16_linear_fp8) on the workload's shapes instead")
     ap.add_argument("--pdl", action="store_true",
                     help="launch with programmatic dependent launch (BF16L_FLAG_PDL): back-to-back calls overlap")
     ap.add_argument("--no-pdl-variant", action="store_true",
@@ -740,6 +811,9 @@ def main():
         return
     if args.sweep:
         sweep(args, points)
+        return
+    if args.fp8:
+        fp8_arm(args, points)
         return
     r = gpu_arm(args, points, rank, world)
     shapes, per_us = r["shapes"], r["per_shape_us"]

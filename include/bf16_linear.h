@@ -323,12 +323,20 @@ size_t bf16_linear_noalloc_scratch_bytes(void);
  *   each.  Any M (groups of 16 tokens); launches one kernel (warp-level e4m3
  *   MMAs, K split over a cluster), allocates nothing.
  *
+ * bf16_linear_fp8_with_plan — the same with an explicit plan: kernel
+ *   BF16L_KERNEL_DOTMMA, threads 128 or 256, split_k 1/2/4/8/16 (at most one
+ *   64-code block per CTA), flags; threads == 0 means the entry point's own
+ *   choice of threads and split.  BF16L_EINVAL for any other plan.
+ *
  * bf16_linear_fp8_split — the K split bf16_linear_fp8 uses for a shape on a
  *   device with num_sms SMs (pure host logic; for tests and tuning).
  */
 int bf16_quant_fp8(const void *x, const float *scale, void *xq, int64_t n, uint32_t flags, bf16l_stream_t stream);
 int bf16_linear_fp8(const void *xq, const void *wq, const float *scale_x, const float *scale_w, const void *bias,
                     void *out, int M, int N, int K, uint32_t flags, bf16l_stream_t stream);
+int bf16_linear_fp8_with_plan(const void *xq, const void *wq, const float *scale_x, const float *scale_w,
+                              const void *bias, void *out, int M, int N, int K, const bf16l_plan *plan,
+                              bf16l_stream_t stream);
 int bf16_linear_fp8_split(int M, int N, int K, int num_sms);
 
 /* Human-readable name of a status code (static string, never NULL). */

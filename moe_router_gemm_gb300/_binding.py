@@ -104,6 +104,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.bf16_quant_fp8.restype = i32
         lib.bf16_linear_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, ctypes.c_uint32, vp]
         lib.bf16_linear_fp8.restype = i32
+        lib.bf16_linear_fp8_with_plan.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, ctypes.POINTER(Plan), vp]
+        lib.bf16_linear_fp8_with_plan.restype = i32
         lib.bf16_linear_fp8_split.argtypes = [i32, i32, i32, i32]
         lib.bf16_linear_fp8_split.restype = i32
         lib.bf16_linear_noalloc_scratch_bytes.argtypes = []
@@ -338,7 +340,8 @@ def quant_fp8(x, scale, out=None, flags: int = 0, stream=None):
     return out
 
 
-def bf16_linear_fp8(xq, wq, scale_x, scale_w, bias=None, out=None, flags: int = 0, stream=None):
+def bf16_linear_fp8(xq, wq, scale_x, scale_w, bias=None, out=None, flags: int = 0, stream=None,
+                    plan_: Plan | None = None):
     """Per-tensor FP8 linear (bf16_linear_fp8): e4m3 codes xq[M,K], wq[N,K] (torch.uint8),
     one-element fp32 CUDA scale tensors, optional bf16 bias[N]; bf16 out[M,N]."""
     import torch
@@ -357,8 +360,13 @@ def bf16_linear_fp8(xq, wq, scale_x, scale_w, bias=None, out=None, flags: int = 
     if out is None:
         out = torch.empty(M, N, dtype=torch.bfloat16, device=xq.device)
     with torch.cuda.device(xq.device):
-        st = load().bf16_linear_fp8(_ptr(xq), _ptr(wq), _ptr(scale_x), _ptr(scale_w), _ptr(bias), _ptr(out),
-                                    M, N, K, int(flags), _stream_handle(stream, xq.device))
+        if plan_ is None:
+            st = load().bf16_linear_fp8(_ptr(xq), _ptr(wq), _ptr(scale_x), _ptr(scale_w), _ptr(bias), _ptr(out),
+                                        M, N, K, int(flags), _stream_handle(stream, xq.device))
+        else:
+            st = load().bf16_linear_fp8_with_plan(_ptr(xq), _ptr(wq), _ptr(scale_x), _ptr(scale_w), _ptr(bias),
+                                                  _ptr(out), M, N, K, ctypes.byref(plan_),
+                                                  _stream_handle(stream, xq.device))
     if st != OK:
         _raise(st, f"bf16_linear_fp8(M={M}, N={N}, K={K})")
     return out

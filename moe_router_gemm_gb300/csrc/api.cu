@@ -249,19 +249,36 @@ extern "C" int bf16_linear_run(const bf16l_call *call) {
 
 extern "C" int bf16_linear_fp8_split(int M, int N, int K, int num_sms) {
     // K splits of the FP8 kernel: the smallest power of two that gives about two
-    // CTAs per SM, at most 16 (one cluster) and at most one 64-code block each.
+    // CTAs per SM, at most 8 (16-CTA clusters measured slower on every shape)
+    // and at most one 64-code block each.
     if (M <= 0 || N <= 0 || K <= 0 || num_sms <= 0) return 1;
     const long long base = (long long)((N + 7) / 8) * ((M + 15) / 16);
     const int nblk = (K / 16 + 3) / 4;
     int S = 1;
-    while (S < 16 && 2 * S <= nblk && base * S < 2LL * num_sms) S *= 2;
+    while (S < 8 && 2 * S <= nblk && base * S < 2LL * num_sms) S *= 2;
     return S;
 }
+
+extern "C" int bf16_linear_fp8_with_plan(const void *xq, const void *wq, const float *scale_x,
+                                         const float *scale_w, const void *bias, void *out, int M, int N, int K,
+                                         const bf16l_plan *plan, bf16l_stream_t stream);
 
 extern "C" int bf16_linear_fp8(const void *xq, const void *wq, const float *scale_x, const float *scale_w,
                                const void *bias, void *out, int M, int N, int K, uint32_t flags,
                                bf16l_stream_t stream) {
+    bf16l_plan p = {};
+    p.kernel = BF16L_KERNEL_DOTMMA;
+    p.threads = 0;  // chosen below, with the split, for this shape
+    p.flags = (int32_t)flags;
+    return bf16_linear_fp8_with_plan(xq, wq, scale_x, scale_w, bias, out, M, N, K, &p, stream);
+}
+
+extern "C" int bf16_linear_fp8_with_plan(const void *xq, const void *wq, const float *scale_x,
+                                         const float *scale_w, const void *bias, void *out, int M, int N, int K,
+                                         const bf16l_plan *plan, bf16l_stream_t stream) {
     using namespace bf16l;
+    if (!plan) return BF16L_EINVAL;
+    const uint32_t flags = (uint32_t)plan->flags;
     if (M < 0 || N <= 0 || K <= 0) return BF16L_EINVAL;
     if (flags & ~BF16L_FLAG_PDL) return BF16L_EINVAL;
     if (M == 0) return BF16L_OK;
@@ -277,8 +294,15 @@ extern "C" int bf16_linear_fp8(const void *xq, const void *wq, const float *scal
     DeviceState *ds = nullptr;
     const int st = current_device(&ds);
     if (st != BF16L_OK) return st;
-    const int S = bf16_linear_fp8_split(M, N, K, ds->dev.num_sms);
-    const int e = launch_dotmma_fp8(xq, wq, scale_x, scale_w, bias, out, M, N, K, S, 128, flags, stream,
+    int S = plan->split_k, threads = plan->threads;
+    if (threads == 0) {  // the entry point's own choice
+        S = bf16_linear_fp8_split(M, N, K, ds->dev.num_sms);
+        threads = 128;
+    } else if (plan->kernel != BF16L_KERNEL_DOTMMA || (threads != 128 && threads != 256) ||
+               (S != 1 && S != 2 && S != 4 && S != 8 && S != 16) || S > (K / 16 + 3) / 4) {
+        return BF16L_EINVAL;
+    }
+    const int e = launch_dotmma_fp8(xq, wq, scale_x, scale_w, bias, out, M, N, K, S, threads, flags, stream,
                                     ds->status);
     if (e) {
         note(e);

@@ -134,11 +134,11 @@ def test_fp8_validation_and_split_without_gpu(lib):
     assert q(A, S1, O, -5, 0, None) == -1
     assert q(ctypes.c_void_p(0x10001), S1, O, 8, 0, None) == -2
     assert q(A, S1, ctypes.c_void_p(0x10004), 8, 0, None) == -1          # codes over their own input
-    # K split: about two CTAs per SM, a power of two, at most 16 and one 64-code block each
+    # K split: about two CTAs per SM, a power of two, at most 8 and one 64-code block each
     assert lib.fp8_split(16, 384, 7168) == 8       # 48 row groups x 8 >= 304
     assert lib.fp8_split(1, 14336, 4096) == 1      # 1792 row groups already
     assert lib.fp8_split(4, 8, 64) == 1            # a single 64-code block
-    assert lib.fp8_split(4, 8, 4096, num_sms=1000) == 16
+    assert lib.fp8_split(4, 8, 4096, num_sms=1000) == 8
 
 
 def test_forced_plan_rules_without_gpu(lib):
