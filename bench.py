@@ -716,7 +716,14 @@ def fp8_arm(args, points):
             for S, t in itertools.product((1, 2, 4, 8, 16), (128, 256)):
                 if S > (K // 16 + 3) // 4:
                     continue
-                tried.append((round(timed(lib.make_plan("dotmma", threads=t, rows_per_cta=8, split_k=S)), 3), S, t))
+                tried.append((round(timed(lib.make_plan("dotmma", threads=t, rows_per_cta=8, split_k=S)), 3),
+                              "split", S, t))
+            if M <= 16 and M * K <= 200 * 1024:
+                for t, w, c in ((1024, 8, 1), (1024, 16, 1), (512, 4, 2), (512, 8, 2), (256, 8, 4), (256, 2, 4)):
+                    if c * (M * K + (16384 if w > 1 else 512) + 1024) > 232448:
+                        continue
+                    p = lib.make_plan("warpmma", threads=t, rows_per_cta=w, stages=c)
+                    tried.append((round(timed(p), 3), "warpmma", w, t, c))
             res[key]["sweep"] = sorted(tried)[:4]
         del Ws
         torch.cuda.empty_cache()

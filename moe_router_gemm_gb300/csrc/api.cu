@@ -294,16 +294,48 @@ extern "C" int bf16_linear_fp8_with_plan(const void *xq, const void *wq, const f
     DeviceState *ds = nullptr;
     const int st = current_device(&ds);
     if (st != BF16L_OK) return st;
-    int S = plan->split_k, threads = plan->threads;
+    int kernel = plan->kernel, S = plan->split_k, threads = plan->threads, wpr = plan->rows_per_cta,
+        cps = plan->stages;
     if (threads == 0) {  // the entry point's own choice
-        S = bf16_linear_fp8_split(M, N, K, ds->dev.num_sms);
-        threads = 128;
-    } else if (plan->kernel != BF16L_KERNEL_DOTMMA || (threads != 128 && threads != 256) ||
-               (S != 1 && S != 2 && S != 4 && S != 8 && S != 16) || S > (K / 16 + 3) / 4) {
+        if (M <= kWarpMmaMaxTokens && (size_t)M * K <= (size_t)kWarpMmaMaxSmem && N >= 1024) {
+            // Many rows: the persistent warp-MMA form.  Measured on GB300: more,
+            // smaller CTAs per SM win where x is small enough to stage that often.
+            kernel = BF16L_KERNEL_WARPMMA;
+            const long long xs = (long long)M * K + 32 * 32 * 4 * 4 + 1024;
+            if (N >= 8192 && M <= 4 && 4 * xs <= 232448) {
+                threads = 256, wpr = 2, cps = 4;
+            } else if (2 * xs <= 232448) {
+                threads = 512, wpr = N >= 8192 ? 4 : 8, cps = 2;
+            } else {
+                threads = 1024, wpr = 8, cps = 1;
+            }
+        } else {
+            kernel = BF16L_KERNEL_DOTMMA;
+            S = bf16_linear_fp8_split(M, N, K, ds->dev.num_sms);
+            threads = 128;
+        }
+    }
+    int e = 0;
+    if (kernel == BF16L_KERNEL_DOTMMA) {
+        if ((threads != 128 && threads != 256) || (S != 1 && S != 2 && S != 4 && S != 8 && S != 16) ||
+            S > (K / 16 + 3) / 4)
+            return BF16L_EINVAL;
+        e = launch_dotmma_fp8(xq, wq, scale_x, scale_w, bias, out, M, N, K, S, threads, flags, stream, ds->status);
+    } else if (kernel == BF16L_KERNEL_WARPMMA) {
+        // x (M x K codes) staged in shared memory; 8 W rows per group of wpr warps
+        if (M > kWarpMmaMaxTokens || (size_t)M * K > (size_t)kWarpMmaMaxSmem) return BF16L_EUNSUPPORTED;
+        const int static_smem = (wpr > 1 ? 32 * 32 * 4 * 4 : 512) + 1024;
+        if ((threads != 256 && threads != 512 && threads != 1024) ||
+            (wpr != 1 && wpr != 2 && wpr != 4 && wpr != 8 && wpr != 16) || (threads / 32) % wpr != 0 ||
+            (wpr > 1 && (threads / 32) / wpr > 15) || S != 0 || cps < 1 || cps > 4 || threads * cps > 1024 ||
+            (long long)cps * ((long long)M * K + static_smem) > 232448)
+            return BF16L_EINVAL;
+        const long long ctas = (long long)ds->dev.num_sms * cps, groups = (N + 7) / 8;
+        e = launch_warpmma_fp8(xq, wq, scale_x, scale_w, bias, out, M, N, K, wpr, threads,
+                               (int)(ctas < groups ? ctas : groups), flags, stream, ds->status);
+    } else {
         return BF16L_EINVAL;
     }
-    const int e = launch_dotmma_fp8(xq, wq, scale_x, scale_w, bias, out, M, N, K, S, threads, flags, stream,
-                                    ds->status);
     if (e) {
         note(e);
         return BF16L_ELAUNCH;

@@ -50,6 +50,16 @@ __device__ __forceinline__ void mma_m16n8k16(float (&d)[4], uint32_t a0, uint32_
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// e4m3 form: 4 codes per register, 32 k positions per instruction.
+__device__ __forceinline__ void mma_m16n8k32_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                                  uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 }  // namespace
 
 int warpmma_smem_bytes(int M, int K) { return M * K * 2; }
@@ -59,13 +69,16 @@ int warpmma_smem_bytes(int M, int K) { return M * K * 2; }
 // (tokens 8..15 in the MMA's upper rows).  XR: x fragments loaded from L2 into
 // registers with each weight batch instead of staged in shared memory (for x
 // too large to stage, e.g. 16 tokens of K = 7168); 512 threads per SM then, as
-// the batch of x fragments takes another 64 registers a thread.
-template <int WPR, int NT, bool HI, bool XR, typename OutT>
+// the batch of x fragments takes another 64 registers a thread.  F8: x and W
+// are e4m3 codes (m16n8k32 MMAs on the same registers; the sum is scaled by
+// *scale_x * *scale_w before bias).  Rows of x and W are RB bytes.
+template <int WPR, int NT, bool HI, bool XR, bool F8, typename OutT>
 __global__ void __launch_bounds__(NT, XR ? 1 : 1024 / NT)
-    warpmma_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ W, const uint16_t *__restrict__ bias,
-                   OutT *__restrict__ out, int M, int N, int K, int32_t *status) {
-    constexpr int U = 8;                           // 32-wide K blocks per lane per batch
-    extern __shared__ uint4 xs[];                  // x[m][k] as 16-byte vectors, [M][K / 8]
+    warpmma_kernel(const uint8_t *__restrict__ x, const uint8_t *__restrict__ W, const uint16_t *__restrict__ bias,
+                   OutT *__restrict__ out, int M, int N, int RB, int32_t *status, const float *__restrict__ scale_x,
+                   const float *__restrict__ scale_w) {
+    constexpr int U = 8;                           // K blocks (4 x 16 bytes across a lane quad) per lane per batch
+    extern __shared__ uint4 xs[];                  // x[m] rows as 16-byte vectors, [M][RB / 16]
     __shared__ float part[WPR > 1 ? kWmMaxWarps : 1][32][4];  // WPR > 1: every lane's four sums
     __shared__ __align__(8) uint64_t xbar;
 
@@ -74,7 +87,7 @@ __global__ void __launch_bounds__(NT, XR ? 1 : 1024 / NT)
     const int nw = (int)blockDim.x >> 5;
     const int groups = nw / WPR;
     const int grp = warp / WPR, gw = warp - grp * WPR;
-    const int nvec = K >> 3;
+    const int nvec = RB >> 4;
     // this warp's K slice in 16-byte vectors, whole 32-wide blocks (4 vectors)
     const int nblk = (nvec + 3) >> 2;
     const int per = (nblk + WPR - 1) / WPR;
@@ -94,7 +107,7 @@ __global__ void __launch_bounds__(NT, XR ? 1 : 1024 / NT)
     uint4 wv[U];
     auto load_batch = [&](int n0, int vb) {  // the batch of blocks starting at vector vb
         const int row = n0 + g;
-        const uint4 *wr = reinterpret_cast<const uint4 *>(W + (size_t)(row < N ? row : N - 1) * K);
+        const uint4 *wr = reinterpret_cast<const uint4 *>(W + (size_t)(row < N ? row : N - 1) * RB);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int vv = vb + 4 * u + t;
@@ -109,9 +122,9 @@ __global__ void __launch_bounds__(NT, XR ? 1 : 1024 / NT)
     __syncthreads();
     if constexpr (!XR) {
         if (tid == 0 && q1 > q0) {
-            mbar_arrive_expect_tx(&xbar, (uint32_t)(M * K * 2));
+            mbar_arrive_expect_tx(&xbar, (uint32_t)(M * RB));
             for (int m = 0; m < M; ++m)
-                bulk_load(xs + (size_t)m * nvec, x + (size_t)m * K, (uint32_t)(K * 2), &xbar);
+                bulk_load(xs + (size_t)m * nvec, x + (size_t)m * RB, (uint32_t)RB, &xbar);
         }
         const bool staged = q1 > q0 ? mbar_wait(&xbar, 0, status, kSiteStage) : true;
         if (!__syncthreads_and(staged)) return;  // the whole CTA leaves together (only after a timeout)
@@ -119,8 +132,8 @@ __global__ void __launch_bounds__(NT, XR ? 1 : 1024 / NT)
 
     const uint4 *xlo = xs + (size_t)(tok_lo ? g : 0) * nvec;
     const uint4 *xhi = xs + (size_t)(tok_hi ? g + 8 : 0) * nvec;
-    const uint4 *glo = reinterpret_cast<const uint4 *>(x + (size_t)(tok_lo ? g : 0) * K);
-    const uint4 *ghi = reinterpret_cast<const uint4 *>(x + (size_t)(tok_hi ? g + 8 : 0) * K);
+    const uint4 *glo = reinterpret_cast<const uint4 *>(x + (size_t)(tok_lo ? g : 0) * RB);
+    const uint4 *ghi = reinterpret_cast<const uint4 *>(x + (size_t)(tok_hi ? g + 8 : 0) * RB);
     for (bool first = true; q < q1; q += groups, first = false) {
         const int n0 = 8 * q;
         float d[4] = {0.f, 0.f, 0.f, 0.f};
@@ -150,9 +163,14 @@ __global__ void __launch_bounds__(NT, XR ? 1 : 1024 / NT)
                         if (tok_hi && in) hi = xhi[vv];
                     }
                 }
-                // this lane's block positions 8t..8t+7: step 0 takes +0..3, step 1 takes +4..7
-                mma_m16n8k16(d, lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
-                mma_m16n8k16(d, lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
+                // this lane's 16 block bytes: step 0 takes the first 8, step 1 the last 8
+                if constexpr (F8) {
+                    mma_m16n8k32_e4m3(d, lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
+                    mma_m16n8k32_e4m3(d, lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
+                } else {
+                    mma_m16n8k16(d, lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
+                    mma_m16n8k16(d, lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
+                }
             }
         }
         if constexpr (WPR > 1) {
@@ -169,6 +187,11 @@ __global__ void __launch_bounds__(NT, XR ? 1 : 1024 / NT)
             }
         }
         if (WPR == 1 || gw == 0) {
+            if constexpr (F8) {  // per-tensor scales (read after the grid-dependency wait)
+                const float sxw = __ldg(scale_x) * __ldg(scale_w);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) d[j] *= sxw;
+            }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int m = g + (j >> 1) * 8, n = n0 + 2 * t + (j & 1);
@@ -186,30 +209,39 @@ __global__ void __launch_bounds__(NT, XR ? 1 : 1024 / NT)
 namespace {
 
 template <typename OutT>
-using WmFn = void (*)(const uint16_t *, const uint16_t *, const uint16_t *, OutT *, int, int, int, int32_t *);
+using WmFn = void (*)(const uint8_t *, const uint8_t *, const uint16_t *, OutT *, int, int, int, int32_t *,
+                      const float *, const float *);
 
-template <int WPR, bool HI, bool XR, typename OutT>
+template <int WPR, bool HI, bool XR, bool F8, typename OutT>
 WmFn<OutT> pick_nt(int threads) {
-    if constexpr (XR) return warpmma_kernel<WPR, 512, HI, true, OutT>;  // at most 512 threads
-    return threads > 512 ? warpmma_kernel<WPR, 1024, HI, false, OutT> : warpmma_kernel<WPR, 512, HI, false, OutT>;
+    if constexpr (XR) return warpmma_kernel<WPR, 512, HI, true, F8, OutT>;  // at most 512 threads
+    return threads > 512 ? warpmma_kernel<WPR, 1024, HI, false, F8, OutT>
+                         : warpmma_kernel<WPR, 512, HI, false, F8, OutT>;
 }
 
-template <bool HI, bool XR, typename OutT>
+template <bool HI, bool XR, bool F8, typename OutT>
 WmFn<OutT> pick_wpr(int wpr, int threads) {
     switch (wpr) {
-        case 1: return pick_nt<1, HI, XR, OutT>(threads);
-        case 2: return pick_nt<2, HI, XR, OutT>(threads);
-        case 4: return pick_nt<4, HI, XR, OutT>(threads);
-        case 8: return pick_nt<8, HI, XR, OutT>(threads);
-        case 16: return pick_nt<16, HI, XR, OutT>(threads);
+        case 1: return pick_nt<1, HI, XR, F8, OutT>(threads);
+        case 2: return pick_nt<2, HI, XR, F8, OutT>(threads);
+        case 4: return pick_nt<4, HI, XR, F8, OutT>(threads);
+        case 8: return pick_nt<8, HI, XR, F8, OutT>(threads);
+        case 16: return pick_nt<16, HI, XR, F8, OutT>(threads);
         default: return nullptr;
     }
 }
 
 template <typename OutT>
 WmFn<OutT> pick_wm(int M, int wpr, int threads, bool xr) {
-    if (xr) return M > 8 ? pick_wpr<true, true, OutT>(wpr, threads) : pick_wpr<false, true, OutT>(wpr, threads);
-    return M > 8 ? pick_wpr<true, false, OutT>(wpr, threads) : pick_wpr<false, false, OutT>(wpr, threads);
+    if (xr)
+        return M > 8 ? pick_wpr<true, true, false, OutT>(wpr, threads) : pick_wpr<false, true, false, OutT>(wpr, threads);
+    return M > 8 ? pick_wpr<true, false, false, OutT>(wpr, threads) : pick_wpr<false, false, false, OutT>(wpr, threads);
+}
+
+// e4m3 operands: x staged in shared memory, bf16 out.
+WmFn<uint16_t> pick_wm_f8(int M, int wpr, int threads) {
+    return M > 8 ? pick_wpr<true, false, true, uint16_t>(wpr, threads)
+                 : pick_wpr<false, false, true, uint16_t>(wpr, threads);
 }
 
 template <typename OutT>
@@ -226,23 +258,31 @@ int set_wm_attrs() {
 }
 
 template <typename OutT>
-int launch_wm_t(const LaunchArgs &a, const bf16l_plan &p) {
-    const bool xr = p.split_k == 1;
-    WmFn<OutT> fn = pick_wm<OutT>(a.M, p.rows_per_cta, p.threads, xr);
+int launch_wm_common(WmFn<OutT> fn, const void *x, const void *W, const void *bias, OutT *out, int M, int N,
+                     int RB, int grid, int threads, size_t smem, uint32_t flags, void *stream, int32_t *status,
+                     const float *sx, const float *sw) {
     if (!fn) return (int)cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.grid);
-    cfg.blockDim = dim3((unsigned)p.threads);
-    cfg.dynamicSmemBytes = xr ? 0 : (size_t)warpmma_smem_bytes(a.M, a.K);
-    cfg.stream = (cudaStream_t)a.stream;
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = (cudaStream_t)stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = (p.flags & BF16L_FLAG_PDL) ? 1 : 0;
+    attr[0].val.programmaticStreamSerializationAllowed = (flags & BF16L_FLAG_PDL) ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return (int)cudaLaunchKernelEx(&cfg, fn, static_cast<const uint16_t *>(a.x), static_cast<const uint16_t *>(a.W),
-                                   static_cast<const uint16_t *>(a.bias), static_cast<OutT *>(a.out), a.M, a.N, a.K,
-                                   a.status);
+    return (int)cudaLaunchKernelEx(&cfg, fn, static_cast<const uint8_t *>(x), static_cast<const uint8_t *>(W),
+                                   static_cast<const uint16_t *>(bias), out, M, N, RB, status, sx, sw);
+}
+
+template <typename OutT>
+int launch_wm_t(const LaunchArgs &a, const bf16l_plan &p) {
+    const bool xr = p.split_k == 1;
+    return launch_wm_common(pick_wm<OutT>(a.M, p.rows_per_cta, p.threads, xr), a.x, a.W, a.bias,
+                            static_cast<OutT *>(a.out), a.M, a.N, a.K * 2, p.grid, p.threads,
+                            xr ? 0 : (size_t)warpmma_smem_bytes(a.M, a.K), (uint32_t)p.flags, a.stream, a.status,
+                            nullptr, nullptr);
 }
 
 }  // namespace
@@ -250,11 +290,24 @@ int launch_wm_t(const LaunchArgs &a, const bf16l_plan &p) {
 int init_warpmma() {
     int e = set_wm_attrs<uint16_t>();
     if (!e) e = set_wm_attrs<float>();
+    for (int M : {8, 16})
+        for (int wpr : {1, 2, 4, 8, 16})
+            for (int t : {512, 1024})
+                if (!e)
+                    e = (int)cudaFuncSetAttribute(pick_wm_f8(M, wpr, t), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  kWarpMmaMaxSmem);
     return e;
 }
 
 int launch_warpmma(const LaunchArgs &a, const bf16l_plan &p) {
     return a.out_f32 ? launch_wm_t<float>(a, p) : launch_wm_t<uint16_t>(a, p);
+}
+
+int launch_warpmma_fp8(const void *xq, const void *wq, const float *sx, const float *sw, const void *bias, void *out,
+                       int M, int N, int K, int wpr, int threads, int grid, uint32_t flags, void *stream,
+                       int32_t *status) {
+    return launch_wm_common(pick_wm_f8(M, wpr, threads), xq, wq, bias, static_cast<uint16_t *>(out), M, N, K, grid,
+                            threads, (size_t)M * K, flags, stream, status, sx, sw);
 }
 
 }  // namespace bf16l

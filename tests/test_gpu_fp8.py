@@ -112,6 +112,36 @@ def test_linear_fp8_deterministic_and_pdl(lib):
         assert torch.equal(o, a)
 
 
+WM_CFGS = [(1024, 8, 1), (512, 4, 2), (256, 1, 4), (1024, 16, 1), (512, 2, 1)]
+
+
+@pytest.mark.parametrize("cfg", WM_CFGS, ids=lambda c: "t%d_wpr%d_cps%d" % c)
+@pytest.mark.parametrize("shape", [(4, 2112, 7168), (16, 1000, 1024), (1, 14336, 4096), (9, 77, 2048)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_linear_fp8_warpmma_form(lib, shape, cfg):
+    M, N, K = shape
+    t, w, c = cfg
+    p = lib.make_plan("warpmma", threads=t, rows_per_cta=w, stages=c)
+    for bias in (False, True):
+        x, W, b, xq, wq, sx, sw = _fp8_inputs(M, N, K, M + N + K + w, bias)
+        bd = b.to(DEV) if b is not None else None
+        xd, wd = torch.from_numpy(xq).to(DEV), torch.from_numpy(wq).to(DEV)
+        out = lib.bf16_linear_fp8(xd, wd, _scale(sx), _scale(sw), bd, plan_=p)
+        torch.cuda.synchronize()
+        check_close(tensor_bits(out), oracle.linear_fp8(xq, wq, sx, sw, wl.bits(b)),
+                    f"fp8 warpmma M={M} N={N} K={K} cfg={cfg} bias={bias}")
+
+
+@pytest.mark.parametrize("S,t", [(1, 128), (4, 256), (8, 128), (16, 256)])
+def test_linear_fp8_split_form(lib, S, t):
+    M, N, K = 16, 256, 7168
+    x, W, b, xq, wq, sx, sw = _fp8_inputs(M, N, K, S, True)
+    out = lib.bf16_linear_fp8(torch.from_numpy(xq).to(DEV), torch.from_numpy(wq).to(DEV), _scale(sx), _scale(sw),
+                              b.to(DEV), plan_=lib.make_plan("dotmma", threads=t, rows_per_cta=8, split_k=S))
+    torch.cuda.synchronize()
+    check_close(tensor_bits(out), oracle.linear_fp8(xq, wq, sx, sw, wl.bits(b)), f"fp8 split S={S} t={t}")
+
+
 def test_linear_fp8_rejects(lib):
     xq = torch.zeros(4, 40, dtype=torch.uint8, device=DEV)
     wq = torch.zeros(8, 40, dtype=torch.uint8, device=DEV)
@@ -121,3 +151,8 @@ def test_linear_fp8_rejects(lib):
     wq = torch.zeros(8, 64, dtype=torch.uint8, device=DEV)
     with pytest.raises(ValueError):
         lib.bf16_linear_fp8(xq, wq, torch.ones(2, device=DEV), _scale(1.0))
+    with pytest.raises(lib.BF16LinearError):  # a kernel the FP8 entry does not run
+        lib.bf16_linear_fp8(xq, wq, _scale(1.0), _scale(1.0), plan_=lib.make_plan("tile", threads=192))
+    with pytest.raises(lib.BF16LinearError):  # 17 tokens do not fit the warp-MMA form
+        lib.bf16_linear_fp8(torch.zeros(17, 64, dtype=torch.uint8, device=DEV), wq, _scale(1.0), _scale(1.0),
+                            plan_=lib.make_plan("warpmma", threads=512, rows_per_cta=4, stages=1))
