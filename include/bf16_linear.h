@@ -327,10 +327,11 @@ size_t bf16_linear_noalloc_scratch_bytes(void);
  *   BF16L_KERNEL_DOTMMA (threads 128 or 256, split_k 1/2/4/8/16, at most one
  *   64-code block per CTA; any M) or BF16L_KERNEL_WARPMMA (the persistent
  *   warp-MMA form: threads 256/512/1024, rows_per_cta = warps per 8-row group,
- *   stages = CTAs per SM, split_k 0; M <= 16 and M * K <= 200 KB), flags;
- *   threads == 0 means the entry point's own choice (the warp-MMA form for
- *   N >= 1024 when it applies, else the split form).  BF16L_EINVAL for any
- *   other plan.
+ *   stages = CTAs per SM, split_k 0; M <= 16 and M * K <= 200 KB) or
+ *   BF16L_KERNEL_TILE (the tcgen05 kind::f8f6f4 tile form: threads 192,
+ *   stages 2..4; any M), flags; threads == 0 means the entry point's own
+ *   choice (the tile form for M > 16, else the warp-MMA form for N >= 1024
+ *   when it applies, else the split form).  BF16L_EINVAL for any other plan.
  *
  * bf16_linear_fp8_split — the K split bf16_linear_fp8 uses for a shape on a
  *   device with num_sms SMs (pure host logic; for tests and tuning).

@@ -189,8 +189,8 @@ __global__ void selftest_wait_kernel(int32_t *status, uint64_t limit_ns) {
 
 }  // namespace
 
-int make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
-                      uint32_t box_cols, CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo) {
+// cuTensorMapEncodeTiled, looked up once from the driver.
+static PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     std::call_once(g_encode_once, [] {
         void *fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -199,13 +199,31 @@ int make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_
             q == cudaDriverEntryPointSuccess)
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     });
-    if (!g_encode) return (int)CUDA_ERROR_NOT_FOUND;
+    return g_encode;
+}
+
+static int make_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, uint64_t esize, const void *base,
+                        uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_cols,
+                        CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+    if (!enc) return (int)CUDA_ERROR_NOT_FOUND;
     const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols * 2};  // bytes between rows
+    const cuuint64_t strides[1] = {cols * esize};  // bytes between rows
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    return (int)g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return (int)enc(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+int make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                      uint32_t box_cols, CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo) {
+    return make_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, rows, cols, box_rows, box_cols, swizzle,
+                        promo);
+}
+
+int make_tmap_u8_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                    uint32_t box_cols, CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo) {
+    return make_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, rows, cols, box_rows, box_cols, swizzle, promo);
 }
 
 }  // namespace bf16l
@@ -297,7 +315,11 @@ extern "C" int bf16_linear_fp8_with_plan(const void *xq, const void *wq, const f
     int kernel = plan->kernel, S = plan->split_k, threads = plan->threads, wpr = plan->rows_per_cta,
         cps = plan->stages;
     if (threads == 0) {  // the entry point's own choice
-        if (M <= kWarpMmaMaxTokens && (size_t)M * K <= (size_t)kWarpMmaMaxSmem && N >= 1024) {
+        if (M > 16) {  // a dense contraction: the tcgen05 tile form (kind::f8f6f4)
+            kernel = BF16L_KERNEL_TILE;
+            threads = kTileThreads;
+            cps = kTileMaxStages;
+        } else if (M <= kWarpMmaMaxTokens && (size_t)M * K <= (size_t)kWarpMmaMaxSmem && N >= 1024) {
             // Many rows: the persistent warp-MMA form.  Measured on GB300: more,
             // smaller CTAs per SM win where x is small enough to stage that often.
             kernel = BF16L_KERNEL_WARPMMA;
@@ -333,6 +355,12 @@ extern "C" int bf16_linear_fp8_with_plan(const void *xq, const void *wq, const f
         const long long ctas = (long long)ds->dev.num_sms * cps, groups = (N + 7) / 8;
         e = launch_warpmma_fp8(xq, wq, scale_x, scale_w, bias, out, M, N, K, wpr, threads,
                                (int)(ctas < groups ? ctas : groups), flags, stream, ds->status);
+    } else if (kernel == BF16L_KERNEL_TILE) {
+        // stages = ring depth; tiles of 128 x rows by 256 W rows, 128 codes per 128-byte swizzle row
+        if (threads != kTileThreads || cps < kTileMinStages || cps > kTileMaxStages) return BF16L_EINVAL;
+        const long long tiles = (long long)((M + kTileBM - 1) / kTileBM) * ((N + kTileBN - 1) / kTileBN);
+        const int grid = (int)(tiles < ds->dev.num_sms ? tiles : ds->dev.num_sms);
+        e = launch_tile_fp8(xq, wq, scale_x, scale_w, bias, out, M, N, K, cps, grid, flags, stream, ds->status);
     } else {
         return BF16L_EINVAL;
     }

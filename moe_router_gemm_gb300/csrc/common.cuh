@@ -298,6 +298,23 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int mma_m, int mma_n) {
            | ((uint32_t)(mma_n >> 3) << 17) | ((uint32_t)(mma_m >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f8f6f4 with both operands e4m3 (format code 0):
+// D fp32, K-major A and B, N>>3 at bit 17, M>>4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int mma_m, int mma_n) {
+    return (1u << 4) | ((uint32_t)(mma_n >> 3) << 17) | ((uint32_t)(mma_m >> 4) << 24);
+}
+
+// One e4m3 MMA (K = 32 codes per instruction): D[tmem] (+)= A[smem] * B[smem]^T.
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // One MMA: D[tmem] (+)= A[smem] * B[smem]^T, issued by a single thread.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t accumulate) {
@@ -490,5 +507,8 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 // ---------------------------------------------------------------------------
 int make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
                       uint32_t box_cols, CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo);
+// The same for one-byte elements (e4m3 codes): cols in bytes.
+int make_tmap_u8_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                    uint32_t box_cols, CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo);
 
 }  // namespace bf16l

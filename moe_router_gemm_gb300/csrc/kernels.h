@@ -137,6 +137,8 @@ int launch_dotmma_fp8(const void *xq, const void *wq, const float *sx, const flo
 int launch_warpmma_fp8(const void *xq, const void *wq, const float *sx, const float *sw, const void *bias, void *out,
                        int M, int N, int K, int wpr, int threads, int grid, uint32_t flags, void *stream,
                        int32_t *status);
+int launch_tile_fp8(const void *xq, const void *wq, const float *sx, const float *sw, const void *bias, void *out,
+                    int M, int N, int K, int stages, int grid, uint32_t flags, void *stream, int32_t *status);
 int launch_quant_fp8(const void *x, const float *scale, void *q, long long n, int num_sms, uint32_t flags,
                      void *stream);
 

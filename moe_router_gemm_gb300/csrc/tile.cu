@@ -38,6 +38,7 @@ constexpr int kStageBytes = kABytes + kBBytes;   // 48 KB
 constexpr int kAccCols = kBN;                    // fp32 accumulator columns per buffer
 constexpr int kTmemCols = 2 * kAccCols;          // double buffer = all 512 columns
 constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN);
+constexpr uint32_t kIdescF8 = idesc_e4m3_f32(kBM, kBN);
 constexpr int kGroupN = 8;                       // N tiles per raster group
 
 struct TileShared {
@@ -63,11 +64,17 @@ __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int
 
 }  // namespace
 
-template <typename OutT>
+// F8: x and W are e4m3 codes (per-tensor FP8).  A 128-byte swizzle row then
+// holds 128 codes instead of 64 bf16 values, each MMA (kind::f8f6f4) takes 32
+// of them, and the epilogue scales the fp32 sum by *scale_x * *scale_w before
+// bias; the shared-memory geometry of a stage is the same.  K counts elements.
+template <typename OutT, bool F8 = false>
 __global__ void __launch_bounds__(kTileThreads, 1)
     tile_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                 const uint16_t *__restrict__ bias, OutT *__restrict__ out, int M, int N, int K, int stages,
-                int32_t *status) {
+                int32_t *status, const float *__restrict__ scale_x = nullptr,
+                const float *__restrict__ scale_w = nullptr) {
+    constexpr int kChunk = F8 ? 2 * kChunkK : kChunkK;  // elements per 128-byte row
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -76,7 +83,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int m_tiles = (M + kBM - 1) / kBM, n_tiles = (N + kBN - 1) / kBN;
     const int num_tiles = m_tiles * n_tiles;
-    const int C = (K + kChunkK - 1) / kChunkK;
+    const int C = (K + kChunk - 1) / kChunk;
 
     if (tid == 0) {
         tma_prefetch_desc(&tm_x);
@@ -120,8 +127,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                     if (*((volatile int32_t *)&sh.aborted)) goto producer_done;
                     uint8_t *st = ring + s * kStageBytes;
                     mbar_arrive_expect_tx(&sh.full[s], kStageBytes);
-                    tma_load_2d(st, &tm_x, &sh.full[s], c * kChunkK, m0);
-                    tma_load_2d(st + kABytes, &tm_w, &sh.full[s], c * kChunkK, n0);
+                    tma_load_2d(st, &tm_x, &sh.full[s], c * kChunk, m0);
+                    tma_load_2d(st + kABytes, &tm_w, &sh.full[s], c * kChunk, n0);
                 }
             }
         producer_done:
@@ -156,8 +163,12 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                     const uint64_t adesc = smem_desc_sw128(smem_u32(st));
                     const uint64_t bdesc = smem_desc_sw128(smem_u32(st + kABytes));
 #pragma unroll
-                    for (int kk = 0; kk < kChunkK / 16; ++kk)
-                        mma_bf16(acc, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (c > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk) {  // 32 bytes of each row per MMA
+                        if constexpr (F8)
+                            mma_e4m3(acc, adesc + 2 * kk, bdesc + 2 * kk, kIdescF8, (c > 0 || kk > 0) ? 1u : 0u);
+                        else
+                            mma_bf16(acc, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (c > 0 || kk > 0) ? 1u : 0u);
+                    }
                     mma_commit(&sh.empty[s]);
                 }
                 if (!ok) {
@@ -186,6 +197,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
             const uint32_t acc = tmem + (uint32_t)(b * kAccCols) + ((uint32_t)(q * 32) << 16);
             if (have) {
                 pdl_wait();
+                const float sxw = F8 ? __ldg(scale_x) * __ldg(scale_w) : 1.0f;
 #pragma unroll 1
                 for (int c = 0; c < kBN; c += 32) {
                     uint32_t r0[16], r1[16];
@@ -200,6 +212,10 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                         for (int j = 0; j < 16; ++j) {
                             v[j] = __uint_as_float(r0[j]);
                             v[16 + j] = __uint_as_float(r1[j]);
+                        }
+                        if constexpr (F8) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] *= sxw;
                         }
                         if (bias) {
 #pragma unroll
@@ -246,6 +262,9 @@ int init_tile() {
     if (!e)
         e = (int)cudaFuncSetAttribute(tile_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       tile_smem_bytes(kTileMaxStages));
+    if (!e)
+        e = (int)cudaFuncSetAttribute(tile_kernel<uint16_t, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      tile_smem_bytes(kTileMaxStages));
     return e;
 }
 
@@ -269,11 +288,35 @@ static int launch_tile_t(const LaunchArgs &a, const bf16l_plan &p) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return (int)cudaLaunchKernelEx(&cfg, tile_kernel<OutT>, tx, tw, static_cast<const uint16_t *>(a.bias),
-                                   static_cast<OutT *>(a.out), a.M, a.N, a.K, p.stages, a.status);
+                                   static_cast<OutT *>(a.out), a.M, a.N, a.K, p.stages, a.status,
+                                   static_cast<const float *>(nullptr), static_cast<const float *>(nullptr));
 }
 
 int launch_tile(const LaunchArgs &a, const bf16l_plan &p) {
     return a.out_f32 ? launch_tile_t<float>(a, p) : launch_tile_t<uint16_t>(a, p);
+}
+
+int launch_tile_fp8(const void *xq, const void *wq, const float *sx, const float *sw, const void *bias, void *out,
+                    int M, int N, int K, int stages, int grid, uint32_t flags, void *stream, int32_t *status) {
+    CUtensorMap tx, tw;  // 128-byte rows of 128 codes, as the bf16 form's 64 values
+    int r = make_tmap_u8_2d(&tx, xq, (uint64_t)M, (uint64_t)K, kBM, 2 * kChunkK, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    if (r) return (int)cudaErrorInvalidValue;
+    r = make_tmap_u8_2d(&tw, wq, (uint64_t)N, (uint64_t)K, kBN, 2 * kChunkK, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    if (r) return (int)cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kTileThreads);
+    cfg.dynamicSmemBytes = (size_t)tile_smem_bytes(stages);
+    cfg.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = (flags & BF16L_FLAG_PDL) ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return (int)cudaLaunchKernelEx(&cfg, tile_kernel<uint16_t, true>, tx, tw, static_cast<const uint16_t *>(bias),
+                                   static_cast<uint16_t *>(out), M, N, K, stages, status, sx, sw);
 }
 
 }  // namespace bf16l

@@ -142,6 +142,49 @@ def test_linear_fp8_split_form(lib, S, t):
     check_close(tensor_bits(out), oracle.linear_fp8(xq, wq, sx, sw, wl.bits(b)), f"fp8 split S={S} t={t}")
 
 
+def _tile(lib, stages=4):
+    return lib.make_plan("tile", threads=192, stages=stages)
+
+
+@pytest.mark.parametrize("shape", [(128, 256, 128), (300, 520, 1040), (17, 2112, 7168), (256, 14336, 4096)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_linear_fp8_tile_form(lib, shape):
+    M, N, K = shape
+    for bias in (False, True):
+        x, W, b, xq, wq, sx, sw = _fp8_inputs(M, N, K, M + N + K, bias)
+        bd = b.to(DEV) if b is not None else None
+        out = lib.bf16_linear_fp8(torch.from_numpy(xq).to(DEV), torch.from_numpy(wq).to(DEV), _scale(sx),
+                                  _scale(sw), bd, plan_=_tile(lib, 2 if K <= 1040 else 4))
+        torch.cuda.synchronize()
+        rows = np.unique(np.concatenate([np.arange(0, M, 127), [M - 1], np.arange(0, M, 128)]))
+        rows = rows[rows < M]
+        want = oracle.linear_fp8(xq[rows], wq, sx, sw, wl.bits(b))
+        check_close(tensor_bits(out)[rows], want, f"fp8 tile M={M} N={N} K={K} bias={bias}")
+
+
+def test_linear_fp8_tile_prefill_sampled(lib):
+    M, N, K = 2048, 7168, 7168
+    x, W, _, xq, wq, sx, sw = _fp8_inputs(M, N, K, 21, False)
+    out = lib.bf16_linear_fp8(torch.from_numpy(xq).to(DEV), torch.from_numpy(wq).to(DEV), _scale(sx), _scale(sw))
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, 127, 128, 1000, 2047])
+    check_close(tensor_bits(out)[rows], oracle.linear_fp8(xq[rows], wq, sx, sw), "fp8 prefill sampled rows")
+
+
+def test_linear_fp8_tile_exact(lib):
+    M, N, K = 200, 264, 384
+    rng = np.random.default_rng(4)
+    wq = rng.integers(0, 256, (N, K)).astype(np.uint8)
+    wq[(wq & 0x7F) == 0x7F] = 0x38
+    ks = rng.integers(0, K, M)
+    xq = np.zeros((M, K), dtype=np.uint8)
+    xq[np.arange(M), ks] = 0x38
+    out = lib.bf16_linear_fp8(torch.from_numpy(xq).to(DEV), torch.from_numpy(wq).to(DEV), _scale(0.5), _scale(0.25),
+                              plan_=_tile(lib, 3))
+    torch.cuda.synchronize()
+    assert np.array_equal(tensor_bits(out), oracle.linear_fp8(xq, wq, 0.5, 0.25))
+
+
 def test_linear_fp8_rejects(lib):
     xq = torch.zeros(4, 40, dtype=torch.uint8, device=DEV)
     wq = torch.zeros(8, 40, dtype=torch.uint8, device=DEV)
