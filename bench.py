@@ -532,6 +532,14 @@ def candidate_plans(lib, M, N, K):
     if K % 8 == 0 and M <= 16 and N > 1024:  # x fragments from L2 (any K)
         for t, w, c in ((512, 4, 1), (512, 8, 1), (512, 16, 1), (256, 4, 2), (256, 8, 2)):
             cands.append(lib.make_plan("warpmma", threads=t, rows_per_cta=w, stages=c, split_k=1))
+    if K % 8 == 0 and 16 < M <= 64:  # the router MMA split-K in 16-token groups
+        for S, t, xr in itertools.product((1, 2, 4, 8), (128, 256), (1,)):
+            p = lib.make_plan("dotmma", threads=t, rows_per_cta=8, split_k=S, stages=xr)
+            try:
+                lib.plan_check(M, N, K, p)
+            except Exception:
+                continue
+            cands.append(p)
     if K % 8 == 0 and M <= 16 and N <= 1024:
         for S, t, xr in itertools.product((8, 16, 32), (128, 256), (0, 1)):
             p = lib.make_plan("dotmma_ws", threads=t, rows_per_cta=8, split_k=S, stages=xr)

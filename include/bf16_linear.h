@@ -76,7 +76,7 @@ typedef enum {
                                   warps computes one W row at a time from 16-byte loads, x in shared memory */
     BF16L_KERNEL_WARPMMA = 7,  /* persistent kernel for M <= 16 and many rows: 16-byte weight loads feed the
                                   warp-level tensor-core MMA (m16n8k16) directly; 8 W rows per group of warps */
-    BF16L_KERNEL_DOTMMA = 8,   /* router-sized N, M <= 16: 8 W rows per CTA, K split over a cluster of 1..16 CTAs,
+    BF16L_KERNEL_DOTMMA = 8,   /* router-sized N, M <= 64 (16-token groups): 8 W rows per CTA, K over a cluster of 1..16 CTAs,
                                   16-byte loads feed m16n8k16 MMAs, partials summed by rank 0 over DSMEM */
     BF16L_KERNEL_DOTMMA_WS = 9 /* the same without a cluster: K split over 2..64 CTAs whose partial tiles meet in
                                   a caller-provided workspace (see bf16_linear_run); the last CTA reduces */

@@ -353,7 +353,7 @@ int launch_dm_t(const LaunchArgs &a, const bf16l_plan &p) {
         tiles = reinterpret_cast<float4 *>(static_cast<uint8_t *>(a.workspace) + dotmma_ws_counter_bytes(groups));
     }
     const bool xr = p.stages == 1;
-    const size_t smem = xr ? 0 : (size_t)dotmma_smem_bytes(a.M, a.K, S);
+    const size_t smem = xr ? 0 : (size_t)dotmma_smem_bytes(a.M < 16 ? a.M : 16, a.K, S);  // one token group
     return launch_dm_common(pick_dm<OutT>(a.M, xr, ws), a.x, a.W, a.bias, static_cast<OutT *>(a.out), a.M, a.N,
                             a.K * 2, S, p.threads, smem, S > 1 && !ws, (uint32_t)p.flags, a.stream, a.status,
                             counters, tiles, nullptr, nullptr);

@@ -176,7 +176,9 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
         }
         case BF16L_KERNEL_DOTMMA:
         case BF16L_KERNEL_DOTMMA_WS: {
-            if (K % 8 != 0 || M > kDotMmaMaxTokens) return BF16L_EUNSUPPORTED;
+            // the cluster form takes up to 64 tokens in groups of 16 (grid.z); the workspace form 16
+            if (K % 8 != 0 || M > (p->kernel == BF16L_KERNEL_DOTMMA ? 4 * kDotMmaMaxTokens : kDotMmaMaxTokens))
+                return BF16L_EUNSUPPORTED;
             const int S = p->split_k;
             // clusters: 1..16 CTAs along K; the workspace form: any power of two up to 64
             const bool s_ok = p->kernel == BF16L_KERNEL_DOTMMA
@@ -186,8 +188,9 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
                 S > ceil_div(K / 8, 4) || (p->stages != 0 && p->stages != 1))
                 return BF16L_EINVAL;
             // stages 1: x straight from global memory; 0: the CTA's x slice staged in shared memory
-            if (p->stages == 0 && dotmma_smem_bytes(M, K, S) > kDotMmaMaxSmem) return BF16L_EUNSUPPORTED;
-            p->grid = M == 0 ? 0 : S * ceil_div(N, 8);
+            const int mg = M < kDotMmaMaxTokens ? M : kDotMmaMaxTokens;  // tokens of one group
+            if (p->stages == 0 && dotmma_smem_bytes(mg, K, S) > kDotMmaMaxSmem) return BF16L_EUNSUPPORTED;
+            p->grid = M == 0 ? 0 : S * ceil_div(N, 8) * ceil_div(M, kDotMmaMaxTokens);
             return BF16L_OK;
         }
         case BF16L_KERNEL_TILE2: {

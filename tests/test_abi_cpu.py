@@ -253,8 +253,12 @@ def test_dotmma_plans_on_cpu(lib):
         lib.plan_check(16, 384, 7168, mk(256, 1))   # x (229 KB) does not fit one CTA's shared memory
     xr = lib.make_plan("dotmma", threads=256, rows_per_cta=8, split_k=1, stages=1)
     assert lib.plan_check(16, 384, 7168, xr).grid == 48  # ... but x straight from L2 needs none
+    assert lib.plan_check(17, 384, 4096, xr).grid == 48 * 2       # two groups of 16 tokens along grid.z
+    assert lib.plan_check(64, 384, 4096, mk(256, 4)).grid == 4 * 48 * 4
     with pytest.raises(lib.BF16LinearError):
-        lib.plan_check(17, 384, 4096, mk(256, 4))   # at most 16 tokens
+        lib.plan_check(65, 384, 4096, mk(256, 4))   # at most 64 tokens (4 groups)
+    with pytest.raises(lib.BF16LinearError):
+        lib.plan_check(17, 384, 4096, lib.make_plan("dotmma_ws", threads=256, rows_per_cta=8, split_k=4))
     with pytest.raises(lib.BF16LinearError):
         lib.plan_check(4, 384, 40, mk(256, 4))      # two 32-wide K blocks cannot feed 4 CTAs
 

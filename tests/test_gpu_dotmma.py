@@ -122,6 +122,18 @@ def test_dotmma_workspace_needs_workspace(lib):
         lib.bf16_linear_with_plan(x, W, None, plan_=p)  # no workspace given
 
 
+@pytest.mark.parametrize("shape", [(32, 2112, 7168), (64, 256, 4096), (17, 300, 1032), (50, 128, 2880)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_dotmma_token_groups(lib, shape):
+    """More than 16 tokens: groups of 16 along grid.z, the last one ragged."""
+    M, N, K = shape
+    for xr in (0, 1):
+        x, W, b = wl.make_inputs(M, N, K, M + N, True)
+        got = tensor_bits(_run(lib, x, W, b, _plan(lib, 4, 256, xr)))
+        want = oracle.linear_bf16(wl.bits(x), wl.bits(W), wl.bits(b))
+        check_close(got, want, f"dotmma token groups M={M} N={N} K={K} xr={xr}")
+
+
 def test_dotmma_deterministic_and_f32(lib):
     M, N, K = 14, 384, 7168
     x, W, b = wl.make_inputs(M, N, K, 2, True)
