@@ -455,6 +455,9 @@ def candidate_plans(lib, M, N, K):
             for R in (1, 2, 4):
                 for threads in (128, 256):
                     cands.append(lib.make_plan("dotprod", threads=threads, rows_per_cta=R, tokens_per_cta=t))
+                    if M <= 4:  # x straight from L2 instead of a staged copy
+                        cands.append(lib.make_plan("dotprod", threads=threads, rows_per_cta=R, tokens_per_cta=t,
+                                                   stages=1))
     if K % 8 == 0 and M <= 64:
         chunks = -(-K // 64)
         tokens = max(8, -(-M // 8) * 8)

@@ -103,7 +103,8 @@ typedef struct {
                               DOTMMA_WS: CTAs along K (a power of two, 2..64);
                               WARPMMA: 1 = x fragments loaded from global memory into registers (512 threads per
                               SM at most), 0 = x staged in shared memory */
-    int32_t stages;        /* SPLITK / TILE: shared-memory ring depth (64-wide K chunks);
+    int32_t stages;        /* SPLITK / TILE: shared-memory ring depth (64-wide K chunks); DOTPROD: 1 = x read
+                              from global memory (L2) instead of staged in shared memory;
                               WARPROW / WARPMMA: CTAs per SM; DOTMMA: 1 = x fragments loaded from global
                               memory into registers, 0 = each CTA's x slice staged in shared memory */
     int32_t grid;          /* CTAs launched (informational; computed by the plan) */

@@ -252,7 +252,8 @@ int launch_dotprod_t(const LaunchArgs &a, const bf16l_plan &p) {
     const int t = p.tokens_per_cta > 0 ? p.tokens_per_cta : kDotMaxTokens;
     const int MT = a.M < t ? a.M : t;
     const size_t xbytes = (size_t)MT * a.K * 2;
-    const int kind = (a.K % 8 != 0) ? 2 : (xbytes <= (size_t)kXSmemMax ? 0 : 1);
+    // x from shared memory when it fits, unless the plan asks for x straight from L2 (stages == 1)
+    const int kind = (a.K % 8 != 0) ? 2 : ((xbytes <= (size_t)kXSmemMax && p.stages == 0) ? 0 : 1);
     DotFn<OutT> fn = pick<OutT>(MT, p.rows_per_cta, kind);
     if (!fn) return (int)cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};

@@ -98,6 +98,7 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
             if (!in_list(p->threads, kDotThreads, 3) || !in_list(p->rows_per_cta, kDotRows, 3))
                 return BF16L_EINVAL;
             if (p->tokens_per_cta < 0 || p->tokens_per_cta > kDotMaxTokens) return BF16L_EINVAL;
+            if (p->stages != 0 && p->stages != 1) return BF16L_EINVAL;  // 1: x read from L2, not staged
             p->grid = M == 0 ? 0 : ceil_div(N, p->rows_per_cta) * dot_token_groups(M, p->tokens_per_cta);
             return BF16L_OK;
         }

@@ -155,6 +155,17 @@ def test_dotprod_token_groups(lib, case):
     assert np.array_equal(loop, _run(lib, x, W, b, plan))
 
 
+@pytest.mark.parametrize("shape", [(1, 256, 7168), (4, 300, 2056), (3, 17, 2880)], ids=lambda s: "x".join(map(str, s)))
+def test_dotprod_x_from_l2(lib, shape):
+    """x read from L2 (stages = 1) instead of staged: the same products in the same order, the same bits."""
+    M, N, K = shape
+    x, W, b = _inputs(M, N, K, 8, True)
+    staged = _run(lib, x, W, b, lib.make_plan("dotprod", threads=128, rows_per_cta=2))
+    direct = _run(lib, x, W, b, lib.make_plan("dotprod", threads=128, rows_per_cta=2, stages=1))
+    assert np.array_equal(staged, direct)
+    check_close(direct, _expect(x, W, b), f"dotprod x from L2 M={M} N={N} K={K}")
+
+
 @pytest.mark.parametrize("threads", [64, 256])
 def test_dotprod_block_sizes(lib, threads):
     _check(lib, 4, 384, 7168, seed=5, plan=dot_plan(lib, 2, threads))
