@@ -331,8 +331,9 @@ size_t bf16_linear_noalloc_scratch_bytes(void);
  *   stages = CTAs per SM, split_k 0; M <= 16 and M * K <= 200 KB) or
  *   BF16L_KERNEL_TILE (the tcgen05 kind::f8f6f4 tile form: threads 192,
  *   stages 2..4; any M), flags; threads == 0 means the entry point's own
- *   choice (the tile form for M > 16, else the warp-MMA form for N >= 1024
- *   when it applies, else the split form).  BF16L_EINVAL for any other plan.
+ *   choice (the tile form for M > 16 with at least 32 tiles of 128 x 256, else
+ *   the warp-MMA form for N >= 1024 when it applies, else the split form).
+ *   BF16L_EINVAL for any other plan.
  *
  * bf16_linear_fp8_split — the K split bf16_linear_fp8 uses for a shape on a
  *   device with num_sms SMs (pure host logic; for tests and tuning).

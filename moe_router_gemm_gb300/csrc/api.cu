@@ -315,7 +315,8 @@ extern "C" int bf16_linear_fp8_with_plan(const void *xq, const void *wq, const f
     int kernel = plan->kernel, S = plan->split_k, threads = plan->threads, wpr = plan->rows_per_cta,
         cps = plan->stages;
     if (threads == 0) {  // the entry point's own choice
-        if (M > 16) {  // a dense contraction: the tcgen05 tile form (kind::f8f6f4)
+        const long long tiles = (long long)((M + kTileBM - 1) / kTileBM) * ((N + kTileBN - 1) / kTileBN);
+        if (M > 16 && tiles >= 32) {  // a dense contraction with enough tiles: the tcgen05 tile form
             kernel = BF16L_KERNEL_TILE;
             threads = kTileThreads;
             cps = kTileMaxStages;
