@@ -103,7 +103,7 @@ def workload_desc(name):
 def kernel_source_hash(kernel_name):
     src = {"dotprod": ("dotprod.cuh", "dotprod.cu"), "splitk": ("splitk.cu",), "splitk_ws": ("splitk.cu",),
            "tile": ("tile.cu",), "stream": ("stream.cu",), "tile2": ("tile2.cu",), "warprow": ("warprow.cu",),
-           "warpmma": ("warpmma.cu",), "dotmma": ("dotmma.cu",),
+           "warpmma": ("warpmma.cu", "warpmma_ks.cu"), "dotmma": ("dotmma.cu",),
            "dotmma_ws": ("dotmma.cu",)}[kernel_name]
     h = hashlib.sha256()
     for f in src + ("common.cuh", "kernels.h"):
@@ -482,6 +482,16 @@ def candidate_plans(lib, M, N, K):
                     except Exception:
                         continue
                 cands.append(p)
+                if M > 8 and tiles * split > 152:  # more CTAs than SMs: shallower rings, two or three per SM
+                    for st in (6, 4, 3, 2):
+                        if st < p.stages:
+                            q = lib.make_plan("splitk", threads=128, rows_per_cta=rows, tokens_per_cta=tokens,
+                                              split_k=split, stages=st)
+                            try:
+                                lib.plan_check(M, N, K, q)
+                                cands.append(q)
+                            except Exception:
+                                pass
     if K % 8 == 0 and M <= 64:
         chunks = -(-K // 64)
         tokens = max(8, -(-M // 8) * 8)
@@ -535,6 +545,17 @@ def candidate_plans(lib, M, N, K):
     if K % 8 == 0 and M <= 16 and N > 1024:  # x fragments from L2 (any K)
         for t, w, c in ((512, 4, 1), (512, 8, 1), (512, 16, 1), (256, 4, 2), (256, 8, 2)):
             cands.append(lib.make_plan("warpmma", threads=t, rows_per_cta=w, stages=c, split_k=1))
+    if K % 8 == 0 and M <= 64 and N >= 1024:  # the warp-MMA kernel's cluster form: K over S CTAs
+        cfgs = (((1024, 8, 1), (1024, 4, 1), (1024, 16, 1), (512, 4, 2), (512, 8, 2), (256, 2, 4), (256, 4, 4))
+                if M <= 16 else ((512, 4, 1), (512, 8, 1), (512, 16, 1), (256, 2, 2), (256, 4, 2), (256, 8, 2)))
+        for S in (2, 3, 4, 6, 8):
+            for t, w, c in cfgs:
+                p = lib.make_plan("warpmma", threads=t, rows_per_cta=w, stages=c, split_k=S)
+                try:
+                    lib.plan_check(M, N, K, p)
+                except Exception:
+                    continue
+                cands.append(p)
     if K % 8 == 0 and 16 < M <= 64:  # the router MMA split-K in 16-token groups
         for S, t, xr in itertools.product((1, 2, 4, 8), (128, 256), (1,)):
             p = lib.make_plan("dotmma", threads=t, rows_per_cta=8, split_k=S, stages=xr)
@@ -582,6 +603,9 @@ def sweep(args, points):
         R = min(base.R, 64)  # 64 rotated copies keep every call L2-cold for these sizes
         rows = []
         cands = candidate_plans(lib, pt["M"], pt["N"], pt["K"])
+        if args.sweep_kernels:  # a partial sweep over some kernels only
+            keep = set(args.sweep_kernels.split(","))
+            cands = [p for p in cands if lib.KERNEL_NAMES[p.kernel] in keep]
         need = max([lib.workspace_size(pt["M"], pt["N"], pt["K"], p) for p in cands] + [256])
         base.ws = lib.new_workspace(need, device)
         for p in cands:
@@ -609,6 +633,8 @@ def sweep(args, points):
             except Exception as e:  # an unusable candidate is skipped, not fatal
                 rows.append((float("inf"), dict(p.as_dict(), error=str(e)[:80])))
         rows.sort(key=lambda r: r[0])
+        if not rows:  # a partial sweep with no candidate for this shape
+            continue
         best_plain = next((r for r in rows if r[1].get("kernel") not in WS_KERNELS), rows[0])
         default = lib.plan(pt["M"], pt["N"], pt["K"]).as_dict()
         results.append({"M": pt["M"], "N": pt["N"], "K": pt["K"], "best_us": rows[0][0], "best": rows[0][1],
@@ -770,6 +796,8 @@ def main():
                          "(kernel by name, e.g. tile2,192,256,256,0,6); for profiling one kernel")
     ap.add_argument("--only", action="append", default=[],
                     help="restrict to shapes M,N,K[,bias] (repeatable); for profiling")
+    ap.add_argument("--sweep-kernels", default="",
+                    help="with --sweep: time only the candidates of these kernels (comma-separated names)")
     ap.add_argument("--sweep", action="store_true",
                     help="time every candidate plan of the workload's shapes and write dispatch_table.inc "
                          "(to gpurun_out/ when that folder exists)")

@@ -75,7 +75,9 @@ typedef enum {
     BF16L_KERNEL_WARPROW = 6,  /* persistent CUDA-core kernel for M <= 8 and many rows: a group of 1, 2 or 4
                                   warps computes one W row at a time from 16-byte loads, x in shared memory */
     BF16L_KERNEL_WARPMMA = 7,  /* persistent kernel for M <= 16 and many rows: 16-byte weight loads feed the
-                                  warp-level tensor-core MMA (m16n8k16) directly; 8 W rows per group of warps */
+                                  warp-level tensor-core MMA (m16n8k16) directly; 8 W rows per group of warps.
+                                  With split_k >= 2, its cluster form: K over S CTAs of a cluster, M <= 64, each
+                                  CTA staging its K slice of x, partial tiles summed over DSMEM in rank order */
     BF16L_KERNEL_DOTMMA = 8,   /* router-sized N, M <= 64 (16-token groups): 8 W rows per CTA, K over a cluster of 1..16 CTAs,
                                   16-byte loads feed m16n8k16 MMAs, partials summed by rank 0 over DSMEM */
     BF16L_KERNEL_DOTMMA_WS = 9 /* the same without a cluster: K split over 2..64 CTAs whose partial tiles meet in
@@ -102,7 +104,8 @@ typedef struct {
                               DOTMMA: CTAs per cluster along K (1, 2, 4, 8 or 16);
                               DOTMMA_WS: CTAs along K (a power of two, 2..64);
                               WARPMMA: 1 = x fragments loaded from global memory into registers (512 threads per
-                              SM at most), 0 = x staged in shared memory */
+                              SM at most), 0 = x staged in shared memory, S = 2..8: the cluster form (K over S
+                              CTAs; 1024-thread blocks only for M <= 16, else at most 512 threads per SM) */
     int32_t stages;        /* SPLITK / TILE: shared-memory ring depth (64-wide K chunks); DOTPROD: 1 = x read
                               from global memory (L2) instead of staged in shared memory;
                               WARPROW / WARPMMA: CTAs per SM; DOTMMA: 1 = x fragments loaded from global

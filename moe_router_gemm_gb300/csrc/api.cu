@@ -62,6 +62,7 @@ void init_device(DeviceState &s) {
         if (!e) e = init_tile2();
         if (!e) e = init_warprow();
         if (!e) e = init_warpmma();
+        if (!e) e = init_warpmma_ks();
         if (!e) e = init_dotmma();
     }
     s.err = e;

@@ -75,6 +75,14 @@ constexpr int kWarpMmaMaxTokens = 16;
 constexpr int kWarpMmaMaxSmem = 200 * 1024;
 int warpmma_smem_bytes(int M, int K);
 int init_warpmma();
+// Its cluster form (WARPMMA plans with split_k = S >= 2): K split over S CTAs
+// of a cluster, each staging its K slice of up to 64 tokens; partial tiles
+// summed through distributed shared memory.  `clusters` of S CTAs.
+constexpr int kWarpMmaKsMaxTokens = 64;
+constexpr int kWarpMmaKsMaxCluster = 8;
+constexpr int kWarpMmaKsMaxSmem = 231424;  // 226 KB dynamic: the kernel has static barriers too
+int warpmma_ks_smem_bytes(int M, int N, int K, int S, int clusters, int threads, int wpr);
+int init_warpmma_ks();
 
 // Router split-K on warp-level MMAs: 8 W rows per CTA, K over a cluster of
 // 1, 2, 4 or 8 CTAs, M <= 16, each CTA stages its K slice of x.
@@ -128,6 +136,7 @@ int launch_stream(const LaunchArgs &a, const bf16l_plan &p);
 int launch_tile2(const LaunchArgs &a, const bf16l_plan &p);
 int launch_warprow(const LaunchArgs &a, const bf16l_plan &p);
 int launch_warpmma(const LaunchArgs &a, const bf16l_plan &p);
+int launch_warpmma_ks(const LaunchArgs &a, const bf16l_plan &p);
 int launch_dotmma(const LaunchArgs &a, const bf16l_plan &p);
 // Per-tensor FP8: the router MMA split-K kernel with e4m3 operands (K in bytes
 // = codes; grid.z covers any M in groups of 16 tokens), and the static

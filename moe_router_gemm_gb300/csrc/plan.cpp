@@ -157,6 +157,25 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
             return BF16L_OK;
         }
         case BF16L_KERNEL_WARPMMA: {
+            if (p->split_k >= 2) {
+                // the cluster form: K over S CTAs, up to 64 tokens; 1024-thread blocks only for <= 16 tokens
+                // (64 registers a thread), otherwise at most 512 threads per SM (128 registers)
+                const int S = p->split_k, t = p->threads, wpr = p->rows_per_cta, cps = p->stages;
+                if (K % 8 != 0 || M > kWarpMmaKsMaxTokens) return BF16L_EUNSUPPORTED;
+                if ((t != 256 && t != 512 && t != 1024) || (t == 1024 && M > 16) ||
+                    (wpr != 1 && wpr != 2 && wpr != 4 && wpr != 8 && wpr != 16) || (t / 32) % wpr != 0 ||
+                    (wpr > 1 && (t / 32) / wpr > 15) || S > kWarpMmaKsMaxCluster || S > ceil_div(K / 8, 4) ||
+                    cps < 1 || cps > 4 || t * cps > (M > 16 ? 512 : 1024))
+                    return BF16L_EINVAL;
+                int64_t clusters = (int64_t)dev.num_sms * cps / S;
+                const int64_t groups = ceil_div(N, 8);
+                if (clusters > groups) clusters = groups;
+                if (clusters < 1) return BF16L_EINVAL;
+                const int smem = warpmma_ks_smem_bytes(M, N, K, S, (int)clusters, t, wpr);
+                if (smem > kWarpMmaKsMaxSmem || (int64_t)cps * (smem + 1024) > 233472) return BF16L_EINVAL;
+                p->grid = M == 0 ? 0 : (int)(clusters * S);
+                return BF16L_OK;
+            }
             // split_k 1: x fragments from L2 into registers (no shared-memory x, at most 512 threads per SM)
             const bool xr = p->split_k == 1;
             if (K % 8 != 0 || M > kWarpMmaMaxTokens || (!xr && warpmma_smem_bytes(M, K) > kWarpMmaMaxSmem))

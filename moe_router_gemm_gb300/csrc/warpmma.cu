@@ -300,6 +300,7 @@ int init_warpmma() {
 }
 
 int launch_warpmma(const LaunchArgs &a, const bf16l_plan &p) {
+    if (p.split_k >= 2) return launch_warpmma_ks(a, p);  // the cluster form (warpmma_ks.cu)
     return a.out_f32 ? launch_wm_t<float>(a, p) : launch_wm_t<uint16_t>(a, p);
 }
 

@@ -240,6 +240,29 @@ def test_warpmma_plans_on_cpu(lib):
         lib.plan_check(16, 2112, 7168, mk(512, 1, 1))   # x (229 KB) does not fit in shared memory
 
 
+def test_warpmma_cluster_plans_on_cpu(lib):
+    mk = lambda t, w, c, S: lib.make_plan("warpmma", threads=t, rows_per_cta=w, stages=c, split_k=S)
+    assert lib.plan_check(16, 2112, 7168, mk(1024, 8, 1, 2)).grid == 152   # 76 clusters of 2
+    assert lib.plan_check(64, 2112, 7168, mk(512, 4, 1, 8)).grid == 152    # 19 clusters of 8
+    assert lib.plan_check(32, 2112, 7168, mk(256, 2, 2, 8)).grid == 304    # two 256-thread CTAs per SM
+    assert lib.plan_check(5, 24, 4096, mk(512, 4, 1, 2)).grid == 6         # no more clusters than row groups
+    for bad in (mk(1024, 8, 1, 9), mk(512, 3, 1, 2), mk(512, 8, 0, 2), mk(512, 8, 3, 2), mk(1024, 2, 1, 2)):
+        with pytest.raises(lib.BF16LinearError):
+            lib.plan_check(16, 2112, 7168, bad)
+    with pytest.raises(lib.BF16LinearError):
+        lib.plan_check(32, 2112, 7168, mk(1024, 8, 1, 4))   # more than 16 tokens: at most 512 threads per SM
+    with pytest.raises(lib.BF16LinearError):
+        lib.plan_check(32, 2112, 7168, mk(512, 8, 2, 4))
+    with pytest.raises(lib.BF16LinearError):
+        lib.plan_check(65, 2112, 7168, mk(512, 4, 1, 8))    # at most 64 tokens
+    with pytest.raises(lib.BF16LinearError):
+        lib.plan_check(64, 2112, 7168, mk(512, 4, 1, 2))    # a 466 KB x slice does not fit
+    with pytest.raises(lib.BF16LinearError):
+        lib.plan_check(16, 2112, 7168, mk(512, 8, 2, 2))    # two 127 KB CTAs do not fit one SM
+    with pytest.raises(lib.BF16LinearError):
+        lib.plan_check(4, 64, 32, mk(512, 4, 1, 2))         # one 32-wide K block cannot be split
+
+
 def test_dotmma_plans_on_cpu(lib):
     mk = lambda t, S: lib.make_plan("dotmma", threads=t, rows_per_cta=8, split_k=S)
     assert lib.plan_check(16, 384, 7168, mk(256, 4)).grid == 4 * 48

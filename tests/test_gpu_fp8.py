@@ -194,8 +194,12 @@ def test_linear_fp8_rejects(lib):
     wq = torch.zeros(8, 64, dtype=torch.uint8, device=DEV)
     with pytest.raises(ValueError):
         lib.bf16_linear_fp8(xq, wq, torch.ones(2, device=DEV), _scale(1.0))
-    with pytest.raises(lib.BF16LinearError):  # a kernel the FP8 entry does not run
-        lib.bf16_linear_fp8(xq, wq, _scale(1.0), _scale(1.0), plan_=lib.make_plan("tile", threads=192))
+    for p in (lib.make_plan("splitk", threads=256, split_k=2), lib.make_plan("stream", threads=256),
+              lib.make_plan("tile2", threads=192, stages=4)):  # kernels the FP8 entry does not run
+        with pytest.raises(lib.BF16LinearError):
+            lib.bf16_linear_fp8(xq, wq, _scale(1.0), _scale(1.0), plan_=p)
+    with pytest.raises(lib.BF16LinearError):  # the tile form needs a ring of at least two stages
+        lib.bf16_linear_fp8(xq, wq, _scale(1.0), _scale(1.0), plan_=lib.make_plan("tile", threads=192, stages=1))
     with pytest.raises(lib.BF16LinearError):  # 17 tokens do not fit the warp-MMA form
         lib.bf16_linear_fp8(torch.zeros(17, 64, dtype=torch.uint8, device=DEV), wq, _scale(1.0), _scale(1.0),
                             plan_=lib.make_plan("warpmma", threads=512, rows_per_cta=4, stages=1))
