@@ -548,7 +548,7 @@ def candidate_plans(lib, M, N, K):
     if K % 8 == 0 and M <= 64 and N >= 1024:  # the warp-MMA kernel's cluster form: K over S CTAs
         cfgs = (((1024, 8, 1), (1024, 4, 1), (1024, 16, 1), (512, 4, 2), (512, 8, 2), (256, 2, 4), (256, 4, 4))
                 if M <= 16 else ((512, 4, 1), (512, 8, 1), (512, 16, 1), (256, 2, 2), (256, 4, 2), (256, 8, 2)))
-        for S in (2, 3, 4, 6, 8):
+        for S in (2, 4, 8, 16):
             for t, w, c in cfgs:
                 p = lib.make_plan("warpmma", threads=t, rows_per_cta=w, stages=c, split_k=S)
                 try:

@@ -104,7 +104,7 @@ typedef struct {
                               DOTMMA: CTAs per cluster along K (1, 2, 4, 8 or 16);
                               DOTMMA_WS: CTAs along K (a power of two, 2..64);
                               WARPMMA: 1 = x fragments loaded from global memory into registers (512 threads per
-                              SM at most), 0 = x staged in shared memory, S = 2..8: the cluster form (K over S
+                              SM at most), 0 = x staged in shared memory, S = 2..16: the cluster form (K over S
                               CTAs; 1024-thread blocks only for M <= 16, else at most 512 threads per SM) */
     int32_t stages;        /* SPLITK / TILE: shared-memory ring depth (64-wide K chunks); DOTPROD: 1 = x read
                               from global memory (L2) instead of staged in shared memory;

@@ -120,6 +120,16 @@ struct OutStore<float> {
     }
 };
 
+// floor(a * b / c) for 0 <= a, 0 <= b <= c and 0 < c < 65536, exactly, in
+// 32-bit arithmetic (a 64-bit division is a long software routine, and these
+// bounds sit in front of a kernel's first weight load): with a = q c + r,
+// a b / c = q b + r b / c, where q b <= a and r b < c * c.
+__device__ __forceinline__ int mul_div(int a, int b, int c) {
+    const unsigned ua = (unsigned)a, ub = (unsigned)b, uc = (unsigned)c;
+    const unsigned q = ua / uc, r = ua - q * uc;
+    return (int)(q * ub + (r * ub) / uc);
+}
+
 // ---------------------------------------------------------------------------
 // Shared-memory addresses and mbarriers.
 // ---------------------------------------------------------------------------
@@ -415,6 +425,18 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
 // ---------------------------------------------------------------------------
 // Thread-block clusters and distributed shared memory.
 // ---------------------------------------------------------------------------
+// Index of this CTA's cluster in the grid (x), and the number of clusters along x.
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %nclusterid.x;" : "=r"(r));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %cluster_ctarank;" : "=r"(r));

@@ -117,10 +117,10 @@ __global__ void __launch_bounds__(kDmWarps * 32)
     const int n0 = 8 * (int)blockIdx.y;
     const int nvec = RB >> 4, nblk = (nvec + 3) >> 2;
     // this CTA's vectors [cv0, cv1) and this warp's blocks
-    const int cb0 = dm_blk(nblk, rank, S), cb1 = dm_blk(nblk, rank + 1, S);
+    const int cb0 = mul_div(nblk, rank, S), cb1 = mul_div(nblk, rank + 1, S);  // = dm_blk
     const int cv0 = 4 * cb0, cv1 = min(nvec, 4 * cb1);
-    const int wb0 = cb0 + (int)(((long long)(cb1 - cb0) * warp) / nw);
-    const int wb1 = cb0 + (int)(((long long)(cb1 - cb0) * (warp + 1)) / nw);
+    const int wb0 = cb0 + mul_div(cb1 - cb0, warp, nw);
+    const int wb1 = cb0 + mul_div(cb1 - cb0, warp + 1, nw);
     const int wv0 = 4 * wb0, wv1 = min(cv1, 4 * wb1);
     const int sv = cv1 - cv0;  // vectors in this CTA's x slice
     const bool tok_lo = g < M, tok_hi = HI && (g + 8 < M);

@@ -79,7 +79,7 @@ int init_warpmma();
 // of a cluster, each staging its K slice of up to 64 tokens; partial tiles
 // summed through distributed shared memory.  `clusters` of S CTAs.
 constexpr int kWarpMmaKsMaxTokens = 64;
-constexpr int kWarpMmaKsMaxCluster = 8;
+constexpr int kWarpMmaKsMaxCluster = 16;  // above 8: a non-portable cluster size
 constexpr int kWarpMmaKsMaxSmem = 231424;  // 226 KB dynamic: the kernel has static barriers too
 int warpmma_ks_smem_bytes(int M, int N, int K, int S, int clusters, int threads, int wpr);
 int init_warpmma_ks();

@@ -60,7 +60,7 @@ struct SplitShared {  // bookkeeping placed after the receive buffer (<= 512 byt
     int32_t last;      // (workspace mode) this CTA arrived last for its tile
 };
 
-__device__ __forceinline__ int part_begin(int d, int T, int S) { return (int)(((long long)d * T) / S); }
+__device__ __forceinline__ int part_begin(int d, int T, int S) { return mul_div(T, d, S); }
 
 }  // namespace
 
@@ -141,8 +141,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     const int S = (int)gridDim.x;  // the K split spans the whole x dimension of the grid
     const int n0 = blockIdx.y * BN;
     const int C = (K + kChunkK - 1) / kChunkK;
-    const int c_begin = (int)(((long long)rank * C) / S);
-    const int nchunks = (int)(((long long)(rank + 1) * C) / S) - c_begin;
+    const int c_begin = mul_div(C, rank, S);
+    const int nchunks = mul_div(C, rank + 1, S) - c_begin;
     const int first = nchunks < stages ? nchunks : stages;  // chunks whose weights go out at once
 
     if (tid == 0) {

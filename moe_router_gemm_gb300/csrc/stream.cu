@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = (int)gridDim.x, b = (int)blockIdx.x;
-    const int r0 = (int)(((long long)N * b) / G), r1 = (int)(((long long)N * (b + 1)) / G);
+    const int r0 = mul_div(N, b, G), r1 = mul_div(N, b + 1, G);
     const int nrows = r1 - r0;
     const int ngroups = (nrows + rg - 1) / rg;
     const int first = ngroups < stages ? ngroups : stages;

@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(NT, XR ? 1 : 1024 / NT)
     // CTA b owns the 8-row groups [RG*b/G, RG*(b+1)/G)
     const int RG = (N + 7) >> 3;
     const int G = (int)gridDim.x, b = (int)blockIdx.x;
-    const int q0 = (int)(((long long)RG * b) / G), q1 = (int)(((long long)RG * (b + 1)) / G);
+    const int q0 = mul_div(RG, b, G), q1 = mul_div(RG, b + 1, G);
     const bool tok_lo = g < M, tok_hi = HI && (g + 8 < M);
 
     if (tid == 0) {

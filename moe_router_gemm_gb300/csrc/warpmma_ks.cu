@@ -1,5 +1,5 @@
 // warpmma_ks.cu — the persistent warp-level tensor-core kernel with K split
-// over a thread-block cluster, for decode-sized weights and up to 64 tokens.
+// over a thread-block cluster (2..16 CTAs), for decode-sized weights and up to 64 tokens.
 //
 // Prior art: the cluster split-K kernel on the vLLM PR #42562 page ("实现拆解"
 // items 2-3): K spread over the CTAs of a cluster, fp32 partial tiles reduced
@@ -54,9 +54,6 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// First 32-wide K block of rank r's run (nblk blocks over S ranks).
-__host__ __device__ inline int ks_blk(int nblk, int r, int S) { return (int)(((long long)nblk * r) / S); }
-
 // Row stride of the staged x slice in 16-byte vectors: 4 (mod 8), so that the
 // two token rows a quarter-warp reads land in different halves of the banks.
 __host__ __device__ inline int ks_stride(int sv) { return sv + (12 - sv % 8) % 8; }
@@ -90,39 +87,20 @@ __global__ void __launch_bounds__(NT, TT == 1 ? 1024 / NT : 1)
     extern __shared__ __align__(16) uint8_t ks_smem[];
     __shared__ __align__(8) uint64_t xbar, rbar;
 
+    // Only what the first weight batch needs comes before it is issued (all 32-bit).
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int nw = (int)blockDim.x >> 5;
-    const int GW = nw / WPR;  // 8-row groups in flight in this CTA
     const int grp = warp / WPR, gw = warp - grp * WPR;
-    const int rank = (int)cluster_ctarank();
-    const int C = (int)gridDim.x / S, c = (int)blockIdx.x / S;
-    const KsLayout L = ks_layout(M, N, RB, S, C, nw, WPR, TT);
-    uint4 *xs = reinterpret_cast<uint4 *>(ks_smem);
-    float4 *part = reinterpret_cast<float4 *>(ks_smem + L.part_off);
-    float4 *recv = reinterpret_cast<float4 *>(ks_smem + L.recv_off);
-
+    const int rank = (int)cluster_ctarank(), c = (int)cluster_id_x(), C = (int)cluster_count_x();
     // this rank's vectors [cv0, cv1) of every row, and this warp's share of them
     const int nvec = RB >> 4, nblk = (nvec + 3) >> 2;
-    const int cb0 = ks_blk(nblk, rank, S), cb1 = ks_blk(nblk, rank + 1, S);
-    const int cv0 = 4 * cb0, cv1 = min(nvec, 4 * cb1);
-    const int sv = cv1 - cv0, sp = ks_stride(sv);
-    const int wb0 = cb0 + (int)(((long long)(cb1 - cb0) * gw) / WPR);
-    const int wb1 = cb0 + (int)(((long long)(cb1 - cb0) * (gw + 1)) / WPR);
+    const int cb0 = mul_div(nblk, rank, S), cb1 = mul_div(nblk, rank + 1, S);  // floor(nblk * r / S)
+    const int cv1 = min(nvec, 4 * cb1);
+    const int wb0 = cb0 + (cb1 - cb0) * gw / WPR, wb1 = cb0 + (cb1 - cb0) * (gw + 1) / WPR;
     const int wv0 = 4 * wb0, wv1 = min(cv1, 4 * wb1);
     // this cluster's 8-row groups; rank r finishes local groups i with i % S == r
     const int RG = (N + 7) >> 3;
-    const int q0 = (int)(((long long)RG * c) / C), q1 = (int)(((long long)RG * (c + 1)) / C);
-    const int own = (q1 - q0) > rank ? (q1 - q0 - rank + S - 1) / S : 0;
-
-    if (tid == 0) {
-        mbar_init(&xbar, 1);
-        mbar_init(&rbar, 1);
-        fence_barrier_init();
-    }
-    __syncthreads();
-    if (tid == 0 && own > 0) mbar_arrive_expect_tx(&rbar, (uint32_t)(own * (S - 1) * TT * 512));
-    cluster_arrive_relaxed();  // phase 1: "my receive barrier is initialised"
+    const int q0 = mul_div(RG, c, C), q1 = mul_div(RG, c + 1, C);
 
     uint4 wv[U];
     auto load_batch = [&](int n0, int vb) {  // the batch of blocks starting at vector vb
@@ -138,6 +116,24 @@ __global__ void __launch_bounds__(NT, TT == 1 ? 1024 / NT : 1)
     bool pre = q < q1;
     if (pre) load_batch(8 * q, wv0);
 
+    const int nw = (int)blockDim.x >> 5;
+    const int GW = nw / WPR;  // 8-row groups in flight in this CTA
+    const KsLayout L = ks_layout(M, N, RB, S, C, nw, WPR, TT);
+    uint4 *xs = reinterpret_cast<uint4 *>(ks_smem);
+    float4 *part = reinterpret_cast<float4 *>(ks_smem + L.part_off);
+    float4 *recv = reinterpret_cast<float4 *>(ks_smem + L.recv_off);
+    const int cv0 = 4 * cb0, sv = cv1 - cv0, sp = ks_stride(sv);
+    const int own = (q1 - q0) > rank ? (q1 - q0 - rank + S - 1) / S : 0;
+
+    if (tid == 0) {
+        mbar_init(&xbar, 1);
+        mbar_init(&rbar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (tid == 0 && own > 0) mbar_arrive_expect_tx(&rbar, (uint32_t)(own * (S - 1) * TT * 512));
+    cluster_arrive_relaxed();  // phase 1: "my receive barrier is initialised"
+
     pdl_launch_dependents();
     pdl_wait();  // x may be written, and out still read, by the previous kernel
     const bool stage = q1 > q0 && sv > 0;
@@ -150,6 +146,9 @@ __global__ void __launch_bounds__(NT, TT == 1 ? 1024 / NT : 1)
     const bool ok = __syncthreads_and(staged) != 0;
     cluster_wait_acquire();  // phase 1 done: every rank's receive barrier exists
 
+    // this lane's token rows in the staged slice, indexed by vector: tokens 16j + g (lo) and 16j + g + 8 (hi)
+    const uint4 *xlo = xs + (g * sp - cv0), *xhi = xs + ((g + 8) * sp - cv0);
+    const int tstep = 16 * sp;  // vectors from one 16-token tile to the next
     for (; q < q1; q += GW) {
         const int n0 = 8 * q;
         float d[TT][4];
@@ -164,9 +163,8 @@ __global__ void __launch_bounds__(NT, TT == 1 ? 1024 / NT : 1)
                     const bool in = vv < wv1;
 #pragma unroll
                     for (int j = 0; j < TT; ++j) {
-                        const int mlo = 16 * j + g, mhi = mlo + 8;
-                        const uint4 lo = (in && mlo < M) ? xs[(size_t)mlo * sp + (vv - cv0)] : make_uint4(0u, 0u, 0u, 0u);
-                        const uint4 hi = (in && mhi < M) ? xs[(size_t)mhi * sp + (vv - cv0)] : make_uint4(0u, 0u, 0u, 0u);
+                        const uint4 lo = (in && 16 * j + g < M) ? xlo[j * tstep + vv] : make_uint4(0u, 0u, 0u, 0u);
+                        const uint4 hi = (in && 16 * j + g + 8 < M) ? xhi[j * tstep + vv] : make_uint4(0u, 0u, 0u, 0u);
                         // this lane's 16 block bytes: step 0 takes the first 8, step 1 the last 8
                         mma_16816(d[j], lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
                         mma_16816(d[j], lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
@@ -289,9 +287,11 @@ int set_ks_attrs() {
     for (int M : {16, 32, 64})
         for (int wpr : {1, 2, 4, 8, 16})
             for (int t : {512, 1024}) {
-                const int e = (int)cudaFuncSetAttribute(pick_ks<OutT>(M, wpr, t),
-                                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                        kWarpMmaKsMaxSmem);
+                int e = (int)cudaFuncSetAttribute(pick_ks<OutT>(M, wpr, t),
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kWarpMmaKsMaxSmem);
+                if (!e)
+                    e = (int)cudaFuncSetAttribute(pick_ks<OutT>(M, wpr, t),
+                                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
                 if (e) return e;
             }
     return 0;

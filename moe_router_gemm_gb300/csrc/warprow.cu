@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
     const int per = (nvec + WPR - 1) / WPR;
     const int kv0 = gw * per, kv1 = (kv0 + per) < nvec ? (kv0 + per) : nvec;
     const int G = (int)gridDim.x, b = (int)blockIdx.x;
-    const int r0 = (int)(((long long)N * b) / G), r1 = (int)(((long long)N * (b + 1)) / G);
+    const int r0 = mul_div(N, b, G), r1 = mul_div(N, b + 1, G);
 
     if (tid == 0) {
         mbar_init(&xbar, 1);

@@ -1,10 +1,10 @@
 """GPU parity of the cluster form of the warp-MMA kernel (WARPMMA plans with split_k >= 2).
 
-K is split over S = 2..8 CTAs of a cluster; each stages its K slice of up to 64
+K is split over S = 2..16 CTAs of a cluster; each stages its K slice of up to 64
 tokens (1 to 4 tiles of 16 on the MMA rows) and the partial tiles of every
 8-row group are summed, in rank order, by the rank that finishes the group.
 The cases cover every group size, 256/512/1024-thread blocks, one and two CTAs
-per SM, S from 2 to 8, K runs that end inside a 32-wide block or leave a rank a
+per SM, S from 2 to 16 (a non-portable cluster size above 8), K runs that end inside a 32-wide block or leave a rank a
 single block, N not a multiple of 8 and smaller than the cluster count, M from
 1 to 64 (ragged last tile, 3 tiles on the 4-tile instance), bias on and off,
 the decode and MLP shapes (sampled rows at M = 64 of the MLP weight), the fp32
@@ -23,7 +23,7 @@ DEV = "cuda:0"
 
 # (threads, warps per 8-row group, CTAs per SM, cluster size)
 CFGS = [(1024, 8, 1, 2), (1024, 4, 1, 4), (1024, 16, 1, 2), (512, 4, 1, 8), (512, 1, 1, 2), (256, 2, 2, 4),
-        (512, 16, 1, 3), (256, 8, 1, 8)]
+        (512, 16, 1, 3), (256, 8, 1, 8), (256, 2, 4, 16)]
 SHAPES = [(1, 300, 1032), (3, 517, 2880), (16, 203, 1024), (12, 96, 2056), (9, 1, 40), (20, 1000, 2048),
           (33, 77, 4096), (64, 130, 1024), (48, 2112, 512), (17, 2112, 7168)]
 
