@@ -545,17 +545,20 @@ def candidate_plans(lib, M, N, K):
     if K % 8 == 0 and M <= 16 and N > 1024:  # x fragments from L2 (any K)
         for t, w, c in ((512, 4, 1), (512, 8, 1), (512, 16, 1), (256, 4, 2), (256, 8, 2)):
             cands.append(lib.make_plan("warpmma", threads=t, rows_per_cta=w, stages=c, split_k=1))
-    if K % 8 == 0 and M <= 64 and N >= 1024:  # the warp-MMA kernel's cluster form: K over S CTAs
+    if K % 8 == 0 and M <= 64 and (N >= 1024 or M > 4):  # the warp-MMA kernel's cluster form: K over S CTAs
         cfgs = (((1024, 8, 1), (1024, 4, 1), (1024, 16, 1), (512, 4, 2), (512, 8, 2), (256, 2, 4), (256, 4, 4))
                 if M <= 16 else ((512, 4, 1), (512, 8, 1), (512, 16, 1), (256, 2, 2), (256, 4, 2), (256, 8, 2)))
         for S in (2, 4, 8, 16):
             for t, w, c in cfgs:
-                p = lib.make_plan("warpmma", threads=t, rows_per_cta=w, stages=c, split_k=S)
-                try:
-                    lib.plan_check(M, N, K, p)
-                except Exception:
-                    continue
-                cands.append(p)
+                for gpc in ((0,) if N >= 1024 else (0, 2, 4)):  # router N: several row groups per cluster
+                    if gpc > (t // 32) // w:
+                        continue
+                    p = lib.make_plan("warpmma", threads=t, rows_per_cta=w, stages=c, split_k=S, tokens_per_cta=gpc)
+                    try:
+                        lib.plan_check(M, N, K, p)
+                    except Exception:
+                        continue
+                    cands.append(p)
     if K % 8 == 0 and 16 < M <= 64:  # the router MMA split-K in 16-token groups
         for S, t, xr in itertools.product((1, 2, 4, 8), (128, 256), (1,)):
             p = lib.make_plan("dotmma", threads=t, rows_per_cta=8, split_k=S, stages=xr)

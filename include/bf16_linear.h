@@ -99,7 +99,8 @@ typedef struct {
                               WARPMMA: warps that share one group of 8 rows (1, 2, 4, 8 or 16) */
     int32_t tokens_per_cta;/* SPLITK: x rows loaded per chunk (M rounded up to 8, <= 64);  TILE: x rows per tile;
                               DOTPROD: tokens per CTA, 1..8 (0 = min(M, 8)); ceil(M / tokens) CTAs then share each
-                              row slice, one token group each, instead of one CTA looping over the groups */
+                              row slice, one token group each, instead of one CTA looping over the groups;
+                              WARPMMA cluster form: 8-row groups per cluster (0 = as many clusters as fit) */
     int32_t split_k;       /* SPLITK: CTAs per cluster along K (1..16); SPLITK_WS: CTAs along K (1..64);
                               DOTMMA: CTAs per cluster along K (1, 2, 4, 8 or 16);
                               DOTMMA_WS: CTAs along K (a power of two, 2..64);

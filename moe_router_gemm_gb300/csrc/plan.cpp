@@ -170,6 +170,11 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
                 int64_t clusters = (int64_t)dev.num_sms * cps / S;
                 const int64_t groups = ceil_div(N, 8);
                 if (clusters > groups) clusters = groups;
+                // tokens_per_cta > 0: that many 8-row groups per cluster (fewer clusters, one x slice per CTA
+                // serving several groups)
+                if (p->tokens_per_cta < 0) return BF16L_EINVAL;
+                if (p->tokens_per_cta > 0 && ceil_div(groups, p->tokens_per_cta) < clusters)
+                    clusters = ceil_div(groups, p->tokens_per_cta);
                 if (clusters < 1) return BF16L_EINVAL;
                 const int smem = warpmma_ks_smem_bytes(M, N, K, S, (int)clusters, t, wpr);
                 if (smem > kWarpMmaKsMaxSmem || (int64_t)cps * (smem + 1024) > 233472) return BF16L_EINVAL;

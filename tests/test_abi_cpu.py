@@ -247,6 +247,9 @@ def test_warpmma_cluster_plans_on_cpu(lib):
     assert lib.plan_check(32, 2112, 7168, mk(256, 2, 2, 8)).grid == 304    # two 256-thread CTAs per SM
     assert lib.plan_check(5, 24, 4096, mk(512, 4, 1, 2)).grid == 6         # no more clusters than row groups
     assert lib.plan_check(16, 2112, 7168, mk(256, 2, 4, 16)).grid == 608  # 38 clusters of 16
+    g4 = mk(256, 2, 4, 16)
+    g4.tokens_per_cta = 4
+    assert lib.plan_check(16, 256, 7168, g4).grid == 8 * 16              # 4 of the 32 row groups per cluster
     for bad in (mk(1024, 8, 1, 17), mk(512, 3, 1, 2), mk(512, 8, 0, 2), mk(512, 8, 3, 2), mk(1024, 2, 1, 2)):
         with pytest.raises(lib.BF16LinearError):
             lib.plan_check(16, 2112, 7168, bad)

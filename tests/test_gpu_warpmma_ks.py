@@ -84,6 +84,15 @@ def test_warpmma_cluster_mlp_sampled(lib):
         lib.plan_check(64, 14336, 4096, _plan(lib, 512, 4, 1, 4))
 
 
+@pytest.mark.parametrize("gpc", [1, 2, 3, 5])
+def test_warpmma_cluster_groups_per_cluster(lib, gpc):
+    # fewer clusters, each CTA's x slice serving several row groups (more groups than warp groups too)
+    p = _plan(lib, 256, 2, 4, 8)
+    p.tokens_per_cta = gpc
+    for M, N, K in ((16, 256, 7168), (7, 384, 4096), (13, 203, 2880)):
+        _check(lib, M, N, K, seed=gpc + M, bias=True, plan=p)
+
+
 def test_warpmma_cluster_agrees_across_forms(lib):
     # the same K slices in another cluster size give another summation order: both within tolerance,
     # each bitwise reproducible
