@@ -526,7 +526,7 @@ def candidate_plans(lib, M, N, K):
                 cands.append(p)
     if K % 8 == 0 and M <= 8 and M * K * 2 <= 200 * 1024:
         for t, w, c in ((512, 1, 2), (512, 2, 2), (512, 4, 2), (1024, 1, 1), (1024, 2, 1), (1024, 4, 1),
-                        (256, 1, 4), (256, 2, 4)):
+                        (256, 1, 4), (256, 2, 4), (128, 1, 8), (128, 2, 8), (128, 4, 8)):
             p = lib.make_plan("warprow", threads=t, rows_per_cta=w, stages=c)
             try:
                 lib.plan_check(M, N, K, p)
@@ -535,7 +535,7 @@ def candidate_plans(lib, M, N, K):
             cands.append(p)
     if K % 8 == 0 and M <= 16 and M * K * 2 <= 200 * 1024:
         for t, w, c in ((512, 1, 2), (512, 2, 2), (512, 4, 2), (512, 8, 2), (1024, 1, 1), (1024, 4, 1),
-                        (1024, 8, 1), (1024, 16, 1), (256, 1, 4), (256, 2, 4), (256, 8, 4)):
+                        (1024, 8, 1), (1024, 16, 1), (256, 1, 4), (256, 2, 4), (256, 8, 4), (128, 2, 8), (128, 4, 8)):
             p = lib.make_plan("warpmma", threads=t, rows_per_cta=w, stages=c)
             try:
                 lib.plan_check(M, N, K, p)
@@ -546,7 +546,8 @@ def candidate_plans(lib, M, N, K):
         for t, w, c in ((512, 4, 1), (512, 8, 1), (512, 16, 1), (256, 4, 2), (256, 8, 2)):
             cands.append(lib.make_plan("warpmma", threads=t, rows_per_cta=w, stages=c, split_k=1))
     if K % 8 == 0 and M <= 64 and (N >= 1024 or M > 4):  # the warp-MMA kernel's cluster form: K over S CTAs
-        cfgs = (((1024, 8, 1), (1024, 4, 1), (1024, 16, 1), (512, 4, 2), (512, 8, 2), (256, 2, 4), (256, 4, 4))
+        cfgs = (((1024, 8, 1), (1024, 4, 1), (1024, 16, 1), (512, 4, 2), (512, 8, 2), (256, 2, 4), (256, 4, 4),
+                 (128, 2, 8), (128, 4, 8))
                 if M <= 16 else ((512, 4, 1), (512, 8, 1), (512, 16, 1), (256, 2, 2), (256, 4, 2), (256, 8, 2)))
         for S in (2, 4, 8, 16):
             for t, w, c in cfgs:

@@ -158,7 +158,10 @@ __global__ void __launch_bounds__(kDmWarps * 32)
         ok = __syncthreads_and(staged) != 0;
     }
 
-    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    // two independent accumulator chains: step s of every block goes to chain s
+    float c[2][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) c[i][0] = c[i][1] = c[i][2] = c[i][3] = 0.f;
     if (ok) {
         const uint4 *xlo = xs + (size_t)(tok_lo ? g : 0) * sv;  // indexed by vector - cv0
         const uint4 *xhi = xs + (size_t)(tok_hi ? g + 8 : 0) * sv;
@@ -191,15 +194,18 @@ __global__ void __launch_bounds__(kDmWarps * 32)
                     }
                 }
                 if constexpr (F8) {
-                    mma16832_e4m3(d, lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
-                    mma16832_e4m3(d, lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
+                    mma16832_e4m3(c[0], lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
+                    mma16832_e4m3(c[1], lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
                 } else {
-                    mma16816(d, lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
-                    mma16816(d, lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
+                    mma16816(c[0], lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
+                    mma16816(c[1], lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
                 }
             }
         }
     }
+    float d[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) d[j] = c[0][j] + c[1][j];
     part[warp][lane] = make_float4(d[0], d[1], d[2], d[3]);
     __syncthreads();
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);

@@ -146,10 +146,12 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
             if (K % 8 != 0 || M > kWarpRowMaxTokens || warprow_smem_bytes(M, K) > kWarpRowMaxSmem)
                 return BF16L_EUNSUPPORTED;
             const int t = p->threads, wpr = p->rows_per_cta, cps = p->stages;
-            if ((t != 256 && t != 512 && t != 1024) || (wpr != 1 && wpr != 2 && wpr != 4)) return BF16L_EINVAL;
+            if ((t != 128 && t != 256 && t != 512 && t != 1024) || (wpr != 1 && wpr != 2 && wpr != 4) ||
+                (t / 32) % wpr != 0)
+                return BF16L_EINVAL;
             // a named barrier per row group (ids 1..15) when warps share a row
             if (wpr > 1 && (t / 32) / wpr > 15) return BF16L_EINVAL;
-            if (cps < 1 || cps > 4 || t * cps > 2048 ||
+            if (cps < 1 || cps > 8 || t * cps > 2048 ||
                 cps * (warprow_smem_bytes(M, K) + 2048) > 232448)
                 return BF16L_EINVAL;
             const int64_t ctas = (int64_t)dev.num_sms * cps;
@@ -162,10 +164,10 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
                 // (64 registers a thread), otherwise at most 512 threads per SM (128 registers)
                 const int S = p->split_k, t = p->threads, wpr = p->rows_per_cta, cps = p->stages;
                 if (K % 8 != 0 || M > kWarpMmaKsMaxTokens) return BF16L_EUNSUPPORTED;
-                if ((t != 256 && t != 512 && t != 1024) || (t == 1024 && M > 16) ||
+                if ((t != 128 && t != 256 && t != 512 && t != 1024) || (t == 1024 && M > 16) ||
                     (wpr != 1 && wpr != 2 && wpr != 4 && wpr != 8 && wpr != 16) || (t / 32) % wpr != 0 ||
                     (wpr > 1 && (t / 32) / wpr > 15) || S > kWarpMmaKsMaxCluster || S > ceil_div(K / 8, 4) ||
-                    cps < 1 || cps > 4 || t * cps > (M > 16 ? 512 : 1024))
+                    cps < 1 || cps > 8 || t * cps > (M > 16 ? 512 : 1024))
                     return BF16L_EINVAL;
                 int64_t clusters = (int64_t)dev.num_sms * cps / S;
                 const int64_t groups = ceil_div(N, 8);
@@ -186,13 +188,13 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
             if (K % 8 != 0 || M > kWarpMmaMaxTokens || (!xr && warpmma_smem_bytes(M, K) > kWarpMmaMaxSmem))
                 return BF16L_EUNSUPPORTED;
             const int t = p->threads, wpr = p->rows_per_cta, cps = p->stages;
-            if ((t != 256 && t != 512 && t != 1024) ||
+            if ((t != 128 && t != 256 && t != 512 && t != 1024) ||
                 (wpr != 1 && wpr != 2 && wpr != 4 && wpr != 8 && wpr != 16) || (t / 32) % wpr != 0 ||
                 (p->split_k != 0 && p->split_k != 1))
                 return BF16L_EINVAL;
             if (wpr > 1 && (t / 32) / wpr > 15) return BF16L_EINVAL;  // named barriers 1..15
             const int static_smem = (wpr > 1 ? 32 * 32 * 4 * 4 : 512) + 1024;
-            if (cps < 1 || cps > 4 || t * cps > (xr ? 512 : 1024) ||
+            if (cps < 1 || cps > 8 || t * cps > (xr ? 512 : 1024) ||
                 cps * ((xr ? 0 : warpmma_smem_bytes(M, K)) + static_smem) > 232448)
                 return BF16L_EINVAL;
             const int64_t ctas = (int64_t)dev.num_sms * cps, groups = ceil_div(N, 8);

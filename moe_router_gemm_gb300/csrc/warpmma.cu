@@ -136,7 +136,12 @@ __global__ void __launch_bounds__(NT, XR ? 1 : 1024 / NT)
     const uint4 *ghi = reinterpret_cast<const uint4 *>(x + (size_t)(tok_hi ? g + 8 : 0) * RB);
     for (bool first = true; q < q1; q += groups, first = false) {
         const int n0 = 8 * q;
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        // two independent accumulator chains: step s of every block goes to chain s (the same
+        // order whether x comes from shared memory or L2), summed at the end
+        constexpr int NC = 2;
+        float c[NC][4];
+#pragma unroll
+        for (int i = 0; i < NC; ++i) c[i][0] = c[i][1] = c[i][2] = c[i][3] = 0.f;
         for (int vb = vb0; vb < vb1; vb += 4 * U) {  // warp-uniform trip count: mma.sync is warp-wide
             if (!(first && vb == vb0)) load_batch(n0, vb);
             uint4 xl[XR ? U : 1], xh[XR ? U : 1];
@@ -165,14 +170,17 @@ __global__ void __launch_bounds__(NT, XR ? 1 : 1024 / NT)
                 }
                 // this lane's 16 block bytes: step 0 takes the first 8, step 1 the last 8
                 if constexpr (F8) {
-                    mma_m16n8k32_e4m3(d, lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
-                    mma_m16n8k32_e4m3(d, lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
+                    mma_m16n8k32_e4m3(c[0], lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
+                    mma_m16n8k32_e4m3(c[1], lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
                 } else {
-                    mma_m16n8k16(d, lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
-                    mma_m16n8k16(d, lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
+                    mma_m16n8k16(c[0], lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
+                    mma_m16n8k16(c[1], lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
                 }
             }
         }
+        float d[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) d[j] = c[0][j] + c[1][j];
         if constexpr (WPR > 1) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) part[warp][lane][j] = d[j];

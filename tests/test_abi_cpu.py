@@ -216,7 +216,9 @@ def test_warprow_plans_on_cpu(lib):
     mk = lambda t, w, c: lib.make_plan("warprow", threads=t, rows_per_cta=w, stages=c)
     assert lib.plan_check(1, 2112, 7168, mk(512, 2, 2)).grid == 304
     assert lib.plan_check(1, 100, 7168, mk(512, 2, 2)).grid == 100  # never more CTAs than rows
-    for bad in (mk(128, 1, 1), mk(512, 3, 1), mk(1024, 1, 3), mk(512, 1, 5), mk(256, 1, 0)):
+    assert lib.plan_check(1, 2112, 7168, mk(128, 2, 8)).grid == 1216  # eight 128-thread CTAs per SM
+    for bad in (mk(64, 1, 1), mk(512, 3, 1), mk(1024, 1, 3), mk(512, 1, 5), mk(256, 1, 0), mk(128, 8, 1),
+                mk(128, 1, 9)):
         with pytest.raises(lib.BF16LinearError):
             lib.plan_check(4, 2112, 7168, bad)
     with pytest.raises(lib.BF16LinearError):
@@ -231,7 +233,9 @@ def test_warpmma_plans_on_cpu(lib):
     mk = lambda t, w, c: lib.make_plan("warpmma", threads=t, rows_per_cta=w, stages=c)
     assert lib.plan_check(16, 14336, 4096, mk(1024, 4, 1)).grid == 152
     assert lib.plan_check(4, 2112, 7168, mk(512, 4, 2)).grid == 264  # 264 groups of 8 rows < 304 CTAs
-    for bad in (mk(512, 3, 1), mk(256, 16, 1), mk(1024, 2, 1), mk(1024, 1, 2), mk(512, 1, 0), mk(128, 1, 1)):
+    assert lib.plan_check(1, 2112, 4096, mk(128, 4, 8)).grid == 264  # eight 128-thread CTAs per SM, 264 groups
+    for bad in (mk(512, 3, 1), mk(256, 16, 1), mk(1024, 2, 1), mk(1024, 1, 2), mk(512, 1, 0), mk(64, 1, 1),
+                mk(128, 8, 1), mk(128, 1, 9)):
         with pytest.raises(lib.BF16LinearError):
             lib.plan_check(4, 2112, 7168, bad)
     with pytest.raises(lib.BF16LinearError):

@@ -19,7 +19,7 @@ from tolerance import check_close, tensor_bits
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
-CFGS = [(512, 1, 2), (512, 2, 2), (512, 4, 2), (512, 16, 1), (1024, 1, 1), (1024, 4, 1), (1024, 8, 1),
+CFGS = [(128, 4, 8), (128, 1, 8), (512, 1, 2), (512, 2, 2), (512, 4, 2), (512, 16, 1), (1024, 1, 1), (1024, 4, 1), (1024, 8, 1),
         (256, 1, 4), (256, 8, 4)]
 SHAPES = [(1, 300, 1032), (3, 517, 2880), (8, 64, 4096), (5, 1000, 136), (2, 5, 64), (16, 203, 1024),
           (12, 96, 2056), (9, 1, 40)]

@@ -23,7 +23,7 @@ DEV = "cuda:0"
 
 # (threads, warps per 8-row group, CTAs per SM, cluster size)
 CFGS = [(1024, 8, 1, 2), (1024, 4, 1, 4), (1024, 16, 1, 2), (512, 4, 1, 8), (512, 1, 1, 2), (256, 2, 2, 4),
-        (512, 16, 1, 3), (256, 8, 1, 8), (256, 2, 4, 16)]
+        (512, 16, 1, 3), (256, 8, 1, 8), (256, 2, 4, 16), (128, 2, 8, 4)]
 SHAPES = [(1, 300, 1032), (3, 517, 2880), (16, 203, 1024), (12, 96, 2056), (9, 1, 40), (20, 1000, 2048),
           (33, 77, 4096), (64, 130, 1024), (48, 2112, 512), (17, 2112, 7168)]
 

@@ -41,7 +41,7 @@ def _check(lib, M, N, K, seed, bias, plan, rows=None):
 
 
 @pytest.mark.parametrize("cfg", [(512, 1, 1), (512, 2, 1), (512, 4, 1), (1024, 1, 1), (1024, 4, 1),
-                                 (256, 1, 4), (256, 2, 2), (512, 2, 2)],
+                                 (256, 1, 4), (256, 2, 2), (512, 2, 2), (128, 1, 8), (128, 4, 8)],
                          ids=lambda c: "t%d_wpr%d_cps%d" % c)
 @pytest.mark.parametrize("shape", [(1, 300, 1032), (3, 517, 2880), (8, 64, 4096), (5, 1000, 136), (2, 5, 64)],
                          ids=lambda s: "x".join(map(str, s)))
