@@ -543,8 +543,10 @@ def candidate_plans(lib, M, N, K):
                 continue
             cands.append(p)
     if K % 8 == 0 and M <= 16 and N > 1024:  # x fragments from L2 (any K)
-        for t, w, c in ((512, 4, 1), (512, 8, 1), (512, 16, 1), (256, 4, 2), (256, 8, 2)):
-            cands.append(lib.make_plan("warpmma", threads=t, rows_per_cta=w, stages=c, split_k=1))
+        for t, w, c in ((512, 4, 1), (512, 8, 1), (512, 16, 1), (256, 4, 2), (256, 8, 2), (128, 4, 4)):
+            for ng in (0, 2, 4):  # one, two or four 8-row groups per warp
+                cands.append(lib.make_plan("warpmma", threads=t, rows_per_cta=w, stages=c, split_k=1,
+                                           tokens_per_cta=ng))
     if K % 8 == 0 and M <= 64 and (N >= 1024 or M > 4):  # the warp-MMA kernel's cluster form: K over S CTAs
         cfgs = (((1024, 8, 1), (1024, 4, 1), (1024, 16, 1), (512, 4, 2), (512, 8, 2), (256, 2, 4), (256, 4, 4),
                  (128, 2, 8), (128, 4, 8))

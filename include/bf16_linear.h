@@ -100,7 +100,8 @@ typedef struct {
     int32_t tokens_per_cta;/* SPLITK: x rows loaded per chunk (M rounded up to 8, <= 64);  TILE: x rows per tile;
                               DOTPROD: tokens per CTA, 1..8 (0 = min(M, 8)); ceil(M / tokens) CTAs then share each
                               row slice, one token group each, instead of one CTA looping over the groups;
-                              WARPMMA cluster form: 8-row groups per cluster (0 = as many clusters as fit) */
+                              WARPMMA: 8-row groups a warp covers per x fragment, 1, 2 or 4 (2 and 4 only with
+                              split_k = 1; 0 = 1); WARPMMA cluster form: 8-row groups per cluster (0 = as many clusters as fit) */
     int32_t split_k;       /* SPLITK: CTAs per cluster along K (1..16); SPLITK_WS: CTAs along K (1..64);
                               DOTMMA: CTAs per cluster along K (1, 2, 4, 8 or 16);
                               DOTMMA_WS: CTAs along K (a power of two, 2..64);

@@ -193,11 +193,15 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
                 (p->split_k != 0 && p->split_k != 1))
                 return BF16L_EINVAL;
             if (wpr > 1 && (t / 32) / wpr > 15) return BF16L_EINVAL;  // named barriers 1..15
+            // tokens_per_cta: 8-row groups per warp, 0/1, 2 or 4 (2 and 4 only with x from L2)
+            const int ng = p->tokens_per_cta > 1 ? p->tokens_per_cta : 1;
+            if (p->tokens_per_cta < 0 || p->tokens_per_cta == 3 || p->tokens_per_cta > 4 || (ng > 1 && !xr))
+                return BF16L_EINVAL;
             const int static_smem = (wpr > 1 ? 32 * 32 * 4 * 4 : 512) + 1024;
             if (cps < 1 || cps > 8 || t * cps > (xr ? 512 : 1024) ||
                 cps * ((xr ? 0 : warpmma_smem_bytes(M, K)) + static_smem) > 232448)
                 return BF16L_EINVAL;
-            const int64_t ctas = (int64_t)dev.num_sms * cps, groups = ceil_div(N, 8);
+            const int64_t ctas = (int64_t)dev.num_sms * cps, groups = ceil_div(N, 8 * ng);
             p->grid = M == 0 ? 0 : (int)(ctas < groups ? ctas : groups);
             return BF16L_OK;
         }

@@ -71,13 +71,16 @@ int warpmma_smem_bytes(int M, int K) { return M * K * 2; }
 // too large to stage, e.g. 16 tokens of K = 7168); 512 threads per SM then, as
 // the batch of x fragments takes another 64 registers a thread.  F8: x and W
 // are e4m3 codes (m16n8k32 MMAs on the same registers; the sum is scaled by
-// *scale_x * *scale_w before bias).  Rows of x and W are RB bytes.
-template <int WPR, int NT, bool HI, bool XR, bool F8, typename OutT>
+// *scale_x * *scale_w before bias).  NG: 8-row groups a warp covers with each
+// x fragment it reads (1, 2 or 4; with 2 the x bytes read per weight byte halve,
+// which matters once 9..16 tokens make x twice the weight bytes a warp moves).
+// Rows of x and W are RB bytes.
+template <int WPR, int NT, bool HI, bool XR, bool F8, typename OutT, int NG = 1>
 __global__ void __launch_bounds__(NT, XR ? 1 : 1024 / NT)
     warpmma_kernel(const uint8_t *__restrict__ x, const uint8_t *__restrict__ W, const uint16_t *__restrict__ bias,
                    OutT *__restrict__ out, int M, int N, int RB, int32_t *status, const float *__restrict__ scale_x,
                    const float *__restrict__ scale_w) {
-    constexpr int U = 8;                           // K blocks (4 x 16 bytes across a lane quad) per lane per batch
+    constexpr int U = 8 / NG;                      // K blocks (4 x 16 bytes across a lane quad) per lane per batch
     extern __shared__ uint4 xs[];                  // x[m] rows as 16-byte vectors, [M][RB / 16]
     __shared__ float part[WPR > 1 ? kWmMaxWarps : 1][32][4];  // WPR > 1: every lane's four sums
     __shared__ __align__(8) uint64_t xbar;
@@ -93,10 +96,10 @@ __global__ void __launch_bounds__(NT, XR ? 1 : 1024 / NT)
     const int per = (nblk + WPR - 1) / WPR;
     const int vb0 = 4 * gw * per;
     const int vb1 = min(nvec, 4 * (gw + 1) * per);
-    // CTA b owns the 8-row groups [RG*b/G, RG*(b+1)/G)
-    const int RG = (N + 7) >> 3;
+    // CTA b owns the (8 NG)-row slabs [RS*b/G, RS*(b+1)/G)
+    const int RS = (N + 8 * NG - 1) / (8 * NG);
     const int G = (int)gridDim.x, b = (int)blockIdx.x;
-    const int q0 = mul_div(RG, b, G), q1 = mul_div(RG, b + 1, G);
+    const int q0 = mul_div(RS, b, G), q1 = mul_div(RS, b + 1, G);
     const bool tok_lo = g < M, tok_hi = HI && (g + 8 < M);
 
     if (tid == 0) {
@@ -104,18 +107,21 @@ __global__ void __launch_bounds__(NT, XR ? 1 : 1024 / NT)
         fence_barrier_init();
     }
 
-    uint4 wv[U];
+    uint4 wv[U][NG];
     auto load_batch = [&](int n0, int vb) {  // the batch of blocks starting at vector vb
-        const int row = n0 + g;
-        const uint4 *wr = reinterpret_cast<const uint4 *>(W + (size_t)(row < N ? row : N - 1) * RB);
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int vv = vb + 4 * u + t;
-            wv[u] = (vv < vb1 && row < N) ? ldg_stream_v4(wr + vv) : make_uint4(0u, 0u, 0u, 0u);
+        for (int j = 0; j < NG; ++j) {
+            const int row = n0 + 8 * j + g;
+            const uint4 *wr = reinterpret_cast<const uint4 *>(W + (size_t)(row < N ? row : N - 1) * RB);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int vv = vb + 4 * u + t;
+                wv[u][j] = (vv < vb1 && row < N) ? ldg_stream_v4(wr + vv) : make_uint4(0u, 0u, 0u, 0u);
+            }
         }
     };
     int q = q0 + grp;
-    if (q < q1) load_batch(8 * q, vb0);
+    if (q < q1) load_batch(8 * NG * q, vb0);
 
     pdl_launch_dependents();
     pdl_wait();  // x may be written, and out still read, by the previous kernel
@@ -135,13 +141,14 @@ __global__ void __launch_bounds__(NT, XR ? 1 : 1024 / NT)
     const uint4 *glo = reinterpret_cast<const uint4 *>(x + (size_t)(tok_lo ? g : 0) * RB);
     const uint4 *ghi = reinterpret_cast<const uint4 *>(x + (size_t)(tok_hi ? g + 8 : 0) * RB);
     for (bool first = true; q < q1; q += groups, first = false) {
-        const int n0 = 8 * q;
-        // two independent accumulator chains: step s of every block goes to chain s (the same
-        // order whether x comes from shared memory or L2), summed at the end
-        constexpr int NC = 2;
-        float c[NC][4];
+        const int n0 = 8 * NG * q;
+        // per 8-row group, two independent accumulator chains: step s of every block goes to chain
+        // s (the same order whether x comes from shared memory or L2), summed at the end
+        float c[NG][2][4];
 #pragma unroll
-        for (int i = 0; i < NC; ++i) c[i][0] = c[i][1] = c[i][2] = c[i][3] = 0.f;
+        for (int j = 0; j < NG; ++j)
+#pragma unroll
+            for (int i = 0; i < 2; ++i) c[j][i][0] = c[j][i][1] = c[j][i][2] = c[j][i][3] = 0.f;
         for (int vb = vb0; vb < vb1; vb += 4 * U) {  // warp-uniform trip count: mma.sync is warp-wide
             if (!(first && vb == vb0)) load_batch(n0, vb);
             uint4 xl[XR ? U : 1], xh[XR ? U : 1];
@@ -168,49 +175,56 @@ __global__ void __launch_bounds__(NT, XR ? 1 : 1024 / NT)
                         if (tok_hi && in) hi = xhi[vv];
                     }
                 }
-                // this lane's 16 block bytes: step 0 takes the first 8, step 1 the last 8
-                if constexpr (F8) {
-                    mma_m16n8k32_e4m3(c[0], lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
-                    mma_m16n8k32_e4m3(c[1], lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
-                } else {
-                    mma_m16n8k16(c[0], lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
-                    mma_m16n8k16(c[1], lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
+                // this lane's 16 block bytes: step 0 takes the first 8, step 1 the last 8; the same
+                // x fragment feeds every 8-row group of the slab
+#pragma unroll
+                for (int j = 0; j < NG; ++j) {
+                    if constexpr (F8) {
+                        mma_m16n8k32_e4m3(c[j][0], lo.x, hi.x, lo.y, hi.y, wv[u][j].x, wv[u][j].y);
+                        mma_m16n8k32_e4m3(c[j][1], lo.z, hi.z, lo.w, hi.w, wv[u][j].z, wv[u][j].w);
+                    } else {
+                        mma_m16n8k16(c[j][0], lo.x, hi.x, lo.y, hi.y, wv[u][j].x, wv[u][j].y);
+                        mma_m16n8k16(c[j][1], lo.z, hi.z, lo.w, hi.w, wv[u][j].z, wv[u][j].w);
+                    }
                 }
             }
         }
-        float d[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) d[j] = c[0][j] + c[1][j];
-        if constexpr (WPR > 1) {
+        for (int jg = 0; jg < NG; ++jg) {  // each 8-row group of the slab: reduce over the WPR warps, store
+            float d[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) part[warp][lane][j] = d[j];
-            asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(WPR * 32) : "memory");
-            if (gw == 0) {
+            for (int j = 0; j < 4; ++j) d[j] = c[jg][0][j] + c[jg][1][j];
+            if constexpr (WPR > 1) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) part[warp][lane][j] = d[j];
+                asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(WPR * 32) : "memory");
+                if (gw == 0) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        float s = 0.f;
+                        for (int w = 0; w < WPR; ++w) s += part[grp * WPR + w][lane][j];
+                        d[j] = s;
+                    }
+                }
+            }
+            if (WPR == 1 || gw == 0) {
+                if constexpr (F8) {  // per-tensor scales (read after the grid-dependency wait)
+                    const float sxw = __ldg(scale_x) * __ldg(scale_w);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) d[j] *= sxw;
+                }
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    float s = 0.f;
-                    for (int w = 0; w < WPR; ++w) s += part[grp * WPR + w][lane][j];
-                    d[j] = s;
+                    const int m = g + (j >> 1) * 8, n = n0 + 8 * jg + 2 * t + (j & 1);
+                    if (m < M && n < N) {
+                        float s = d[j];
+                        if (bias) s += bf16_to_f32(bias[n]);
+                        OutStore<OutT>::one(out + (size_t)m * N + n, s);
+                    }
                 }
             }
+            if constexpr (WPR > 1) asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(WPR * 32) : "memory");
         }
-        if (WPR == 1 || gw == 0) {
-            if constexpr (F8) {  // per-tensor scales (read after the grid-dependency wait)
-                const float sxw = __ldg(scale_x) * __ldg(scale_w);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) d[j] *= sxw;
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int m = g + (j >> 1) * 8, n = n0 + 2 * t + (j & 1);
-                if (m < M && n < N) {
-                    float s = d[j];
-                    if (bias) s += bf16_to_f32(bias[n]);
-                    OutStore<OutT>::one(out + (size_t)m * N + n, s);
-                }
-            }
-        }
-        if constexpr (WPR > 1) asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(WPR * 32) : "memory");
     }
 }
 
@@ -220,27 +234,37 @@ template <typename OutT>
 using WmFn = void (*)(const uint8_t *, const uint8_t *, const uint16_t *, OutT *, int, int, int, int32_t *,
                       const float *, const float *);
 
-template <int WPR, bool HI, bool XR, bool F8, typename OutT>
+template <int WPR, bool HI, bool XR, bool F8, typename OutT, int NG>
 WmFn<OutT> pick_nt(int threads) {
-    if constexpr (XR) return warpmma_kernel<WPR, 512, HI, true, F8, OutT>;  // at most 512 threads
-    return threads > 512 ? warpmma_kernel<WPR, 1024, HI, false, F8, OutT>
-                         : warpmma_kernel<WPR, 512, HI, false, F8, OutT>;
+    if constexpr (XR) {
+        return warpmma_kernel<WPR, 512, HI, true, F8, OutT, NG>;  // at most 512 threads
+    } else {
+        return threads > 512 ? warpmma_kernel<WPR, 1024, HI, false, F8, OutT, NG>
+                             : warpmma_kernel<WPR, 512, HI, false, F8, OutT, NG>;
+    }
 }
 
-template <bool HI, bool XR, bool F8, typename OutT>
+template <bool HI, bool XR, bool F8, typename OutT, int NG = 1>
 WmFn<OutT> pick_wpr(int wpr, int threads) {
     switch (wpr) {
-        case 1: return pick_nt<1, HI, XR, F8, OutT>(threads);
-        case 2: return pick_nt<2, HI, XR, F8, OutT>(threads);
-        case 4: return pick_nt<4, HI, XR, F8, OutT>(threads);
-        case 8: return pick_nt<8, HI, XR, F8, OutT>(threads);
-        case 16: return pick_nt<16, HI, XR, F8, OutT>(threads);
+        case 1: return pick_nt<1, HI, XR, F8, OutT, NG>(threads);
+        case 2: return pick_nt<2, HI, XR, F8, OutT, NG>(threads);
+        case 4: return pick_nt<4, HI, XR, F8, OutT, NG>(threads);
+        case 8: return pick_nt<8, HI, XR, F8, OutT, NG>(threads);
+        case 16: return pick_nt<16, HI, XR, F8, OutT, NG>(threads);
         default: return nullptr;
     }
 }
 
+// ng: 8-row groups per warp (2 or 4 only with x from L2, whose 128 registers hold the groups' weights).
 template <typename OutT>
-WmFn<OutT> pick_wm(int M, int wpr, int threads, bool xr) {
+WmFn<OutT> pick_wm(int M, int wpr, int threads, bool xr, int ng = 1) {
+    if (xr && ng == 4)
+        return M > 8 ? pick_wpr<true, true, false, OutT, 4>(wpr, threads)
+                     : pick_wpr<false, true, false, OutT, 4>(wpr, threads);
+    if (xr && ng == 2)
+        return M > 8 ? pick_wpr<true, true, false, OutT, 2>(wpr, threads)
+                     : pick_wpr<false, true, false, OutT, 2>(wpr, threads);
     if (xr)
         return M > 8 ? pick_wpr<true, true, false, OutT>(wpr, threads) : pick_wpr<false, true, false, OutT>(wpr, threads);
     return M > 8 ? pick_wpr<true, false, false, OutT>(wpr, threads) : pick_wpr<false, false, false, OutT>(wpr, threads);
@@ -287,7 +311,8 @@ int launch_wm_common(WmFn<OutT> fn, const void *x, const void *W, const void *bi
 template <typename OutT>
 int launch_wm_t(const LaunchArgs &a, const bf16l_plan &p) {
     const bool xr = p.split_k == 1;
-    return launch_wm_common(pick_wm<OutT>(a.M, p.rows_per_cta, p.threads, xr), a.x, a.W, a.bias,
+    const int ng = p.tokens_per_cta > 1 ? p.tokens_per_cta : 1;
+    return launch_wm_common(pick_wm<OutT>(a.M, p.rows_per_cta, p.threads, xr, ng), a.x, a.W, a.bias,
                             static_cast<OutT *>(a.out), a.M, a.N, a.K * 2, p.grid, p.threads,
                             xr ? 0 : (size_t)warpmma_smem_bytes(a.M, a.K), (uint32_t)p.flags, a.stream, a.status,
                             nullptr, nullptr);

@@ -238,6 +238,13 @@ def test_warpmma_plans_on_cpu(lib):
                 mk(128, 8, 1), mk(128, 1, 9)):
         with pytest.raises(lib.BF16LinearError):
             lib.plan_check(4, 2112, 7168, bad)
+    xr2 = lib.make_plan("warpmma", threads=256, rows_per_cta=8, stages=2, split_k=1, tokens_per_cta=2)
+    assert lib.plan_check(16, 2112, 7168, xr2).grid == 132  # 16-row slabs: 132 < 304 CTAs
+    for bad in (lib.make_plan("warpmma", threads=256, rows_per_cta=8, stages=2, split_k=0, tokens_per_cta=2),
+                lib.make_plan("warpmma", threads=256, rows_per_cta=8, stages=2, split_k=1, tokens_per_cta=3),
+                lib.make_plan("warpmma", threads=256, rows_per_cta=8, stages=2, split_k=1, tokens_per_cta=8)):
+        with pytest.raises(lib.BF16LinearError):
+            lib.plan_check(4, 2112, 7168, bad)           # several groups per warp only with x from L2; 1, 2 or 4
     with pytest.raises(lib.BF16LinearError):
         lib.plan_check(17, 2112, 4096, mk(512, 1, 1))   # at most 16 tokens
     with pytest.raises(lib.BF16LinearError):

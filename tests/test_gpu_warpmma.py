@@ -75,11 +75,28 @@ def test_warpmma_x_from_l2(lib, shape, cfg):
         _check(lib, M, N, K, seed=M + N + K + 1, bias=bias, plan=_plan(lib, *cfg, xr=1))
 
 
+@pytest.mark.parametrize("ng", [2, 4])
+@pytest.mark.parametrize("cfg", XR_CFGS + [(128, 4, 4)], ids=lambda c: "t%d_wpr%d_cps%d" % c)
+@pytest.mark.parametrize("shape", SHAPES + [(16, 333, 7168), (13, 2112, 7168)], ids=lambda s: "x".join(map(str, s)))
+def test_warpmma_groups_per_warp(lib, shape, cfg, ng):
+    """x from L2, each x fragment feeding 2 or 4 8-row groups (16 or 32 W rows per warp, slabs past N ragged)."""
+    M, N, K = shape
+    p = _plan(lib, *cfg, xr=1)
+    p.tokens_per_cta = ng
+    for bias in (False, True):
+        _check(lib, M, N, K, seed=M + N + K + 2, bias=bias, plan=p)
+
+
 def test_warpmma_x_paths_agree(lib):
-    # the same fragments reach the same MMAs from shared memory or from L2: the same bits
+    # the same fragments reach the same MMAs in the same order from shared memory or from L2, one
+    # or two 8-row groups per warp: the same bits
     x, W, b = wl.make_inputs(12, 2112, 4096, 4, True)
     a = tensor_bits(_run(lib, x, W, b, _plan(lib, 512, 4, 1, 0)))
     assert np.array_equal(a, tensor_bits(_run(lib, x, W, b, _plan(lib, 512, 4, 1, 1))))
+    for ng in (2, 4):
+        p = _plan(lib, 512, 4, 1, 1)
+        p.tokens_per_cta = ng
+        assert np.array_equal(a, tensor_bits(_run(lib, x, W, b, p)))
 
 
 @pytest.mark.parametrize("M", [9, 16])
