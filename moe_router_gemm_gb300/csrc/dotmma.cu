@@ -127,14 +127,6 @@ __global__ void __launch_bounds__(kDmWarps * 32)
     const int row = n0 + g;
     const uint4 *wr = reinterpret_cast<const uint4 *>(W + (size_t)(row < N ? row : N - 1) * RB);
 
-    if (tid == 0) {
-        mbar_init(&xbar, 1);
-        mbar_init(&rbar, 1);
-        fence_barrier_init();
-    }
-    __syncthreads();
-    if (clus) cluster_arrive_relaxed();  // phase 1: "my receive barrier is initialised"
-
     uint4 wv[U];
     auto load_batch = [&](int vb) {
 #pragma unroll
@@ -143,7 +135,15 @@ __global__ void __launch_bounds__(kDmWarps * 32)
             wv[u] = (vv < wv1 && row < N) ? ldg_stream_v4(wr + vv) : make_uint4(0u, 0u, 0u, 0u);
         }
     };
-    load_batch(wv0);  // in flight before anything waits
+    load_batch(wv0);  // in flight before anything waits, the barrier set-up included
+
+    if (tid == 0) {
+        mbar_init(&xbar, 1);
+        mbar_init(&rbar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (clus) cluster_arrive_relaxed();  // phase 1: "my receive barrier is initialised"
 
     pdl_launch_dependents();
     pdl_wait();  // x may be written, and out still read, by the previous kernel

@@ -87,6 +87,20 @@ __global__ void __launch_bounds__(256) dotprod_kernel(const uint16_t *__restrict
         wrow[r] = W + (size_t)n * K;
     }
 
+    Vec<VEC> wv[U][R];
+    auto load_batch = [&](int v0) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int v = v0 + u * nt;
+            if (v < nvec) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) wv[u][r].load_stream(wrow[r] + (size_t)v * VEC);
+            }
+        }
+    };
+    // the first pass's first weight batch is in flight before the barrier set-up and before x is touched
+    if ((int)blockIdx.y * MT < M) load_batch(tid);
+
     if constexpr (XSMEM) {
         if (tid == 0) {
             mbar_init(&xbar, 1);
@@ -102,18 +116,7 @@ __global__ void __launch_bounds__(256) dotprod_kernel(const uint16_t *__restrict
 #pragma unroll
             for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
 
-        Vec<VEC> wv[U][R];
-        auto load_batch = [&](int v0) {
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int v = v0 + u * nt;
-                if (v < nvec) {
-#pragma unroll
-                    for (int r = 0; r < R; ++r) wv[u][r].load_stream(wrow[r] + (size_t)v * VEC);
-                }
-            }
-        };
-        load_batch(tid);  // first weight batch in flight before x is touched
+        if (pass > 0) load_batch(tid);  // this pass's first weight batch
         if (pass == 0) {
             pdl_launch_dependents();  // (no-ops unless launched with programmatic serialization)
             pdl_wait();               // x may be written by the previous kernel; out may still be read by it
