@@ -671,19 +671,15 @@ def e2e_arm(args, shapes, lib, device, stream):
         x, W, b = s.host
         host.append((x.pin_memory(), W.pin_memory(), b.pin_memory() if b is not None else None,
                      torch.empty(s.M, s.N, dtype=torch.bfloat16).pin_memory()))
-    dev = [(torch.empty_like(s.x), torch.empty_like(s.Ws[0]), torch.empty_like(s.b) if s.b is not None else None,
-            torch.empty_like(s.out)) for s in shapes]
+    # one device staging buffer per shape: bf16_linear_host copies x, W (and bias) into it, runs the
+    # planned kernel and copies out back, all on the stream (one C-ABI call per shape and step)
+    staging = [lib.new_host_staging(s.M, s.N, s.K, s.b is not None, device=device) for s in shapes]
     h2d = sum(h[0].numel() * 2 + h[1].numel() * 2 + (h[2].numel() * 2 if h[2] is not None else 0) for h in host)
     d2h = sum(h[3].numel() * 2 for h in host)
 
     def one_step():
-        for (hx, hW, hb, ho), (dx, dW, db, do), s_ in zip(host, dev, shapes):
-            dx.copy_(hx, non_blocking=True)
-            dW.copy_(hW, non_blocking=True)
-            if hb is not None:
-                db.copy_(hb, non_blocking=True)
-            lib.run(dx, dW, db, do, workspace=s_.ws)
-            ho.copy_(do, non_blocking=True)
+        for (hx, hW, hb, ho), st in zip(host, staging):
+            lib.bf16_linear_host(hx, hW, hb, ho, staging=st, stream=stream)
 
     steps = max(1, min(args.steps, 5))
     with torch.cuda.stream(stream):

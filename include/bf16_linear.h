@@ -182,6 +182,32 @@ int bf16_linear_ex(const void *x, const void *W, const void *bias, void *out,
                    int M, int N, int K, uint32_t flags, bf16l_stream_t stream);
 
 /*
+ * bf16_linear_host — bf16_linear_ex on HOST buffers: copies x, W and bias from
+ * host memory into a caller-provided device staging buffer, runs the planned
+ * kernel there, and copies out back to host memory, all enqueued on `stream`
+ * (one cudaMemcpyAsync per buffer, in that order).
+ *
+ * x: host bf16 [M][K]; W: host bf16 [N][K]; bias: host bf16 [N] or NULL;
+ * out: host bf16 [M][N], written in full once the stream reaches the copy.
+ * Page-locked host memory gives asynchronous copies; pageable memory works
+ * but the driver then stages each copy synchronously.  staging: device memory
+ * of at least bf16_linear_host_staging_bytes(M, N, K, bias != NULL) bytes,
+ * 256-byte aligned, owned by the caller; the library lays out x, W, bias and
+ * out in it at 256-byte aligned offsets and allocates nothing.  The host
+ * buffers and the staging must stay valid, and unread/unwritten by the caller,
+ * until the stream passes the final copy.
+ * Returns BF16L_OK (M == 0: nothing enqueued), BF16L_EINVAL (sizes, NULL
+ * x/W/out/staging, staging too small, unknown flags), BF16L_EALIGN (staging
+ * not 256-byte aligned), BF16L_EARCH, or BF16L_ELAUNCH (a copy or the launch
+ * failed; bf16_linear_cuda_error has the CUDA code).
+ */
+int bf16_linear_host(const void *x, const void *W, const void *bias, void *out, int M, int N, int K,
+                     void *staging, size_t staging_bytes, uint32_t flags, bf16l_stream_t stream);
+
+/* Device staging bytes bf16_linear_host needs for this shape (0 for invalid sizes).  Pure host code. */
+size_t bf16_linear_host_staging_bytes(int M, int N, int K, int with_bias);
+
+/*
  * bf16_linear_f32out — the router-logits variant: the same product and bias,
  * but out is fp32 [M][N] (each output is the fp32 accumulation plus the bias,
  * not rounded to bf16).  The vLLM PR #42562 page's split-K router kernel

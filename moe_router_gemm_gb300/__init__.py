@@ -11,6 +11,7 @@ from ._binding import (BF16LinearError, Call, Device, KERNEL_DOTPROD, KERNEL_NAM
                        KERNEL_SPLITK_WS, KERNEL_STREAM, KERNEL_TILE2, KERNEL_WARPROW,
                        KERNEL_WARPMMA, KERNEL_DOTMMA, KERNEL_DOTMMA_WS, new_workspace, plan_ws, run, workspace_size,
                        KERNEL_TILE, LIB_PATH, FLAG_PDL, Plan, bf16_linear, bf16_linear_ex, bf16_linear_f32out,
-                       bf16_linear_noalloc, bf16_linear_fp8, quant_fp8, fp8_split,
+                       bf16_linear_noalloc, bf16_linear_fp8, quant_fp8, fp8_split, bf16_linear_host,
+                       host_staging_bytes, new_host_staging,
                        bf16_linear_with_plan, device_status,
                        load, make_plan, plan, plan_check, selftest_wait, strerror, version)

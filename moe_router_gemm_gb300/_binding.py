@@ -81,6 +81,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.bf16_linear.restype = i32
         lib.bf16_linear_ex.argtypes = [vp, vp, vp, vp, i32, i32, i32, ctypes.c_uint32, vp]
         lib.bf16_linear_ex.restype = i32
+        lib.bf16_linear_host.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, ctypes.c_size_t, ctypes.c_uint32, vp]
+        lib.bf16_linear_host.restype = i32
+        lib.bf16_linear_host_staging_bytes.argtypes = [i32, i32, i32, i32]
+        lib.bf16_linear_host_staging_bytes.restype = ctypes.c_size_t
         lib.bf16_linear_f32out.argtypes = [vp, vp, vp, vp, i32, i32, i32, ctypes.c_uint32, vp]
         lib.bf16_linear_f32out.restype = i32
         lib.bf16_linear_f32out_with_plan.argtypes = [vp, vp, vp, vp, i32, i32, i32, ctypes.POINTER(Plan), vp]
@@ -219,6 +223,54 @@ def _stream_handle(stream, device):
     if stream is None:
         stream = torch.cuda.current_stream(device)
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def host_staging_bytes(M: int, N: int, K: int, with_bias: bool) -> int:
+    """Device staging bytes bf16_linear_host needs (bf16_linear_host_staging_bytes)."""
+    return int(load().bf16_linear_host_staging_bytes(int(M), int(N), int(K), 1 if with_bias else 0))
+
+
+def new_host_staging(M: int, N: int, K: int, with_bias: bool, device=None):
+    """A device staging tensor for bf16_linear_host (the caching allocator aligns blocks to 512 bytes)."""
+    import torch
+    return torch.empty(max(256, host_staging_bytes(M, N, K, with_bias)), dtype=torch.uint8,
+                       device=device or "cuda")
+
+
+def bf16_linear_host(x, W, bias=None, out=None, *, staging, flags: int = 0, stream=None):
+    """bf16_linear_host: x[M,K], W[N,K], bias[N] and out[M,N] are CPU bf16 tensors (page-locked for
+    asynchronous copies; out is allocated page-locked when None); the library copies them through the
+    CUDA tensor `staging`, runs the planned kernel and copies out back, all on the given (or current)
+    stream.  Returns out, complete once the stream has reached the final copy."""
+    import torch
+    for name, t in (("x", x), ("W", W), ("bias", bias)):
+        if t is not None and (t.dtype != torch.bfloat16 or t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CPU bf16 tensor")
+    if x.dim() != 2 or W.dim() != 2 or x.shape[1] != W.shape[1]:
+        raise ValueError(f"need x[M,K] and W[N,K], got {tuple(x.shape)} and {tuple(W.shape)}")
+    M, K = x.shape
+    N = W.shape[0]
+    if bias is not None and tuple(bias.shape) != (N,):
+        raise ValueError(f"bias must be [{N}], got {tuple(bias.shape)}")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    elif out.dtype != torch.bfloat16 or out.is_cuda or tuple(out.shape) != (M, N) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous CPU bf16 tensor of shape [M, N]")
+    if not staging.is_cuda or not staging.is_contiguous():
+        raise ValueError("staging must be a contiguous CUDA tensor")
+    dev = staging.device
+    if torch.cuda.current_device() == dev.index:  # (entering a device context costs more than the call)
+        h = _stream_handle(stream, dev)
+        st = load().bf16_linear_host(_ptr(x), _ptr(W), _ptr(bias), _ptr(out), M, N, K, _ptr(staging),
+                                     staging.numel() * staging.element_size(), int(flags), h)
+    else:
+        with torch.cuda.device(dev):
+            st = load().bf16_linear_host(_ptr(x), _ptr(W), _ptr(bias), _ptr(out), M, N, K, _ptr(staging),
+                                         staging.numel() * staging.element_size(), int(flags),
+                                         _stream_handle(stream, dev))
+    if st != OK:
+        _raise(st, f"bf16_linear_host(M={M}, N={N}, K={K})")
+    return out
 
 
 def bf16_linear(x, W, bias=None, out=None, stream=None):

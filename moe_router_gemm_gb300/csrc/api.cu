@@ -242,6 +242,48 @@ extern "C" int bf16_linear_ex(const void *x, const void *W, const void *bias, vo
     return bf16l::run(x, W, bias, out, M, N, K, nullptr, flags, stream);
 }
 
+namespace {
+size_t up256(size_t v) { return (v + 255) / 256 * 256; }
+}  // namespace
+
+extern "C" size_t bf16_linear_host_staging_bytes(int M, int N, int K, int with_bias) {
+    if (M < 0 || N <= 0 || K <= 0) return 0;
+    return up256(2ull * (size_t)M * (size_t)K) + up256(2ull * (size_t)N * (size_t)K) +
+           (with_bias ? up256(2ull * (size_t)N) : 0) + up256(2ull * (size_t)M * (size_t)N);
+}
+
+extern "C" int bf16_linear_host(const void *x, const void *W, const void *bias, void *out, int M, int N, int K,
+                                void *staging, size_t staging_bytes, uint32_t flags, bf16l_stream_t stream) {
+    using namespace bf16l;
+    if (M < 0 || N <= 0 || K <= 0 || (flags & ~BF16L_FLAG_PDL)) return BF16L_EINVAL;
+    if (M == 0) return BF16L_OK;
+    if (!x || !W || !out || !staging) return BF16L_EINVAL;
+    if (reinterpret_cast<uintptr_t>(staging) & 255u) return BF16L_EALIGN;
+    if (staging_bytes < bf16_linear_host_staging_bytes(M, N, K, bias != nullptr)) return BF16L_EINVAL;
+    const size_t bx = 2ull * (size_t)M * (size_t)K, bw = 2ull * (size_t)N * (size_t)K, bb = 2ull * (size_t)N,
+                 bo = 2ull * (size_t)M * (size_t)N;
+    uint8_t *dx = static_cast<uint8_t *>(staging);
+    uint8_t *dw = dx + up256(bx);
+    uint8_t *db = bias ? dw + up256(bw) : nullptr;
+    uint8_t *dout = dw + up256(bw) + (bias ? up256(bb) : 0);
+    const cudaStream_t s = (cudaStream_t)stream;
+    int e = (int)cudaMemcpyAsync(dx, x, bx, cudaMemcpyHostToDevice, s);
+    if (!e) e = (int)cudaMemcpyAsync(dw, W, bw, cudaMemcpyHostToDevice, s);
+    if (!e && bias) e = (int)cudaMemcpyAsync(db, bias, bb, cudaMemcpyHostToDevice, s);
+    if (e) {
+        note(e);
+        return BF16L_ELAUNCH;
+    }
+    const int st = bf16l::run(dx, dw, db, dout, M, N, K, nullptr, flags, stream);
+    if (st != BF16L_OK) return st;
+    e = (int)cudaMemcpyAsync(out, dout, bo, cudaMemcpyDeviceToHost, s);
+    if (e) {
+        note(e);
+        return BF16L_ELAUNCH;
+    }
+    return BF16L_OK;
+}
+
 extern "C" int bf16_linear_f32out(const void *x, const void *W, const void *bias, float *out, int M, int N, int K,
                                   uint32_t flags, bf16l_stream_t stream) {
     return bf16l::run(x, W, bias, out, M, N, K, nullptr, flags, stream, 1);

@@ -251,6 +251,16 @@ def test_warpmma_plans_on_cpu(lib):
         lib.plan_check(16, 2112, 7168, mk(512, 1, 1))   # x (229 KB) does not fit in shared memory
 
 
+def test_host_staging_bytes(lib):
+    # x, W, (bias,) out at 256-byte aligned offsets
+    assert lib.host_staging_bytes(4, 256, 2048, False) == 16384 + 1048576 + 2048
+    assert lib.host_staging_bytes(4, 256, 2048, True) == 16384 + 1048576 + 512 + 2048
+    assert lib.host_staging_bytes(3, 5, 8, True) == 4 * 256
+    assert lib.host_staging_bytes(0, 5, 8, False) == 256  # W only
+    for bad in ((-1, 5, 8), (3, 0, 8), (3, 5, 0)):
+        assert lib.host_staging_bytes(*bad, False) == 0
+
+
 def test_warpmma_cluster_plans_on_cpu(lib):
     mk = lambda t, w, c, S: lib.make_plan("warpmma", threads=t, rows_per_cta=w, stages=c, split_k=S)
     assert lib.plan_check(16, 2112, 7168, mk(1024, 8, 1, 2)).grid == 152   # 76 clusters of 2
