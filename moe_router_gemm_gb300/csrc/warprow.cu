@@ -89,9 +89,10 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
     if (!__syncthreads_and(staged)) return;  // the whole CTA leaves together (only after a timeout)
 
     for (bool first = true; n < r1; n += groups, first = false) {
-        float acc[MT];
+        // two independent fma chains per token (the low and the high 8 bytes of each vector), summed at the end
+        float acc[MT], acc2[MT];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+        for (int m = 0; m < MT; ++m) acc[m] = acc2[m] = 0.f;
         for (int v = kv0 + lane; v < kv1; v += 32 * U) {
             if (!(first && v == kv0 + lane)) load_batch(n, v);
 #pragma unroll
@@ -101,18 +102,20 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
 #pragma unroll
                     for (int m = 0; m < MT; ++m) {
                         const uint4 xv = xs[m * nvec + vv];
-                        float a = acc[m];
+                        float a = acc[m], a2 = acc2[m];
                         a = fma2_bf16(xv.x, wv[u].x, a);
+                        a2 = fma2_bf16(xv.z, wv[u].z, a2);
                         a = fma2_bf16(xv.y, wv[u].y, a);
-                        a = fma2_bf16(xv.z, wv[u].z, a);
-                        a = fma2_bf16(xv.w, wv[u].w, a);
+                        a2 = fma2_bf16(xv.w, wv[u].w, a2);
                         acc[m] = a;
+                        acc2[m] = a2;
                     }
                 }
             }
         }
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
+            acc[m] += acc2[m];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], off);
         }
