@@ -588,7 +588,8 @@ def candidate_plans(lib, M, N, K):
                 cands.append(p)
     if K % 8 == 0 and M > 64:
         for st in (6, 5, 4):
-            cands.append(lib.make_plan("tile2", threads=192, rows_per_cta=256, tokens_per_cta=256, stages=st))
+            for bn in (256, 192):  # W rows per pair tile
+                cands.append(lib.make_plan("tile2", threads=192, rows_per_cta=bn, tokens_per_cta=256, stages=st))
     if K % 8 == 0 and M > 32:
         for st in (4, 3):
             cands.append(lib.make_plan("tile", threads=192, rows_per_cta=256, tokens_per_cta=128, stages=st))

@@ -71,7 +71,7 @@ typedef enum {
     BF16L_KERNEL_STREAM = 4,   /* persistent CUDA-core kernel for M <= 4 and K <= 8192: one CTA per SM streams
                                   a contiguous row range through a bulk-copy ring (large N: decode, MLP) */
     BF16L_KERNEL_TILE2 = 5,    /* persistent tcgen05 tile GEMM on CTA pairs (cta_group::2, clusters of 2):
-                                  256 x 256 tiles, each CTA stages half of each operand; large M */
+                                  256 x 256 (or 256 x 192) tiles, each CTA stages half of each operand; large M */
     BF16L_KERNEL_WARPROW = 6,  /* persistent CUDA-core kernel for M <= 8 and many rows: a group of 1, 2 or 4
                                   warps computes one W row at a time from 16-byte loads, x in shared memory */
     BF16L_KERNEL_WARPMMA = 7,  /* persistent kernel for M <= 16 and many rows: 16-byte weight loads feed the
@@ -94,6 +94,7 @@ typedef struct {
     int32_t kernel;        /* bf16l_kernel */
     int32_t threads;       /* threads per CTA */
     int32_t rows_per_cta;  /* W rows per CTA (DOTPROD 1/2/4; SPLITK 16..256, the MMA N); TILE: W rows per tile;
+                              TILE2: W rows per pair tile (256 or 192);
                               STREAM: W rows per ring stage (1, 2, or 4 when M <= 3);
                               WARPROW: warps that share one row (1, 2 or 4);
                               WARPMMA: warps that share one group of 8 rows (1, 2, 4, 8 or 16) */

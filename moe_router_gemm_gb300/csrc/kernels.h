@@ -101,7 +101,7 @@ int init_dotmma();
 // 32 KB ring stages per CTA.
 constexpr int kTile2MinStages = 2;
 constexpr int kTile2MaxStages = 6;
-int tile2_smem_bytes(int stages);
+int tile2_smem_bytes(int stages, int bn);  // bn: W rows per pair tile, 256 or 192
 int init_tile2();
 
 constexpr int kChunkK = 64;  // K elements per TMA box row (128 bytes, the swizzle width)

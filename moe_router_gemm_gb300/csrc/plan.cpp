@@ -225,12 +225,14 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
             return BF16L_OK;
         }
         case BF16L_KERNEL_TILE2: {
-            // A pair tile is 256 x rows x 256 W rows; threads and tile sizes are fixed.
+            // A pair tile is 256 x rows x rows_per_cta W rows (256, or 192: 75 tiles for N = 14336, one per
+            // pair of SMs); threads and the x rows are fixed.
             if (K % 8 != 0) return BF16L_EUNSUPPORTED;
-            if (p->threads != kTileThreads || p->rows_per_cta != 2 * kTileBM || p->tokens_per_cta != 2 * kTileBM)
+            if (p->threads != kTileThreads || (p->rows_per_cta != 2 * kTileBM && p->rows_per_cta != 192) ||
+                p->tokens_per_cta != 2 * kTileBM)
                 return BF16L_EINVAL;
             if (p->stages < kTile2MinStages || p->stages > kTile2MaxStages) return BF16L_EINVAL;
-            const int64_t units = (int64_t)ceil_div(M, 2 * kTileBM) * ceil_div(N, 2 * kTileBM);
+            const int64_t units = (int64_t)ceil_div(M, 2 * kTileBM) * ceil_div(N, p->rows_per_cta);
             const int64_t pairs = dev.num_sms / 2;
             p->grid = M == 0 ? 0 : 2 * (int)(units < pairs ? units : pairs);
             return BF16L_OK;

@@ -23,7 +23,10 @@
 //   * each CTA's 4 epilogue warps drain their own TMEM rows and arrive on the
 //     leader's `acc_empty` (8 arrivals free an accumulator buffer);
 //   * fp32 accumulators double-buffered in TMEM (2 x 256 columns);
-//   * persistent: each cluster walks 256 x 256 tiles in groups of 8 N-tiles.
+//   * persistent: each cluster walks 256 x 256 tiles in groups of 8 N-tiles;
+//   * a 256 x 192 pair tile (each CTA staging 96 W rows, 28 KB stages) is the
+//     other instance: for a bandwidth-bound M = 256 it makes N = 14336 into 75
+//     tiles, one per pair of SMs, instead of 56 that leave 40 SMs idle.
 // Cross-CTA lifetime: a cluster barrier after set-up (every barrier exists
 // before any remote arrival) and one before TMEM is freed and the CTAs exit
 // (no remote arrival or copy is left in flight).  Every wait is bounded.
@@ -38,13 +41,18 @@ namespace bf16l {
 
 namespace {
 
-constexpr int kHalf = 128;                              // rows of A and of B per CTA
+constexpr int kHalf = 128;                              // rows of A per CTA
 constexpr int kPairBM = 2 * kHalf;                      // x rows per pair tile
-constexpr int kPairBN = 2 * kHalf;                      // W rows per pair tile
-constexpr int kHalfBytes = kHalf * kChunkK * 2;         // 16 KB
-constexpr int kStage2Bytes = 2 * kHalfBytes;            // A half + B half = 32 KB per CTA
-constexpr int kAcc2Cols = kPairBN;                      // fp32 columns of one accumulator
-constexpr uint32_t kIdesc2 = idesc_bf16_f32(kPairBM, kPairBN);
+constexpr int kHalfBytes = kHalf * kChunkK * 2;         // 16 KB: the A half of a stage
+// BN: W rows per pair tile (256, or 192 so that N = 14336 makes 75 tiles: one per
+// pair of SMs); each CTA stages BN / 2 of them per chunk.
+template <int BN>
+struct Pair {
+    static constexpr int kBHalfBytes = (BN / 2) * kChunkK * 2;        // 16 or 12 KB
+    static constexpr int kStageBytes = kHalfBytes + kBHalfBytes;      // 32 or 28 KB per CTA
+    static constexpr int kAccCols = BN;                               // fp32 columns of one accumulator
+    static constexpr uint32_t kIdesc = idesc_bf16_f32(kPairBM, BN);
+};
 constexpr int kGroup2N = 8;
 constexpr int kEpiWarps = 4;
 // TMEM accumulator buffers: 2 lets the epilogue of one tile overlap the MMAs
@@ -54,6 +62,8 @@ constexpr int kEpiWarps = 4;
 #endif
 constexpr int kAccBufs = BF16L_TILE2_ACC_BUFS;
 static_assert(kAccBufs == 1 || kAccBufs == 2, "one or two accumulator buffers");
+// TMEM columns to allocate: a power of two that holds the accumulator buffers.
+__host__ __device__ constexpr uint32_t tmem_cols_for(int cols) { return cols <= 256 ? 256u : 512u; }
 
 struct Tile2Shared {
     uint64_t full[kTile2MaxStages];   // leader only: all 64 KB of a stage (both CTAs) landed
@@ -67,22 +77,24 @@ struct Tile2Shared {
     int32_t consumed;  // leader: chunks whose arrival the MMA thread saw
 };
 
-__device__ __forceinline__ void tile2_coords(int u, int mp_tiles, int n_tiles, int &m0, int &n0) {
+__device__ __forceinline__ void tile2_coords(int u, int mp_tiles, int n_tiles, int bn, int &m0, int &n0) {
     const int per_group = kGroup2N * mp_tiles;
     const int g = u / per_group, r = u - g * per_group;
     const int gn = (n_tiles - g * kGroup2N) < kGroup2N ? (n_tiles - g * kGroup2N) : kGroup2N;
     const int mi = r / gn, ni = g * kGroup2N + (r - mi * gn);
     m0 = mi * kPairBM;
-    n0 = ni * kPairBN;
+    n0 = ni * bn;
 }
 
 }  // namespace
 
-template <typename OutT>
+template <typename OutT, int BN>
 __global__ void __launch_bounds__(kTileThreads, 1)
     tile2_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                  const uint16_t *__restrict__ bias, OutT *__restrict__ out, int M, int N, int K, int stages,
                  int32_t *status) {
+    using P = Pair<BN>;
+    constexpr int kStage2Bytes = P::kStageBytes, kAcc2Cols = P::kAccCols, kPairBN = BN;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -95,7 +107,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     const int units = mp_tiles * n_tiles;
     const int cl = (int)blockIdx.x >> 1, ncl = (int)gridDim.x >> 1;
     const int C = (K + kChunkK - 1) / kChunkK;
-    constexpr uint32_t kCols = kAccBufs * kAcc2Cols;
+    constexpr uint32_t kCols = tmem_cols_for(kAccBufs * kAcc2Cols);
 
     if (tid == 0) {
         tma_prefetch_desc(&tm_x);
@@ -147,8 +159,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
             int it = 0;
             for (int u = cl; u < units; u += ncl) {
                 int m0, n0;
-                tile2_coords(u, mp_tiles, n_tiles, m0, n0);
-                const int am = m0 + (int)rank * kHalf, bn = n0 + (int)rank * kHalf;
+                tile2_coords(u, mp_tiles, n_tiles, BN, m0, n0);
+                const int am = m0 + (int)rank * kHalf, bn = n0 + (int)rank * (BN / 2);
                 for (int c = 0; c < C; ++c, ++it) {
                     const int s = it % stages;
                     if (it >= stages && !mbar_wait(&sh.empty[s], ((it / stages) - 1) & 1, status, kSiteEmpty)) {
@@ -204,7 +216,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                     const uint64_t bdesc = smem_desc_sw128(smem_u32(st + kHalfBytes));
 #pragma unroll
                     for (int kk = 0; kk < kChunkK / 16; ++kk)
-                        mma_bf16_pair(acc, adesc + 2 * kk, bdesc + 2 * kk, kIdesc2, (c > 0 || kk > 0) ? 1u : 0u);
+                        mma_bf16_pair(acc, adesc + 2 * kk, bdesc + 2 * kk, P::kIdesc, (c > 0 || kk > 0) ? 1u : 0u);
                     mma_commit_pair(&sh.empty[s], (uint16_t)0x3);
                 }
                 if (!ok) {  // release both epilogues at once
@@ -226,7 +238,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         const uint32_t acc_empty0 = mapa_shared(smem_u32(&sh.acc_empty[0]), 0);
         for (int u = cl; u < units; u += ncl, ++tile_iter) {
             int m0, n0;
-            tile2_coords(u, mp_tiles, n_tiles, m0, n0);
+            tile2_coords(u, mp_tiles, n_tiles, BN, m0, n0);
             const int b = tile_iter % kAccBufs;
             const bool ok = mbar_wait(&sh.acc_full[b], (tile_iter / kAccBufs) & 1, status, kSiteAccum);
             tc_fence_after();
@@ -297,8 +309,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
 
 // At least 116 KB, so that no two CTAs share an SM: each holds all 512 TMEM
 // columns, and two pairs waiting on each other's SMs for TMEM must not happen.
-int tile2_smem_bytes(int stages) {
-    const int need = 1024 + stages * kStage2Bytes + 256;
+int tile2_smem_bytes(int stages, int bn) {
+    const int need = 1024 + stages * (bn == 192 ? Pair<192>::kStageBytes : Pair<256>::kStageBytes) + 256;
     return need > 116 * 1024 ? need : 116 * 1024;
 }
 
@@ -309,8 +321,12 @@ int g_pair_clusters[kMaxDev2];  // co-resident clusters of 2 at the largest ring
 
 template <typename OutT>
 int set_tile2_attrs() {
-    return (int)cudaFuncSetAttribute(tile2_kernel<OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     tile2_smem_bytes(kTile2MaxStages));
+    int e = (int)cudaFuncSetAttribute(tile2_kernel<OutT, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      tile2_smem_bytes(kTile2MaxStages, 256));
+    if (!e)
+        e = (int)cudaFuncSetAttribute(tile2_kernel<OutT, 192>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      tile2_smem_bytes(kTile2MaxStages, 192));
+    return e;
 }
 
 }  // namespace
@@ -325,7 +341,7 @@ int init_tile2() {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * kGb300Sms);
     cfg.blockDim = dim3(kTileThreads);
-    cfg.dynamicSmemBytes = (size_t)tile2_smem_bytes(kTile2MaxStages);
+    cfg.dynamicSmemBytes = (size_t)tile2_smem_bytes(kTile2MaxStages, 256);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -335,7 +351,7 @@ int init_tile2() {
     cfg.numAttrs = 1;
     int n = 0;
     // A failed query only loses the clamp (launches then use the plan's grid).
-    if (cudaOccupancyMaxActiveClusters(&n, tile2_kernel<uint16_t>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, tile2_kernel<uint16_t, 256>, &cfg) != cudaSuccess) {
         n = 0;
         (void)cudaGetLastError();
     }
@@ -343,13 +359,13 @@ int init_tile2() {
     return 0;
 }
 
-template <typename OutT>
+template <typename OutT, int BN>
 static int launch_tile2_t(const LaunchArgs &a, const bf16l_plan &p) {
     CUtensorMap tx, tw;
     int r = make_tmap_bf16_2d(&tx, a.x, (uint64_t)a.M, (uint64_t)a.K, kHalf, kChunkK, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (r) return (int)cudaErrorInvalidValue;
-    r = make_tmap_bf16_2d(&tw, a.W, (uint64_t)a.N, (uint64_t)a.K, kHalf, kChunkK, CU_TENSOR_MAP_SWIZZLE_128B,
+    r = make_tmap_bf16_2d(&tw, a.W, (uint64_t)a.N, (uint64_t)a.K, BN / 2, kChunkK, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (r) return (int)cudaErrorInvalidValue;
     int dev = 0;
@@ -362,7 +378,7 @@ static int launch_tile2_t(const LaunchArgs &a, const bf16l_plan &p) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * clusters));
     cfg.blockDim = dim3(kTileThreads);
-    cfg.dynamicSmemBytes = (size_t)tile2_smem_bytes(p.stages);
+    cfg.dynamicSmemBytes = (size_t)tile2_smem_bytes(p.stages, BN);
     cfg.stream = (cudaStream_t)a.stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -373,12 +389,13 @@ static int launch_tile2_t(const LaunchArgs &a, const bf16l_plan &p) {
     attr[1].val.programmaticStreamSerializationAllowed = (p.flags & BF16L_FLAG_PDL) ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return (int)cudaLaunchKernelEx(&cfg, tile2_kernel<OutT>, tx, tw, static_cast<const uint16_t *>(a.bias),
+    return (int)cudaLaunchKernelEx(&cfg, tile2_kernel<OutT, BN>, tx, tw, static_cast<const uint16_t *>(a.bias),
                                    static_cast<OutT *>(a.out), a.M, a.N, a.K, p.stages, a.status);
 }
 
 int launch_tile2(const LaunchArgs &a, const bf16l_plan &p) {
-    return a.out_f32 ? launch_tile2_t<float>(a, p) : launch_tile2_t<uint16_t>(a, p);
+    if (p.rows_per_cta == 192) return a.out_f32 ? launch_tile2_t<float, 192>(a, p) : launch_tile2_t<uint16_t, 192>(a, p);
+    return a.out_f32 ? launch_tile2_t<float, 256>(a, p) : launch_tile2_t<uint16_t, 256>(a, p);
 }
 
 }  // namespace bf16l

@@ -204,7 +204,10 @@ def test_pair_tile_plans_on_cpu(lib):
     assert lib.plan_check(2048, 7168, 7168, p).grid == 152
     assert lib.plan_check(256, 256, 64, p).grid == 2
     assert lib.plan_check(300, 300, 64, p).grid == 2 * 2 * 2
-    for bad in (dict(stages=7), dict(stages=1), dict(rows_per_cta=128), dict(tokens_per_cta=128), dict(threads=128)):
+    p192 = lib.make_plan("tile2", threads=192, rows_per_cta=192, tokens_per_cta=256, stages=6)
+    assert lib.plan_check(256, 14336, 4096, p192).grid == 150  # 75 pair tiles of 256 x 192
+    for bad in (dict(stages=7), dict(stages=1), dict(rows_per_cta=128), dict(rows_per_cta=224), dict(tokens_per_cta=128),
+                dict(threads=128)):
         q = lib.make_plan("tile2", **dict(dict(threads=192, rows_per_cta=256, tokens_per_cta=256, stages=4), **bad))
         with pytest.raises(lib.BF16LinearError):
             lib.plan_check(2048, 7168, 7168, q)

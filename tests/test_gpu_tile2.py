@@ -20,8 +20,8 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
-def _plan(lib, stages=4):
-    return lib.make_plan("tile2", threads=192, rows_per_cta=256, tokens_per_cta=256, stages=stages)
+def _plan(lib, stages=4, bn=256):
+    return lib.make_plan("tile2", threads=192, rows_per_cta=bn, tokens_per_cta=256, stages=stages)
 
 
 def _run(lib, x, W, b, plan, f32=False):
@@ -73,11 +73,22 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("bn", [256, 192])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c)))
-def test_tile2_forced(lib, case):
+def test_tile2_forced(lib, case, bn):
     M, N, K, st = case
     for bias in (False, True):
-        _check(lib, M, N, K, seed=M + N + K, bias=bias, plan=_plan(lib, st))
+        _check(lib, M, N, K, seed=M + N + K, bias=bias, plan=_plan(lib, st, bn))
+
+
+def test_tile2_192_mlp_shape(lib):
+    # the bandwidth-bound M = 256 MLP weight: 75 pair tiles of 256 x 192 (the last one 128 rows past N)
+    _check(lib, 256, 14336, 4096, seed=13, bias=True, plan=_plan(lib, 6, 192), sampled=True)
+    x, W, b = wl.make_inputs(200, 400, 1024, 14, True)
+    a = tensor_bits(_run(lib, x, W, b, _plan(lib, 4, 192)))
+    check_close(a, oracle.linear_bf16(wl.bits(x), wl.bits(W), wl.bits(b)), "tile2 192 ragged")
+    f = _run(lib, x, W, b, _plan(lib, 4, 192), f32=True)
+    assert np.array_equal(tensor_bits(f.to(torch.bfloat16)), a)
 
 
 def test_tile2_persistent_many_tiles(lib):
