@@ -87,6 +87,20 @@ def test_warpmma_groups_per_warp(lib, shape, cfg, ng):
         _check(lib, M, N, K, seed=M + N + K + 2, bias=bias, plan=p)
 
 
+def test_warpmma_groups_per_warp_f32_and_pdl(lib):
+    # the fp32 epilogue rounds to the bf16 result of the same plan; the launch flag changes nothing
+    M, N, K = 14, 1000, 3000
+    x, W, b = wl.make_inputs(M, N, K, 6, True)
+    for ng in (2, 4):
+        p = _plan(lib, 256, 8, 2, 1)
+        p.tokens_per_cta = ng
+        a = tensor_bits(_run(lib, x, W, b, p))
+        f = _run(lib, x, W, b, p, f32=True)
+        assert np.array_equal(tensor_bits(f.to(torch.bfloat16)), a)
+        p.flags = lib.FLAG_PDL
+        assert np.array_equal(tensor_bits(_run(lib, x, W, b, p)), a)
+
+
 def test_warpmma_x_paths_agree(lib):
     # the same fragments reach the same MMAs in the same order from shared memory or from L2, one
     # or two 8-row groups per warp: the same bits
