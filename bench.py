@@ -836,11 +836,11 @@ def main():
         if world > 1 and rank != 0:
             return
         smp = OracleSample(points, budget_s=args.cpu_budget / max(1, args.steps))
-        smp.run(1)  # one untimed warm-up pass
+        smp.run(args.warmup)  # untimed warm-up passes (at least three)
         wall = smp.run(args.steps)
         value = smp.value(wall, args.steps, large)
         line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": 1, "ms_per_step": 1000.0 * wall / args.steps,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * wall / args.steps,
                 "higher_is_better": large, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "config": config,
                 "cpu_baseline": {"value": value, "unit": unit, "cores": smp.threads, "kind": "oracle",
