@@ -191,8 +191,9 @@ int bf16_linear_ex(const void *x, const void *W, const void *bias, void *out,
  * x: host bf16 [M][K]; W: host bf16 [N][K]; bias: host bf16 [N] or NULL;
  * out: host bf16 [M][N], written in full once the stream reaches the copy.
  * Page-locked host memory gives asynchronous copies; pageable memory works
- * but the driver then stages each copy synchronously.  staging: device memory
- * of at least bf16_linear_host_staging_bytes(M, N, K, bias != NULL) bytes,
+ * but the driver then stages each copy synchronously.  staging: memory of the
+ * current device (the one `stream` belongs to) of at least
+ * bf16_linear_host_staging_bytes(M, N, K, bias != NULL) bytes,
  * 256-byte aligned, owned by the caller; the library lays out x, W, bias and
  * out in it at 256-byte aligned offsets and allocates nothing.  The host
  * buffers and the staging must stay valid, and unread/unwritten by the caller,
