@@ -12,7 +12,7 @@
  *
  * Conventions shared by every entry point:
  *  - All tensor pointers are DEVICE pointers owned by the caller, on the
- *    current CUDA device.  The library keeps no reference after the call
+ *    current CUDA device (bf16_linear_host alone takes host buffers).  The library keeps no reference after the call
  *    returns (the launch is asynchronous: buffers must stay valid until the
  *    stream reaches it).
  *  - Layouts are dense row-major with no padding: x[M][K], W[N][K] (the
