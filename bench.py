@@ -31,6 +31,7 @@ import hashlib
 import itertools
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -192,6 +193,26 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU oracle (reference arm and cpu_baseline)
 # ---------------------------------------------------------------------------
+
+def cpu_model():
+    """The host CPU's model name (/proc/cpuinfo, else lscpu), for the baseline's record."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine()
+
 
 class OracleSample:
     """A bounded sample of the workload for the CPU oracle, run on host threads.
@@ -843,7 +864,7 @@ def main():
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * wall / args.steps,
                 "higher_is_better": large, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "config": config,
-                "cpu_baseline": {"value": value, "unit": unit, "cores": smp.threads, "kind": "oracle",
+                "cpu_baseline": {"value": value, "unit": unit, "cores": smp.threads, "cpu_model": cpu_model(), "kind": "oracle",
                                  "sample": smp.desc},
                 "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
@@ -904,7 +925,7 @@ def main():
     if rank == 0 and not args.no_cpu_baseline:
         smp = OracleSample(points, budget_s=args.cpu_budget)
         wall = smp.run(1)
-        cpu = {"value": smp.value(wall, 1, large), "unit": unit, "cores": smp.threads, "kind": "oracle",
+        cpu = {"value": smp.value(wall, 1, large), "unit": unit, "cores": smp.threads, "cpu_model": cpu_model(), "kind": "oracle",
                "sample": smp.desc}
 
     e2e = r["e2e"]
