@@ -507,6 +507,32 @@ __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
 // ---------------------------------------------------------------------------
 // Global loads.
 // ---------------------------------------------------------------------------
+// Warp-level tensor-core MMAs (mma.sync) used by the kernels that feed their
+// operands straight from 16-byte loads.
+// D (16x8 fp32) += A (16x16 bf16, row-major) * B (16x8 bf16, column-major).
+// Lane (g = lane / 4, t = lane % 4): A {a0: row g, k 2t..2t+1; a1: row g+8, k 2t..;
+// a2: row g, k 2t+8..; a3: row g+8, k 2t+8..}; B {b0: k 2t..2t+1, col g;
+// b1: k 2t+8.., col g}; D {(g, 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1)}.
+__device__ __forceinline__ void mma_m16n8k16_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                                  uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// The e4m3 form: 4 codes per register, 32 k positions per instruction, the
+// fragments in the same registers as above.
+__device__ __forceinline__ void mma_m16n8k32_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                                  uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------------------
 // 16-byte streaming load that bypasses L1 allocation (weights: read once).
 __device__ __forceinline__ uint4 ldg_stream_v4(const void *p) {
     uint4 v;

@@ -39,26 +39,6 @@ namespace {
 
 constexpr int kDmWarps = 8;  // at most 256 threads
 
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// The e4m3 form: each 32-bit register holds 4 codes, so one instruction takes
-// 32 k positions (m16n8k32); the fragments sit in the same registers as above.
-__device__ __forceinline__ void mma16832_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                              uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
-        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 // K blocks (of 4 16-byte vectors = 32 elements) of CTA rank r out of S.
 __host__ __device__ inline int dm_blk(int nblk, int r, int S) { return (int)(((long long)nblk * r) / S); }
 
@@ -194,11 +174,11 @@ __global__ void __launch_bounds__(kDmWarps * 32)
                     }
                 }
                 if constexpr (F8) {
-                    mma16832_e4m3(c[0], lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
-                    mma16832_e4m3(c[1], lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
+                    mma_m16n8k32_e4m3(c[0], lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
+                    mma_m16n8k32_e4m3(c[1], lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
                 } else {
-                    mma16816(c[0], lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
-                    mma16816(c[1], lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
+                    mma_m16n8k16_bf16(c[0], lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
+                    mma_m16n8k16_bf16(c[1], lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
                 }
             }
         }

@@ -37,29 +37,6 @@ namespace {
 
 constexpr int kWmMaxWarps = 32;
 
-// D (16x8 fp32) += A (16x16 bf16, row-major) * B (16x8 bf16, column-major).
-// Fragments: lane (g, t): A {a0: row g, k 2t..2t+1; a1: row g+8, k 2t..; a2: row g,
-// k 2t+8..; a3: row g+8, k 2t+8..}; B {b0: k 2t..2t+1, col g; b1: k 2t+8.., col g};
-// D {d0: row g, col 2t; d1: row g, col 2t+1; d2, d3: row g+8}.
-__device__ __forceinline__ void mma_m16n8k16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                             uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// e4m3 form: 4 codes per register, 32 k positions per instruction.
-__device__ __forceinline__ void mma_m16n8k32_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                                  uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
-        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 }  // namespace
 
 int warpmma_smem_bytes(int M, int K) { return M * K * 2; }
@@ -183,8 +160,8 @@ __global__ void __launch_bounds__(NT, XR ? 1 : 1024 / NT)
                         mma_m16n8k32_e4m3(c[j][0], lo.x, hi.x, lo.y, hi.y, wv[u][j].x, wv[u][j].y);
                         mma_m16n8k32_e4m3(c[j][1], lo.z, hi.z, lo.w, hi.w, wv[u][j].z, wv[u][j].w);
                     } else {
-                        mma_m16n8k16(c[j][0], lo.x, hi.x, lo.y, hi.y, wv[u][j].x, wv[u][j].y);
-                        mma_m16n8k16(c[j][1], lo.z, hi.z, lo.w, hi.w, wv[u][j].z, wv[u][j].w);
+                        mma_m16n8k16_bf16(c[j][0], lo.x, hi.x, lo.y, hi.y, wv[u][j].x, wv[u][j].y);
+                        mma_m16n8k16_bf16(c[j][1], lo.z, hi.z, lo.w, hi.w, wv[u][j].z, wv[u][j].w);
                     }
                 }
             }

@@ -41,19 +41,6 @@ namespace bf16l {
 
 namespace {
 
-// D (16x8 fp32) += A (16x16 bf16, row-major) * B (16x8 bf16, column-major).
-// Lane (g, t): A {row g, k 2t..2t+1; row g+8, k 2t..; row g, k 2t+8..; row g+8,
-// k 2t+8..}; B {k 2t..2t+1, col g; k 2t+8.., col g}; D {(g, 2t), (g, 2t+1),
-// (g+8, 2t), (g+8, 2t+1)}.
-__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                          uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 // Row stride of the staged x slice in 16-byte vectors: 4 (mod 8), so that the
 // two token rows a quarter-warp reads land in different halves of the banks.
 __host__ __device__ inline int ks_stride(int sv) { return sv + (12 - sv % 8) % 8; }
@@ -166,8 +153,8 @@ __global__ void __launch_bounds__(NT, TT == 1 ? 1024 / NT : 1)
                         const uint4 lo = (in && 16 * j + g < M) ? xlo[j * tstep + vv] : make_uint4(0u, 0u, 0u, 0u);
                         const uint4 hi = (in && 16 * j + g + 8 < M) ? xhi[j * tstep + vv] : make_uint4(0u, 0u, 0u, 0u);
                         // this lane's 16 block bytes: step 0 takes the first 8, step 1 the last 8
-                        mma_16816(d[j], lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
-                        mma_16816(d[j], lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
+                        mma_m16n8k16_bf16(d[j], lo.x, hi.x, lo.y, hi.y, wv[u].x, wv[u].y);
+                        mma_m16n8k16_bf16(d[j], lo.z, hi.z, lo.w, hi.w, wv[u].z, wv[u].w);
                     }
                 }
             }
