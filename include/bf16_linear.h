@@ -139,20 +139,30 @@ typedef struct {
 } bf16l_device;
 
 /*
- * bf16_linear_plan — choose the kernel and parameters for (M, N, K) on `dev`.
+ * bf16_linear_plan — choose the kernel and parameters for (M, N, K) on a GB300
+ * (cc 10.3, 152 SMs).
  *
- * Pure host code: makes no CUDA call and touches no device.  dev == NULL means
- * a GB300 (cc 10.3, 152 SMs).  Rules (vLLM PR #48774 page, LLBf16Gemm.dispatch
- * and _arch_tuned_configs, with the thresholds re-measured on GB300): a table
- * measured on GB300 keyed by (K, N) with one entry per M decides; shapes not in
- * the table use size rules (dot product for tiny M or K % 8 != 0, cluster
- * split-K for skinny M, the tile kernel for large M).
+ * Pure host code: makes no CUDA call and touches no device.  Rules (vLLM PR
+ * #48774 page, LLBf16Gemm.dispatch and _arch_tuned_configs, with the
+ * thresholds re-measured on GB300): a table measured on GB300 keyed by (K, N)
+ * with one entry per M decides; shapes not in the table use size rules (dot
+ * product for tiny M or K % 8 != 0, cluster split-K for skinny M, the tile
+ * kernel for large M).
  *
- * Returns BF16L_OK and fills *plan; BF16L_EINVAL for M < 0, N <= 0, K <= 0 or
- * plan == NULL; BF16L_EARCH when dev is not compute capability 10.3.  M == 0
- * yields a plan with grid == 0 (nothing to launch).
+ * Returns BF16L_OK and fills *out_plan; BF16L_EINVAL for M < 0, N <= 0, K <= 0
+ * or out_plan == NULL.  M == 0 yields a plan with grid == 0 (nothing to launch).
  */
-int bf16_linear_plan(int M, int N, int K, const bf16l_device *dev, bf16l_plan *plan);
+int bf16_linear_plan(int M, int N, int K, bf16l_plan *out_plan);
+
+/*
+ * bf16_linear_plan_for_device — bf16_linear_plan for the device `dev`
+ * describes (NULL = a GB300).  The device is data, not a query, so tests can
+ * plan for fake devices (the mock-device pattern of the sglang PR #34042
+ * page's backend tests).  Same returns as bf16_linear_plan, plus BF16L_EARCH
+ * when dev is not compute capability 10.3 and BF16L_EINVAL for
+ * dev->num_sms <= 0.
+ */
+int bf16_linear_plan_for_device(int M, int N, int K, const bf16l_device *dev, bf16l_plan *plan);
 
 /*
  * bf16_linear_plan_check — validate an explicit plan for (M, N, K) on `dev`
@@ -300,7 +310,7 @@ size_t bf16_linear_workspace_size(int M, int N, int K, const bf16l_plan *plan);
 
 /*
  * The dispatcher's choice when `workspace_bytes` of workspace are available
- * (bf16_linear_plan is this with workspace_bytes == 0).  Pure host code.
+ * (bf16_linear_plan_for_device is this with workspace_bytes == 0).  Pure host code.
  */
 int bf16_linear_plan_ws(int M, int N, int K, const bf16l_device *dev, size_t workspace_bytes, bf16l_plan *plan);
 
@@ -319,8 +329,12 @@ int bf16_linear_plan_ws(int M, int N, int K, const bf16l_device *dev, size_t wor
  * its scratch fits, and a shape that does not fit even unsplit (about
  * M * N * 4 bytes > 4 MiB) returns BF16L_ENOSCRATCH.
  *
- * The first call on a device looks up the array's device address once (with
- * that device current); make that first call before any stream capture.
+ * The first call on a device looks up the array's device address (with that
+ * device current) and keeps it; make that first call before any stream
+ * capture.  A lookup that fails returns BF16L_ELAUNCH (the CUDA code through
+ * bf16_linear_cuda_error) and is tried again on the next call.  As every
+ * entry point, it returns BF16L_EARCH on a device that is not a GB300,
+ * before touching the device.
  * Each call clears the array's counters on `stream` before its launch.  All
  * calls share the one array, so calls that can overlap on the GPU (different
  * streams, or PDL) race and give wrong results; issue them on one stream.
@@ -378,6 +392,23 @@ int bf16_linear_fp8_with_plan(const void *xq, const void *wq, const float *scale
                               const void *bias, void *out, int M, int N, int K, const bf16l_plan *plan,
                               bf16l_stream_t stream);
 int bf16_linear_fp8_split(int M, int N, int K, int num_sms);
+
+/*
+ * bf16_linear_probe_read — a measurement probe, not part of the linear layer
+ * (no counterpart on the pages).  Launches `grid` CTAs of `threads` threads
+ * that read the `bytes` bytes at `src` once, with the 16-byte loads the
+ * weight-streaming kernels use, and XOR every 32-bit word they read into
+ * *sink (a device uint32 the caller zeroes first, if it wants the checksum).
+ * Nothing else is computed, so its time for a W-sized buffer is the floor of
+ * any kernel that must read that weight, launched the same way; with
+ * bytes == 0 it is an empty launch (src and sink may then be NULL), whose
+ * time in a graph of back-to-back launches is the per-call launch cost.
+ * bytes % 16 == 0, src 16-byte aligned, sink 4-byte aligned, 1 <= grid,
+ * threads a multiple of 32 in 32..1024.  Asynchronous; returns BF16L_OK,
+ * BF16L_EINVAL, BF16L_EALIGN, BF16L_EARCH or BF16L_ELAUNCH.
+ */
+int bf16_linear_probe_read(const void *src, size_t bytes, int grid, int threads, uint32_t *sink,
+                           bf16l_stream_t stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *bf16_linear_strerror(int status);

@@ -91,8 +91,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.bf16_linear_f32out_with_plan.restype = i32
         lib.bf16_linear_with_plan.argtypes = [vp, vp, vp, vp, i32, i32, i32, ctypes.POINTER(Plan), vp]
         lib.bf16_linear_with_plan.restype = i32
-        lib.bf16_linear_plan.argtypes = [i32, i32, i32, ctypes.POINTER(Device), ctypes.POINTER(Plan)]
+        lib.bf16_linear_plan.argtypes = [i32, i32, i32, ctypes.POINTER(Plan)]
         lib.bf16_linear_plan.restype = i32
+        lib.bf16_linear_plan_for_device.argtypes = [i32, i32, i32, ctypes.POINTER(Device), ctypes.POINTER(Plan)]
+        lib.bf16_linear_plan_for_device.restype = i32
         lib.bf16_linear_plan_check.argtypes = [i32, i32, i32, ctypes.POINTER(Device), ctypes.POINTER(Plan)]
         lib.bf16_linear_plan_check.restype = i32
         lib.bf16_linear_run.argtypes = [ctypes.POINTER(Call)]
@@ -112,6 +114,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.bf16_linear_fp8_with_plan.restype = i32
         lib.bf16_linear_fp8_split.argtypes = [i32, i32, i32, i32]
         lib.bf16_linear_fp8_split.restype = i32
+        lib.bf16_linear_probe_read.argtypes = [vp, ctypes.c_size_t, i32, i32, vp, vp]
+        lib.bf16_linear_probe_read.restype = i32
         lib.bf16_linear_noalloc_scratch_bytes.argtypes = []
         lib.bf16_linear_noalloc_scratch_bytes.restype = ctypes.c_size_t
         lib.bf16_linear_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32), i32]
@@ -143,9 +147,11 @@ def _raise(status: int, what: str):
 def plan(M: int, N: int, K: int, device: tuple[int, int, int] | None = None) -> Plan:
     """The kernel and parameters chosen for (M, N, K); device = (cc_major, cc_minor, num_sms)."""
     p = Plan()
-    dev = Device(*device) if device is not None else None
-    st = load().bf16_linear_plan(int(M), int(N), int(K), ctypes.byref(dev) if dev is not None else None,
-                                 ctypes.byref(p))
+    if device is None:
+        st = load().bf16_linear_plan(int(M), int(N), int(K), ctypes.byref(p))
+    else:
+        st = load().bf16_linear_plan_for_device(int(M), int(N), int(K), ctypes.byref(Device(*device)),
+                                                ctypes.byref(p))
     if st != OK:
         _raise(st, f"bf16_linear_plan({M},{N},{K})")
     return p
@@ -427,6 +433,19 @@ def bf16_linear_fp8(xq, wq, scale_x, scale_w, bias=None, out=None, flags: int = 
 def fp8_split(M: int, N: int, K: int, num_sms: int = 152) -> int:
     """The K split bf16_linear_fp8 uses for a shape (host logic, no GPU)."""
     return int(load().bf16_linear_fp8_split(M, N, K, num_sms))
+
+
+def probe_read(src, grid: int, threads: int, sink, nbytes: int | None = None, stream=None):
+    """Launch the read-floor probe (bf16_linear_probe_read) over the bytes of the CUDA tensor `src`
+    (the first nbytes of them, or none when src is None); the checksum is XORed into the one-element
+    int32 CUDA tensor `sink`."""
+    import torch
+    nb = 0 if src is None else (src.numel() * src.element_size() if nbytes is None else int(nbytes))
+    dev = sink.device if sink is not None else torch.device("cuda", torch.cuda.current_device())
+    st = load().bf16_linear_probe_read(_ptr(src), nb, int(grid), int(threads), _ptr(sink),
+                                       _stream_handle(stream, dev))
+    if st != OK:
+        _raise(st, f"bf16_linear_probe_read(bytes={nb}, grid={grid}, threads={threads})")
 
 
 def device_status(clear: bool = False) -> int:

@@ -190,6 +190,15 @@ __global__ void selftest_wait_kernel(int32_t *status, uint64_t limit_ns) {
 
 }  // namespace
 
+int current_device_checked(bf16l_device *dev) {
+    DeviceState *ds = nullptr;
+    const int st = current_device(&ds);
+    if (st == BF16L_OK && dev) *dev = ds->dev;
+    return st;
+}
+
+int note_cuda_error(int cuda_err) { return note(cuda_err); }
+
 // cuTensorMapEncodeTiled, looked up once from the driver.
 static PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     std::call_once(g_encode_once, [] {

@@ -109,6 +109,13 @@ constexpr int kChunkK = 64;  // K elements per TMA box row (128 bytes, the swizz
 // GB300 default device description (cc 10.3, 152 SMs).
 constexpr int kGb300Sms = 152;
 
+// The current device, initialised once (kernel attributes) and checked to be
+// compute capability 10.3: BF16L_OK and *dev filled, else the status to return
+// (a failed CUDA call is recorded for bf16_linear_cuda_error).  Defined in api.cu.
+int current_device_checked(bf16l_device *dev);
+// Record a CUDA error code for bf16_linear_cuda_error (0 is ignored); returns it.
+int note_cuda_error(int cuda_err);
+
 // Validate a plan against a shape; BF16L_OK or the error to return.  Fills
 // plan->grid.  Pure host logic.
 int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *plan);

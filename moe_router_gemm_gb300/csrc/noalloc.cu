@@ -14,10 +14,9 @@
 // Every GPU that loads the library holds that memory until the process exits.
 // No call here allocates or frees anything.  The first call on a device looks
 // up the array's device address (cudaGetSymbolAddress, with that device
-// current) once; make that first call before any stream capture.
+// current) and keeps it; make that first call before any stream capture.
 #include <cuda_runtime.h>
 
-#include <functional>
 #include <mutex>
 
 #include "common.cuh"
@@ -27,7 +26,7 @@
 // partial tiles of one call (see bf16_linear_noalloc for the shapes that fit).
 // In host code this name is only a stand-in for the device symbol, never a
 // device address: the address comes from cudaGetSymbolAddress in
-// noalloc_setup().
+// noalloc_scratch().
 #define BF16L_NOALLOC_BYTES (4u << 20)
 static __device__ __align__(256) uint8_t g_noalloc_scratch[BF16L_NOALLOC_BYTES];
 
@@ -39,21 +38,29 @@ constexpr size_t kNoAllocBytes = BF16L_NOALLOC_BYTES;
 constexpr int kNoAllocMaxDevices = 64;
 
 struct NoAllocDevice {
-    std::once_flag once;
-    int err = 0;      // cudaError_t of the set-up
-    void *scratch = nullptr;
-    int num_sms = 0;
+    std::mutex mu;
+    void *scratch = nullptr;  // set once the lookup has succeeded; never cleared
 };
 NoAllocDevice g_noalloc_devices[kNoAllocMaxDevices];
 
-// Once per device, with that device current: the array's device address and
-// the SM count the plan is sized for.
-void noalloc_setup(NoAllocDevice &d, int device) {
-    void *p = nullptr;
-    int e = (int)cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (!e) e = (int)cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, device);
-    d.scratch = e ? nullptr : p;
-    d.err = e;
+// The array's device address on the current device, looked up on first use.
+// Only a successful lookup is kept: a failed one (for example, made during a
+// stream capture) is reported and retried on the next call.  Returns a
+// cudaError_t value.
+int noalloc_scratch(int device, void **out) {
+    NoAllocDevice &d = g_noalloc_devices[device];
+    std::lock_guard<std::mutex> lock(d.mu);
+    if (!d.scratch) {
+        void *p = nullptr;
+        const int e = (int)cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e) {
+            (void)cudaGetLastError();  // leave no sticky error behind for the caller's next check
+            return e;
+        }
+        d.scratch = p;
+    }
+    *out = d.scratch;
+    return 0;
 }
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -78,12 +85,24 @@ extern "C" int bf16_linear_noalloc(const void *x, const void *W, const void *bia
     if (align & 15u) return BF16L_EALIGN;
     if (M > kSplitMaxTokens || K % 8 != 0) return BF16L_EUNSUPPORTED;
 
+    // The device check of every entry point (compute capability 10.3, kernel
+    // attributes set) comes before anything else touches the device.
+    bf16l_device dev = {};
+    const int st = current_device_checked(&dev);
+    if (st != BF16L_OK) return st;
     int device = 0;
     int e = (int)cudaGetDevice(&device);
-    if (e || device < 0 || device >= kNoAllocMaxDevices) return BF16L_ELAUNCH;
-    NoAllocDevice &d = g_noalloc_devices[device];
-    std::call_once(d.once, noalloc_setup, std::ref(d), device);
-    if (d.err || !d.scratch) return BF16L_ELAUNCH;
+    if (e) {
+        note_cuda_error(e);
+        return BF16L_ELAUNCH;
+    }
+    if (device < 0 || device >= kNoAllocMaxDevices) return BF16L_ELAUNCH;
+    void *scratch = nullptr;
+    e = noalloc_scratch(device, &scratch);
+    if (e) {
+        note_cuda_error(e);
+        return BF16L_ELAUNCH;
+    }
 
     // Plan: tokens on the MMA M side, 64 weight rows per CTA (128 for large N),
     // about one CTA per SM, then as few K splits as needed to fit the array.
@@ -94,7 +113,7 @@ extern "C" int bf16_linear_noalloc(const void *x, const void *W, const void *bia
     p.tokens_per_cta = ((M + 7) / 8) * 8;
     const int tiles = ceil_div(N, p.rows_per_cta);
     const int chunks = ceil_div(K, kChunkK);
-    int split = d.num_sms / tiles;
+    int split = dev.num_sms / tiles;
     if (split < 1) split = 1;
     if (split > kSplitWsMaxSplit) split = kSplitWsMaxSplit;
     if (split > chunks) split = chunks;
@@ -109,8 +128,11 @@ extern "C" int bf16_linear_noalloc(const void *x, const void *W, const void *bia
 
     // The array keeps the last call's contents; the arrival counters must
     // start at zero, so clear them (stream-ordered, nothing allocated).
-    e = (int)cudaMemsetAsync(d.scratch, 0, split_ws_counter_bytes(tiles), (cudaStream_t)stream);
-    if (e) return BF16L_ELAUNCH;
+    e = (int)cudaMemsetAsync(scratch, 0, split_ws_counter_bytes(tiles), (cudaStream_t)stream);
+    if (e) {
+        note_cuda_error(e);
+        return BF16L_ELAUNCH;
+    }
 
     bf16l_call c = {};
     c.x = x;
@@ -121,7 +143,7 @@ extern "C" int bf16_linear_noalloc(const void *x, const void *W, const void *bia
     c.N = N;
     c.K = K;
     c.plan = &p;
-    c.workspace = d.scratch;
+    c.workspace = scratch;
     c.workspace_bytes = kNoAllocBytes;
     c.stream = stream;
     return bf16_linear_run(&c);

@@ -285,8 +285,12 @@ extern "C" int bf16_linear_plan_ws(int M, int N, int K, const bf16l_device *devp
     return BF16L_OK;
 }
 
-extern "C" int bf16_linear_plan(int M, int N, int K, const bf16l_device *devp, bf16l_plan *plan) {
+extern "C" int bf16_linear_plan_for_device(int M, int N, int K, const bf16l_device *devp, bf16l_plan *plan) {
     return bf16_linear_plan_ws(M, N, K, devp, 0, plan);
+}
+
+extern "C" int bf16_linear_plan(int M, int N, int K, bf16l_plan *out_plan) {
+    return bf16_linear_plan_ws(M, N, K, nullptr, 0, out_plan);
 }
 
 extern "C" size_t bf16_linear_workspace_size(int M, int N, int K, const bf16l_plan *plan) {
