@@ -299,13 +299,29 @@ class Shape:
         # the cluster-free split-K where that is faster.
         self.ws = lib.new_workspace(max(256, lib.workspace_size(M, N, K)), device)
         self.plan = plan_override or lib.plan_ws(M, N, K, self.ws.numel())
-        self.plan.flags = 1 if pdl else 0  # BF16L_FLAG_PDL
+        self.plan.flags = 1 if pdl else 0  # BF16L_FLAG_PDL, else the default launch mode
         self.kernel = lib.KERNEL_NAMES[self.plan.kernel]
         self.lib = lib
         self.graph = None
 
     def call(self, i):
         self.lib.run(self.x, self.Ws[i % self.R], self.b, self.out, plan_=self.plan, workspace=self.ws)
+
+    def time_graph(self, stream, replays, warm=False):
+        """Median in-graph microseconds per call over `replays` replays of one graph of R calls."""
+        with torch.cuda.stream(stream):
+            self.capture(stream, warm=warm)
+            self.graph.replay()  # warm-up replay (brings the weight into L2 for the warm form)
+            ms = []
+            for _ in range(replays):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                self.graph.replay()
+                b.record(stream)
+                ms.append((a, b))
+        torch.cuda.synchronize()
+        self.graph = None
+        return 1000.0 * statistics.median([a.elapsed_time(b) for a, b in ms]) / self.R
 
     def capture(self, stream, warm=False):
         """One graph of R back-to-back calls: on the R weight copies in turn (L2-cold),
@@ -372,16 +388,15 @@ def gpu_arm(args, points, rank, world):
         per_shape_us.append(1000.0 * statistics.median(ms) / s.R)
     launches = args.steps * sum(s.R for s in shapes)
 
-    # ---- the same shapes launched with programmatic dependent launch (BF16L_FLAG_PDL) ----
-    pdl_us = None
-    if not args.pdl and not args.no_pdl_variant:
+    # ---- the same shapes in the other launch modes: early weights (BF16L_FLAG_PDL) and serial ----
+    def variant_us(flags):
         for s_ in shapes:
-            s_.plan.flags = 1
+            s_.plan.flags = flags
         with torch.cuda.stream(stream):
             for s_ in shapes:
                 s_.capture(stream)
         torch.cuda.synchronize()
-        pdl_ms = [[] for _ in shapes]
+        ms = [[] for _ in shapes]
         with torch.cuda.stream(stream):
             for k in range(max(3, args.steps // 2)):
                 for j, s_ in enumerate(shapes):
@@ -389,12 +404,18 @@ def gpu_arm(args, points, rank, world):
                     a.record(stream)
                     s_.graph.replay()
                     b.record(stream)
-                    pdl_ms[j].append((a, b))
+                    ms[j].append((a, b))
         torch.cuda.synchronize()
-        pdl_us = [1000.0 * statistics.median([a.elapsed_time(b) for a, b in pdl_ms[j]]) / s_.R
-                  for j, s_ in enumerate(shapes)]
         for s_ in shapes:
-            s_.plan.flags = 0
+            s_.plan.flags = base_flags
+        return [1000.0 * statistics.median([a.elapsed_time(b) for a, b in ms[j]]) / s_.R
+                for j, s_ in enumerate(shapes)]
+
+    base_flags = 1 if args.pdl else 0
+    pdl_us = serial_us = None
+    if not args.pdl and not args.no_pdl_variant:
+        pdl_us = variant_us(1)     # BF16L_FLAG_PDL
+        serial_us = variant_us(2)  # BF16L_FLAG_SERIAL
 
     # ---- L2-warm: the same calls, every one on the same weight copy ----
     warm_us = None
@@ -422,8 +443,124 @@ def gpu_arm(args, points, rank, world):
     # ---- e2e: public API from pinned host buffers, copies inside the timed region ----
     e2e = e2e_arm(args, shapes, lib, device, stream)
 
+    # ---- the measured per-call floors and the other workloads of the metric (outside the timed region) ----
+    floor, records = None, None
+    if args.workload == "router" and not args.no_workloads and not args.only and not args.plan:
+        floor = floor_record(shapes, lib, device, stream, max(3, args.sub_replays))
+        for s_ in shapes:  # keep each shape's description, free its device buffers
+            s_.graph, s_.Ws, s_.x, s_.out, s_.ws, s_.b = None, [], None, None, None, None
+        torch.cuda.empty_cache()
+        peaks = load_peaks()
+        records = {}
+        for name in ("smallest", "decode", "mlp", "prefill"):
+            records[name] = workload_record(name, lib, device, stream, peaks, max(3, args.sub_replays))
+
     return dict(shapes=shapes, per_shape_us=per_shape_us, total_ms=total_ms, launches=launches,
-                clocks=clocks, e2e=e2e, pdl_us=pdl_us, warm_us=warm_us)
+                clocks=clocks, e2e=e2e, pdl_us=pdl_us, serial_us=serial_us, warm_us=warm_us, floor=floor,
+                records=records)
+
+
+def plan_str(p):
+    d = p.as_dict()
+    return (f"{d['kernel_name']}(threads={d['threads']},rows={d['rows_per_cta']},tokens={d['tokens_per_cta']},"
+            f"split={d['split_k']},stages={d['stages']},grid={d['grid']})")
+
+
+def workload_record(name, lib, device, stream, peaks, replays):
+    """One workload's shapes through the dispatcher: L2-cold and L2-warm us per call, and each shape's
+    fraction of its roofline (HBM for arithmetic intensity below the ridge point, else the bf16 tensor
+    peak), with the kernel that ran.  Shapes are timed one at a time and freed (prefill holds GBs)."""
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    rows, tot_flops, tot_us, hbm_fracs = [], 0.0, 0.0, []
+    for pt in workload_points(name):
+        s = Shape(pt, device, lib)
+        cold = s.time_graph(stream, replays)
+        warm = s.time_graph(stream, replays, warm=True)
+        nbytes, flops = algo_bytes(s.M, s.N, s.K, s.bias), algo_flops(s.M, s.N, s.K, s.bias)
+        r = {"M": s.M, "N": s.N, "K": s.K, "bias": s.bias, "kernel": s.kernel, "plan": plan_str(s.plan),
+             "us_cold": round(cold, 3), "us_warm": round(warm, 3), "weight_copies": s.R}
+        if flops / nbytes < ridge:
+            gbs = nbytes / (cold * 1e-6) / 1e9
+            r.update(bound="hbm", GBps=round(gbs, 1), frac=round(gbs / peaks["hbm_gbs"], 4),
+                     frac_warm=round(nbytes / (warm * 1e-6) / 1e9 / peaks["hbm_gbs"], 4))
+            hbm_fracs.append(r["frac"])
+        else:
+            tf = flops / (cold * 1e-6) / 1e12
+            r.update(bound="tensor", TFLOPs=round(tf, 1), frac=round(tf / peaks["bf16_tflops"], 4),
+                     frac_sustained=round(tf / peaks["bf16_tflops_sustained"], 4))
+            tot_flops += flops
+            tot_us += cold
+        rows.append(r)
+        del s
+        torch.cuda.empty_cache()
+    rec = {"workload": workload_desc(name), "unit": "us/call", "shapes": rows,
+           "mean_us_cold": round(statistics.mean(r["us_cold"] for r in rows), 3),
+           "mean_us_warm": round(statistics.mean(r["us_warm"] for r in rows), 3)}
+    if hbm_fracs:
+        rec["hbm_frac_min"], rec["hbm_frac_max"] = min(hbm_fracs), max(hbm_fracs)
+    if tot_us:
+        tf = tot_flops / (tot_us * 1e-6) / 1e12
+        rec["tensor_TFLOPs"] = round(tf, 1)
+        rec["tensor_frac"] = round(tf / peaks["bf16_tflops"], 4)
+        rec["tensor_frac_sustained"] = round(tf / peaks["bf16_tflops_sustained"], 4)
+    return rec
+
+
+FLOOR_CONFIGS = ((152, 1024), (304, 512), (608, 256), (1216, 128), (304, 1024), (608, 512), (1216, 256),
+                 (152, 512), (304, 256), (608, 128))
+
+
+def floor_record(shapes, lib, device, stream, replays):
+    """Per-call floors measured the way the router calls are: (1) an empty kernel launched back to back
+    in a graph (the launch cost alone), (2) for each router weight size, a pure 16-byte-load read of the
+    same rotated weight copies (L2-cold), the best over a few grid shapes.  No kernel that must read W
+    can beat (2); the router shapes' fraction of the HBM roofline is bounded by it."""
+    sink = torch.zeros(max(g for g, _ in FLOOR_CONFIGS), dtype=torch.int32, device=device)
+
+    def graph_us(calls, n):
+        with torch.cuda.stream(stream):
+            for c in calls[:2]:
+                c()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for c in calls:
+                    c()
+            g.replay()
+            ms = []
+            for _ in range(replays):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+                ms.append((a, b))
+        torch.cuda.synchronize()
+        return 1000.0 * statistics.median([a.elapsed_time(b) for a, b in ms]) / n
+
+    n_empty = 256
+    launch_us = graph_us([lambda: lib.probe_read(None, 152, 32, sink, stream=stream)] * n_empty, n_empty)
+    launch1_us = graph_us([lambda: lib.probe_read(None, 1, 32, sink, stream=stream)] * n_empty, n_empty)
+    read = {}
+    seen = set()
+    for s in shapes:
+        key = f"K{s.K}_N{s.N}"
+        if key in seen:
+            continue
+        seen.add(key)
+        best = None
+        for grid, threads in FLOOR_CONFIGS:
+            calls = [(lambda w=w, g_=grid, t=threads: lib.probe_read(w, g_, t, sink, stream=stream)) for w in s.Ws]
+            us = graph_us(calls, len(calls))
+            if best is None or us < best[0]:
+                best = (us, grid, threads)
+        nbytes = 2 * s.N * s.K
+        read[key] = {"us": round(best[0], 3), "weight_bytes": nbytes, "grid": best[1], "threads": best[2],
+                     "GBps": round(nbytes / (best[0] * 1e-6) / 1e9, 1)}
+    return {"note": "in-graph us per launch, L2-cold rotation as for the router calls: an empty kernel, and a "
+                    "read of each router weight with 16-byte loads and no arithmetic (best of the grid shapes "
+                    "tried); bf16_linear_probe_read",
+            "empty_launch_us": round(launch_us, 3), "empty_launch_1cta_us": round(launch1_us, 3),
+            "read_weight": read}
 
 
 def forced_plan(lib, spec):
@@ -611,10 +748,28 @@ def candidate_plans(lib, M, N, K):
         for st in (6, 5, 4):
             for bn in (256, 192):  # W rows per pair tile
                 cands.append(lib.make_plan("tile2", threads=192, rows_per_cta=bn, tokens_per_cta=256, stages=st))
-    if K % 8 == 0 and M > 32:
-        for st in (4, 3):
-            cands.append(lib.make_plan("tile", threads=192, rows_per_cta=256, tokens_per_cta=128, stages=st))
+    if K % 8 == 0 and M > 32:  # the plain tile: W-tile widths, ring depths, raster groups
+        for bn in (128, 192, 224, 240, 256):
+            most = tile_max_stages(bn)
+            for st in (most, most - 1):
+                for grp in (0, 1, 2, 4, 16):
+                    cands.append(lib.make_plan("tile", threads=192, rows_per_cta=bn, tokens_per_cta=128, stages=st,
+                                               split_k=grp))
+    if K % 8 == 0 and 16 < M <= 512:  # the swap-AB tile: W rows on the MMA M side, tokens on N
+        for bn in (32, 64, 128, 192, 256):
+            if bn > 2 * max(32, M) or 4 * bn < M:
+                continue
+            most = tile_max_stages(bn)
+            for st in (most, max(2, most - 2)):
+                for grp in (0, 1):
+                    cands.append(lib.make_plan("tile_t", threads=192, rows_per_cta=128, tokens_per_cta=bn,
+                                               stages=st, split_k=grp))
     return cands
+
+
+def tile_max_stages(bn):
+    """Ring stages of the tile kernels that fit 227 KB of shared memory (at most 8)."""
+    return min(8, (232448 - 1024 - 256) // (128 * 128 + bn * 128))
 
 
 def sweep(args, points):
@@ -625,7 +780,8 @@ def sweep(args, points):
     device = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.Stream(device)
     results = []
-    out_dir = os.path.join(ROOT, "gpurun_out") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ROOT
+    out_dir = args.out_dir
+    os.makedirs(out_dir, exist_ok=True)
     for pt in points:
         base = Shape(pt, device, lib)
         R = min(base.R, 64)  # 64 rotated copies keep every call L2-cold for these sizes
@@ -824,7 +980,13 @@ def main():
                     help="with --sweep: time only the candidates of these kernels (comma-separated names)")
     ap.add_argument("--sweep", action="store_true",
                     help="time every candidate plan of the workload's shapes and write dispatch_table.inc "
-                         "(to gpurun_out/ when that folder exists)")
+                         "and sweep_results.json into --out-dir")
+    ap.add_argument("--out-dir", default=".", help="with --sweep: where the sweep writes its files")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="router sweep only: skip the per-workload records (smallest, decode, MLP, prefill) "
+                         "and the measured floors")
+    ap.add_argument("--sub-replays", type=int, default=5,
+                    help="graph replays per shape for the per-workload records")
     ap.add_argument("--eager", action="store_true",
                     help="profiling mode: each step calls every shape once per rotation copy, no graphs, "
                          "no e2e/cpu legs; prints per-shape timings only")
@@ -846,11 +1008,17 @@ def main():
     peaks = load_peaks()
     large = args.workload == "prefill"
     metric = ("bf16 GEMM TFLOP/s (prefill, tile path)" if large else
-              "M<=16 bf16 GEMM us per call (L2-cold), mean over the router sweep")
+              "M\u226416 bf16 GEMM \u00b5s & % HBM roofline (L2-cold); large-M TFLOP/s % bf16 peak")
     unit = "TFLOP/s" if large else "us/call"
     config = {"workload": workload_desc(args.workload), "shapes": len(points),
+              "value": ("TFLOP/s over the prefill shapes" if large else
+                        "mean us per call over the workload's shapes, L2-cold (the router sweep by default; "
+                        "the other workloads of the metric, with their roofline fractions, under 'workloads')"),
               "l2": "cold: weights rotated over copies totalling >=256 MB per shape; x L2-hot",
               "timing": "CUDA graph of R back-to-back calls per shape, CUDA events on the launching stream",
+              "launch": ("early weights (BF16L_FLAG_PDL)" if args.pdl else
+                         "the library's default: programmatic dependent launch, every read after the "
+                         "grid-dependency wait"),
               "pdl": bool(args.pdl)}
 
     if args.impl == "reference":
@@ -938,6 +1106,13 @@ def main():
     for s, us in zip(shapes, per_us):
         key = f"K{s.K}_N{s.N}"
         per_shape.setdefault(key, []).append(round(us, 3))
+    if r["floor"] is not None:
+        rf = r["floor"]["read_weight"]
+        floors = [rf[f"K{s.K}_N{s.N}"]["us"] for s in shapes]
+        r["floor"]["router_mean_read_floor_us"] = round(statistics.mean(floors), 3)
+        r["floor"]["router_mean_frac_of_floor"] = round(statistics.mean(f / u for f, u in zip(floors, per_us)), 4)
+        r["floor"]["read_floor_frac_hbm"] = round(statistics.mean(
+            algo_bytes(s.M, s.N, s.K, s.bias) / (f * 1e-6) / 1e9 / peaks["hbm_gbs"] for s, f in zip(shapes, floors)), 4)
     line = {
         "metric": metric, "value": round(value, 4), "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": large,
@@ -954,6 +1129,13 @@ def main():
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
         "kernel_share": {k: round(v[0] / sum(x[0] for x in share.values()), 4) for k, v in share.items()},
+        "serial_variant": None if r["serial_us"] is None else {
+            "note": "same shapes and rotation, launched with BF16L_FLAG_SERIAL (no programmatic dependent "
+                    "launch: each call starts only after the previous one completed); timed after the main region",
+            "value": round(statistics.mean(r["serial_us"]), 4) if not large else None,
+            "unit": unit,
+            "per_shape_us": {k: [round(u, 3) for s_, u in zip(shapes, r["serial_us"]) if f"K{s_.K}_N{s_.N}" == k]
+                             for k in per_shape}},
         "pdl_variant": None if r["pdl_us"] is None else {
             "note": "same shapes and rotation, launched with BF16L_FLAG_PDL (weights fetched before the "
                     "grid-dependency wait, so back-to-back calls overlap); timed after the main region",
@@ -973,6 +1155,8 @@ def main():
             "pct_hbm_roofline_per_shape": None if large else {
                 k: [round(100.0 * algo_bytes(s.M, s.N, s.K, s.bias) / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 1)
                     for s, us in zip(shapes, r["warm_us"]) if f"K{s.K}_N{s.N}" == k] for k in per_shape}},
+        "floor": r["floor"],
+        "workloads": r["records"],
         "per_shape_us": per_shape,
         "pct_hbm_roofline_per_shape": None if large else {
             k: [round(100.0 * algo_bytes(s.M, s.N, s.K, s.bias) / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 1)

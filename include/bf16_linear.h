@@ -80,8 +80,10 @@ typedef enum {
                                   CTA staging its K slice of x, partial tiles summed over DSMEM in rank order */
     BF16L_KERNEL_DOTMMA = 8,   /* router-sized N, M <= 64 (16-token groups): 8 W rows per CTA, K over a cluster of 1..16 CTAs,
                                   16-byte loads feed m16n8k16 MMAs, partials summed by rank 0 over DSMEM */
-    BF16L_KERNEL_DOTMMA_WS = 9 /* the same without a cluster: K split over 2..64 CTAs whose partial tiles meet in
+    BF16L_KERNEL_DOTMMA_WS = 9, /* the same without a cluster: K split over 2..64 CTAs whose partial tiles meet in
                                   a caller-provided workspace (see bf16_linear_run); the last CTA reduces */
+    BF16L_KERNEL_TILE_T = 10   /* the tile kernel in the swap-AB orientation: 128 W rows on the MMA M side,
+                                  tokens_per_cta tokens (32, 64, 128, 192 or 256) on the N side; mid-size M */
 } bf16l_kernel;
 
 /*
@@ -93,23 +95,28 @@ typedef enum {
 typedef struct {
     int32_t kernel;        /* bf16l_kernel */
     int32_t threads;       /* threads per CTA */
-    int32_t rows_per_cta;  /* W rows per CTA (DOTPROD 1/2/4; SPLITK 16..256, the MMA N); TILE: W rows per tile;
+    int32_t rows_per_cta;  /* W rows per CTA (DOTPROD 1/2/4; SPLITK 16..256, the MMA N); TILE: W rows per tile
+                              (the MMA N: 128, 192, 224, 240 or 256); TILE_T: 128 (the MMA M);
                               TILE2: W rows per pair tile (256 or 192);
                               STREAM: W rows per ring stage (1, 2, or 4 when M <= 3);
                               WARPROW: warps that share one row (1, 2 or 4);
                               WARPMMA: warps that share one group of 8 rows (1, 2, 4, 8 or 16) */
-    int32_t tokens_per_cta;/* SPLITK: x rows loaded per chunk (M rounded up to 8, <= 64);  TILE: x rows per tile;
+    int32_t tokens_per_cta;/* SPLITK: x rows loaded per chunk (M rounded up to 8, <= 64);  TILE: x rows per tile
+                              (128); TILE_T: tokens per tile (the MMA N: 32, 64, 128, 192 or 256);
                               DOTPROD: tokens per CTA, 1..8 (0 = min(M, 8)); ceil(M / tokens) CTAs then share each
                               row slice, one token group each, instead of one CTA looping over the groups;
                               WARPMMA: 8-row groups a warp covers per x fragment, 1, 2 or 4 (2 and 4 only with
                               split_k = 1; 0 = 1); WARPMMA cluster form: 8-row groups per cluster (0 = as many clusters as fit) */
     int32_t split_k;       /* SPLITK: CTAs per cluster along K (1..16); SPLITK_WS: CTAs along K (1..64);
+                              TILE / TILE_T: raster group, the N-side tiles walked together before the next row
+                              of M-side tiles (0 = 8 for TILE, all of them for TILE_T);
                               DOTMMA: CTAs per cluster along K (1, 2, 4, 8 or 16);
                               DOTMMA_WS: CTAs along K (a power of two, 2..64);
                               WARPMMA: 1 = x fragments loaded from global memory into registers (512 threads per
                               SM at most), 0 = x staged in shared memory, S = 2..16: the cluster form (K over S
                               CTAs; 1024-thread blocks only for M <= 16, else at most 512 threads per SM) */
-    int32_t stages;        /* SPLITK / TILE: shared-memory ring depth (64-wide K chunks); DOTPROD: 1 = x read
+    int32_t stages;        /* SPLITK / TILE / TILE_T: shared-memory ring depth (64-wide K chunks; TILE and TILE_T:
+                              2 up to what fits 227 KB, at most 8); DOTPROD: 1 = x read
                               from global memory (L2) instead of staged in shared memory;
                               WARPROW / WARPMMA: CTAs per SM; DOTMMA: 1 = x fragments loaded from global
                               memory into registers, 0 = each CTA's x slice staged in shared memory */
@@ -118,14 +125,29 @@ typedef struct {
 } bf16l_plan;
 
 /*
- * Launch flag: programmatic dependent launch.  The kernel reads W (and
- * issues its TMA weight loads) before waiting for the preceding kernel in the
- * stream, and reads x / writes out only after that wait; it also lets the
- * following kernel start early.  Use only when W and bias are not written by
- * the kernel launched just before this call on the same stream (true for
- * weights).  Honoured by the split-K and dot-product kernels.
+ * Launch modes.  By default every kernel is launched with programmatic
+ * dependent launch (the mode the sglang PR #28333 page turns on wherever the
+ * GPU supports it): it may be scheduled while the kernel before it on the
+ * stream finishes, runs its set-up, and then waits for that kernel to complete
+ * (griddepcontrol.wait) before it reads x, W or bias or writes out.  This is
+ * always correct, whatever the previous kernel does; it hides the launch cost
+ * of back-to-back calls.  It also lets the next kernel on the stream be
+ * scheduled early; a kernel of another library that is launched with
+ * programmatic dependent launch after this one must wait before it reads out,
+ * as that launch mode requires.
+ *
+ * BF16L_FLAG_PDL: in addition, the kernel reads W and bias (and issues its
+ * weight copies) BEFORE that wait, overlapping the weight fetch with the end
+ * of the previous kernel.  Use only when W and bias are not written by the
+ * kernel launched just before this call on the same stream (true for
+ * weights).  x is still read, and out written, only after the wait.
+ *
+ * BF16L_FLAG_SERIAL: launch without programmatic dependent launch (the call
+ * starts only once everything before it on the stream has completed).
+ * BF16L_FLAG_PDL and BF16L_FLAG_SERIAL together are refused (BF16L_EINVAL).
  */
 #define BF16L_FLAG_PDL 1u
+#define BF16L_FLAG_SERIAL 2u
 
 /*
  * Describe the device a plan is made for.  bf16_linear() fills this from the
@@ -187,7 +209,8 @@ int bf16_linear(const void *x, const void *W, const void *bias, void *out,
 
 /*
  * bf16_linear_ex — as bf16_linear, with BF16L_FLAG_* launch flags (0 = the
- * same as bf16_linear).  Unknown flag bits return BF16L_EINVAL.
+ * same as bf16_linear).  Unknown flag bits, or BF16L_FLAG_PDL together with
+ * BF16L_FLAG_SERIAL, return BF16L_EINVAL.
  */
 int bf16_linear_ex(const void *x, const void *W, const void *bias, void *out,
                    int M, int N, int K, uint32_t flags, bf16l_stream_t stream);
@@ -397,8 +420,9 @@ int bf16_linear_fp8_split(int M, int N, int K, int num_sms);
  * bf16_linear_probe_read — a measurement probe, not part of the linear layer
  * (no counterpart on the pages).  Launches `grid` CTAs of `threads` threads
  * that read the `bytes` bytes at `src` once, with the 16-byte loads the
- * weight-streaming kernels use, and XOR every 32-bit word they read into
- * *sink (a device uint32 the caller zeroes first, if it wants the checksum).
+ * weight-streaming kernels use; CTA b XORs every 32-bit word it read into
+ * sink[b] (sink: device uint32[grid], zeroed by the caller if it wants the
+ * checksum, which is then the XOR of the grid words).
  * Nothing else is computed, so its time for a W-sized buffer is the floor of
  * any kernel that must read that weight, launched the same way; with
  * bytes == 0 it is an empty launch (src and sink may then be NULL), whose

@@ -17,13 +17,14 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libbf16_linear.so")
 
 OK, EINVAL, EALIGN, EARCH, ELAUNCH, ETIMEOUT, EUNSUPPORTED, ENOSCRATCH = 0, -1, -2, -3, -4, -5, -6, -7
-FLAG_PDL = 1
+FLAG_PDL = 1      # weights read before the grid-dependency wait
+FLAG_SERIAL = 2   # no programmatic dependent launch
 (KERNEL_DOTPROD, KERNEL_SPLITK, KERNEL_TILE, KERNEL_SPLITK_WS, KERNEL_STREAM, KERNEL_TILE2, KERNEL_WARPROW,
- KERNEL_WARPMMA, KERNEL_DOTMMA, KERNEL_DOTMMA_WS) = range(10)
+ KERNEL_WARPMMA, KERNEL_DOTMMA, KERNEL_DOTMMA_WS, KERNEL_TILE_T) = range(11)
 KERNEL_NAMES = {KERNEL_DOTPROD: "dotprod", KERNEL_SPLITK: "splitk", KERNEL_TILE: "tile",
                 KERNEL_SPLITK_WS: "splitk_ws", KERNEL_STREAM: "stream", KERNEL_TILE2: "tile2",
                 KERNEL_WARPROW: "warprow", KERNEL_WARPMMA: "warpmma", KERNEL_DOTMMA: "dotmma",
-                KERNEL_DOTMMA_WS: "dotmma_ws"}
+                KERNEL_DOTMMA_WS: "dotmma_ws", KERNEL_TILE_T: "tile_t"}
 
 
 class Plan(ctypes.Structure):
@@ -437,9 +438,11 @@ def fp8_split(M: int, N: int, K: int, num_sms: int = 152) -> int:
 
 def probe_read(src, grid: int, threads: int, sink, nbytes: int | None = None, stream=None):
     """Launch the read-floor probe (bf16_linear_probe_read) over the bytes of the CUDA tensor `src`
-    (the first nbytes of them, or none when src is None); the checksum is XORed into the one-element
-    int32 CUDA tensor `sink`."""
+    (the first nbytes of them, or none when src is None); CTA b XORs its checksum into sink[b] of the
+    int32 CUDA tensor `sink` (at least `grid` elements)."""
     import torch
+    if sink is not None and sink.numel() < grid:
+        raise ValueError(f"sink needs {grid} elements, has {sink.numel()}")
     nb = 0 if src is None else (src.numel() * src.element_size() if nbytes is None else int(nbytes))
     dev = sink.device if sink is not None else torch.device("cuda", torch.cuda.current_device())
     st = load().bf16_linear_probe_read(_ptr(src), nb, int(grid), int(threads), _ptr(sink),

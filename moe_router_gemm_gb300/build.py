@@ -20,8 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libbf16_linear.so")
 
-SOURCES = ["api.cu", "plan.cpp", "dotprod.cu", "dotprod_f32.cu", "splitk.cu", "tile.cu", "stream.cu", "noalloc.cu", "tile2.cu", "warprow.cu", "warpmma.cu", "warpmma_ks.cu", "dotmma.cu", "fp8.cu"]
-HEADERS = ["common.cuh", "kernels.h", "dotprod.cuh", "dispatch_table.inc"]
+SOURCES = ["api.cu", "plan.cpp", "dotprod.cu", "dotprod_f32.cu", "splitk.cu", "tile.cu", "tile_t.cu", "stream.cu", "noalloc.cu", "tile2.cu", "warprow.cu", "warpmma.cu", "warpmma_ks.cu", "dotmma.cu", "fp8.cu", "probe.cu"]
+HEADERS = ["common.cuh", "kernels.h", "dotprod.cuh", "tile.cuh", "dispatch_table.inc"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "-I" + INCLUDE, "-I" + CSRC]

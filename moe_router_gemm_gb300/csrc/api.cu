@@ -113,7 +113,7 @@ int run(const bf16l_call &c) {
     const uint32_t flags = forced ? (uint32_t)forced->flags : c.flags;
     int st = check_args(c.x, c.W, c.bias, c.out, c.M, c.N, c.K, c.out_f32 ? 4 : 2);
     if (st != BF16L_OK) return st;
-    if (flags & ~BF16L_FLAG_PDL) return BF16L_EINVAL;
+    if (!flags_valid(flags)) return BF16L_EINVAL;
     if (c.workspace && (reinterpret_cast<uintptr_t>(c.workspace) & 255u)) return BF16L_EALIGN;
     if (c.M == 0) return BF16L_OK;
     if (forced) {
@@ -145,7 +145,8 @@ int run(const bf16l_call &c) {
         case BF16L_KERNEL_DOTPROD: e = launch_dotprod(a, p); break;
         case BF16L_KERNEL_SPLITK:
         case BF16L_KERNEL_SPLITK_WS: e = launch_splitk(a, p); break;
-        case BF16L_KERNEL_TILE: e = launch_tile(a, p); break;
+        case BF16L_KERNEL_TILE:
+        case BF16L_KERNEL_TILE_T: e = launch_tile(a, p); break;
         case BF16L_KERNEL_STREAM: e = launch_stream(a, p); break;
         case BF16L_KERNEL_TILE2: e = launch_tile2(a, p); break;
         case BF16L_KERNEL_WARPROW: e = launch_warprow(a, p); break;
@@ -264,7 +265,7 @@ extern "C" size_t bf16_linear_host_staging_bytes(int M, int N, int K, int with_b
 extern "C" int bf16_linear_host(const void *x, const void *W, const void *bias, void *out, int M, int N, int K,
                                 void *staging, size_t staging_bytes, uint32_t flags, bf16l_stream_t stream) {
     using namespace bf16l;
-    if (M < 0 || N <= 0 || K <= 0 || (flags & ~BF16L_FLAG_PDL)) return BF16L_EINVAL;
+    if (M < 0 || N <= 0 || K <= 0 || !flags_valid(flags)) return BF16L_EINVAL;
     if (M == 0) return BF16L_OK;
     if (!x || !W || !out || !staging) return BF16L_EINVAL;
     if (reinterpret_cast<uintptr_t>(staging) & 255u) return BF16L_EALIGN;
@@ -350,7 +351,7 @@ extern "C" int bf16_linear_fp8_with_plan(const void *xq, const void *wq, const f
     if (!plan) return BF16L_EINVAL;
     const uint32_t flags = (uint32_t)plan->flags;
     if (M < 0 || N <= 0 || K <= 0) return BF16L_EINVAL;
-    if (flags & ~BF16L_FLAG_PDL) return BF16L_EINVAL;
+    if (!flags_valid(flags)) return BF16L_EINVAL;
     if (M == 0) return BF16L_OK;
     if (!xq || !wq || !out || !scale_x || !scale_w) return BF16L_EINVAL;
     if (misaligned(xq) || misaligned(wq) || misaligned(out) || (bias && misaligned(bias)) ||
@@ -371,7 +372,7 @@ extern "C" int bf16_linear_fp8_with_plan(const void *xq, const void *wq, const f
         if (M > 16 && tiles >= 32) {  // a dense contraction with enough tiles: the tcgen05 tile form
             kernel = BF16L_KERNEL_TILE;
             threads = kTileThreads;
-            cps = kTileMaxStages;
+            cps = tile_max_stages(kTileBN);
         } else if (M <= kWarpMmaMaxTokens && (size_t)M * K <= (size_t)kWarpMmaMaxSmem && N >= 1024) {
             // Many rows: the persistent warp-MMA form.  Measured on GB300: more,
             // smaller CTAs per SM win where x is small enough to stage that often.
@@ -410,7 +411,7 @@ extern "C" int bf16_linear_fp8_with_plan(const void *xq, const void *wq, const f
                                (int)(ctas < groups ? ctas : groups), flags, stream, ds->status);
     } else if (kernel == BF16L_KERNEL_TILE) {
         // stages = ring depth; tiles of 128 x rows by 256 W rows, 128 codes per 128-byte swizzle row
-        if (threads != kTileThreads || cps < kTileMinStages || cps > kTileMaxStages) return BF16L_EINVAL;
+        if (threads != kTileThreads || cps < kTileMinStages || cps > tile_max_stages(kTileBN)) return BF16L_EINVAL;
         const long long tiles = (long long)((M + kTileBM - 1) / kTileBM) * ((N + kTileBN - 1) / kTileBN);
         const int grid = (int)(tiles < ds->dev.num_sms ? tiles : ds->dev.num_sms);
         e = launch_tile_fp8(xq, wq, scale_x, scale_w, bias, out, M, N, K, cps, grid, flags, stream, ds->status);
@@ -427,7 +428,7 @@ extern "C" int bf16_linear_fp8_with_plan(const void *xq, const void *wq, const f
 extern "C" int bf16_quant_fp8(const void *x, const float *scale, void *xq, int64_t n, uint32_t flags,
                               bf16l_stream_t stream) {
     using namespace bf16l;
-    if (n < 0 || (flags & ~BF16L_FLAG_PDL)) return BF16L_EINVAL;
+    if (n < 0 || !flags_valid(flags)) return BF16L_EINVAL;
     if (n == 0) return BF16L_OK;
     if (!x || !scale || !xq) return BF16L_EINVAL;
     if ((reinterpret_cast<uintptr_t>(x) & 1u) || (reinterpret_cast<uintptr_t>(scale) & 3u)) return BF16L_EALIGN;

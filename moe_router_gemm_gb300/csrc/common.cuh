@@ -542,6 +542,14 @@ __device__ __forceinline__ uint4 ldg_stream_v4(const void *p) {
     return v;
 }
 
+// Launch modes from the BF16L_FLAG_* bits (host side).  Every launch uses
+// programmatic dependent launch unless BF16L_FLAG_SERIAL: the kernel may be
+// scheduled while the previous kernel on the stream finishes, and waits for it
+// (griddepcontrol.wait) before it reads anything.  With BF16L_FLAG_PDL the
+// weight (and bias) loads may go out before that wait.
+inline int pdl_attr_of(uint32_t flags) { return (flags & BF16L_FLAG_SERIAL) ? 0 : 1; }
+inline int w_early_of(uint32_t flags) { return (flags & BF16L_FLAG_PDL) ? 1 : 0; }
+
 // Programmatic dependent launch hooks (no-ops when the launch did not enable PDL).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {

@@ -76,7 +76,9 @@ template <bool HI, bool XR, bool WS, bool F8, typename OutT>
 __global__ void __launch_bounds__(kDmWarps * 32)
     dotmma_kernel(const uint8_t *__restrict__ x, const uint8_t *__restrict__ W, const uint16_t *__restrict__ bias,
                   OutT *__restrict__ out, int M, int N, int RB, int S, int32_t *status, uint32_t *counters,
-                  float4 *tiles, const float *__restrict__ scale_x, const float *__restrict__ scale_w) {
+                  float4 *tiles, const float *__restrict__ scale_x, const float *__restrict__ scale_w,
+                  int w_early) {
+    if (!w_early) pdl_wait();  // default launch: nothing is read before the previous kernel has finished
     constexpr int U = 8;  // K blocks (4 x 16 bytes across the lane quad) per lane per batch
     extern __shared__ uint4 xs[];
     __shared__ float4 part[kDmWarps][32];  // per warp, lane (g, t): tokens g, g+8 x rows 2t, 2t+1
@@ -270,7 +272,7 @@ namespace {
 
 template <typename OutT>
 using DmFn = void (*)(const uint8_t *, const uint8_t *, const uint16_t *, OutT *, int, int, int, int, int32_t *,
-                      uint32_t *, float4 *, const float *, const float *);
+                      uint32_t *, float4 *, const float *, const float *, int);
 
 template <bool WS, typename OutT>
 DmFn<OutT> pick_dm_ws(int M, bool xr) {
@@ -314,7 +316,7 @@ int launch_dm_common(DmFn<OutT> fn, const void *x, const void *W, const void *bi
     cfg.stream = (cudaStream_t)stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = (flags & BF16L_FLAG_PDL) ? 1 : 0;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_attr_of(flags);
     attr[1].id = cudaLaunchAttributeClusterDimension;
     attr[1].val.clusterDim.x = (unsigned)S;
     attr[1].val.clusterDim.y = 1;
@@ -323,7 +325,7 @@ int launch_dm_common(DmFn<OutT> fn, const void *x, const void *W, const void *bi
     cfg.numAttrs = cluster ? 2 : 1;
     return (int)cudaLaunchKernelEx(&cfg, fn, static_cast<const uint8_t *>(x), static_cast<const uint8_t *>(W),
                                    static_cast<const uint16_t *>(bias), out, M, N, RB, S, status, counters, tiles,
-                                   sx, sw);
+                                   sx, sw, w_early_of(flags));
 }
 
 template <typename OutT>

@@ -68,7 +68,8 @@ __global__ void __launch_bounds__(256) dotprod_kernel(const uint16_t *__restrict
                                                       const uint16_t *__restrict__ W,
                                                       const uint16_t *__restrict__ bias,
                                                       OutT *__restrict__ out, int M, int N, int K,
-                                                      int32_t *status) {
+                                                      int32_t *status, int w_early) {
+    if (!w_early) pdl_wait();  // default launch: nothing is read before the previous kernel has finished
     constexpr int U = (VEC == 8) ? 8 : 4;  // vectors per row a thread loads before computing
     __shared__ float red[8][R * MT];
     __shared__ __align__(8) uint64_t xbar;
@@ -201,7 +202,7 @@ __global__ void __launch_bounds__(256) dotprod_kernel(const uint16_t *__restrict
 namespace dot_detail {
 
 template <typename OutT>
-using DotFn = void (*)(const uint16_t *, const uint16_t *, const uint16_t *, OutT *, int, int, int, int32_t *);
+using DotFn = void (*)(const uint16_t *, const uint16_t *, const uint16_t *, OutT *, int, int, int, int32_t *, int);
 
 // kind: 0 = 16-byte vectors with x in shared memory, 1 = 16-byte vectors with
 // x from global memory, 2 = scalar (K % 8 != 0).
@@ -267,12 +268,12 @@ int launch_dotprod_t(const LaunchArgs &a, const bf16l_plan &p) {
     cfg.stream = (cudaStream_t)a.stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = (p.flags & BF16L_FLAG_PDL) ? 1 : 0;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_attr_of((uint32_t)p.flags);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return (int)cudaLaunchKernelEx(&cfg, fn, static_cast<const uint16_t *>(a.x), static_cast<const uint16_t *>(a.W),
                                    static_cast<const uint16_t *>(a.bias), static_cast<OutT *>(a.out), a.M, a.N,
-                                   a.K, a.status);
+                                   a.K, a.status, w_early_of((uint32_t)p.flags));
 }
 
 }  // namespace dot_detail

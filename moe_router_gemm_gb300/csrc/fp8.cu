@@ -79,7 +79,7 @@ int launch_quant_fp8(const void *x, const float *scale, void *q, long long n, in
     cfg.stream = (cudaStream_t)stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = (flags & BF16L_FLAG_PDL) ? 1 : 0;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_attr_of(flags);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return (int)cudaLaunchKernelEx(&cfg, quant_fp8_kernel, static_cast<const uint16_t *>(x), scale,

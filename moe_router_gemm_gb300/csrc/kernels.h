@@ -55,12 +55,25 @@ constexpr int kStreamThreads = 288;
 int stream_smem_bytes(int K, int rows, int stages);
 int init_stream();
 
-// Tile kernel: BM x rows, BN W rows per tile, 64-wide K chunks.
+// Tile kernel: 128 rows of one operand on the MMA M side by BN rows of the
+// other on the N side, 64-wide K chunks.  Plain form (BF16L_KERNEL_TILE): x rows
+// on M, BN W rows on N; swap-AB form (BF16L_KERNEL_TILE_T): W rows on M, BN
+// tokens on N.  The ring takes as many stages as fit 227 KB, at most 8.
 constexpr int kTileBM = 128;
 constexpr int kTileBN = 256;
 constexpr int kTileMinStages = 2;
-constexpr int kTileMaxStages = 4;
+constexpr int kTileMaxStages = 8;
 constexpr int kTileThreads = 192;
+constexpr int kTileDefaultGroup = 8;  // raster group (N-tiles) of the plain form when a plan gives 0
+constexpr int kTileBNs[] = {128, 192, 224, 240, 256};  // plain form: W rows per tile
+constexpr int kTileTBNs[] = {32, 64, 128, 192, 256};   // swap-AB form: tokens per tile
+constexpr int tile_max_stages(int bn) {
+    return (232448 - 1024 - 256) / (128 * 128 + bn * 128) < kTileMaxStages
+               ? (232448 - 1024 - 256) / (128 * 128 + bn * 128)
+               : kTileMaxStages;
+}
+int tile_smem_bytes(int stages, int bn);
+int init_tile_t();
 
 // Warp-per-row kernel: M <= 8 tokens staged in shared memory (M*K*2 bytes),
 // 256/512/1024 threads, 1/2/4 warps per row, a few CTAs per SM.
@@ -116,6 +129,12 @@ int current_device_checked(bf16l_device *dev);
 // Record a CUDA error code for bf16_linear_cuda_error (0 is ignored); returns it.
 int note_cuda_error(int cuda_err);
 
+// BF16L_FLAG_* bits a call may pass: known bits only, and not PDL with SERIAL.
+inline bool flags_valid(uint32_t f) {
+    return (f & ~(BF16L_FLAG_PDL | BF16L_FLAG_SERIAL)) == 0 && (f & (BF16L_FLAG_PDL | BF16L_FLAG_SERIAL)) !=
+                                                                    (BF16L_FLAG_PDL | BF16L_FLAG_SERIAL);
+}
+
 // Validate a plan against a shape; BF16L_OK or the error to return.  Fills
 // plan->grid.  Pure host logic.
 int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *plan);
@@ -138,7 +157,8 @@ struct LaunchArgs {
 // Each returns a cudaError_t value (0 on success).
 int launch_dotprod(const LaunchArgs &a, const bf16l_plan &p);
 int launch_splitk(const LaunchArgs &a, const bf16l_plan &p);
-int launch_tile(const LaunchArgs &a, const bf16l_plan &p);
+int launch_tile(const LaunchArgs &a, const bf16l_plan &p);   // both tile forms
+int launch_tile_swap(const LaunchArgs &a, const bf16l_plan &p);
 int launch_stream(const LaunchArgs &a, const bf16l_plan &p);
 int launch_tile2(const LaunchArgs &a, const bf16l_plan &p);
 int launch_warprow(const LaunchArgs &a, const bf16l_plan &p);

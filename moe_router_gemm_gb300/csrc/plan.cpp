@@ -85,14 +85,14 @@ void plan_tile(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
     p->threads = kTileThreads;
     p->rows_per_cta = kTileBN;
     p->tokens_per_cta = kTileBM;
-    p->stages = kTileMaxStages;
+    p->stages = tile_max_stages(kTileBN);
 }
 
 }  // namespace
 
 int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
     if (M < 0 || N <= 0 || K <= 0) return BF16L_EINVAL;
-    if ((uint32_t)p->flags & ~BF16L_FLAG_PDL) return BF16L_EINVAL;
+    if (!flags_valid((uint32_t)p->flags)) return BF16L_EINVAL;
     switch (p->kernel) {
         case BF16L_KERNEL_DOTPROD: {
             if (!in_list(p->threads, kDotThreads, 3) || !in_list(p->rows_per_cta, kDotRows, 3))
@@ -132,12 +132,19 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
             p->grid = M == 0 ? 0 : (N < dev.num_sms ? N : dev.num_sms);
             return BF16L_OK;
         }
-        case BF16L_KERNEL_TILE: {
+        case BF16L_KERNEL_TILE:
+        case BF16L_KERNEL_TILE_T: {
+            // plain: 128 x rows by rows_per_cta W rows per tile; swap-AB: 128 W rows by tokens_per_cta tokens
             if (K % 8 != 0) return BF16L_EUNSUPPORTED;
-            if (p->threads != kTileThreads || p->rows_per_cta != kTileBN || p->tokens_per_cta != kTileBM)
+            const bool swap = p->kernel == BF16L_KERNEL_TILE_T;
+            const int bn = swap ? p->tokens_per_cta : p->rows_per_cta;
+            if (p->threads != kTileThreads || (swap ? p->rows_per_cta : p->tokens_per_cta) != kTileBM ||
+                !(swap ? in_list(bn, kTileTBNs, 5) : in_list(bn, kTileBNs, 5)))
                 return BF16L_EINVAL;
-            if (p->stages < kTileMinStages || p->stages > kTileMaxStages) return BF16L_EINVAL;
-            const int64_t tiles = (int64_t)ceil_div(M, kTileBM) * ceil_div(N, kTileBN);
+            if (p->stages < kTileMinStages || p->stages > tile_max_stages(bn)) return BF16L_EINVAL;
+            if (p->split_k < 0 || p->split_k > 1024) return BF16L_EINVAL;  // raster group
+            const int64_t tiles = swap ? (int64_t)ceil_div(N, kTileBM) * ceil_div(M, bn)
+                                       : (int64_t)ceil_div(M, kTileBM) * ceil_div(N, bn);
             const int64_t grid = tiles < dev.num_sms ? tiles : dev.num_sms;
             p->grid = M == 0 ? 0 : (int)grid;
             return BF16L_OK;

@@ -118,7 +118,9 @@ template <int BN, typename OutT, bool kClus>
 __global__ void __launch_bounds__(kSplitThreads, 1)
     splitk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                   const uint16_t *__restrict__ bias, OutT *__restrict__ out, int M, int N, int K, int tokp,
-                  int stages, int32_t *status, float *__restrict__ ws, uint32_t *__restrict__ counters) {
+                  int stages, int32_t *status, float *__restrict__ ws, uint32_t *__restrict__ counters,
+                  int w_early) {
+    if (!w_early) pdl_wait();  // default launch: nothing is read before the previous kernel has finished
     constexpr uint32_t kIdesc = idesc_bf16_f32(kMmaM, BN);
     constexpr int kAcc = split_acc_count(BN);
     constexpr int kCols = kAcc * BN <= 32 ? 32 : kAcc * BN <= 64 ? 64 : kAcc * BN <= 128 ? 128 : 256;
@@ -408,7 +410,7 @@ namespace {
 
 template <typename OutT, bool kClus>
 using SplitFn = void (*)(CUtensorMap, CUtensorMap, const uint16_t *, OutT *, int, int, int, int, int, int32_t *,
-                         float *, uint32_t *);
+                         float *, uint32_t *, int);
 
 template <typename OutT, bool kClus>
 SplitFn<OutT, kClus> pick(int BN) {
@@ -464,7 +466,7 @@ int launch_split_t(const LaunchArgs &a, const bf16l_plan &p) {
     cudaLaunchAttribute attr[2];
     int na = 0;
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[na].val.programmaticStreamSerializationAllowed = (p.flags & BF16L_FLAG_PDL) ? 1 : 0;
+    attr[na].val.programmaticStreamSerializationAllowed = pdl_attr_of((uint32_t)p.flags);
     ++na;
     if (kClus) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
@@ -477,7 +479,7 @@ int launch_split_t(const LaunchArgs &a, const bf16l_plan &p) {
     cfg.numAttrs = na;
     return (int)cudaLaunchKernelEx(&cfg, fn, tw, tx, static_cast<const uint16_t *>(a.bias),
                                    static_cast<OutT *>(a.out), a.M, a.N, a.K, p.tokens_per_cta, p.stages,
-                                   a.status, parts, counters);
+                                   a.status, parts, counters, w_early_of((uint32_t)p.flags));
 }
 
 }  // namespace

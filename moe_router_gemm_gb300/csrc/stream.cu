@@ -47,7 +47,9 @@ int stream_smem_bytes(int K, int rg, int stages) {
 template <int MT, int RG, typename OutT>
 __global__ void __launch_bounds__(kStreamThreads, 1)
     stream_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ W, const uint16_t *__restrict__ bias,
-                  OutT *__restrict__ out, int M, int N, int K, int rg_unused, int stages, int32_t *status) {
+                  OutT *__restrict__ out, int M, int N, int K, int rg_unused, int stages, int32_t *status,
+                  int w_early) {
+    if (!w_early) pdl_wait();  // default launch: nothing is read before the previous kernel has finished
     constexpr int rg = RG;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -174,7 +176,7 @@ namespace {
 
 template <typename OutT>
 using StreamFn = void (*)(const uint16_t *, const uint16_t *, const uint16_t *, OutT *, int, int, int, int, int,
-                          int32_t *);
+                          int32_t *, int);
 
 template <int MT, typename OutT>
 StreamFn<OutT> pick_rg(int RG) {
@@ -208,12 +210,12 @@ int launch_stream_t(const LaunchArgs &a, const bf16l_plan &p) {
     cfg.stream = (cudaStream_t)a.stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = (p.flags & BF16L_FLAG_PDL) ? 1 : 0;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_attr_of((uint32_t)p.flags);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return (int)cudaLaunchKernelEx(&cfg, fn, static_cast<const uint16_t *>(a.x), static_cast<const uint16_t *>(a.W),
                                    static_cast<const uint16_t *>(a.bias), static_cast<OutT *>(a.out), a.M, a.N, a.K,
-                                   p.rows_per_cta, p.stages, a.status);
+                                   p.rows_per_cta, p.stages, a.status, w_early_of((uint32_t)p.flags));
 }
 
 template <typename OutT>

@@ -386,7 +386,7 @@ static int launch_tile2_t(const LaunchArgs &a, const bf16l_plan &p) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = (p.flags & BF16L_FLAG_PDL) ? 1 : 0;
+    attr[1].val.programmaticStreamSerializationAllowed = pdl_attr_of((uint32_t)p.flags);
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     return (int)cudaLaunchKernelEx(&cfg, tile2_kernel<OutT, BN>, tx, tw, static_cast<const uint16_t *>(a.bias),

@@ -56,7 +56,8 @@ template <int WPR, int NT, bool HI, bool XR, bool F8, typename OutT, int NG = 1>
 __global__ void __launch_bounds__(NT, XR ? 1 : 1024 / NT)
     warpmma_kernel(const uint8_t *__restrict__ x, const uint8_t *__restrict__ W, const uint16_t *__restrict__ bias,
                    OutT *__restrict__ out, int M, int N, int RB, int32_t *status, const float *__restrict__ scale_x,
-                   const float *__restrict__ scale_w) {
+                   const float *__restrict__ scale_w, int w_early) {
+    if (!w_early) pdl_wait();  // default launch: nothing is read before the previous kernel has finished
     constexpr int U = 8 / NG;                      // K blocks (4 x 16 bytes across a lane quad) per lane per batch
     extern __shared__ uint4 xs[];                  // x[m] rows as 16-byte vectors, [M][RB / 16]
     __shared__ float part[WPR > 1 ? kWmMaxWarps : 1][32][4];  // WPR > 1: every lane's four sums
@@ -209,7 +210,7 @@ namespace {
 
 template <typename OutT>
 using WmFn = void (*)(const uint8_t *, const uint8_t *, const uint16_t *, OutT *, int, int, int, int32_t *,
-                      const float *, const float *);
+                      const float *, const float *, int);
 
 template <int WPR, bool HI, bool XR, bool F8, typename OutT, int NG>
 WmFn<OutT> pick_nt(int threads) {
@@ -278,11 +279,12 @@ int launch_wm_common(WmFn<OutT> fn, const void *x, const void *W, const void *bi
     cfg.stream = (cudaStream_t)stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = (flags & BF16L_FLAG_PDL) ? 1 : 0;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_attr_of(flags);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return (int)cudaLaunchKernelEx(&cfg, fn, static_cast<const uint8_t *>(x), static_cast<const uint8_t *>(W),
-                                   static_cast<const uint16_t *>(bias), out, M, N, RB, status, sx, sw);
+                                   static_cast<const uint16_t *>(bias), out, M, N, RB, status, sx, sw,
+                                   w_early_of(flags));
 }
 
 template <typename OutT>

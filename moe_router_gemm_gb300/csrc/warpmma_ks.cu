@@ -69,7 +69,8 @@ __host__ __device__ inline KsLayout ks_layout(int M, int N, int RB, int S, int C
 template <int WPR, int NT, int TT, typename OutT>
 __global__ void __launch_bounds__(NT, TT == 1 ? 1024 / NT : 1)
     warpmma_ks_kernel(const uint8_t *__restrict__ x, const uint8_t *__restrict__ W, const uint16_t *__restrict__ bias,
-                      OutT *__restrict__ out, int M, int N, int RB, int S, int32_t *status) {
+                      OutT *__restrict__ out, int M, int N, int RB, int S, int32_t *status, int w_early) {
+    if (!w_early) pdl_wait();  // default launch: nothing is read before the previous kernel has finished
     constexpr int U = 8;  // K blocks (4 x 16 bytes across a lane quad) per lane per batch
     extern __shared__ __align__(16) uint8_t ks_smem[];
     __shared__ __align__(8) uint64_t xbar, rbar;
@@ -233,7 +234,7 @@ __global__ void __launch_bounds__(NT, TT == 1 ? 1024 / NT : 1)
 namespace {
 
 template <typename OutT>
-using KsFn = void (*)(const uint8_t *, const uint8_t *, const uint16_t *, OutT *, int, int, int, int, int32_t *);
+using KsFn = void (*)(const uint8_t *, const uint8_t *, const uint16_t *, OutT *, int, int, int, int, int32_t *, int);
 
 // 16-token tiles an instance covers for M tokens (3 tiles run the 4-tile instance).
 int ks_tiles(int M) {
@@ -348,12 +349,12 @@ int launch_ks_t(const LaunchArgs &a, const bf16l_plan &p) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = (p.flags & BF16L_FLAG_PDL) ? 1 : 0;
+    attr[1].val.programmaticStreamSerializationAllowed = pdl_attr_of((uint32_t)p.flags);
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     return (int)cudaLaunchKernelEx(&cfg, fn, static_cast<const uint8_t *>(a.x), static_cast<const uint8_t *>(a.W),
                                    static_cast<const uint16_t *>(a.bias), static_cast<OutT *>(a.out), a.M, a.N,
-                                   a.K * 2, S, a.status);
+                                   a.K * 2, S, a.status, w_early_of((uint32_t)p.flags));
 }
 
 }  // namespace

@@ -44,7 +44,8 @@ int warprow_smem_bytes(int M, int K) { return M * K * 2; }
 template <int MT, int WPR, int NT, typename OutT>
 __global__ void __launch_bounds__(NT, 1024 / NT)
     warprow_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ W, const uint16_t *__restrict__ bias,
-                   OutT *__restrict__ out, int M, int N, int K, int32_t *status) {
+                   OutT *__restrict__ out, int M, int N, int K, int32_t *status, int w_early) {
+    if (!w_early) pdl_wait();  // default launch: nothing is read before the previous kernel has finished
     constexpr int U = 8;  // 16-byte weight vectors per lane per batch (128 KB in flight per SM)
     extern __shared__ uint4 xs[];          // x[m][k] as 16-byte vectors, [MT][K / 8]
     __shared__ float part[kWrMaxWarps][MT];
@@ -148,7 +149,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
 namespace {
 
 template <typename OutT>
-using WrFn = void (*)(const uint16_t *, const uint16_t *, const uint16_t *, OutT *, int, int, int, int32_t *);
+using WrFn = void (*)(const uint16_t *, const uint16_t *, const uint16_t *, OutT *, int, int, int, int32_t *, int);
 
 template <int MT, int WPR, typename OutT>
 WrFn<OutT> pick_nt(int threads) {
@@ -204,12 +205,12 @@ int launch_wr_t(const LaunchArgs &a, const bf16l_plan &p) {
     cfg.stream = (cudaStream_t)a.stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = (p.flags & BF16L_FLAG_PDL) ? 1 : 0;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_attr_of((uint32_t)p.flags);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return (int)cudaLaunchKernelEx(&cfg, fn, static_cast<const uint16_t *>(a.x), static_cast<const uint16_t *>(a.W),
                                    static_cast<const uint16_t *>(a.bias), static_cast<OutT *>(a.out), a.M, a.N, a.K,
-                                   a.status);
+                                   a.status, w_early_of((uint32_t)p.flags));
 }
 
 }  // namespace

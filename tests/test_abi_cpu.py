@@ -60,10 +60,10 @@ def test_plan_size_rules(lib):
     assert lib.plan(4, 256, 3000).kernel == lib.KERNEL_DOTPROD
     assert lib.plan(40, 256, 2881).kernel == lib.KERNEL_DOTPROD
     assert lib.plan(300, 256, 2881).kernel == lib.KERNEL_DOTPROD
-    # large M -> tile kernel
-    p = lib.plan(8192, 14336, 4096)
+    # large M -> tile kernel (K = 4104: no measured table entry, so the size rules decide)
+    p = lib.plan(8192, 14336, 4104)
     assert p.kernel == lib.KERNEL_TILE and p.grid == 152
-    p = lib.plan(8192, 14336, 4096, device=(10, 3, 100))
+    p = lib.plan(8192, 14336, 4104, device=(10, 3, 100))
     assert p.grid == 100
 
 
@@ -124,7 +124,8 @@ def test_fp8_validation_and_split_without_gpu(lib):
     assert f(A, B, S1, S2, None, O, 0, 8, 64, 0, None) == 0            # M == 0: nothing to do
     assert f(A, B, S1, S2, None, O, -1, 8, 64, 0, None) == -1
     assert f(A, B, None, S2, None, O, 4, 8, 64, 0, None) == -1          # scales required
-    assert f(A, B, S1, S2, None, O, 4, 8, 64, 2, None) == -1            # unknown flag
+    assert f(A, B, S1, S2, None, O, 4, 8, 64, 4, None) == -1            # unknown flag
+    assert f(A, B, S1, S2, None, O, 4, 8, 64, 3, None) == -1            # PDL with SERIAL
     assert f(ctypes.c_void_p(0x10008), B, S1, S2, None, O, 4, 8, 64, 0, None) == -2
     assert f(A, B, ctypes.c_void_p(0x50000002), S2, None, O, 4, 8, 64, 0, None) == -2
     assert f(A, B, S1, S2, None, O, 4, 8, 40, 0, None) == -6            # K % 16 != 0
@@ -159,7 +160,8 @@ def test_forced_plan_rules_without_gpu(lib):
     assert run(8, 256, 2048, **{**split, "tokens_per_cta": 12}) == -1   # not a multiple of 8
     assert run(8, 256, 2048, **{**split, "rows_per_cta": 24}) == -1     # no kernel for 24 rows
     assert run(8, 256, 2048, **{**split, "rows_per_cta": 512}) == -1
-    assert run(8, 256, 2048, **{**split, "flags": 2}) == -1             # unknown launch flag
+    assert run(8, 256, 2048, **{**split, "flags": 4}) == -1             # unknown launch flag
+    assert run(8, 256, 2048, **{**split, "flags": 3}) == -1             # early weights with serial
     assert run(8, 256, 2048, kernel="dotprod", threads=96, rows_per_cta=2) == -1
     assert run(8, 256, 2048, kernel="dotprod", threads=128, rows_per_cta=3) == -1
     assert run(8, 256, 2048, kernel="tile", threads=192, rows_per_cta=256, tokens_per_cta=128, stages=9) == -1
@@ -334,3 +336,56 @@ def test_workspace_plans_on_cpu(lib):
     c.workspace, c.workspace_bytes = 0x50000010, 1 << 20
     assert L.bf16_linear_run(ctypes.byref(c)) == -2
     assert L.bf16_linear_run(None) == -1
+
+
+def test_probe_read_validates_before_touching_a_device(lib):
+    import ctypes as C
+    L = lib.load()
+    for bytes_, grid, threads in [(17, 1, 32), (16, 0, 32), (16, 1, 48), (16, 1, 2048), (16, 1, 0)]:
+        assert L.bf16_linear_probe_read(C.c_void_p(4096), bytes_, grid, threads, C.c_void_p(8192), None) == -1
+    assert L.bf16_linear_probe_read(None, 16, 1, 32, C.c_void_p(8192), None) == -1   # NULL src with bytes
+    assert L.bf16_linear_probe_read(C.c_void_p(4104), 16, 1, 32, C.c_void_p(8192), None) == -2  # src misaligned
+
+
+def test_tile_tactic_space(lib):
+    """Plain tile widths 128..256 and swap-AB token widths 32..256; rings as deep as fit 227 KB (8 at
+    most); any other width, or the wrong fixed side, is refused."""
+    mk = lambda k, **f: lib.make_plan(k, **dict(dict(threads=192), **f))
+    for bn, most in ((128, 7), (192, 5), (224, 5), (240, 4), (256, 4)):
+        p = mk("tile", rows_per_cta=bn, tokens_per_cta=128, stages=most, split_k=2)
+        assert lib.plan_check(2048, 7168, 7168, p).grid == 152
+        with pytest.raises(lib.BF16LinearError):
+            lib.plan_check(2048, 7168, 7168, mk("tile", rows_per_cta=bn, tokens_per_cta=128, stages=most + 1))
+    for bn, most in ((32, 8), (64, 8), (128, 7), (192, 5), (256, 4)):
+        p = mk("tile_t", rows_per_cta=128, tokens_per_cta=bn, stages=most)
+        # 14336 / 128 = 112 W tiles times ceil(64 / bn) token tiles
+        assert lib.plan_check(64, 14336, 4096, p).grid == min(152, 112 * -(-64 // bn))
+    for bad in (mk("tile", rows_per_cta=160, tokens_per_cta=128, stages=4),
+                mk("tile", rows_per_cta=256, tokens_per_cta=64, stages=4),
+                mk("tile_t", rows_per_cta=256, tokens_per_cta=64, stages=4),
+                mk("tile_t", rows_per_cta=128, tokens_per_cta=48, stages=4),
+                mk("tile_t", rows_per_cta=128, tokens_per_cta=64, stages=1),
+                mk("tile", rows_per_cta=256, tokens_per_cta=128, stages=4, split_k=-1)):
+        with pytest.raises(lib.BF16LinearError):
+            lib.plan_check(256, 14336, 4096, bad)
+    with pytest.raises(lib.BF16LinearError) as e:  # K % 8 != 0: a TMA kernel cannot run it
+        lib.plan_check(256, 1024, 1001, mk("tile_t", rows_per_cta=128, tokens_per_cta=64, stages=4))
+    assert e.value.status == -6
+
+
+def test_launch_flags_validated_without_gpu(lib):
+    """Unknown flag bits, and the early-weights mode together with the serial one, are refused before any
+    CUDA call; the plan check applies the same rule to a plan's flags."""
+    import ctypes as C
+    L = lib.load()
+    x, W, o = C.c_void_p(1 << 16), C.c_void_p(1 << 29), C.c_void_p(1 << 30)
+    for bad in (4, 3, 0x80000000):
+        assert L.bf16_linear_ex(x, W, None, o, 4, 256, 2048, bad, None) == -1
+        assert L.bf16_quant_fp8(x, C.c_void_p(1 << 20), o, 64, bad, None) == -1
+    p = lib.make_plan("dotprod", threads=128, rows_per_cta=2)
+    for ok in (0, lib.FLAG_PDL, lib.FLAG_SERIAL):
+        p.flags = ok
+        lib.plan_check(4, 256, 2048, p)
+    p.flags = lib.FLAG_PDL | lib.FLAG_SERIAL
+    with pytest.raises(lib.BF16LinearError):
+        lib.plan_check(4, 256, 2048, p)

@@ -1,17 +1,19 @@
 """Programmatic dependent launch across a real producer -> consumer chain.
 
-A kernel launched with BF16L_FLAG_PDL starts before the previous kernel on its
-stream has finished: it may read W (and issue its weight copies) early, and must
-read x and write out only after its grid-dependency wait.  The hazard PDL
-brings in is therefore a consumer reading its x before the producer has written
-it, or writing its out while the producer still reads it.  Each case here
-chains two launches on one stream, both with PDL:
+Every launch of the library uses programmatic dependent launch unless told
+otherwise: the kernel may start before the previous kernel on its stream has
+finished and waits for it before reading anything (the default), or, with
+BF16L_FLAG_PDL, reads W (and issues its weight copies) early and only x and out
+wait.  The hazard either mode brings in is a consumer reading its x before the
+producer has written it, or writing its out while the producer still reads it.
+Each case here chains two launches on one stream:
 
     A (the dispatcher's plan):  y  = x0 @ W1^T          y [M, K1]
     B (one kernel family):      x0 = y @ W2^T + b2      B's out overwrites A's input
 
 so B reads what A writes (read after write) and writes what A reads (write after
-read).  y is poisoned before A runs.  The results are checked against the
+read).  A runs with BF16L_FLAG_PDL; B runs in each mode (early weights, and the
+default).  y is poisoned before A runs.  The results are checked against the
 oracle: A's output against oracle(x0, W1), B's output against the oracle applied
 to A's GPU output and against the oracle applied to A's oracle output.  The same
 chain also runs as a captured CUDA graph, replayed with fresh inputs.  The
@@ -53,16 +55,17 @@ def _families(lib):
                       16, 256, 2048),
         "tile": (mk("tile", threads=192, rows_per_cta=256, tokens_per_cta=128, stages=4), 256, 512, 1024),
         "tile2": (mk("tile2", threads=192, rows_per_cta=256, tokens_per_cta=256, stages=4), 256, 512, 1024),
+        "tile_t": (mk("tile_t", threads=192, rows_per_cta=128, tokens_per_cta=64, stages=4), 64, 512, 1024),
     }
 
 
 NAMES = ["dotprod", "dotprod_x_l2", "dotprod_groups", "stream", "warprow", "warpmma", "warpmma_x_l2",
          "warpmma_cluster", "warpmma_cluster_m40", "dotmma", "dotmma_x_l2", "dotmma_m40", "dotmma_ws", "splitk",
-         "splitk_ws", "tile", "tile2"]
+         "splitk_ws", "tile", "tile2", "tile_t"]
 
 
 def test_family_list_is_complete(lib):
-    """Every kernel the library launches with BF16L_FLAG_PDL appears in the chain."""
+    """Every kernel the library launches appears in the chain."""
     fams = _families(lib)
     assert sorted(fams) == sorted(NAMES)
     kernels = {lib.KERNEL_NAMES[p.kernel] for p, *_ in fams.values()}
@@ -70,11 +73,11 @@ def test_family_list_is_complete(lib):
 
 
 class Chain:
-    def __init__(self, lib, name, seed):
+    def __init__(self, lib, name, seed, flags):
         plan, M, K0, K1 = _families(lib)[name]
         self.lib, self.name, self.M, self.K0, self.K1 = lib, name, M, K0, K1
         self.plan = plan
-        self.plan.flags = lib.FLAG_PDL
+        self.plan.flags = flags
         lib.plan_check(M, K0, K1, self.plan)  # B: x[M, K1] @ W2[K0, K1]^T
         _, W1, _ = wl.make_inputs(1, K1, K0, seed, False)
         _, W2, b2 = wl.make_inputs(1, K0, K1, seed + 1, True)
@@ -110,9 +113,13 @@ def _fresh_x(M, K0, seed):
     return x
 
 
+MODES = {"early_weights": 1, "default": 0}
+
+
+@pytest.mark.parametrize("mode", list(MODES))
 @pytest.mark.parametrize("name", NAMES)
-def test_pdl_chain(lib, name):
-    ch = Chain(lib, name, seed=37 * NAMES.index(name))
+def test_pdl_chain(lib, name, mode):
+    ch = Chain(lib, name, seed=37 * NAMES.index(name), flags=MODES[mode])
     stream = torch.cuda.Stream(DEV)
     for rep in range(2):
         x = _fresh_x(ch.M, ch.K0, 100 + rep)
@@ -124,9 +131,10 @@ def test_pdl_chain(lib, name):
     assert lib.device_status() == 0
 
 
+@pytest.mark.parametrize("mode", list(MODES))
 @pytest.mark.parametrize("name", NAMES)
-def test_pdl_chain_in_graph(lib, name):
-    ch = Chain(lib, name, seed=500 + 37 * NAMES.index(name))
+def test_pdl_chain_in_graph(lib, name, mode):
+    ch = Chain(lib, name, seed=500 + 37 * NAMES.index(name), flags=MODES[mode])
     stream = torch.cuda.Stream(DEV)
     ch.src.copy_(_fresh_x(ch.M, ch.K0, 7).to(DEV))
     torch.cuda.synchronize()

@@ -91,3 +91,89 @@ def test_tile_ragged_f32_logits(lib):
     xf, Wf = x.double().numpy(), W.double().numpy()
     mag = np.abs(xf) @ np.abs(Wf).T + np.abs(b.double().numpy())[None, :]
     assert np.all(np.abs(got - exact) <= (K + 2) * 2.0 ** -24 * mag + 1e-30)
+
+
+# ---- the tactic space: tile widths, ring depths, raster groups, and the swap-AB form ----
+
+WIDTH_CASES = [
+    # BN (W rows per tile), M, N, K, stages, raster group
+    (128, 130, 300, 520, 7, 0),
+    (192, 1000, 700, 136, 5, 1),
+    (224, 129, 2112, 2056, 4, 3),
+    (240, 384, 2112, 1032, 4, 16),
+    (256, 300, 1000, 200, 2, 1),
+]
+
+
+@pytest.mark.parametrize("case", WIDTH_CASES, ids=lambda c: "x".join(map(str, c)))
+def test_tile_widths(lib, case):
+    """Every plain-form width, with ragged M, N and K, against the oracle; the raster group only
+    reorders tiles, so it must not change a bit (checked against group 0)."""
+    bn, M, N, K, st, grp = case
+    plan = lib.make_plan("tile", threads=192, rows_per_cta=bn, tokens_per_cta=128, stages=st, split_k=grp)
+    base = lib.make_plan("tile", threads=192, rows_per_cta=bn, tokens_per_cta=128, stages=2, split_k=0)
+    for bias in (False, True):
+        x, W, b = wl.make_inputs(M, N, K, bn + M + bias, bias)
+        xd, Wd, bd = x.to(DEV), W.to(DEV), (b.to(DEV) if b is not None else None)
+        got = tensor_bits(lib.bf16_linear_with_plan(xd, Wd, bd, plan_=plan))
+        ref = tensor_bits(lib.bf16_linear_with_plan(xd, Wd, bd, plan_=base))
+        torch.cuda.synchronize()
+        check_close(got, oracle.linear_bf16(wl.bits(x), wl.bits(W), wl.bits(b)),
+                    f"tile BN={bn} M={M} N={N} K={K} stages={st} group={grp} bias={bias}")
+        assert np.array_equal(got, ref)
+    assert lib.device_status() == 0
+
+
+SWAP_CASES = [
+    # BN (tokens per tile), M, N, K, stages, raster group
+    (32, 17, 300, 520, 8, 0),       # one partial token tile, N tail inside a W tile, K tail
+    (64, 64, 2112, 7168, 8, 0),     # decode M = 64: one token tile, 16.5 W tiles
+    (64, 100, 1000, 136, 6, 1),     # two token tiles (the second partial), raster one token tile at a time
+    (128, 200, 257, 72, 5, 0),      # one W row past a tile
+    (192, 256, 14336, 1024, 5, 0),  # MLP-like N: 112 W tiles, 2 token tiles, more tiles than SMs
+    (256, 256, 520, 4096, 4, 0),    # MLP M = 256 in one token tile
+    (256, 40, 384, 2880, 3, 2),     # tokens far fewer than the tile: TMA zero fill past M
+]
+
+
+@pytest.mark.parametrize("case", SWAP_CASES, ids=lambda c: "x".join(map(str, c)))
+def test_tile_swap_ab(lib, case):
+    """The swap-AB form (W rows on the MMA M side, tokens on N) against the oracle, bias on and off;
+    its fp32 epilogue rounds to its bf16 epilogue bit for bit."""
+    bn, M, N, K, st, grp = case
+    plan = lib.make_plan("tile_t", threads=192, rows_per_cta=128, tokens_per_cta=bn, stages=st, split_k=grp)
+    sampled = M * N * K > 2e9
+    for bias in (False, True):
+        x, W, b = wl.make_inputs(M, N, K, 3 * bn + M + bias, bias)
+        xd, Wd, bd = x.to(DEV), W.to(DEV), (b.to(DEV) if b is not None else None)
+        out = lib.bf16_linear_with_plan(xd, Wd, bd, plan_=plan)
+        f32 = lib.bf16_linear_f32out(xd, Wd, bd, plan_=plan)
+        torch.cuda.synchronize()
+        got = tensor_bits(out)
+        assert np.array_equal(tensor_bits(f32.to(torch.bfloat16)), got)
+        if sampled:
+            rows = sorted({0, M // 2, M - 1})
+            want = oracle.linear_rows_bf16(wl.bits(x), wl.bits(W), wl.bits(b), np.array(rows, dtype=np.int64))
+            check_close(got[rows], want, f"tile_t BN={bn} M={M} N={N} K={K} rows={rows}")
+        else:
+            check_close(got, oracle.linear_bf16(wl.bits(x), wl.bits(W), wl.bits(b)),
+                        f"tile_t BN={bn} M={M} N={N} K={K} stages={st} bias={bias}")
+    assert lib.device_status() == 0
+
+
+def test_tile_swap_ab_exact_cases(lib):
+    """One-hot token rows reproduce W^T bit for bit and x = 0 gives the bias, through the transposed
+    epilogue (a swapped index would put W[n, k] at the wrong output)."""
+    M, N, K = 48, 320, 256
+    plan = lib.make_plan("tile_t", threads=192, rows_per_cta=128, tokens_per_cta=64, stages=4)
+    _, W, b = wl.make_inputs(1, N, K, 9, True)
+    x = torch.zeros(M, K, dtype=torch.bfloat16)
+    ks = [(7 * m + 3) % K for m in range(M)]
+    for m, k in enumerate(ks):
+        x[m, k] = 1.0
+    out = tensor_bits(lib.bf16_linear_with_plan(x.to(DEV), W.to(DEV), None, plan_=plan))
+    want = tensor_bits(W[:, ks].t().contiguous())
+    assert np.array_equal(out, want)
+    zero = tensor_bits(lib.bf16_linear_with_plan(torch.zeros(M, K, dtype=torch.bfloat16, device=DEV), W.to(DEV),
+                                                 b.to(DEV), plan_=plan))
+    assert np.array_equal(zero, np.broadcast_to(tensor_bits(b), (M, N)))
