@@ -25,6 +25,12 @@ decoding from the format definition, the static quantisation of the page's
 kernel (binary32 reciprocal and product, clamp to +-448, round to nearest
 even), and the FP8 linear (exact f64 sum of e4m3 products, times both scales,
 plus bias, one rounding to bf16).  e4m3 codes cross the boundary as uint8.
+
+MXFP8 (oracle.c, third part; the sglang PR #34042 page, read as the OCP
+microscaling format): 32-element blocks along K sharing one E8M0 scale byte,
+the block quantisation (scale exponent floor(log2 max|v|) - 8, elements
+rounded to nearest even e4m3 with saturation), and the block-scaled linear
+(exact f64 terms summed in ascending k, plus bias, one rounding to bf16).
 """
 from __future__ import annotations
 
@@ -96,9 +102,17 @@ class Oracle:
         lib.oracle_linear_fp8.argtypes = [_u8p, _u8p, ctypes.c_float, ctypes.c_float, opt, _i64, _i64, _i64, _u16p]
         lib.oracle_linear_fp8_f64.argtypes = [_u8p, _u8p, ctypes.c_float, ctypes.c_float, opt, _i64, _i64, _i64,
                                               _f64p]
+        lib.oracle_e8m0_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_e8m0_to_f64.restype = ctypes.c_double
+        lib.oracle_quant_mxfp8.argtypes = [_u16p, _i64, _i64, _u8p, _u8p]
+        lib.oracle_linear_mxfp8.argtypes = [_u8p, _u8p, _u8p, _u8p, opt, _i64, _i64, _i64, _u16p]
+        lib.oracle_linear_mxfp8_f64.argtypes = [_u8p, _u8p, _u8p, _u8p, opt, _i64, _i64, _i64, _f64p]
+        lib.oracle_linear_rows_mxfp8.argtypes = [_u8p, _u8p, _u8p, _u8p, opt, _i64, _i64, _i64, _i64p, _i64,
+                                                 _u16p]
         for fn in ("oracle_linear_f64", "oracle_linear_bf16", "oracle_linear_f32",
                    "oracle_linear_rows_bf16", "oracle_linear_rows_f64", "oracle_quant_fp8",
-                   "oracle_linear_fp8", "oracle_linear_fp8_f64"):
+                   "oracle_linear_fp8", "oracle_linear_fp8_f64", "oracle_quant_mxfp8",
+                   "oracle_linear_mxfp8", "oracle_linear_mxfp8_f64", "oracle_linear_rows_mxfp8"):
             getattr(lib, fn).restype = None
         self.lib = lib
         self.path = lib_path
@@ -208,6 +222,57 @@ class Oracle:
         self.lib.oracle_linear_fp8_f64(xq, wq, float(sx), float(sw), _bias_ptr(bias), M, N, K, out)
         return out
 
+    # ---- MXFP8: e4m3 codes (uint8) with one E8M0 scale byte per 32 elements along K ----
+
+    def e8m0_to_f64(self, scales) -> np.ndarray:
+        """Exact value 2^(e - 127) of each E8M0 scale byte (NaN for 255)."""
+        c = np.asarray(scales, dtype=np.uint8).ravel()
+        f = self.lib.oracle_e8m0_to_f64
+        return np.array([f(int(v)) for v in c], dtype=np.float64)
+
+    def quant_mxfp8(self, x):
+        """MXFP8 quantisation of bf16 bits x[rows, K] (K % 32 == 0): (codes[rows, K], scales[rows, K/32])."""
+        x = np.ascontiguousarray(x, dtype=np.uint16)
+        if x.ndim != 2 or x.shape[1] % 32:
+            raise ValueError(f"x shape {x.shape}: need [rows, K] with K % 32 == 0")
+        rows, K = x.shape
+        q = np.empty((rows, K), dtype=np.uint8)
+        s = np.empty((rows, K // 32), dtype=np.uint8)
+        self.lib.oracle_quant_mxfp8(x.reshape(-1), rows, K, q.reshape(-1), s.reshape(-1))
+        return q, s
+
+    def _mx_prep(self, xq, sx, wq, sw, bias):
+        xq, wq, bias, M, N, K = self._fp8_prep(xq, wq, bias)
+        if K % 32:
+            raise ValueError(f"K = {K}: need K % 32 == 0")
+        sx = np.ascontiguousarray(sx, dtype=np.uint8)
+        sw = np.ascontiguousarray(sw, dtype=np.uint8)
+        if sx.shape != (M, K // 32) or sw.shape != (N, K // 32):
+            raise ValueError(f"scale shapes {sx.shape}, {sw.shape}: need ({M}, {K // 32}), ({N}, {K // 32})")
+        return xq, sx, wq, sw, bias, M, N, K
+
+    def linear_mxfp8(self, xq, sx, wq, sw, bias=None) -> np.ndarray:
+        """bf16 bits of the MXFP8 linear (block-scaled e4m3 operands, bias, one rounding)."""
+        xq, sx, wq, sw, bias, M, N, K = self._mx_prep(xq, sx, wq, sw, bias)
+        out = np.empty((M, N), dtype=np.uint16)
+        self.lib.oracle_linear_mxfp8(xq, sx, wq, sw, _bias_ptr(bias), M, N, K, out)
+        return out
+
+    def linear_mxfp8_f64(self, xq, sx, wq, sw, bias=None) -> np.ndarray:
+        """The unrounded MXFP8 result (f64)."""
+        xq, sx, wq, sw, bias, M, N, K = self._mx_prep(xq, sx, wq, sw, bias)
+        out = np.empty((M, N), dtype=np.float64)
+        self.lib.oracle_linear_mxfp8_f64(xq, sx, wq, sw, _bias_ptr(bias), M, N, K, out)
+        return out
+
+    def linear_rows_mxfp8(self, xq, sx, wq, sw, bias, rows) -> np.ndarray:
+        """bf16 bits of the selected output rows of the MXFP8 linear."""
+        xq, sx, wq, sw, bias, M, N, K = self._mx_prep(xq, sx, wq, sw, bias)
+        rows = _rows(rows, M)
+        out = np.empty((rows.size, N), dtype=np.uint16)
+        self.lib.oracle_linear_rows_mxfp8(xq, sx, wq, sw, _bias_ptr(bias), M, N, K, rows, rows.size, out)
+        return out
+
 
 def _prep(x, W, bias):
     x = np.ascontiguousarray(x, dtype=np.uint16)
@@ -297,3 +362,23 @@ def linear_fp8(xq, wq, sx, sw, bias=None):
 
 def linear_fp8_f64(xq, wq, sx, sw, bias=None):
     return default().linear_fp8_f64(xq, wq, sx, sw, bias)
+
+
+def e8m0_to_f64(scales):
+    return default().e8m0_to_f64(scales)
+
+
+def quant_mxfp8(x):
+    return default().quant_mxfp8(x)
+
+
+def linear_mxfp8(xq, sx, wq, sw, bias=None):
+    return default().linear_mxfp8(xq, sx, wq, sw, bias)
+
+
+def linear_mxfp8_f64(xq, sx, wq, sw, bias=None):
+    return default().linear_mxfp8_f64(xq, sx, wq, sw, bias)
+
+
+def linear_rows_mxfp8(xq, sx, wq, sw, bias, rows):
+    return default().linear_rows_mxfp8(xq, sx, wq, sw, bias, rows)

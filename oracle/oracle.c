@@ -285,3 +285,125 @@ void oracle_linear_fp8(const uint8_t *xq, const uint8_t *wq, float sx, float sw,
         for (int64_t n = 0; n < N; ++n)
             out[m * N + n] = oracle_rne_bf16(dot_row_fp8(xq + m * K, wq + n * K, sxw, bias, n, K));
 }
+
+/*
+ * ---------------------------------------------------------------------------
+ * MXFP8 linear (the scope's MXFP8 row).
+ *
+ * Source: the sglang PR #34042 page ("执行摘要", "实现拆解" items 2-3): a dense
+ * MXFP8 GEMM on SM10x whose weights carry block scales (weight_scale_inv, fed
+ * to the kernel in a swizzled layout), with activations quantised the same
+ * way.  The page does not spell the format out.  Reading (also in the design
+ * notes): the OCP microscaling format MXFP8 -- each run of 32 consecutive
+ * elements along K shares one E8M0 scale byte e (value 2^(e - 127), e = 255
+ * is NaN and never produced), the elements are e4m3 codes as above; a block's
+ * value is scale x element.  Scales are stored plainly, row-major [rows][K/32]
+ * (the swizzle is a layout for the hardware, not arithmetic).
+ *
+ * Quantisation of one block of bf16 values v (the OCP conversion):
+ *   s = floor(log2(max |v|)) - 8   (8: the exponent of e4m3's largest binade),
+ *   clamped below at -127 (an all-zero block gets s = -127), e = s + 127,
+ *   code_i = e4m3 of v_i * 2^-s, rounded to nearest even, values past 448
+ *   saturating to +-448.
+ * The linear: out[m,n] = RNE_bf16( sum_k e4m3(xq[m,k]) e4m3(wq[n,k])
+ *   * 2^(sx[m][k/32]-127) * 2^(sw[n][k/32]-127) + bias[n] ), every term exact
+ *   in f64 and summed in ascending k.
+ * ---------------------------------------------------------------------------
+ */
+static double pow2_exact(int e)
+{
+    double v = 1.0;
+    for (int i = 0; i < e; ++i) v *= 2.0;
+    for (int i = e; i < 0; ++i) v *= 0.5;
+    return v;
+}
+
+double oracle_e8m0_to_f64(uint8_t e)
+{
+    if (e == 255) {
+        uint64_t qnan = 0x7FF8000000000000ULL;
+        double v;
+        memcpy(&v, &qnan, sizeof v);
+        return v;
+    }
+    return pow2_exact((int)e - 127);
+}
+
+/* x[rows][K] bf16, K % 32 == 0 -> q[rows][K] e4m3 codes, scales[rows][K/32] E8M0. */
+void oracle_quant_mxfp8(const uint16_t *x, int64_t rows, int64_t K, uint8_t *q, uint8_t *scales)
+{
+    const int64_t nb = K / 32;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < nb; ++b) {
+            const uint16_t *v = x + r * K + b * 32;
+            double amax = 0.0;
+            for (int i = 0; i < 32; ++i) {
+                const double f = bf16_to_f64(v[i]);
+                const double a = f < 0.0 ? -f : f;
+                if (a > amax) amax = a;
+            }
+            int s = -127;
+            if (amax > 0.0) {
+                uint64_t bits;
+                memcpy(&bits, &amax, sizeof bits);
+                const int lg = (int)((bits >> 52) & 0x7FF) - 1023; /* floor(log2(amax)): amax is an f64 normal */
+                s = lg - 8;
+                if (s < -127) s = -127;
+                if (s > 127) s = 127;
+            }
+            scales[r * nb + b] = (uint8_t)(s + 127);
+            const double inv = pow2_exact(-s);
+            for (int i = 0; i < 32; ++i) {
+                double y = bf16_to_f64(v[i]) * inv;             /* exact: a power of two */
+                if (y > 448.0) y = 448.0;
+                if (y < -448.0) y = -448.0;
+                q[r * K + b * 32 + i] = rne_e4m3(y);
+            }
+        }
+}
+
+static double dot_row_mxfp8(const uint8_t *xr, const uint8_t *xs, const uint8_t *wr, const uint8_t *ws,
+                            const uint16_t *bias, int64_t n, int64_t K)
+{
+    double acc = 0.0;
+    for (int64_t k = 0; k < K; ++k)
+        acc += e4m3_to_f64(xr[k]) * e4m3_to_f64(wr[k]) * pow2_exact((int)xs[k / 32] - 127) *
+               pow2_exact((int)ws[k / 32] - 127);
+    if (bias)
+        acc += bf16_to_f64(bias[n]);
+    return acc;
+}
+
+void oracle_linear_mxfp8_f64(const uint8_t *xq, const uint8_t *sx, const uint8_t *wq, const uint8_t *sw,
+                             const uint16_t *bias, int64_t M, int64_t N, int64_t K, double *acc)
+{
+    const int64_t nb = K / 32;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            acc[m * N + n] = dot_row_mxfp8(xq + m * K, sx + m * nb, wq + n * K, sw + n * nb, bias, n, K);
+}
+
+void oracle_linear_mxfp8(const uint8_t *xq, const uint8_t *sx, const uint8_t *wq, const uint8_t *sw,
+                         const uint16_t *bias, int64_t M, int64_t N, int64_t K, uint16_t *out)
+{
+    const int64_t nb = K / 32;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            out[m * N + n] =
+                oracle_rne_bf16(dot_row_mxfp8(xq + m * K, sx + m * nb, wq + n * K, sw + n * nb, bias, n, K));
+}
+
+/* Selected output rows of the MXFP8 linear (bf16 bits), for full-size checks on samples. */
+void oracle_linear_rows_mxfp8(const uint8_t *xq, const uint8_t *sx, const uint8_t *wq, const uint8_t *sw,
+                              const uint16_t *bias, int64_t M, int64_t N, int64_t K, const int64_t *rows,
+                              int64_t nrows, uint16_t *out)
+{
+    (void)M;
+    const int64_t nb = K / 32;
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t m = rows[r];
+        for (int64_t n = 0; n < N; ++n)
+            out[r * N + n] =
+                oracle_rne_bf16(dot_row_mxfp8(xq + m * K, sx + m * nb, wq + n * K, sw + n * nb, bias, n, K));
+    }
+}
