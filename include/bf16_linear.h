@@ -434,6 +434,52 @@ int bf16_linear_fp8_split(int M, int N, int K, int num_sms);
 int bf16_linear_probe_read(const void *src, size_t bytes, int grid, int threads, uint32_t *sink,
                            bf16l_stream_t stream);
 
+/*
+ * ---- MXFP8: block-scaled e4m3 ----
+ *
+ * Source: the sglang PR #34042 page ("执行摘要", "实现拆解" items 2-3): the dense
+ * MXFP8 GEMM on SM10x (weights with block scales, activations quantised the
+ * same way), whose small-batch decode kernels the page reports 2-5x faster.
+ * The page does not spell the format out; it is read as the OCP
+ * microscaling MXFP8 format: each run of 32 consecutive elements along K
+ * shares one E8M0 scale byte e (value 2^(e - 127)), the elements are e4m3
+ * codes (as for the per-tensor FP8 entry points).  Scales are row-major
+ * [rows][K / 32] bytes (no swizzle).
+ *
+ * bf16_quant_mxfp8 — quantise x[rows][K] (bf16, K % 32 == 0) into codes
+ *   xq[rows][K] and scales xs[rows][K / 32]: per block, s = floor(log2(max
+ *   |v|)) - 8 clamped below at -127 (an all-zero block gets s = -127),
+ *   xs = s + 127, xq = e4m3 of v * 2^-s rounded to nearest even, saturating
+ *   at +-448.  x and xq 16-byte aligned; no two buffers may overlap.
+ *   Asynchronous; BF16L_EINVAL (sizes, NULL, flags, overlap), BF16L_EALIGN,
+ *   BF16L_EUNSUPPORTED (K % 32 != 0), BF16L_EARCH, BF16L_ELAUNCH.
+ *
+ * bf16_linear_mxfp8 — out[M][N] (bf16) = RNE_bf16( sum over blocks b of
+ *   2^(xs[m][b]-127) * 2^(ws[n][b]-127) * sum_{k in b} e4m3(xq[m][k])
+ *   e4m3(wq[n][k]) (+ bias[n]) ), fp32 accumulation, bias before the one
+ *   rounding.  xq[M][K], wq[N][K] codes and xs[M][K/32], ws[N][K/32] scales
+ *   as above; K % 32 == 0 (else BF16L_EUNSUPPORTED); xq, wq, out and bias
+ *   16-byte aligned; out must not overlap the inputs.  Any M (groups of 16
+ *   tokens); warp-level e4m3 MMAs, one per scale block, K split over a
+ *   cluster; launches one kernel, allocates nothing.  Block-scale products
+ *   2^(xs+ws-254) outside the fp32 range are not supported (quantised data
+ *   stays far inside it).
+ *
+ * bf16_linear_mxfp8_with_plan — the same with an explicit plan: kernel
+ *   BF16L_KERNEL_DOTMMA, threads 128 or 256, split_k 1, 2, 4, 8 or 16 (at
+ *   most K / 32), flags; threads == 0 means the entry point's own choice
+ *   (bf16_linear_mxfp8_split).  BF16L_EINVAL for any other plan.
+ *
+ * bf16_linear_mxfp8_split — the K split the entry point uses with `threads`
+ *   threads per CTA on a device with num_sms SMs (pure host logic).
+ */
+int bf16_quant_mxfp8(const void *x, int64_t rows, int K, void *xq, void *xs, uint32_t flags, bf16l_stream_t stream);
+int bf16_linear_mxfp8(const void *xq, const void *xs, const void *wq, const void *ws, const void *bias, void *out,
+                      int M, int N, int K, uint32_t flags, bf16l_stream_t stream);
+int bf16_linear_mxfp8_with_plan(const void *xq, const void *xs, const void *wq, const void *ws, const void *bias,
+                                void *out, int M, int N, int K, const bf16l_plan *plan, bf16l_stream_t stream);
+int bf16_linear_mxfp8_split(int M, int N, int K, int threads, int num_sms);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *bf16_linear_strerror(int status);
 

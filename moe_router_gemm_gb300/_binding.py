@@ -115,6 +115,14 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.bf16_linear_fp8_with_plan.restype = i32
         lib.bf16_linear_fp8_split.argtypes = [i32, i32, i32, i32]
         lib.bf16_linear_fp8_split.restype = i32
+        lib.bf16_quant_mxfp8.argtypes = [vp, ctypes.c_int64, i32, vp, vp, ctypes.c_uint32, vp]
+        lib.bf16_quant_mxfp8.restype = i32
+        lib.bf16_linear_mxfp8.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, ctypes.c_uint32, vp]
+        lib.bf16_linear_mxfp8.restype = i32
+        lib.bf16_linear_mxfp8_with_plan.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, ctypes.POINTER(Plan), vp]
+        lib.bf16_linear_mxfp8_with_plan.restype = i32
+        lib.bf16_linear_mxfp8_split.argtypes = [i32, i32, i32, i32, i32]
+        lib.bf16_linear_mxfp8_split.restype = i32
         lib.bf16_linear_probe_read.argtypes = [vp, ctypes.c_size_t, i32, i32, vp, vp]
         lib.bf16_linear_probe_read.restype = i32
         lib.bf16_linear_noalloc_scratch_bytes.argtypes = []
@@ -429,6 +437,58 @@ def bf16_linear_fp8(xq, wq, scale_x, scale_w, bias=None, out=None, flags: int = 
     if st != OK:
         _raise(st, f"bf16_linear_fp8(M={M}, N={N}, K={K})")
     return out
+
+
+def quant_mxfp8(x, out=None, scales=None, flags: int = 0, stream=None):
+    """MXFP8 quantisation (bf16_quant_mxfp8) of a contiguous bf16 CUDA tensor x[rows, K], K % 32 == 0:
+    returns (codes uint8 [rows, K], scales uint8 [rows, K / 32])."""
+    import torch
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D bf16 CUDA tensor")
+    rows, K = x.shape
+    if out is None:
+        out = torch.empty((rows, K), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((rows, max(1, K // 32)), dtype=torch.uint8, device=x.device)
+    with torch.cuda.device(x.device):
+        st = load().bf16_quant_mxfp8(_ptr(x), rows, K, _ptr(out), _ptr(scales), int(flags),
+                                     _stream_handle(stream, x.device))
+    if st != OK:
+        _raise(st, f"bf16_quant_mxfp8(rows={rows}, K={K})")
+    return out, scales
+
+
+def bf16_linear_mxfp8(xq, xs, wq, ws, bias=None, out=None, flags: int = 0, stream=None, plan_: Plan | None = None):
+    """MXFP8 linear (bf16_linear_mxfp8): e4m3 codes xq[M,K], wq[N,K] (uint8) with E8M0 block scales
+    xs[M,K/32], ws[N,K/32] (uint8), optional bf16 bias[N]; bf16 out[M,N]."""
+    import torch
+    for name, t in (("xq", xq), ("wq", wq), ("xs", xs), ("ws", ws)):
+        if t.dtype != torch.uint8 or t.dim() != 2 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 2-D uint8 CUDA tensor")
+    M, K = xq.shape
+    N = wq.shape[0]
+    if wq.shape[1] != K or tuple(xs.shape) != (M, K // 32) or tuple(ws.shape) != (N, K // 32):
+        raise ValueError(f"shapes xq{tuple(xq.shape)} xs{tuple(xs.shape)} wq{tuple(wq.shape)} ws{tuple(ws.shape)}")
+    if bias is not None and (bias.dtype != torch.bfloat16 or tuple(bias.shape) != (N,) or not bias.is_cuda):
+        raise ValueError(f"bias must be a bf16 CUDA tensor of shape ({N},)")
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=xq.device)
+    with torch.cuda.device(xq.device):
+        h = _stream_handle(stream, xq.device)
+        if plan_ is None:
+            st = load().bf16_linear_mxfp8(_ptr(xq), _ptr(xs), _ptr(wq), _ptr(ws), _ptr(bias), _ptr(out), M, N, K,
+                                          int(flags), h)
+        else:
+            st = load().bf16_linear_mxfp8_with_plan(_ptr(xq), _ptr(xs), _ptr(wq), _ptr(ws), _ptr(bias), _ptr(out),
+                                                    M, N, K, ctypes.byref(plan_), h)
+    if st != OK:
+        _raise(st, f"bf16_linear_mxfp8(M={M}, N={N}, K={K})")
+    return out
+
+
+def mxfp8_split(M: int, N: int, K: int, threads: int = 128, num_sms: int = 152) -> int:
+    """The K split bf16_linear_mxfp8 uses (host logic, no GPU)."""
+    return int(load().bf16_linear_mxfp8_split(M, N, K, threads, num_sms))
 
 
 def fp8_split(M: int, N: int, K: int, num_sms: int = 152) -> int:

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libbf16_linear.so")
 
-SOURCES = ["api.cu", "plan.cpp", "dotprod.cu", "dotprod_f32.cu", "splitk.cu", "tile.cu", "tile_t.cu", "stream.cu", "noalloc.cu", "tile2.cu", "warprow.cu", "warpmma.cu", "warpmma_ks.cu", "dotmma.cu", "fp8.cu", "probe.cu"]
+SOURCES = ["api.cu", "plan.cpp", "dotprod.cu", "dotprod_f32.cu", "splitk.cu", "tile.cu", "tile_t.cu", "stream.cu", "noalloc.cu", "tile2.cu", "warprow.cu", "warpmma.cu", "warpmma_ks.cu", "dotmma.cu", "fp8.cu", "mxfp8.cu", "probe.cu"]
 HEADERS = ["common.cuh", "kernels.h", "dotprod.cuh", "tile.cuh", "dispatch_table.inc"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")

@@ -64,6 +64,7 @@ void init_device(DeviceState &s) {
         if (!e) e = init_warpmma();
         if (!e) e = init_warpmma_ks();
         if (!e) e = init_dotmma();
+        if (!e) e = init_mxfp8();
     }
     s.err = e;
 }
@@ -442,6 +443,81 @@ extern "C" int bf16_quant_fp8(const void *x, const float *scale, void *xq, int64
         return BF16L_ELAUNCH;
     }
     return BF16L_OK;
+}
+
+// ---- MXFP8 ----
+
+extern "C" int bf16_linear_mxfp8_split(int M, int N, int K, int threads, int num_sms) {
+    return bf16l::mxfp8_split(M, N, K, threads, num_sms);
+}
+
+extern "C" int bf16_quant_mxfp8(const void *x, int64_t rows, int K, void *xq, void *xs, uint32_t flags,
+                                bf16l_stream_t stream) {
+    using namespace bf16l;
+    if (rows < 0 || K <= 0 || !flags_valid(flags)) return BF16L_EINVAL;
+    if (K % 32 != 0) return BF16L_EUNSUPPORTED;
+    if (rows == 0) return BF16L_OK;
+    if (!x || !xq || !xs) return BF16L_EINVAL;
+    if (misaligned(x) || misaligned(xq)) return BF16L_EALIGN;
+    const uint64_t n = (uint64_t)rows * (uint64_t)K;
+    if (n > (1ull << 40)) return BF16L_EINVAL;
+    if (overlaps(xq, n, x, 2 * n) || overlaps(xs, n / 32, x, 2 * n) || overlaps(xs, n / 32, xq, n))
+        return BF16L_EINVAL;
+    DeviceState *ds = nullptr;
+    const int st = current_device(&ds);
+    if (st != BF16L_OK) return st;
+    const int e = launch_quant_mxfp8(x, xq, xs, (long long)n, ds->dev.num_sms, flags, stream);
+    if (e) {
+        note(e);
+        return BF16L_ELAUNCH;
+    }
+    return BF16L_OK;
+}
+
+extern "C" int bf16_linear_mxfp8_with_plan(const void *xq, const void *xs, const void *wq, const void *ws,
+                                           const void *bias, void *out, int M, int N, int K, const bf16l_plan *plan,
+                                           bf16l_stream_t stream) {
+    using namespace bf16l;
+    if (!plan) return BF16L_EINVAL;
+    const uint32_t flags = (uint32_t)plan->flags;
+    if (M < 0 || N <= 0 || K <= 0 || !flags_valid(flags)) return BF16L_EINVAL;
+    if (K % 32 != 0) return BF16L_EUNSUPPORTED;  // whole 32-element scale blocks
+    if (M == 0) return BF16L_OK;
+    if (!xq || !xs || !wq || !ws || !out) return BF16L_EINVAL;
+    if (misaligned(xq) || misaligned(wq) || misaligned(out) || (bias && misaligned(bias))) return BF16L_EALIGN;
+    if ((N + 7) / 8 > 65535 || (M + 15) / 16 > 65535) return BF16L_EUNSUPPORTED;
+    const uint64_t ob = 2ull * (uint64_t)M * (uint64_t)N, nb = (uint64_t)(K / 32);
+    if (overlaps(out, ob, xq, (uint64_t)M * K) || overlaps(out, ob, wq, (uint64_t)N * K) ||
+        overlaps(out, ob, xs, (uint64_t)M * nb) || overlaps(out, ob, ws, (uint64_t)N * nb) ||
+        overlaps(out, ob, bias, bias ? 2ull * N : 0))
+        return BF16L_EINVAL;
+    int threads = plan->threads, S = plan->split_k;
+    if (plan->kernel != BF16L_KERNEL_DOTMMA) return BF16L_EINVAL;
+    if (threads == 0) {
+        threads = 128;
+        S = mxfp8_split(M, N, K, threads, kGb300Sms);
+    }
+    if ((threads != 128 && threads != 256) || (S != 1 && S != 2 && S != 4 && S != 8 && S != 16) || S > K / 32)
+        return BF16L_EINVAL;
+    DeviceState *ds = nullptr;
+    const int st = current_device(&ds);
+    if (st != BF16L_OK) return st;
+    if (plan->threads == 0) S = mxfp8_split(M, N, K, threads, ds->dev.num_sms);
+    const int e = launch_mxfp8(xq, xs, wq, ws, bias, out, M, N, K, S, threads, flags, stream, ds->status);
+    if (e) {
+        note(e);
+        return BF16L_ELAUNCH;
+    }
+    return BF16L_OK;
+}
+
+extern "C" int bf16_linear_mxfp8(const void *xq, const void *xs, const void *wq, const void *ws, const void *bias,
+                                 void *out, int M, int N, int K, uint32_t flags, bf16l_stream_t stream) {
+    bf16l_plan p = {};
+    p.kernel = BF16L_KERNEL_DOTMMA;
+    p.threads = 0;  // the entry point's own choice
+    p.flags = (int32_t)flags;
+    return bf16_linear_mxfp8_with_plan(xq, xs, wq, ws, bias, out, M, N, K, &p, stream);
 }
 
 extern "C" int bf16_linear_device_status(int32_t *status, int clear) {

@@ -177,6 +177,13 @@ int launch_tile_fp8(const void *xq, const void *wq, const float *sx, const float
                     int M, int N, int K, int stages, int grid, uint32_t flags, void *stream, int32_t *status);
 int launch_quant_fp8(const void *x, const float *scale, void *q, long long n, int num_sms, uint32_t flags,
                      void *stream);
+// MXFP8 (mxfp8.cu): block quantisation (n values, n % 32 == 0) and the block-scaled linear on warp-level
+// e4m3 MMAs (K % 32 == 0; grid.z covers any M in groups of 16 tokens; S: CTAs per cluster along K, 1..16).
+int init_mxfp8();
+int mxfp8_split(int M, int N, int K, int threads, int num_sms);
+int launch_quant_mxfp8(const void *x, void *q, void *scales, long long n, int num_sms, uint32_t flags, void *stream);
+int launch_mxfp8(const void *xq, const void *xs, const void *wq, const void *ws, const void *bias, void *out, int M,
+                 int N, int K, int S, int threads, uint32_t flags, void *stream, int32_t *status);
 
 // One-time per-device kernel attribute setup (dynamic shared memory limits,
 // non-portable cluster sizes).  Returns a cudaError_t value.

@@ -389,3 +389,24 @@ def test_launch_flags_validated_without_gpu(lib):
     p.flags = lib.FLAG_PDL | lib.FLAG_SERIAL
     with pytest.raises(lib.BF16LinearError):
         lib.plan_check(4, 256, 2048, p)
+
+
+def test_mxfp8_validation_and_split_without_gpu(lib):
+    import ctypes as C
+    L = lib.load()
+    A, S1, B, S2, O = (C.c_void_p(v) for v in (1 << 16, 1 << 18, 1 << 20, 1 << 22, 1 << 24))
+    f = L.bf16_linear_mxfp8
+    assert f(A, S1, B, S2, None, O, 4, 8, 80, 0, None) == -6        # K % 32 != 0
+    assert f(A, S1, B, S2, None, O, -1, 8, 64, 0, None) == -1
+    assert f(A, S1, B, S2, None, O, 4, 8, 64, 3, None) == -1         # PDL with SERIAL
+    assert f(C.c_void_p((1 << 16) + 8), S1, B, S2, None, O, 4, 8, 64, 0, None) == -2
+    assert f(None, S1, B, S2, None, O, 4, 8, 64, 0, None) == -1
+    assert f(A, S1, B, S2, None, O, 0, 8, 64, 0, None) == 0          # M == 0: nothing to do
+    q = L.bf16_quant_mxfp8
+    assert q(A, 4, 48, B, S2, 0, None) == -6
+    assert q(A, -1, 64, B, S2, 0, None) == -1
+    assert q(A, 4, 64, C.c_void_p(1 << 16), S2, 0, None) == -1      # codes overlap the input
+    # the split: a power of two, at most 16, at least one scale block per warp
+    for M, N, K in [(1, 256, 7168), (16, 384, 7168), (8, 14336, 4096), (64, 2112, 7168), (3, 8, 64)]:
+        s = lib.mxfp8_split(M, N, K)
+        assert s in (1, 2, 4, 8, 16) and s * 4 <= max(4, K // 32)
