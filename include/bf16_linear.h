@@ -358,9 +358,11 @@ int bf16_linear_plan_ws(int M, int N, int K, const bf16l_device *dev, size_t wor
  * bf16_linear_cuda_error) and is tried again on the next call.  As every
  * entry point, it returns BF16L_EARCH on a device that is not a GB300,
  * before touching the device.
- * Each call clears the array's counters on `stream` before its launch.  All
- * calls share the one array, so calls that can overlap on the GPU (different
- * streams, or PDL) race and give wrong results; issue them on one stream.
+ * Each call clears the array's counters on `stream` before its launch (a
+ * memset, which starts only once everything before it on the stream has
+ * completed, so consecutive calls on one stream never overlap).  All calls
+ * share the one array, so calls on different streams that can run at the same
+ * time race and give wrong results; issue them on one stream.
  */
 int bf16_linear_noalloc(const void *x, const void *W, const void *bias, void *out,
                         int M, int N, int K, bf16l_stream_t stream);

@@ -550,6 +550,22 @@ __device__ __forceinline__ uint4 ldg_stream_v4(const void *p) {
 inline int pdl_attr_of(uint32_t flags) { return (flags & BF16L_FLAG_SERIAL) ? 0 : 1; }
 inline int w_early_of(uint32_t flags) { return (flags & BF16L_FLAG_PDL) ? 1 : 0; }
 
+// Ask L2 to fetch [p, p + bytes) (p 16-byte aligned, bytes a multiple of 16), in
+// requests of at most 64 KB.  No data comes back to the thread and nothing is
+// cached nearer than L2, the device's point of coherence for global memory: a
+// kernel may issue it for its weights before the grid-dependency wait, and a
+// write the previous kernel makes to them afterwards still reaches every load
+// issued after the wait.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    const char *c = static_cast<const char *>(p);
+    while (bytes) {
+        const uint32_t n = bytes < 65536u ? bytes : 65536u;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c), "r"(n) : "memory");
+        c += n;
+        bytes -= n;
+    }
+}
+
 // Programmatic dependent launch hooks (no-ops when the launch did not enable PDL).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {

@@ -78,7 +78,6 @@ __global__ void __launch_bounds__(kDmWarps * 32)
                   OutT *__restrict__ out, int M, int N, int RB, int S, int32_t *status, uint32_t *counters,
                   float4 *tiles, const float *__restrict__ scale_x, const float *__restrict__ scale_w,
                   int w_early) {
-    if (!w_early) pdl_wait();  // default launch: nothing is read before the previous kernel has finished
     constexpr int U = 8;  // K blocks (4 x 16 bytes across the lane quad) per lane per batch
     extern __shared__ uint4 xs[];
     __shared__ float4 part[kDmWarps][32];  // per warp, lane (g, t): tokens g, g+8 x rows 2t, 2t+1
@@ -105,6 +104,13 @@ __global__ void __launch_bounds__(kDmWarps * 32)
     const int wb1 = cb0 + mul_div(cb1 - cb0, warp + 1, nw);
     const int wv0 = 4 * wb0, wv1 = min(cv1, 4 * wb1);
     const int sv = cv1 - cv0;  // vectors in this CTA's x slice
+    if (!w_early) {
+        // Default launch: nothing is read before the previous kernel has finished.  Meanwhile this CTA's
+        // slice of its 8 rows is fetched into L2 (one request per row, by the first token group only).
+        if (blockIdx.z == 0 && tid < 8 && n0 + tid < N && sv > 0)
+            prefetch_l2(W + (size_t)(n0 + tid) * RB + (size_t)cv0 * 16, (uint32_t)sv * 16u);
+        pdl_wait();
+    }
     const bool tok_lo = g < M, tok_hi = HI && (g + 8 < M);
     const int row = n0 + g;
     const uint4 *wr = reinterpret_cast<const uint4 *>(W + (size_t)(row < N ? row : N - 1) * RB);

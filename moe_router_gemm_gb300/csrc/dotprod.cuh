@@ -69,7 +69,13 @@ __global__ void __launch_bounds__(256) dotprod_kernel(const uint16_t *__restrict
                                                       const uint16_t *__restrict__ bias,
                                                       OutT *__restrict__ out, int M, int N, int K,
                                                       int32_t *status, int w_early) {
-    if (!w_early) pdl_wait();  // default launch: nothing is read before the previous kernel has finished
+    if (!w_early) {
+        // Default launch: nothing is read before the previous kernel has finished.  Meanwhile this
+        // row slice's weights are fetched into L2 (one request per row; K % 8 == 0 for 16-byte rows).
+        if (blockIdx.y == 0 && (K & 7) == 0 && (int)threadIdx.x < R && (int)blockIdx.x * R + (int)threadIdx.x < N)
+            prefetch_l2(W + (size_t)((int)blockIdx.x * R + (int)threadIdx.x) * K, (uint32_t)K * 2u);
+        pdl_wait();
+    }
     constexpr int U = (VEC == 8) ? 8 : 4;  // vectors per row a thread loads before computing
     __shared__ float red[8][R * MT];
     __shared__ __align__(8) uint64_t xbar;

@@ -110,7 +110,6 @@ __global__ void __launch_bounds__(kMxWarps * 32)
     __shared__ float4 part[kMxWarps][32];
     __shared__ float4 recv[kMxMaxCluster][32];
     __shared__ __align__(8) uint64_t rbar;
-    if (!w_early) pdl_wait();  // default launch: nothing is read before the previous kernel has finished
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -128,6 +127,13 @@ __global__ void __launch_bounds__(kMxWarps * 32)
     const int n0 = 8 * (int)blockIdx.y;
     const int cb0 = mul_div(nb, rank, S), cb1 = mul_div(nb, rank + 1, S);
     const int b0 = cb0 + mul_div(cb1 - cb0, warp, nw), b1 = cb0 + mul_div(cb1 - cb0, warp + 1, nw);
+    if (!w_early) {
+        // Default launch: nothing is read before the previous kernel has finished.  Meanwhile this CTA's
+        // codes of its 8 rows are fetched into L2 (one request per row, by the first token group only).
+        if (blockIdx.z == 0 && tid < 8 && n0 + tid < N && cb1 > cb0)
+            prefetch_l2(wq + (size_t)(n0 + tid) * K + (size_t)cb0 * 32, (uint32_t)(cb1 - cb0) * 32u);
+        pdl_wait();
+    }
     const bool tok_lo = g < M, tok_hi = HI && (g + 8 < M);
     const int row = n0 + g;                                  // this lane's W row (B column g)
     const int na = n0 + 2 * t, nb1 = n0 + 2 * t + 1;         // this lane's accumulator columns

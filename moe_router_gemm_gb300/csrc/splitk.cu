@@ -120,7 +120,6 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
                   const uint16_t *__restrict__ bias, OutT *__restrict__ out, int M, int N, int K, int tokp,
                   int stages, int32_t *status, float *__restrict__ ws, uint32_t *__restrict__ counters,
                   int w_early) {
-    if (!w_early) pdl_wait();  // default launch: nothing is read before the previous kernel has finished
     constexpr uint32_t kIdesc = idesc_bf16_f32(kMmaM, BN);
     constexpr int kAcc = split_acc_count(BN);
     constexpr int kCols = kAcc * BN <= 32 ? 32 : kAcc * BN <= 64 ? 64 : kAcc * BN <= 128 ? 128 : 256;
@@ -146,6 +145,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     const int c_begin = mul_div(C, rank, S);
     const int nchunks = mul_div(C, rank + 1, S) - c_begin;
     const int first = nchunks < stages ? nchunks : stages;  // chunks whose weights go out at once
+    // Default launch: nothing is read before the previous kernel has finished.  (An L2 prefetch of the
+    // first ring's weight boxes here, as the CUDA-core kernels issue, measured 2-4% slower on the decode
+    // and MLP shapes this kernel serves.)
+    if (!w_early) pdl_wait();
 
     if (tid == 0) {
         tma_prefetch_desc(&tm_w);

@@ -49,7 +49,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     stream_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ W, const uint16_t *__restrict__ bias,
                   OutT *__restrict__ out, int M, int N, int K, int rg_unused, int stages, int32_t *status,
                   int w_early) {
-    if (!w_early) pdl_wait();  // default launch: nothing is read before the previous kernel has finished
+    if (!w_early) {
+        // Default launch: nothing is read before the previous kernel has finished.  Meanwhile the start of
+        // this CTA's contiguous row range is fetched into L2.
+        if (threadIdx.x == 0) {
+            const int p0 = mul_div(N, (int)blockIdx.x, (int)gridDim.x), p1 = mul_div(N, (int)blockIdx.x + 1, (int)gridDim.x);
+            const uint32_t bytes = (uint32_t)(p1 - p0) * (uint32_t)K * 2u;  // at most the first 64 KB
+            if (p1 > p0) prefetch_l2(W + (size_t)p0 * K, bytes < 65536u ? bytes : 65536u);
+        }
+        pdl_wait();
+    }
     constexpr int rg = RG;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);

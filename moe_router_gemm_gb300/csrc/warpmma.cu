@@ -57,7 +57,6 @@ __global__ void __launch_bounds__(NT, XR ? 1 : 1024 / NT)
     warpmma_kernel(const uint8_t *__restrict__ x, const uint8_t *__restrict__ W, const uint16_t *__restrict__ bias,
                    OutT *__restrict__ out, int M, int N, int RB, int32_t *status, const float *__restrict__ scale_x,
                    const float *__restrict__ scale_w, int w_early) {
-    if (!w_early) pdl_wait();  // default launch: nothing is read before the previous kernel has finished
     constexpr int U = 8 / NG;                      // K blocks (4 x 16 bytes across a lane quad) per lane per batch
     extern __shared__ uint4 xs[];                  // x[m] rows as 16-byte vectors, [M][RB / 16]
     __shared__ float part[WPR > 1 ? kWmMaxWarps : 1][32][4];  // WPR > 1: every lane's four sums
@@ -79,6 +78,16 @@ __global__ void __launch_bounds__(NT, XR ? 1 : 1024 / NT)
     const int G = (int)gridDim.x, b = (int)blockIdx.x;
     const int q0 = mul_div(RS, b, G), q1 = mul_div(RS, b + 1, G);
     const bool tok_lo = g < M, tok_hi = HI && (g + 8 < M);
+    if (!w_early) {
+        // Default launch: nothing is read before the previous kernel has finished.  Meanwhile the first
+        // 32 KB of this CTA's contiguous rows are fetched into L2.
+        if (tid == 0 && q1 > q0) {
+            const int p0 = 8 * NG * q0, p1 = min(N, 8 * NG * q1);
+            const uint32_t bytes = (uint32_t)(p1 - p0) * (uint32_t)RB;
+            if (p1 > p0) prefetch_l2(W + (size_t)p0 * RB, bytes < 32768u ? bytes : 32768u);
+        }
+        pdl_wait();
+    }
 
     if (tid == 0) {
         mbar_init(&xbar, 1);

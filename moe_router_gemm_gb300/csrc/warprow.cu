@@ -45,7 +45,16 @@ template <int MT, int WPR, int NT, typename OutT>
 __global__ void __launch_bounds__(NT, 1024 / NT)
     warprow_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ W, const uint16_t *__restrict__ bias,
                    OutT *__restrict__ out, int M, int N, int K, int32_t *status, int w_early) {
-    if (!w_early) pdl_wait();  // default launch: nothing is read before the previous kernel has finished
+    if (!w_early) {
+        // Default launch: nothing is read before the previous kernel has finished.  Meanwhile the first
+        // 32 KB of this CTA's contiguous row range are fetched into L2.
+        if (threadIdx.x == 0) {
+            const int p0 = mul_div(N, (int)blockIdx.x, (int)gridDim.x), p1 = mul_div(N, (int)blockIdx.x + 1, (int)gridDim.x);
+            const uint32_t bytes = (uint32_t)(p1 - p0) * (uint32_t)K * 2u;
+            if (p1 > p0) prefetch_l2(W + (size_t)p0 * K, bytes < 32768u ? bytes : 32768u);
+        }
+        pdl_wait();
+    }
     constexpr int U = 8;  // 16-byte weight vectors per lane per batch (128 KB in flight per SM)
     extern __shared__ uint4 xs[];          // x[m][k] as 16-byte vectors, [MT][K / 8]
     __shared__ float part[kWrMaxWarps][MT];
