@@ -70,7 +70,6 @@ template <int WPR, int NT, int TT, typename OutT>
 __global__ void __launch_bounds__(NT, TT == 1 ? 1024 / NT : 1)
     warpmma_ks_kernel(const uint8_t *__restrict__ x, const uint8_t *__restrict__ W, const uint16_t *__restrict__ bias,
                       OutT *__restrict__ out, int M, int N, int RB, int S, int32_t *status, int w_early) {
-    if (!w_early) pdl_wait();  // default launch: nothing is read before the previous kernel has finished
     constexpr int U = 8;  // K blocks (4 x 16 bytes across a lane quad) per lane per batch
     extern __shared__ __align__(16) uint8_t ks_smem[];
     __shared__ __align__(8) uint64_t xbar, rbar;
@@ -89,6 +88,14 @@ __global__ void __launch_bounds__(NT, TT == 1 ? 1024 / NT : 1)
     // this cluster's 8-row groups; rank r finishes local groups i with i % S == r
     const int RG = (N + 7) >> 3;
     const int q0 = mul_div(RG, c, C), q1 = mul_div(RG, c + 1, C);
+    if (!w_early) {
+        // Default launch: nothing is read before the previous kernel has finished.  Meanwhile this rank's
+        // K slice of the rows of its cluster's first 8-row group is fetched into L2 (one request a row).
+        const int row = 8 * q0 + tid;
+        if (tid < 8 && q1 > q0 && row < N && cv1 > 4 * cb0)
+            prefetch_l2(W + (size_t)row * RB + (size_t)cb0 * 64, (uint32_t)(cv1 - 4 * cb0) * 16u);
+        pdl_wait();
+    }
 
     uint4 wv[U];
     auto load_batch = [&](int n0, int vb) {  // the batch of blocks starting at vector vb
