@@ -538,8 +538,10 @@ def floor_record(shapes, lib, device, stream, replays):
         return 1000.0 * statistics.median([a.elapsed_time(b) for a, b in ms]) / n
 
     n_empty = 256
-    launch_us = graph_us([lambda: lib.probe_read(None, 152, 32, sink, stream=stream)] * n_empty, n_empty)
-    launch1_us = graph_us([lambda: lib.probe_read(None, 1, 32, sink, stream=stream)] * n_empty, n_empty)
+    ser = lib.FLAG_SERIAL
+    launch_us = graph_us([lambda: lib.probe_read(None, 152, 32, sink, stream=stream, flags=ser)] * n_empty, n_empty)
+    launch1_us = graph_us([lambda: lib.probe_read(None, 1, 32, sink, stream=stream, flags=ser)] * n_empty, n_empty)
+    launch_pdl_us = graph_us([lambda: lib.probe_read(None, 152, 32, sink, stream=stream)] * n_empty, n_empty)
     read = {}
     seen = set()
     for s in shapes:
@@ -547,20 +549,25 @@ def floor_record(shapes, lib, device, stream, replays):
         if key in seen:
             continue
         seen.add(key)
-        best = None
+        best, best_serial = None, None
         for grid, threads in FLOOR_CONFIGS:
-            calls = [(lambda w=w, g_=grid, t=threads: lib.probe_read(w, g_, t, sink, stream=stream)) for w in s.Ws]
-            us = graph_us(calls, len(calls))
-            if best is None or us < best[0]:
-                best = (us, grid, threads)
+            for flags in (0, ser):
+                calls = [(lambda w=w, g_=grid, t=threads, f=flags: lib.probe_read(w, g_, t, sink, stream=stream,
+                                                                                 flags=f)) for w in s.Ws]
+                us = graph_us(calls, len(calls))
+                if flags == 0 and (best is None or us < best[0]):
+                    best = (us, grid, threads)
+                if flags == ser and (best_serial is None or us < best_serial[0]):
+                    best_serial = (us, grid, threads)
         nbytes = 2 * s.N * s.K
         read[key] = {"us": round(best[0], 3), "weight_bytes": nbytes, "grid": best[1], "threads": best[2],
-                     "GBps": round(nbytes / (best[0] * 1e-6) / 1e9, 1)}
-    return {"note": "in-graph us per launch, L2-cold rotation as for the router calls: an empty kernel, and a "
-                    "read of each router weight with 16-byte loads and no arithmetic (best of the grid shapes "
-                    "tried); bf16_linear_probe_read",
+                     "GBps": round(nbytes / (best[0] * 1e-6) / 1e9, 1), "us_serial": round(best_serial[0], 3)}
+    return {"note": "in-graph us per launch, L2-cold rotation as for the router calls: an empty kernel (serial "
+                    "launches, and in the library's launch mode), and a read of each router weight with 16-byte "
+                    "loads and no arithmetic, launched as the library's kernels are (us) and serially "
+                    "(us_serial), best of the grid shapes tried; bf16_linear_probe_read",
             "empty_launch_us": round(launch_us, 3), "empty_launch_1cta_us": round(launch1_us, 3),
-            "read_weight": read}
+            "empty_launch_pdl_us": round(launch_pdl_us, 3), "read_weight": read}
 
 
 def forced_plan(lib, spec):
@@ -950,6 +957,62 @@ def fp8_arm(args, points):
                       "workload": workload_desc(args.workload), "shapes": res}))
 
 
+def mxfp8_arm(args, points):
+    """MXFP8 linear (bf16_linear_mxfp8) on the workload's shapes, L2-cold, beside the bf16 call.
+
+    x and W are quantised once on the device with the library's own bf16_quant_mxfp8; the weight
+    codes and scales are rotated over copies totalling >= 256 MB; one CUDA graph of R back-to-back
+    calls per shape; algorithmic bytes NK + N(K/32) + MK + M(K/32) + 2MN (+2N bias)."""
+    import moe_router_gemm_gb300 as lib
+    from moe_router_gemm_gb300 import build as _build
+    _build.build()
+    device = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.Stream(device)
+    peaks = load_peaks()
+    res = {}
+    for pt in points:
+        M, N, K, bias = pt["M"], pt["N"], pt["K"], pt["bias"]
+        if K % 32:
+            continue
+        x, W, b = wl.make_inputs(M, N, K, pt["seed"], bias)
+        xq, xs = lib.quant_mxfp8(x.to(device))
+        wq0, ws0 = lib.quant_mxfp8(W.to(device))
+        R = max(2, -(-L2_COLD_BYTES // (N * K)))
+        Wq = [wq0] + [wq0.clone() for _ in range(R - 1)]
+        Ws = [ws0] + [ws0.clone() for _ in range(R - 1)]
+        bd = b.to(device) if b is not None else None
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=device)
+        with torch.cuda.stream(stream):
+            for i in range(2):
+                lib.bf16_linear_mxfp8(xq, xs, Wq[i % R], Ws[i % R], bd, out=out, stream=stream)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(R):
+                    lib.bf16_linear_mxfp8(xq, xs, Wq[i], Ws[i], bd, out=out, stream=stream)
+            g.replay()
+            torch.cuda.synchronize()
+            ms = []
+            for _ in range(max(3, args.steps)):
+                a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g.replay()
+                e.record(stream)
+                torch.cuda.synchronize()
+                ms.append(a.elapsed_time(e))
+        us = 1000.0 * statistics.median(ms) / R
+        nbytes = N * K + N * (K // 32) + M * K + M * (K // 32) + 2 * M * N + (2 * N if bias else 0)
+        res[f"M{M}_N{N}_K{K}"] = {"us": round(us, 3), "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
+                                  "pct_hbm_roofline": round(100.0 * nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 1),
+                                  "split_k": lib.mxfp8_split(M, N, K)}
+        del Wq, Ws
+        torch.cuda.empty_cache()
+    mean = statistics.mean(v["us"] for v in res.values()) if res else None
+    print(json.dumps({"mode": "mxfp8", "metric": "MXFP8 linear us per call (L2-cold)",
+                      "mean_us": None if mean is None else round(mean, 4), "unit": "us/call",
+                      "workload": workload_desc(args.workload), "shapes": res}))
+
+
 # ---------------------------------------------------------------------------
 # main
 # ---------------------------------------------------------------------------
@@ -966,6 +1029,8 @@ def main():
     ap.add_argument("--sweep-fp8", action="store_true", help="with --fp8: also time every (split, threads)")
     ap.add_argument("--fp8", action="store_true",
                     help="time the per-tensor FP8 linear (bf16_linear_fp8) on the workload's shapes instead")
+    ap.add_argument("--mxfp8", action="store_true",
+                    help="time the MXFP8 linear (bf16_linear_mxfp8) on the workload's shapes instead")
     ap.add_argument("--pdl", action="store_true",
                     help="launch with programmatic dependent launch (BF16L_FLAG_PDL): back-to-back calls overlap")
     ap.add_argument("--no-pdl-variant", action="store_true",
@@ -1052,6 +1117,9 @@ def main():
         return
     if args.fp8:
         fp8_arm(args, points)
+        return
+    if args.mxfp8:
+        mxfp8_arm(args, points)
         return
     r = gpu_arm(args, points, rank, world)
     shapes, per_us = r["shapes"], r["per_shape_us"]

@@ -424,16 +424,18 @@ int bf16_linear_fp8_split(int M, int N, int K, int num_sms);
  * that read the `bytes` bytes at `src` once, with the 16-byte loads the
  * weight-streaming kernels use; CTA b XORs every 32-bit word it read into
  * sink[b] (sink: device uint32[grid], zeroed by the caller if it wants the
- * checksum, which is then the XOR of the grid words).
- * Nothing else is computed, so its time for a W-sized buffer is the floor of
- * any kernel that must read that weight, launched the same way; with
- * bytes == 0 it is an empty launch (src and sink may then be NULL), whose
- * time in a graph of back-to-back launches is the per-call launch cost.
- * bytes % 16 == 0, src 16-byte aligned, sink 4-byte aligned, 1 <= grid,
- * threads a multiple of 32 in 32..1024.  Asynchronous; returns BF16L_OK,
- * BF16L_EINVAL, BF16L_EALIGN, BF16L_EARCH or BF16L_ELAUNCH.
+ * checksum, which is then the XOR of the grid words).  Nothing else is
+ * computed, so its time for a W-sized buffer is the floor of any kernel that
+ * must read that weight, launched the same way: by default as the library's
+ * kernels are (programmatic dependent launch, each CTA's share prefetched into
+ * L2 before the grid-dependency wait), serially with BF16L_FLAG_SERIAL (the
+ * only flag it takes).  With bytes == 0 it is an empty launch (src and sink
+ * may then be NULL), whose time in a graph of back-to-back launches is the
+ * per-call launch cost.  bytes % 16 == 0, src 16-byte aligned, sink 4-byte
+ * aligned, 1 <= grid, threads a multiple of 32 in 32..1024.  Asynchronous;
+ * returns BF16L_OK, BF16L_EINVAL, BF16L_EALIGN, BF16L_EARCH or BF16L_ELAUNCH.
  */
-int bf16_linear_probe_read(const void *src, size_t bytes, int grid, int threads, uint32_t *sink,
+int bf16_linear_probe_read(const void *src, size_t bytes, int grid, int threads, uint32_t *sink, uint32_t flags,
                            bf16l_stream_t stream);
 
 /*

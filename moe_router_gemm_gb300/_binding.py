@@ -123,7 +123,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.bf16_linear_mxfp8_with_plan.restype = i32
         lib.bf16_linear_mxfp8_split.argtypes = [i32, i32, i32, i32, i32]
         lib.bf16_linear_mxfp8_split.restype = i32
-        lib.bf16_linear_probe_read.argtypes = [vp, ctypes.c_size_t, i32, i32, vp, vp]
+        lib.bf16_linear_probe_read.argtypes = [vp, ctypes.c_size_t, i32, i32, vp, ctypes.c_uint32, vp]
         lib.bf16_linear_probe_read.restype = i32
         lib.bf16_linear_noalloc_scratch_bytes.argtypes = []
         lib.bf16_linear_noalloc_scratch_bytes.restype = ctypes.c_size_t
@@ -496,16 +496,17 @@ def fp8_split(M: int, N: int, K: int, num_sms: int = 152) -> int:
     return int(load().bf16_linear_fp8_split(M, N, K, num_sms))
 
 
-def probe_read(src, grid: int, threads: int, sink, nbytes: int | None = None, stream=None):
+def probe_read(src, grid: int, threads: int, sink, nbytes: int | None = None, stream=None, flags: int = 0):
     """Launch the read-floor probe (bf16_linear_probe_read) over the bytes of the CUDA tensor `src`
     (the first nbytes of them, or none when src is None); CTA b XORs its checksum into sink[b] of the
-    int32 CUDA tensor `sink` (at least `grid` elements)."""
+    int32 CUDA tensor `sink` (at least `grid` elements).  flags: 0 (the library's launch mode) or
+    FLAG_SERIAL."""
     import torch
     if sink is not None and sink.numel() < grid:
         raise ValueError(f"sink needs {grid} elements, has {sink.numel()}")
     nb = 0 if src is None else (src.numel() * src.element_size() if nbytes is None else int(nbytes))
     dev = sink.device if sink is not None else torch.device("cuda", torch.cuda.current_device())
-    st = load().bf16_linear_probe_read(_ptr(src), nb, int(grid), int(threads), _ptr(sink),
+    st = load().bf16_linear_probe_read(_ptr(src), nb, int(grid), int(threads), _ptr(sink), int(flags),
                                        _stream_handle(stream, dev))
     if st != OK:
         _raise(st, f"bf16_linear_probe_read(bytes={nb}, grid={grid}, threads={threads})")

@@ -342,9 +342,11 @@ def test_probe_read_validates_before_touching_a_device(lib):
     import ctypes as C
     L = lib.load()
     for bytes_, grid, threads in [(17, 1, 32), (16, 0, 32), (16, 1, 48), (16, 1, 2048), (16, 1, 0)]:
-        assert L.bf16_linear_probe_read(C.c_void_p(4096), bytes_, grid, threads, C.c_void_p(8192), None) == -1
-    assert L.bf16_linear_probe_read(None, 16, 1, 32, C.c_void_p(8192), None) == -1   # NULL src with bytes
-    assert L.bf16_linear_probe_read(C.c_void_p(4104), 16, 1, 32, C.c_void_p(8192), None) == -2  # src misaligned
+        assert L.bf16_linear_probe_read(C.c_void_p(4096), bytes_, grid, threads, C.c_void_p(8192), 0, None) == -1
+    assert L.bf16_linear_probe_read(None, 16, 1, 32, C.c_void_p(8192), 0, None) == -1   # NULL src with bytes
+    assert L.bf16_linear_probe_read(C.c_void_p(4104), 16, 1, 32, C.c_void_p(8192), 0, None) == -2  # misaligned
+    for bad_flags in (1, 4):  # only the serial flag applies
+        assert L.bf16_linear_probe_read(C.c_void_p(4096), 16, 1, 32, C.c_void_p(8192), bad_flags, None) == -1
 
 
 def test_tile_tactic_space(lib):

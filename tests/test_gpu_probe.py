@@ -18,11 +18,12 @@ def test_probe_checksum(lib, nbytes, grid, threads):
     rng = np.random.default_rng(nbytes)
     host = rng.integers(0, 2 ** 32, size=nbytes // 4, dtype=np.uint64).astype(np.uint32)
     src = torch.from_numpy(host.view(np.int32)).to(DEV)
-    sink = torch.zeros(grid, dtype=torch.int32, device=DEV)
-    lib.probe_read(src, grid, threads, sink)
-    torch.cuda.synchronize()
     want = np.bitwise_xor.reduce(host)
-    assert int(np.bitwise_xor.reduce(sink.cpu().numpy().view(np.uint32))) == int(want)
+    for flags in (0, lib.FLAG_SERIAL):  # the library's launch mode (L2 prefetch, PDL) and serial
+        sink = torch.zeros(grid, dtype=torch.int32, device=DEV)
+        lib.probe_read(src, grid, threads, sink, flags=flags)
+        torch.cuda.synchronize()
+        assert int(np.bitwise_xor.reduce(sink.cpu().numpy().view(np.uint32))) == int(want)
 
 
 def test_probe_empty_launch(lib):
