@@ -463,16 +463,23 @@ int bf16_linear_probe_read(const void *src, size_t bytes, int grid, int threads,
  *   e4m3(wq[n][k]) (+ bias[n]) ), fp32 accumulation, bias before the one
  *   rounding.  xq[M][K], wq[N][K] codes and xs[M][K/32], ws[N][K/32] scales
  *   as above; K % 32 == 0 (else BF16L_EUNSUPPORTED); xq, wq, out and bias
- *   16-byte aligned; out must not overlap the inputs.  Any M (groups of 16
- *   tokens); warp-level e4m3 MMAs, one per scale block, K split over a
- *   cluster; launches one kernel, allocates nothing.  Block-scale products
- *   2^(xs+ws-254) outside the fp32 range are not supported (quantised data
+ *   16-byte aligned; out must not overlap the inputs.  Any M.  Small M:
+ *   warp-level e4m3 MMAs, one per scale block, K split over a cluster, in
+ *   groups of 16 tokens.  M > 16 with at least 32 tiles of 128 x 256 and
+ *   K % 128 == 0: the tcgen05 tile form, one block-scaled MMA
+ *   (kind::mxf8f6f4.block_scale) per scale block with the scales staged into
+ *   tensor memory (xs and ws 4-byte aligned, else BF16L_EALIGN).  Launches one
+ *   kernel, allocates nothing.  Block-scale products 2^(xs+ws-254) outside
+ *   the fp32 range are not supported by the warp-level form (quantised data
  *   stays far inside it).
  *
  * bf16_linear_mxfp8_with_plan — the same with an explicit plan: kernel
- *   BF16L_KERNEL_DOTMMA, threads 128 or 256, split_k 1, 2, 4, 8 or 16 (at
- *   most K / 32), flags; threads == 0 means the entry point's own choice
- *   (bf16_linear_mxfp8_split).  BF16L_EINVAL for any other plan.
+ *   BF16L_KERNEL_DOTMMA (the warp-level form: threads 128 or 256, split_k 1,
+ *   2, 4, 8 or 16, at most K / 32) or BF16L_KERNEL_TILE (the tile form:
+ *   threads 320, rows_per_cta = W rows per tile, 128 or 256, stages 2..6
+ *   for 128 and 2..4 for 256, split_k = raster group of W tiles, 0 = 8;
+ *   K % 128 == 0, else BF16L_EUNSUPPORTED), flags; threads == 0 means the
+ *   entry point's own choice.  BF16L_EINVAL for any other plan.
  *
  * bf16_linear_mxfp8_split — the K split the entry point uses with `threads`
  *   threads per CTA on a device with num_sms SMs (pure host logic).

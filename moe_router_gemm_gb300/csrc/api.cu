@@ -491,19 +491,47 @@ extern "C" int bf16_linear_mxfp8_with_plan(const void *xq, const void *xs, const
         overlaps(out, ob, xs, (uint64_t)M * nb) || overlaps(out, ob, ws, (uint64_t)N * nb) ||
         overlaps(out, ob, bias, bias ? 2ull * N : 0))
         return BF16L_EINVAL;
-    int threads = plan->threads, S = plan->split_k;
-    if (plan->kernel != BF16L_KERNEL_DOTMMA) return BF16L_EINVAL;
-    if (threads == 0) {
-        threads = 128;
-        S = mxfp8_split(M, N, K, threads, kGb300Sms);
+    int kernel = plan->kernel, threads = plan->threads, S = plan->split_k, stages = plan->stages;
+    int bq = plan->rows_per_cta;
+    if (threads == 0) {  // the entry point's own choice
+        const long long tiles256 = (long long)((M + 127) / 128) * ((N + 255) / 256);
+        if (M > 16 && K % 128 == 0 && tiles256 >= 32) {  // a dense contraction: the tcgen05 tile form
+            kernel = BF16L_KERNEL_TILE;
+            threads = kMxTileThreads;
+            bq = 256;
+            stages = mxtile_max_stages(bq);
+            S = 0;
+        } else {
+            kernel = BF16L_KERNEL_DOTMMA;
+            threads = 128;
+            S = mxfp8_split(M, N, K, threads, kGb300Sms);
+        }
     }
-    if ((threads != 128 && threads != 256) || (S != 1 && S != 2 && S != 4 && S != 8 && S != 16) || S > K / 32)
+    if (kernel == BF16L_KERNEL_TILE) {
+        // 128 x 128 tiles of whole 128-code chunks; scale rows read as 32-bit words (4-byte aligned)
+        if (K % 128 != 0) return BF16L_EUNSUPPORTED;
+        if (threads != kMxTileThreads || (bq != 128 && bq != 256) || stages < 2 || stages > mxtile_max_stages(bq) ||
+            S < 0 || S > 1024)
+            return BF16L_EINVAL;
+        if ((reinterpret_cast<uintptr_t>(xs) & 3u) || (reinterpret_cast<uintptr_t>(ws) & 3u)) return BF16L_EALIGN;
+    } else if (kernel == BF16L_KERNEL_DOTMMA) {
+        if ((threads != 128 && threads != 256) || (S != 1 && S != 2 && S != 4 && S != 8 && S != 16) || S > K / 32)
+            return BF16L_EINVAL;
+    } else {
         return BF16L_EINVAL;
+    }
     DeviceState *ds = nullptr;
     const int st = current_device(&ds);
     if (st != BF16L_OK) return st;
-    if (plan->threads == 0) S = mxfp8_split(M, N, K, threads, ds->dev.num_sms);
-    const int e = launch_mxfp8(xq, xs, wq, ws, bias, out, M, N, K, S, threads, flags, stream, ds->status);
+    int e = 0;
+    if (kernel == BF16L_KERNEL_TILE) {
+        const long long tiles = (long long)((M + 127) / 128) * ((N + bq - 1) / bq);
+        const int grid = (int)(tiles < ds->dev.num_sms ? tiles : ds->dev.num_sms);
+        e = launch_mxfp8_tile(xq, xs, wq, ws, bias, out, M, N, K, bq, stages, S, grid, flags, stream, ds->status);
+    } else {
+        if (plan->threads == 0) S = mxfp8_split(M, N, K, threads, ds->dev.num_sms);
+        e = launch_mxfp8(xq, xs, wq, ws, bias, out, M, N, K, S, threads, flags, stream, ds->status);
+    }
     if (e) {
         note(e);
         return BF16L_ELAUNCH;

@@ -32,7 +32,8 @@ enum WaitSite : int32_t {
     kSiteSelftest = 6,   // bf16_linear_selftest_wait
     kSiteRecv = 7,       // split-K owner waiting for its peers' partials
     kSiteStage = 8,      // dot-product CTA waiting for its copy of x
-    kSitePairTmem = 9    // the two CTAs of a pair got different TMEM addresses (gave up before any MMA)
+    kSitePairTmem = 9,   // the two CTAs of a pair got different TMEM addresses (gave up before any MMA)
+    kSiteScale = 10      // MXFP8 tile: scale-staging warps waiting for a free ring slot
 };
 
 // Default limit for one wait: 1 s of wall-clock time.
@@ -366,6 +367,41 @@ __device__ __forceinline__ void tmem_ld_wait16(uint32_t (&r)[16]) {
                    "+r"(r[14]), "+r"(r[15])
                  :
                  : "memory");
+}
+
+// 32 lanes x 32 bits, 4 consecutive columns from registers: thread t of the warp
+// writes lane (quarter base + t).  Complete before a later read once
+// tmem_st_wait() has returned.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b),
+                 "r"(c), "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Instruction descriptor of the block-scaled e4m3 MMA (kind::mxf8f6f4): A and B
+// e4m3 (format 0), K-major, N>>3 at bit 17, scale format E8M0 at bit 23, M>>4 at
+// bit 24; the byte of each 32-bit scale word to use (the scale factor id, 0..3)
+// at bits 4-5 for B and 29-30 for A.  D is fp32.
+__host__ __device__ constexpr uint32_t idesc_mxf8_f32(int mma_m, int mma_n, int sf_id) {
+    return ((uint32_t)sf_id << 4) | ((uint32_t)(mma_n >> 3) << 17) | (1u << 23) | ((uint32_t)(mma_m >> 4) << 24) |
+           ((uint32_t)sf_id << 29);
+}
+
+// One block-scaled e4m3 MMA, K = 32 codes (one scale block): D[tmem] (+)= (A * sA) (B * sB)^T.
+// Scale words in TMEM: for A row m, lane m of column sfa + m / 32; for B column
+// n, lane n % 32 of column sfb + n / 32, replicated in every lane quarter (the
+// quarter of the D row being computed is the one read).  The byte used is the
+// descriptor's scale factor id.  Keep sfa and sfb at columns that are
+// multiples of 4 (sfa at a multiple of 8): other columns fault the GPU.
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
 }
 
 // ---- CTA pairs (cta_group::2): two CTAs of a cluster share one MMA ----

@@ -184,6 +184,14 @@ int mxfp8_split(int M, int N, int K, int threads, int num_sms);
 int launch_quant_mxfp8(const void *x, void *q, void *scales, long long n, int num_sms, uint32_t flags, void *stream);
 int launch_mxfp8(const void *xq, const void *xs, const void *wq, const void *ws, const void *bias, void *out, int M,
                  int N, int K, int S, int threads, uint32_t flags, void *stream, int32_t *status);
+// The MXFP8 tile form (tcgen05 block-scaled MMAs): 128 x rows by bq (128 or 256) W rows per tile,
+// K % 128 == 0, 320 threads, 2 up to mxtile_max_stages(bq) stages, persistent grid of at most one CTA per
+// SM; group: raster group of W tiles (0 = 8).
+constexpr int kMxTileThreads = 320;
+int mxtile_max_stages(int bq);
+int launch_mxfp8_tile(const void *xq, const void *xs, const void *wq, const void *ws, const void *bias, void *out,
+                      int M, int N, int K, int bq, int stages, int group, int grid, uint32_t flags, void *stream,
+                      int32_t *status);
 
 // One-time per-device kernel attribute setup (dynamic shared memory limits,
 // non-portable cluster sizes).  Returns a cudaError_t value.

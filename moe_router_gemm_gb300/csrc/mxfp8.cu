@@ -37,7 +37,8 @@
 //     the bf16 router kernel.
 // The default launch waits for the previous kernel before any read; with
 // BF16L_FLAG_PDL the weight codes and scales of the first batch are loaded
-// before that wait.
+// before that wait.  For large M the tile form below (tcgen05 block-scaled
+// MMAs, scales in TMEM) takes over.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -243,6 +244,302 @@ __global__ void __launch_bounds__(kMxWarps * 32)
     if (clus) cluster_wait_acquire();  // phase 2 done: rank 0 holds every partial; all may exit
 }
 
+// ---------------------------------------------------------------------------
+// The tile form for large M: tcgen05.mma.kind::mxf8f6f4.block_scale, one
+// instruction per 32-code scale block, scales applied by the tensor core.
+//   * tile 128 x rows (MMA M) x BQ W rows (MMA N, 128 or 256); a stage is one
+//     128-code chunk of both operands (128-byte swizzle rows, TMA) = four
+//     scale blocks;
+//   * warp 0 loads the codes (TMA), warp 1 issues the MMAs and owns TMEM,
+//     warps 2-5 run the epilogue (TMEM lane = x row; bias, bf16 store), warps
+//     6-9 stage each chunk's scale words into TMEM ahead of the MMAs: the word
+//     of row r for chunk c is the four bytes xs[r][4c..4c+3] (k-blocks 0..3 of
+//     the chunk), so MMA step kk selects byte kk (the descriptor's scale id);
+//     the words of the next four chunks are always in flight;
+//   * TMEM: the accumulator (two BQ-column buffers for BQ = 128, one for 256,
+//     whose epilogue then runs between tiles), then one scale slot per ring
+//     stage at a column that is a multiple of 8 (the MMA takes scale addresses
+//     at aligned columns only).  The MMA reads A row m's word from lane m of
+//     column sfa + m / 32 and B row n's from lane n % 32 of column sfb + n / 32
+//     in the lane quarter of the D row it computes: a slot holds A's 4 columns
+//     (quarter q's words in column q) and then, from column 4 (BQ = 128) or 8
+//     (BQ = 256), B's BQ / 32 columns, written by all four scale warps (every
+//     quarter a copy).
+// ---------------------------------------------------------------------------
+constexpr int kMxtThreads = 320;
+constexpr int kMxtBP = 128, kMxtChunk = 128;  // codes per stage
+constexpr int kMxtMaxStages = 6;
+
+__host__ __device__ constexpr int mxt_stage_bytes(int bq) { return (kMxtBP + bq) * 128; }
+
+struct MxtShared {
+    uint64_t full[kMxtMaxStages];
+    uint64_t empty[kMxtMaxStages];
+    uint64_t sfull[kMxtMaxStages];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint32_t tmem_base;
+    int32_t aborted;
+    int32_t issued;
+    int32_t consumed;
+};
+
+__device__ __forceinline__ void mxt_coords(int t, int p_tiles, int q_tiles, int group, int bq, int &p0, int &q0) {
+    const int per_group = group * p_tiles;
+    const int g = t / per_group, r = t - g * per_group;
+    const int gq = (q_tiles - g * group) < group ? (q_tiles - g * group) : group;
+    const int pi = r / gq, qi = g * group + (r - pi * gq);
+    p0 = pi * kMxtBP;
+    q0 = qi * bq;
+}
+
+template <int BQ>
+__global__ void __launch_bounds__(kMxtThreads, 1)
+    mxtile_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                  const uint8_t *__restrict__ xs, const uint8_t *__restrict__ ws, const uint16_t *__restrict__ bias,
+                  uint16_t *__restrict__ out, int M, int N, int K, int stages, int group, int32_t *status) {
+    constexpr int kNbuf = BQ == 128 ? 2 : 1;          // accumulator buffers
+    constexpr int kBcols = BQ / 32;                   // B scale columns per ring slot
+    constexpr int kSlot = 4 + kBcols <= 8 ? 8 : 16;   // columns per slot (a multiple of 8)
+    constexpr int kBoff = kBcols <= 4 ? 4 : 8;        // B's columns within a slot (8-aligned when it has 8)
+    constexpr int kSf = kNbuf * BQ;                   // the scale slots start after the accumulators
+    constexpr int kStageBytes = mxt_stage_bytes(BQ);
+    static_assert(kSf + kMxtMaxStages * kSlot <= 512, "TMEM columns");
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    MxtShared &sh = *reinterpret_cast<MxtShared *>(ring + stages * kStageBytes);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int p_tiles = (M + kMxtBP - 1) / kMxtBP, q_tiles = (N + BQ - 1) / BQ;
+    const int num_tiles = p_tiles * q_tiles;
+    const int C = K / kMxtChunk;
+    const int nb = K >> 5;  // scale bytes per row
+    const int G = group > 0 ? group : 8;
+
+    if (tid == 0) {
+        tma_prefetch_desc(&tm_x);
+        tma_prefetch_desc(&tm_w);
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&sh.full[s], 1);
+            mbar_init(&sh.empty[s], 1);
+            mbar_init(&sh.sfull[s], 4);  // one arrival per scale warp
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sh.acc_full[b], 1);
+            mbar_init(&sh.acc_empty[b], 4);  // one arrival per epilogue warp
+        }
+        sh.aborted = 0;
+        sh.issued = 0;
+        sh.consumed = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&sh.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+    pdl_launch_dependents();
+
+    if (warp == 0) {
+        if (lane == 0) {  // ---- TMA producer: the codes ----
+            pdl_wait();
+            int it = 0;
+            for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+                int p0, q0;
+                mxt_coords(t, p_tiles, q_tiles, G, BQ, p0, q0);
+                for (int c = 0; c < C; ++c, ++it) {
+                    const int s = it % stages;
+                    if (it >= stages && !mbar_wait(&sh.empty[s], ((it / stages) - 1) & 1, status, kSiteEmpty)) {
+                        atomicExch(&sh.aborted, 1);
+                        goto producer_done;
+                    }
+                    if (*((volatile int32_t *)&sh.aborted)) goto producer_done;
+                    uint8_t *st = ring + s * kStageBytes;
+                    mbar_arrive_expect_tx(&sh.full[s], kStageBytes);
+                    tma_load_2d(st, &tm_x, &sh.full[s], c * kMxtChunk, p0);
+                    tma_load_2d(st + kMxtBP * 128, &tm_w, &sh.full[s], c * kMxtChunk, q0);
+                }
+            }
+        producer_done:
+            sh.issued = it;
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {  // ---- MMA issuer ----
+            int it = 0, tile_iter = 0;
+            for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tile_iter) {
+                sh.consumed = it;
+                const int b = tile_iter % kNbuf, use = tile_iter / kNbuf;
+                const uint32_t acc = tmem + (uint32_t)(b * BQ);
+                // wait for the epilogue to have drained this buffer (its previous use)
+                if (use >= 1 && !mbar_wait(&sh.acc_empty[b], (use - 1) & 1, status, kSiteTmemEmpty)) {
+                    atomicExch(&sh.aborted, 1);
+                    break;
+                }
+                tc_fence_after();
+                bool ok = true;
+                for (int c = 0; c < C; ++c, ++it) {
+                    const int s = it % stages;
+                    if (!mbar_wait(&sh.full[s], (it / stages) & 1, status, kSiteFull) ||
+                        !mbar_wait(&sh.sfull[s], (it / stages) & 1, status, kSiteFull)) {
+                        atomicExch(&sh.aborted, 1);
+                        sh.consumed = it;
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint8_t *st = ring + s * kStageBytes;
+                    const uint64_t adesc = smem_desc_sw128(smem_u32(st));
+                    const uint64_t bdesc = smem_desc_sw128(smem_u32(st + kMxtBP * 128));
+                    const uint32_t sfa = tmem + (uint32_t)(kSf + kSlot * s), sfb = sfa + kBoff;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)  // one 32-code scale block per MMA, its byte of the words
+                        mma_mxf8(acc, adesc + 2 * kk, bdesc + 2 * kk, idesc_mxf8_f32(kMxtBP, BQ, kk), sfa, sfb,
+                                 (c > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&sh.empty[s]);  // frees the codes and the scale slot
+                }
+                if (!ok) {
+                    mbar_arrive(&sh.acc_full[b]);
+                    break;
+                }
+                mma_commit(&sh.acc_full[b]);
+            }
+            sh.consumed = it;
+        }
+        __syncwarp();
+    } else if (warp < 6) {
+        // ---- epilogue: warps 2..5; TMEM lane quarter = warp % 4 ----
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        int tile_iter = 0;
+        const bool vec_ok = (N % 8) == 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tile_iter) {
+            int p0, q0;
+            mxt_coords(t, p_tiles, q_tiles, G, BQ, p0, q0);
+            const int b = tile_iter % kNbuf, use = tile_iter / kNbuf;
+            const bool ok = mbar_wait(&sh.acc_full[b], use & 1, status, kSiteAccum);
+            tc_fence_after();
+            const bool have = ok && !*((volatile int32_t *)&sh.aborted);
+            const int m = p0 + row;
+            const uint32_t acc = tmem + (uint32_t)(b * BQ) + ((uint32_t)(quarter * 32) << 16);
+            if (have) {
+                pdl_wait();
+#pragma unroll 1
+                for (int c = 0; c < BQ; c += 32) {
+                    uint32_t r0[16], r1[16];
+                    tmem_ld16(acc + (uint32_t)c, r0);
+                    tmem_ld16(acc + (uint32_t)(c + 16), r1);
+                    tmem_ld_wait16(r0);
+                    tmem_ld_wait16(r1);
+                    const int n = q0 + c;
+                    if (m < M && n < N) {
+                        float v[32];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            v[j] = __uint_as_float(r0[j]);
+                            v[16 + j] = __uint_as_float(r1[j]);
+                        }
+                        if (bias) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (n + j < N) v[j] += bf16_to_f32(bias[n + j]);
+                        }
+                        uint16_t *o = out + (size_t)m * N + n;
+                        if (vec_ok && n + 32 <= N) {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 8) OutStore<uint16_t>::eight(o + j, v + j);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (n + j < N) OutStore<uint16_t>::one(o + j, v[j]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.acc_empty[b]);
+            if (!have) break;
+        }
+    } else {
+        // ---- scale staging: warps 6..9, one per TMEM lane quarter ----
+        const int quarter = warp & 3;
+        const uint32_t qlane = (uint32_t)(quarter * 32) << 16;
+        pdl_wait();  // the scales may be written by the previous kernel
+        int it = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+            int p0, q0;
+            mxt_coords(t, p_tiles, q_tiles, G, BQ, p0, q0);
+            const int ra = p0 + quarter * 32 + lane;  // this lane's x row (A scales, its own quarter)
+            const uint32_t *wa = reinterpret_cast<const uint32_t *>(xs + (size_t)(ra < M ? ra : 0) * nb);
+            const uint32_t *wb[kBcols];
+            bool inb[kBcols];
+#pragma unroll
+            for (int j = 0; j < kBcols; ++j) {
+                const int rb = q0 + 32 * j + lane;  // W rows of B scale column j (every quarter holds them)
+                inb[j] = rb < N;
+                wb[j] = reinterpret_cast<const uint32_t *>(ws + (size_t)(inb[j] ? rb : 0) * nb);
+            }
+            // The words of chunks c..c+3 are in flight together (a[d], bw[j][d] = chunk c + d), so the
+            // L2 round trip of a chunk's words overlaps the three chunks before it.
+            constexpr int PD = 4;
+            uint32_t a[PD], bw[kBcols][PD];
+#pragma unroll
+            for (int d = 0; d < PD; ++d) {
+                a[d] = (d < C && ra < M) ? __ldg(wa + d) : 0x7F7F7F7Fu;
+#pragma unroll
+                for (int j = 0; j < kBcols; ++j) bw[j][d] = (d < C && inb[j]) ? __ldg(wb[j] + d) : 0x7F7F7F7Fu;
+            }
+            bool stop = false;
+            for (int c = 0; c < C; ++c, ++it) {
+                const int s = it % stages;
+                if (it >= stages && !mbar_wait(&sh.empty[s], ((it / stages) - 1) & 1, status, kSiteScale)) {
+                    atomicExch(&sh.aborted, 1);
+                    stop = true;
+                }
+                stop = __any_sync(0xffffffffu, stop) || *((volatile int32_t *)&sh.aborted);
+                if (stop) break;
+                const uint32_t sf = tmem + (uint32_t)(kSf + kSlot * s) + qlane;
+                tmem_st4(sf, a[0], a[0], a[0], a[0]);  // column `quarter` of the four is the one read
+#pragma unroll
+                for (int j = 0; j < kBcols; j += 4)
+                    tmem_st4(sf + kBoff + j, bw[j][0], bw[j + 1][0], bw[j + 2][0], bw[j + 3][0]);
+                // shift the window and fetch chunk c + PD
+#pragma unroll
+                for (int d = 0; d + 1 < PD; ++d) {
+                    a[d] = a[d + 1];
+#pragma unroll
+                    for (int j = 0; j < kBcols; ++j) bw[j][d] = bw[j][d + 1];
+                }
+                const int cn = c + PD;
+                a[PD - 1] = (cn < C && ra < M) ? __ldg(wa + cn) : 0x7F7F7F7Fu;
+#pragma unroll
+                for (int j = 0; j < kBcols; ++j) bw[j][PD - 1] = (cn < C && inb[j]) ? __ldg(wb[j] + cn) : 0x7F7F7F7Fu;
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.sfull[s]);
+            }
+            if (stop) break;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+        for (int i = sh.consumed; i < sh.issued; ++i)
+            mbar_wait(&sh.full[i % stages], (i / stages) & 1, status, kSiteDrain);
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 using MxFn = void (*)(const uint8_t *, const uint8_t *, const uint8_t *, const uint8_t *, const uint16_t *,
                       uint16_t *, int, int, int, int, int32_t *, int);
 
@@ -250,12 +547,54 @@ MxFn pick_mx(int M) { return M > 8 ? mxfp8_linear_kernel<true, uint16_t> : mxfp8
 
 }  // namespace
 
+int mxtile_smem_bytes(int stages, int bq) {
+    const int need = 1024 + stages * mxt_stage_bytes(bq) + 256;
+    return need > 116 * 1024 ? need : 116 * 1024;  // one CTA per SM (each allocates all 512 TMEM columns)
+}
+
+int mxtile_max_stages(int bq) {
+    const int fit = (232448 - 1024 - 256) / mxt_stage_bytes(bq);
+    return fit < kMxtMaxStages ? fit : kMxtMaxStages;
+}
+
 int init_mxfp8() {
     for (int M : {8, 16}) {
         const int e = (int)cudaFuncSetAttribute(pick_mx(M), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e) return e;
     }
-    return 0;
+    int e = (int)cudaFuncSetAttribute(mxtile_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      mxtile_smem_bytes(mxtile_max_stages(128), 128));
+    if (!e)
+        e = (int)cudaFuncSetAttribute(mxtile_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      mxtile_smem_bytes(mxtile_max_stages(256), 256));
+    return e;
+}
+
+int launch_mxfp8_tile(const void *xq, const void *xs, const void *wq, const void *ws, const void *bias, void *out,
+                      int M, int N, int K, int bq, int stages, int group, int grid, uint32_t flags, void *stream,
+                      int32_t *status) {
+    if ((bq != 128 && bq != 256) || stages < 2 || stages > mxtile_max_stages(bq)) return (int)cudaErrorInvalidValue;
+    CUtensorMap tx, tw;  // 128-byte rows of 128 codes
+    int r = make_tmap_u8_2d(&tx, xq, (uint64_t)M, (uint64_t)K, kMxtBP, kMxtChunk, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    if (r) return (int)cudaErrorInvalidValue;
+    r = make_tmap_u8_2d(&tw, wq, (uint64_t)N, (uint64_t)K, (uint32_t)bq, kMxtChunk, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    if (r) return (int)cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kMxtThreads);
+    cfg.dynamicSmemBytes = (size_t)mxtile_smem_bytes(stages, bq);
+    cfg.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_attr_of(flags);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return (int)cudaLaunchKernelEx(&cfg, bq == 128 ? mxtile_kernel<128> : mxtile_kernel<256>, tx, tw,
+                                   static_cast<const uint8_t *>(xs), static_cast<const uint8_t *>(ws),
+                                   static_cast<const uint16_t *>(bias), static_cast<uint16_t *>(out), M, N, K, stages,
+                                   group, status);
 }
 
 int mxfp8_split(int M, int N, int K, int threads, int num_sms) {
@@ -310,5 +649,6 @@ int launch_quant_mxfp8(const void *x, void *q, void *scales, long long n, int nu
     return (int)cudaLaunchKernelEx(&cfg, quant_mxfp8_kernel, static_cast<const uint16_t *>(x),
                                    static_cast<uint8_t *>(q), static_cast<uint8_t *>(scales), nvec);
 }
+
 
 }  // namespace bf16l

@@ -151,3 +151,80 @@ def test_rejects_bad_arguments(lib):
     with pytest.raises(lib.BF16LinearError):
         lib.bf16_linear_mxfp8(_u8(np.zeros((4, 64))), _u8(np.zeros((4, 2))), _u8(np.zeros((4, 64))),
                               _u8(np.zeros((4, 2))), plan_=lib.make_plan("dotmma", threads=128, split_k=3))
+
+
+# ---- the tile form (tcgen05 block-scaled MMAs, scales staged into tensor memory) ----
+
+def _tile_plan(lib, stages=4, group=0, bq=256):
+    return lib.make_plan("tile", threads=320, rows_per_cta=bq, stages=stages, split_k=group)
+
+
+TILE_CASES = [
+    # W rows per tile, M, N, K, stages, raster group
+    (128, 128, 128, 128, 2, 0),     # one tile, one chunk (four scale blocks)
+    (128, 130, 300, 1024, 6, 0),    # ragged M and N, the ring wraps
+    (256, 256, 520, 4096, 4, 1),
+    (128, 1000, 700, 256, 3, 2),    # ragged everything, two chunks on a three-deep ring
+    (256, 1000, 700, 256, 3, 2),    # the same with 256-row weight tiles (one accumulator buffer)
+    (256, 129, 129, 384, 2, 16),    # one row past a tile, N inside one weight tile
+    (256, 600, 2112, 7168, 4, 0),   # 5 x 9 tiles, K = 56 chunks, sampled rows
+    (128, 600, 2112, 7168, 6, 0),
+]
+
+
+@pytest.mark.parametrize("case", TILE_CASES, ids=lambda c: "x".join(map(str, c)))
+def test_tile_matches_oracle(lib, case):
+    bq, M, N, K, st, grp = case
+    plan = _tile_plan(lib, st, grp, bq)
+    sampled = M * N * K > 2e9
+    for bias in (False, True):
+        xq, xs, wq, ws, b = _quantised_inputs(M, N, K, M + N + K + st + bias, bias)
+        got = _run(lib, xq, xs, wq, ws, b, plan=plan)
+        if sampled:
+            rows = np.array(sorted({0, 127, 128, M // 2, M - 1}), dtype=np.int64)
+            check_close(got[rows], oracle.linear_rows_mxfp8(xq, xs, wq, ws, wl.bits(b), rows),
+                        f"mxfp8 tile M={M} N={N} K={K} sampled rows")
+        else:
+            check_close(got, oracle.linear_mxfp8(xq, xs, wq, ws, wl.bits(b)),
+                        f"mxfp8 tile M={M} N={N} K={K} stages={st} group={grp} bias={bias}")
+    assert lib.device_status() == 0
+
+
+def test_tile_random_scales_and_one_hot(lib):
+    """Random codes with random scale bytes, and one-hot rows: each block's scale must reach its own
+    MMA step and each row and column its own scale word."""
+    rng = np.random.default_rng(23)
+    M, N, K = 200, 264, 512
+    finite = [c for c in range(256) if (c & 0x7F) != 0x7F]
+    xq = rng.choice(finite, size=(M, K)).astype(np.uint8)
+    wq = rng.choice(finite, size=(N, K)).astype(np.uint8)
+    xs = rng.integers(110, 145, size=(M, K // 32)).astype(np.uint8)
+    ws = rng.integers(110, 145, size=(N, K // 32)).astype(np.uint8)
+    for bq in (128, 256):
+        got = _run(lib, xq, xs, wq, ws, None, plan=_tile_plan(lib, bq=bq))
+        check_close(got, oracle.linear_mxfp8(xq, xs, wq, ws), f"mxfp8 tile random scales bq={bq}")
+    # one-hot rows: x[m] = 1.0 at k_m (one block), so out[m, n] = e4m3(w[n, k_m]) * 2^(xs[m, b] + ws[n, b] - 254)
+    xo = np.zeros((M, K), dtype=np.uint8)
+    ks = (np.arange(M) * 37 + 5) % K
+    xo[np.arange(M), ks] = 0x38
+    for bq in (128, 256):
+        got = _run(lib, xo, xs, wq, ws, None, plan=_tile_plan(lib, bq=bq))
+        assert np.array_equal(got, oracle.linear_mxfp8(xo, xs, wq, ws))
+
+
+def test_tile_is_the_large_m_choice(lib):
+    """At prefill size the entry point's own choice is the tile form; sampled rows against the oracle."""
+    M, N, K = 2048, 2112, 7168
+    xq, xs, wq, ws, b = _quantised_inputs(M, N, K, 41, True)
+    got = _run(lib, xq, xs, wq, ws, b)
+    rows = np.array([0, 127, 128, 1023, 2047], dtype=np.int64)
+    check_close(got[rows], oracle.linear_rows_mxfp8(xq, xs, wq, ws, wl.bits(b), rows), "mxfp8 prefill sampled rows")
+    forced = _run(lib, xq, xs, wq, ws, b, plan=_tile_plan(lib))
+    assert np.array_equal(got, forced)
+
+
+def test_tile_rejects_partial_chunks(lib):
+    xq, xs, wq, ws, _ = _quantised_inputs(64, 128, 96, 3, False)   # K = 96: not whole 128-code chunks
+    with pytest.raises(lib.BF16LinearError) as e:
+        _run(lib, xq, xs, wq, ws, None, plan=_tile_plan(lib))
+    assert e.value.status == -6
