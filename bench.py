@@ -103,9 +103,11 @@ def workload_desc(name):
 
 def kernel_source_hash(kernel_name):
     src = {"dotprod": ("dotprod.cuh", "dotprod.cu"), "splitk": ("splitk.cu",), "splitk_ws": ("splitk.cu",),
-           "tile": ("tile.cu",), "stream": ("stream.cu",), "tile2": ("tile2.cu",), "warprow": ("warprow.cu",),
-           "warpmma": ("warpmma.cu", "warpmma_ks.cu"), "dotmma": ("dotmma.cu",),
-           "dotmma_ws": ("dotmma.cu",)}[kernel_name]
+           "tile": ("tile.cuh", "tile.cu"), "tile_t": ("tile.cuh", "tile_t.cu"), "stream": ("stream.cu",),
+           "tile2": ("tile2.cu",), "warprow": ("warprow.cu",), "warpmma": ("warpmma.cu", "warpmma_ks.cu"),
+           "dotmma": ("dotmma.cu",), "dotmma_ws": ("dotmma.cu",)}.get(kernel_name)
+    if src is None:
+        return None
     h = hashlib.sha256()
     for f in src + ("common.cuh", "kernels.h"):
         h.update(open(os.path.join(ROOT, "moe_router_gemm_gb300", "csrc", f), "rb").read())
@@ -120,6 +122,8 @@ def ncu_traffic(kernel_name, shapes):
     if not os.path.exists(p):
         return None
     want = kernel_source_hash(kernel_name)
+    if want is None:
+        return None
     table = {}
     for line in open(p):
         if line.startswith("#") or not line.strip():
@@ -571,11 +575,11 @@ def floor_record(shapes, lib, device, stream, replays):
 
 
 def forced_plan(lib, spec):
-    """The plan given by --plan (kernel name, threads, rows, tokens, split, stages), or None."""
+    """The plan given by --plan (kernel name, threads, rows, tokens, split, stages[, chunks per stage]), or None."""
     if not spec:
         return None
     f = spec.split(",")
-    names = ("threads", "rows_per_cta", "tokens_per_cta", "split_k", "stages")
+    names = ("threads", "rows_per_cta", "tokens_per_cta", "split_k", "stages", "chunks_per_stage")
     return lib.make_plan(f[0], **{k: int(v) for k, v in zip(names, f[1:])})
 
 
@@ -647,6 +651,20 @@ def candidate_plans(lib, M, N, K):
                     except Exception:
                         continue
                 cands.append(p)
+                if K % 64 == 0 and split <= -(-chunks // 2):  # two K chunks per stage: half the TMA loads
+                    for st in (8, 6, 5, 4, 3, 2, 1):
+                        q = lib.make_plan("splitk", threads=128, rows_per_cta=rows, tokens_per_cta=tokens,
+                                          split_k=split, stages=min(st, -(-per // 2)), chunks_per_stage=2)
+                        try:
+                            lib.plan_check(M, N, K, q)
+                        except Exception:
+                            continue
+                        cands.append(q)
+                        if M > 8 and tiles * split > 152 and q.stages > 2:
+                            cands.append(lib.make_plan("splitk", threads=128, rows_per_cta=rows,
+                                                       tokens_per_cta=tokens, split_k=split, stages=2,
+                                                       chunks_per_stage=2))
+                        break
                 if M > 8 and tiles * split > 152:  # more CTAs than SMs: shallower rings, two or three per SM
                     for st in (6, 4, 3, 2):
                         if st < p.stages:
@@ -762,6 +780,10 @@ def candidate_plans(lib, M, N, K):
                 for grp in (0, 1, 2, 4, 16):
                     cands.append(lib.make_plan("tile", threads=192, rows_per_cta=bn, tokens_per_cta=128, stages=st,
                                                split_k=grp))
+            if K % 64 == 0 and M <= 1024:  # two K chunks per stage (bandwidth-bound sizes)
+                for grp in (0, 16):
+                    cands.append(lib.make_plan("tile", threads=192, rows_per_cta=bn, tokens_per_cta=128,
+                                               stages=max(2, most // 2), split_k=grp, chunks_per_stage=2))
     if K % 8 == 0 and 16 < M <= 512:  # the swap-AB tile: W rows on the MMA M side, tokens on N
         for bn in (32, 64, 128, 192, 256):
             if bn > 2 * max(32, M) or 4 * bn < M:
@@ -771,6 +793,11 @@ def candidate_plans(lib, M, N, K):
                 for grp in (0, 1):
                     cands.append(lib.make_plan("tile_t", threads=192, rows_per_cta=128, tokens_per_cta=bn,
                                                stages=st, split_k=grp))
+            if K % 64 == 0:  # two K chunks per stage
+                for st in sorted({most // 2, max(2, most // 2 - 1)}, reverse=True):
+                    if st >= 2:
+                        cands.append(lib.make_plan("tile_t", threads=192, rows_per_cta=128, tokens_per_cta=bn,
+                                                   stages=st, split_k=0, chunks_per_stage=2))
     return cands
 
 
@@ -838,14 +865,15 @@ def sweep(args, points):
     with open(os.path.join(out_dir, "sweep_results.json"), "w") as f:
         json.dump(results, f, indent=1)
     lines = ["// Measured GB300 dispatch entries (python bench.py --sweep): fastest plan per shape, L2-cold.",
-             "// {K, N, M, kernel, threads, rows_per_cta, tokens_per_cta, split_k, stages},"]
+             "// {K, N, M, kernel, threads, rows_per_cta, tokens_per_cta, split_k, stages[, chunks_per_stage]},"]
     for r in sorted(results, key=lambda r: (r["K"], r["N"], r["M"])):
         entries = [(r["best"], r["best_us"])]
         if r["best"].get("kernel") in WS_KERNELS:  # needs a workspace: follow it with the best plan that needs none
             entries.append((r["best_plain"], r["best_plain_us"]))
         for b, us in entries:
+            kc = f", {b['chunks_per_stage']}" if b.get("chunks_per_stage", 0) > 1 else ""
             lines.append(f"{{{r['K']}, {r['N']}, {r['M']}, {b['kernel']}, {b['threads']}, {b['rows_per_cta']}, "
-                         f"{b['tokens_per_cta']}, {b['split_k']}, {b['stages']}}},  // {us:.3f} us")
+                         f"{b['tokens_per_cta']}, {b['split_k']}, {b['stages']}{kc}}},  // {us:.3f} us")
     with open(os.path.join(out_dir, "dispatch_table.inc"), "w") as f:
         f.write("\n".join(lines) + "\n")
 

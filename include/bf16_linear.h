@@ -115,13 +115,18 @@ typedef struct {
                               WARPMMA: 1 = x fragments loaded from global memory into registers (512 threads per
                               SM at most), 0 = x staged in shared memory, S = 2..16: the cluster form (K over S
                               CTAs; 1024-thread blocks only for M <= 16, else at most 512 threads per SM) */
-    int32_t stages;        /* SPLITK / TILE / TILE_T: shared-memory ring depth (64-wide K chunks; TILE and TILE_T:
-                              2 up to what fits 227 KB, at most 8); DOTPROD: 1 = x read
+    int32_t stages;        /* SPLITK / TILE / TILE_T: shared-memory ring depth, in stages of chunks_per_stage
+                              64-wide K chunks (TILE and TILE_T: 2 up to what fits 227 KB, stages x chunks at
+                              most 8); DOTPROD: 1 = x read
                               from global memory (L2) instead of staged in shared memory;
                               WARPROW / WARPMMA: CTAs per SM; DOTMMA: 1 = x fragments loaded from global
                               memory into registers, 0 = each CTA's x slice staged in shared memory */
     int32_t grid;          /* CTAs launched (informational; computed by the plan) */
     int32_t flags;         /* BF16L_FLAG_* bits the launch uses */
+    int32_t chunks_per_stage; /* SPLITK / SPLITK_WS / TILE / TILE_T: 64-wide K chunks per ring stage, 0 or 1 = one,
+                              2 = two (K % 64 == 0; each stage is then one TMA box per operand holding two chunk
+                              tiles, so a CTA issues half as many loads; `stages` counts these double stages, and
+                              SPLITK / SPLITK_WS need split_k <= ceil(K / 128)); every other kernel: 0 or 1 */
 } bf16l_plan;
 
 /*

@@ -32,7 +32,7 @@ class Plan(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("threads", ctypes.c_int32),
                 ("rows_per_cta", ctypes.c_int32), ("tokens_per_cta", ctypes.c_int32),
                 ("split_k", ctypes.c_int32), ("stages", ctypes.c_int32),
-                ("grid", ctypes.c_int32), ("flags", ctypes.c_int32)]
+                ("grid", ctypes.c_int32), ("flags", ctypes.c_int32), ("chunks_per_stage", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         d = {f[0]: int(getattr(self, f[0])) for f in self._fields_}

@@ -233,6 +233,20 @@ int make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_
                         promo);
 }
 
+int make_tmap_bf16_chunks(CUtensorMap *map, const void *base, uint64_t rows, uint64_t K, uint32_t box_rows,
+                          uint32_t kc) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+    if (!enc) return (int)CUDA_ERROR_NOT_FOUND;
+    if (K % kChunkK != 0 || kc < 1) return (int)CUDA_ERROR_INVALID_VALUE;
+    const cuuint64_t dims[3] = {(cuuint64_t)kChunkK, rows, K / kChunkK};
+    const cuuint64_t strides[2] = {K * 2, (cuuint64_t)kChunkK * 2};  // bytes between rows, between chunks
+    const cuuint32_t box[3] = {(cuuint32_t)kChunkK, box_rows, kc};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return (int)enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 int make_tmap_u8_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
                     uint32_t box_cols, CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo) {
     return make_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, rows, cols, box_rows, box_cols, swizzle, promo);
@@ -350,6 +364,7 @@ extern "C" int bf16_linear_fp8_with_plan(const void *xq, const void *wq, const f
                                          const bf16l_plan *plan, bf16l_stream_t stream) {
     using namespace bf16l;
     if (!plan) return BF16L_EINVAL;
+    if (plan->chunks_per_stage != 0 && plan->chunks_per_stage != 1) return BF16L_EINVAL;
     const uint32_t flags = (uint32_t)plan->flags;
     if (M < 0 || N <= 0 || K <= 0) return BF16L_EINVAL;
     if (!flags_valid(flags)) return BF16L_EINVAL;
@@ -479,6 +494,7 @@ extern "C" int bf16_linear_mxfp8_with_plan(const void *xq, const void *xs, const
                                            bf16l_stream_t stream) {
     using namespace bf16l;
     if (!plan) return BF16L_EINVAL;
+    if (plan->chunks_per_stage != 0 && plan->chunks_per_stage != 1) return BF16L_EINVAL;
     const uint32_t flags = (uint32_t)plan->flags;
     if (M < 0 || N <= 0 || K <= 0 || !flags_valid(flags)) return BF16L_EINVAL;
     if (K % 32 != 0) return BF16L_EUNSUPPORTED;  // whole 32-element scale blocks

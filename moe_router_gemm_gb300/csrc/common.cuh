@@ -232,6 +232,18 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// Three-dimensional tile load (c0 innermost).  With the chunked weight/activation
+// maps (make_tmap_bf16_chunks: {64 elements, rows, K / 64 chunks}) one box
+// brings kc consecutive 64-wide K chunks of box_rows rows, laid out in shared
+// memory as kc ordinary 128-byte-swizzled chunk tiles one after the other.
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar, int32_t c0,
+                                            int32_t c1, int32_t c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *map, uint64_t *bar, int32_t c0,
                                                  int32_t c1, uint64_t policy) {
     asm volatile(
@@ -615,6 +627,13 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 // ---------------------------------------------------------------------------
 int make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
                       uint32_t box_cols, CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo);
+// A row-major bf16 matrix [rows][K] (K % 64 == 0) seen as {64, rows, K / 64}:
+// element (k, r) at chunk k / 64, offset k % 64.  Strides: 2K bytes between
+// rows, 128 bytes between chunks.  Box {64, box_rows, kc}, 128-byte swizzle:
+// one load brings kc consecutive K chunks of box_rows rows (chunks past K / 64
+// are zero-filled).
+int make_tmap_bf16_chunks(CUtensorMap *map, const void *base, uint64_t rows, uint64_t K, uint32_t box_rows,
+                          uint32_t kc);
 // The same for one-byte elements (e4m3 codes): cols in bytes.
 int make_tmap_u8_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
                     uint32_t box_cols, CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo);

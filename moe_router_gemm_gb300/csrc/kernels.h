@@ -33,10 +33,10 @@ constexpr int kSplitMaxCluster = 16;
 constexpr int kSplitMaxStages = 16;
 constexpr int kSplitThreads = 128;
 // Shared-memory layout arithmetic of the split-K kernel (defined in splitk.cu).
-int split_stage_bytes(int tokens, int rows);
+int split_stage_bytes(int tokens, int rows, int kc = 1);  // kc: 64-wide K chunks per ring stage
 int split_recv_bytes(int tokens, int rows);
-int split_smem_bytes(int tokens, int rows, int stages);
-int split_max_stages(int tokens, int rows);  // 0 when even one stage does not fit
+int split_smem_bytes(int tokens, int rows, int stages, int kc = 1);
+int split_max_stages(int tokens, int rows, int kc = 1);  // 0 when even one stage does not fit
 int split_tmem_cols(int rows);
 bool split_rows_supported(int rows);         // a kernel instance exists for this many rows
 constexpr int kSplitWsMaxSplit = 64;         // K splits of the cluster-free (workspace) variant

@@ -22,6 +22,7 @@ namespace {
 struct TableEntry {
     int K, N, M;
     int kernel, threads, rows_per_cta, tokens_per_cta, split_k, stages;
+    int chunks_per_stage;  // 0 when the entry leaves it out
 };
 
 // Measured on GB300 (sm_103a, 152 SMs).  Regenerate with `python bench.py --sweep`.
@@ -93,6 +94,13 @@ void plan_tile(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
 int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
     if (M < 0 || N <= 0 || K <= 0) return BF16L_EINVAL;
     if (!flags_valid((uint32_t)p->flags)) return BF16L_EINVAL;
+    const int kc = p->chunks_per_stage;
+    if (kc < 0 || kc > 2) return BF16L_EINVAL;
+    const bool ring_kernel = p->kernel == BF16L_KERNEL_SPLITK || p->kernel == BF16L_KERNEL_SPLITK_WS ||
+                             p->kernel == BF16L_KERNEL_TILE || p->kernel == BF16L_KERNEL_TILE_T;
+    if (kc == 2 && !ring_kernel) return BF16L_EINVAL;
+    if (kc == 2 && K % kChunkK != 0) return BF16L_EUNSUPPORTED;  // the chunked tensor maps need whole chunks
+    const int kcs = kc == 2 ? 2 : 1;
     switch (p->kernel) {
         case BF16L_KERNEL_DOTPROD: {
             if (!in_list(p->threads, kDotThreads, 3) || !in_list(p->rows_per_cta, kDotRows, 3))
@@ -112,8 +120,9 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
             if (p->tokens_per_cta < 8 || p->tokens_per_cta > kSplitMaxTokens || p->tokens_per_cta % 8 != 0 ||
                 p->tokens_per_cta < M)
                 return BF16L_EINVAL;
-            if (p->split_k < 1 || p->split_k > max_split || p->split_k > chunks) return BF16L_EINVAL;
-            if (p->stages < 1 || p->stages > split_max_stages(p->tokens_per_cta, p->rows_per_cta))
+            // every rank needs at least one ring stage of kcs chunks
+            if (p->split_k < 1 || p->split_k > max_split || p->split_k > ceil_div(chunks, kcs)) return BF16L_EINVAL;
+            if (p->stages < 1 || p->stages > split_max_stages(p->tokens_per_cta, p->rows_per_cta, kcs))
                 return BF16L_EINVAL;
             const int64_t grid = (int64_t)ceil_div(N, p->rows_per_cta) * p->split_k;
             if (ceil_div(N, p->rows_per_cta) > 65535) return BF16L_EUNSUPPORTED;
@@ -141,7 +150,7 @@ int check_plan(int M, int N, int K, const bf16l_device &dev, bf16l_plan *p) {
             if (p->threads != kTileThreads || (swap ? p->rows_per_cta : p->tokens_per_cta) != kTileBM ||
                 !(swap ? in_list(bn, kTileTBNs, 5) : in_list(bn, kTileBNs, 5)))
                 return BF16L_EINVAL;
-            if (p->stages < kTileMinStages || p->stages > tile_max_stages(bn)) return BF16L_EINVAL;
+            if (p->stages < kTileMinStages || p->stages * kcs > tile_max_stages(bn)) return BF16L_EINVAL;
             if (p->split_k < 0 || p->split_k > 1024) return BF16L_EINVAL;  // raster group
             const int64_t tiles = swap ? (int64_t)ceil_div(N, kTileBM) * ceil_div(M, bn)
                                        : (int64_t)ceil_div(M, kTileBM) * ceil_div(N, bn);
@@ -273,6 +282,7 @@ extern "C" int bf16_linear_plan_ws(int M, int N, int K, const bf16l_device *devp
         p.tokens_per_cta = e->tokens_per_cta;
         p.split_k = e->split_k;
         p.stages = e->stages;
+        p.chunks_per_stage = e->chunks_per_stage;
         from_table = check_plan(M, N, K, dev, &p) == BF16L_OK && plan_ws_bytes(M, N, p) <= workspace_bytes;
     }
     if (!from_table) {

@@ -67,7 +67,7 @@ __device__ __forceinline__ int part_begin(int d, int T, int S) { return mul_div(
 static_assert(sizeof(SplitShared) <= 512, "bookkeeping must fit its reserved space");
 
 // Host-visible layout arithmetic (shared with the planner through kernels.h).
-int split_stage_bytes(int tokens, int rows) { return (tokens + rows) * kChunkK * 2; }
+int split_stage_bytes(int tokens, int rows, int kc) { return kc * (tokens + rows) * kChunkK * 2; }
 
 int split_recv_bytes(int tokens, int rows) {
     // S partials of this CTA's share: at most S * ceil(T / S) <= T + S items of 16 bytes.
@@ -84,17 +84,17 @@ int split_tmem_cols(int rows) {
     return need <= 32 ? 32 : need <= 64 ? 64 : need <= 128 ? 128 : 256;
 }
 
-int split_ring_bytes(int tokens, int rows, int stages) {
+int split_ring_bytes(int tokens, int rows, int stages, int kc) {
     // The ring, which the accumulator staging (tokens x rows fp32) reuses once the MMAs are done.
-    const int ring = stages * split_stage_bytes(tokens, rows), acc = tokens * rows * 4;
+    const int ring = stages * split_stage_bytes(tokens, rows, kc), acc = tokens * rows * 4;
     return ring > acc ? ring : acc;
 }
 
-int split_smem_bytes(int tokens, int rows, int stages) {
-    const int stage = split_stage_bytes(tokens, rows);
-    int body = split_ring_bytes(tokens, rows, stages) + split_recv_bytes(tokens, rows) + 512 /*bookkeeping*/;
-    // The MMA reads a full 64-row A window from the last stage's x chunk on.
-    const int window = (stages - 1) * stage + kATileBytes;
+int split_smem_bytes(int tokens, int rows, int stages, int kc) {
+    const int stage = split_stage_bytes(tokens, rows, kc);
+    int body = split_ring_bytes(tokens, rows, stages, kc) + split_recv_bytes(tokens, rows) + 512 /*bookkeeping*/;
+    // The MMA reads a full 64-row A window from the last stage's last x chunk on.
+    const int window = (stages - 1) * stage + (kc - 1) * tokens * kChunkK * 2 + kATileBytes;
     if (window > body) body = window;
     int bytes = 1024 /*alignment slack*/ + body;
     // Pad so that the CTAs that fit on one SM never ask for more than its 512
@@ -104,10 +104,10 @@ int split_smem_bytes(int tokens, int rows, int stages) {
     return bytes > min_bytes ? bytes : min_bytes;
 }
 
-int split_max_stages(int tokens, int rows) {
+int split_max_stages(int tokens, int rows, int kc) {
     int s = kSplitMaxStages;
-    while (s > 1 && split_smem_bytes(tokens, rows, s) > kSmemPerCta) --s;
-    return split_smem_bytes(tokens, rows, s) <= kSmemPerCta ? s : 0;
+    while (s > 1 && split_smem_bytes(tokens, rows, s, kc) > kSmemPerCta) --s;
+    return split_smem_bytes(tokens, rows, s, kc) <= kSmemPerCta ? s : 0;
 }
 
 // kClus: the S CTAs that share a tile form a thread-block cluster and reduce
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     splitk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                   const uint16_t *__restrict__ bias, OutT *__restrict__ out, int M, int N, int K, int tokp,
                   int stages, int32_t *status, float *__restrict__ ws, uint32_t *__restrict__ counters,
-                  int w_early) {
+                  int w_early, int kc) {
     constexpr uint32_t kIdesc = idesc_bf16_f32(kMmaM, BN);
     constexpr int kAcc = split_acc_count(BN);
     constexpr int kCols = kAcc * BN <= 32 ? 32 : kAcc * BN <= 64 ? 64 : kAcc * BN <= 128 ? 128 : 256;
@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-aligned (128-byte swizzle atoms)
     const int xbytes = tokp * kChunkK * 2;
-    const int stage_bytes = xbytes + kWBytes;
+    const int stage_bytes = kc * (xbytes + kWBytes);  // kc x chunk tiles, then kc weight chunk tiles
     const int T = M * (BN / 4);  // float4 items of the tile's partial sums
     const int ring_bytes = stages * stage_bytes > tokp * BN * 4 ? stages * stage_bytes : tokp * BN * 4;
     float4 *stage_out = reinterpret_cast<float4 *>(ring);  // accumulator staging, [M][BN] fp32, after the MMAs
@@ -141,10 +141,11 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     const int rank = kClus ? (int)cluster_ctarank() : (int)blockIdx.x;
     const int S = (int)gridDim.x;  // the K split spans the whole x dimension of the grid
     const int n0 = blockIdx.y * BN;
-    const int C = (K + kChunkK - 1) / kChunkK;
+    // K moves in ring stages of kc 64-wide chunks (the last one zero-filled past K); the ranks split the stages.
+    const int C = (K + kChunkK * kc - 1) / (kChunkK * kc);
     const int c_begin = mul_div(C, rank, S);
     const int nchunks = mul_div(C, rank + 1, S) - c_begin;
-    const int first = nchunks < stages ? nchunks : stages;  // chunks whose weights go out at once
+    const int first = nchunks < stages ? nchunks : stages;  // stages whose weights go out at once
     // Default launch: nothing is read before the previous kernel has finished.  (An L2 prefetch of the
     // first ring's weight boxes here, as the CUDA-core kernels issue, measured 2-4% slower on the decode
     // and MLP shapes this kernel serves.)
@@ -167,12 +168,19 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         for (int i = 0; i < first; ++i) {
             uint8_t *st = ring + i * stage_bytes;
             mbar_arrive_expect_tx(&sh.full[i], (uint32_t)stage_bytes);
-            tma_load_2d(st + xbytes, &tm_w, &sh.full[i], (c_begin + i) * kChunkK, n0);
+            if (kc == 1)
+                tma_load_2d(st + xbytes, &tm_w, &sh.full[i], (c_begin + i) * kChunkK, n0);
+            else
+                tma_load_3d(st + kc * xbytes, &tm_w, &sh.full[i], 0, n0, (c_begin + i) * kc);
         }
         pdl_launch_dependents();  // the next kernel may start its own weight loads now
         pdl_wait();               // x may be written by the previous kernel
-        for (int i = 0; i < first; ++i)
-            tma_load_2d(ring + i * stage_bytes, &tm_x, &sh.full[i], (c_begin + i) * kChunkK, 0);
+        for (int i = 0; i < first; ++i) {
+            if (kc == 1)
+                tma_load_2d(ring + i * stage_bytes, &tm_x, &sh.full[i], (c_begin + i) * kChunkK, 0);
+            else
+                tma_load_3d(ring + i * stage_bytes, &tm_x, &sh.full[i], 0, 0, (c_begin + i) * kc);
+        }
     }
     if (warp == 1) {
         tmem_alloc(&sh.tmem_base, kCols);
@@ -196,9 +204,14 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
                 }
                 uint8_t *st = ring + s * stage_bytes;
                 mbar_arrive_expect_tx(&sh.full[s], (uint32_t)stage_bytes);
-                const int kc = (c_begin + i) * kChunkK;
-                tma_load_2d(st + xbytes, &tm_w, &sh.full[s], kc, n0);
-                tma_load_2d(st, &tm_x, &sh.full[s], kc, 0);
+                if (kc == 1) {
+                    const int k0 = (c_begin + i) * kChunkK;
+                    tma_load_2d(st + xbytes, &tm_w, &sh.full[s], k0, n0);
+                    tma_load_2d(st, &tm_x, &sh.full[s], k0, 0);
+                } else {
+                    tma_load_3d(st + kc * xbytes, &tm_w, &sh.full[s], 0, n0, (c_begin + i) * kc);
+                    tma_load_3d(st, &tm_x, &sh.full[s], 0, 0, (c_begin + i) * kc);
+                }
             }
             sh.issued = i;
         }
@@ -214,12 +227,17 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
                 }
                 tc_fence_after();
                 const uint8_t *st = ring + s * stage_bytes;
-                const uint64_t adesc = smem_desc_sw128(smem_u32(st));
-                const uint64_t bdesc = smem_desc_sw128(smem_u32(st + xbytes));
+#pragma unroll 1
+                for (int j = 0; j < kc; ++j) {
+                    const uint64_t adesc = smem_desc_sw128(smem_u32(st + j * xbytes));
+                    const uint64_t bdesc = smem_desc_sw128(smem_u32(st + kc * xbytes + j * kWBytes));
 #pragma unroll
-                for (int kk = 0; kk < kChunkK / 16; ++kk)  // 4 MMAs of K = 16 (32 bytes) each
-                    mma_bf16(tmem + (uint32_t)((kk % kAcc) * BN), adesc + 2 * kk, bdesc + 2 * kk, kIdesc,
-                             (i > 0 || kk >= kAcc) ? 1u : 0u);
+                    for (int kk = 0; kk < kChunkK / 16; ++kk) {  // 4 MMAs of K = 16 (32 bytes) each
+                        const int q = j * (kChunkK / 16) + kk;  // MMA index in the stage: accumulator q % kAcc
+                        mma_bf16(tmem + (uint32_t)((q % kAcc) * BN), adesc + 2 * kk, bdesc + 2 * kk, kIdesc,
+                                 (i > 0 || q >= kAcc) ? 1u : 0u);
+                    }
+                }
                 mma_commit(&sh.empty[s]);
             }
             sh.consumed = i;
@@ -413,7 +431,7 @@ namespace {
 
 template <typename OutT, bool kClus>
 using SplitFn = void (*)(CUtensorMap, CUtensorMap, const uint16_t *, OutT *, int, int, int, int, int, int32_t *,
-                         float *, uint32_t *, int);
+                         float *, uint32_t *, int, int);
 
 template <typename OutT, bool kClus>
 SplitFn<OutT, kClus> pick(int BN) {
@@ -446,11 +464,20 @@ int launch_split_t(const LaunchArgs &a, const bf16l_plan &p) {
     SplitFn<OutT, kClus> fn = pick<OutT, kClus>(p.rows_per_cta);
     if (!fn) return (int)cudaErrorInvalidValue;
     CUtensorMap tw, tx;
-    int r = make_tmap_bf16_2d(&tw, a.W, (uint64_t)a.N, (uint64_t)a.K, (uint32_t)p.rows_per_cta, kChunkK,
+    const int kc = p.chunks_per_stage == 2 ? 2 : 1;  // validated by the plan check (K % 64 == 0)
+    int r;
+    if (kc == 1) {
+        r = make_tmap_bf16_2d(&tw, a.W, (uint64_t)a.N, (uint64_t)a.K, (uint32_t)p.rows_per_cta, kChunkK,
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-    if (r) return (int)cudaErrorInvalidValue;
-    r = make_tmap_bf16_2d(&tx, a.x, (uint64_t)a.M, (uint64_t)a.K, (uint32_t)p.tokens_per_cta, kChunkK,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+        if (!r)
+            r = make_tmap_bf16_2d(&tx, a.x, (uint64_t)a.M, (uint64_t)a.K, (uint32_t)p.tokens_per_cta, kChunkK,
+                                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    } else {
+        r = make_tmap_bf16_chunks(&tw, a.W, (uint64_t)a.N, (uint64_t)a.K, (uint32_t)p.rows_per_cta, (uint32_t)kc);
+        if (!r)
+            r = make_tmap_bf16_chunks(&tx, a.x, (uint64_t)a.M, (uint64_t)a.K, (uint32_t)p.tokens_per_cta,
+                                      (uint32_t)kc);
+    }
     if (r) return (int)cudaErrorInvalidValue;
 
     const int tiles = (a.N + p.rows_per_cta - 1) / p.rows_per_cta;
@@ -464,7 +491,7 @@ int launch_split_t(const LaunchArgs &a, const bf16l_plan &p) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.split_k, (unsigned)tiles, 1);
     cfg.blockDim = dim3(kSplitThreads, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)split_smem_bytes(p.tokens_per_cta, p.rows_per_cta, p.stages);
+    cfg.dynamicSmemBytes = (size_t)split_smem_bytes(p.tokens_per_cta, p.rows_per_cta, p.stages, kc);
     cfg.stream = (cudaStream_t)a.stream;
     cudaLaunchAttribute attr[2];
     int na = 0;
@@ -482,7 +509,7 @@ int launch_split_t(const LaunchArgs &a, const bf16l_plan &p) {
     cfg.numAttrs = na;
     return (int)cudaLaunchKernelEx(&cfg, fn, tw, tx, static_cast<const uint16_t *>(a.bias),
                                    static_cast<OutT *>(a.out), a.M, a.N, a.K, p.tokens_per_cta, p.stages,
-                                   a.status, parts, counters, w_early_of((uint32_t)p.flags));
+                                   a.status, parts, counters, w_early_of((uint32_t)p.flags), kc);
 }
 
 }  // namespace

@@ -79,25 +79,27 @@ template <int BN, bool SWAP, typename OutT, bool F8 = false>
 __global__ void __launch_bounds__(kTileThreads, 1)
     tile_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_q,
                 const uint16_t *__restrict__ bias, OutT *__restrict__ out, int M, int N, int K, int stages,
-                int group, int32_t *status, const float *__restrict__ scale_x = nullptr,
-                const float *__restrict__ scale_w = nullptr) {
+                int group, int kc, int32_t *status, const float *__restrict__ scale_x,
+                const float *__restrict__ scale_w) {
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N: a multiple of 16 up to 256");
     static_assert(!(SWAP && F8), "the e4m3 form is plain only");
     constexpr int kChunk = F8 ? 2 * kChunkK : kChunkK;  // elements per 128-byte row
-    constexpr int kStageBytes = tile_stage_bytes(BN);
+    constexpr int kQBytes = BN * 128;  // one chunk of the N-side operand
     constexpr int kAccStride = tile_acc_stride(BN);
     constexpr int kTmemCols = 2 * kAccStride;
     constexpr uint32_t kIdesc = F8 ? idesc_e4m3_f32(kTileBP, BN) : idesc_bf16_f32(kTileBP, BN);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    TileShared &sh = *reinterpret_cast<TileShared *>(ring + stages * kStageBytes);
+    // A stage holds kc consecutive K chunks: kc P chunk tiles, then kc Q chunk tiles.
+    const int stage_bytes = kc * tile_stage_bytes(BN);
+    TileShared &sh = *reinterpret_cast<TileShared *>(ring + stages * stage_bytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int p_rows = SWAP ? N : M, q_rows = SWAP ? M : N;
     const int p_tiles = (p_rows + kTileBP - 1) / kTileBP, q_tiles = (q_rows + BN - 1) / BN;
     const int num_tiles = p_tiles * q_tiles;
-    const int C = (K + kChunk - 1) / kChunk;
+    const int C = (K + kChunk * kc - 1) / (kChunk * kc);  // ring stages per tile (the last one zero-filled past K)
     const int G = group > 0 ? group : q_tiles;
 
     if (tid == 0) {
@@ -140,10 +142,15 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                         goto producer_done;
                     }
                     if (*((volatile int32_t *)&sh.aborted)) goto producer_done;
-                    uint8_t *st = ring + s * kStageBytes;
-                    mbar_arrive_expect_tx(&sh.full[s], kStageBytes);
-                    tma_load_2d(st, &tm_p, &sh.full[s], c * kChunk, p0);
-                    tma_load_2d(st + kTileABytes, &tm_q, &sh.full[s], c * kChunk, q0);
+                    uint8_t *st = ring + s * stage_bytes;
+                    mbar_arrive_expect_tx(&sh.full[s], (uint32_t)stage_bytes);
+                    if (kc == 1) {
+                        tma_load_2d(st, &tm_p, &sh.full[s], c * kChunk, p0);
+                        tma_load_2d(st + kTileABytes, &tm_q, &sh.full[s], c * kChunk, q0);
+                    } else {  // chunked maps: {64, rows, chunks}
+                        tma_load_3d(st, &tm_p, &sh.full[s], 0, p0, c * kc);
+                        tma_load_3d(st + kc * kTileABytes, &tm_q, &sh.full[s], 0, q0, c * kc);
+                    }
                 }
             }
         producer_done:
@@ -174,15 +181,19 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint8_t *st = ring + s * kStageBytes;
-                    const uint64_t adesc = smem_desc_sw128(smem_u32(st));
-                    const uint64_t bdesc = smem_desc_sw128(smem_u32(st + kTileABytes));
+                    const uint8_t *st = ring + s * stage_bytes;
+#pragma unroll 1
+                    for (int j = 0; j < kc; ++j) {
+                        const uint64_t adesc = smem_desc_sw128(smem_u32(st + j * kTileABytes));
+                        const uint64_t bdesc = smem_desc_sw128(smem_u32(st + kc * kTileABytes + j * kQBytes));
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {  // 32 bytes of each row per MMA
-                        if constexpr (F8)
-                            mma_e4m3(acc, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (c > 0 || kk > 0) ? 1u : 0u);
-                        else
-                            mma_bf16(acc, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (c > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < 4; ++kk) {  // 32 bytes of each row per MMA
+                            const uint32_t accum = (c > 0 || j > 0 || kk > 0) ? 1u : 0u;
+                            if constexpr (F8)
+                                mma_e4m3(acc, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, accum);
+                            else
+                                mma_bf16(acc, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, accum);
+                        }
                     }
                     mma_commit(&sh.empty[s]);
                 }
@@ -297,8 +308,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
 // barriers; at least 116 KB, so that no two CTAs share an SM (a second one
 // would find the TMEM columns taken and wait in tcgen05.alloc until the first
 // CTA is done with all of its tiles).
-inline int tile_smem_bytes_bn(int stages, int bn) {
-    const int need = 1024 + stages * tile_stage_bytes(bn) + 256;
+inline int tile_smem_bytes_bn(int stages, int bn, int kc = 1) {
+    const int need = 1024 + stages * kc * tile_stage_bytes(bn) + 256;
     return need > 116 * 1024 ? need : 116 * 1024;
 }
 
@@ -314,16 +325,23 @@ int tile_launch_bn(const LaunchArgs &a, const bf16l_plan &p) {
     CUtensorMap tp, tq;
     const void *pb = SWAP ? a.W : a.x, *qb = SWAP ? a.x : a.W;
     const uint64_t pr = SWAP ? (uint64_t)a.N : (uint64_t)a.M, qr = SWAP ? (uint64_t)a.M : (uint64_t)a.N;
-    int r = make_tmap_bf16_2d(&tp, pb, pr, (uint64_t)a.K, kTileBP, kChunkK, CU_TENSOR_MAP_SWIZZLE_128B,
+    const int kc = p.chunks_per_stage == 2 ? 2 : 1;  // validated by the plan check (K % 64 == 0)
+    int r;
+    if (kc == 1) {
+        r = make_tmap_bf16_2d(&tp, pb, pr, (uint64_t)a.K, kTileBP, kChunkK, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-    if (r) return (int)cudaErrorInvalidValue;
-    r = make_tmap_bf16_2d(&tq, qb, qr, (uint64_t)a.K, BN, kChunkK, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+        if (!r)
+            r = make_tmap_bf16_2d(&tq, qb, qr, (uint64_t)a.K, BN, kChunkK, CU_TENSOR_MAP_SWIZZLE_128B,
+                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    } else {
+        r = make_tmap_bf16_chunks(&tp, pb, pr, (uint64_t)a.K, kTileBP, (uint32_t)kc);
+        if (!r) r = make_tmap_bf16_chunks(&tq, qb, qr, (uint64_t)a.K, BN, (uint32_t)kc);
+    }
     if (r) return (int)cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid);
     cfg.blockDim = dim3(kTileThreads);
-    cfg.dynamicSmemBytes = (size_t)tile_smem_bytes_bn(p.stages, BN);
+    cfg.dynamicSmemBytes = (size_t)tile_smem_bytes_bn(p.stages, BN, kc);
     cfg.stream = (cudaStream_t)a.stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -332,7 +350,7 @@ int tile_launch_bn(const LaunchArgs &a, const bf16l_plan &p) {
     cfg.numAttrs = 1;
     return (int)cudaLaunchKernelEx(&cfg, tile_kernel<BN, SWAP, OutT>, tp, tq, static_cast<const uint16_t *>(a.bias),
                                    static_cast<OutT *>(a.out), a.M, a.N, a.K, p.stages,
-                                   p.split_k > 0 ? p.split_k : (SWAP ? 0 : kTileDefaultGroup), a.status,
+                                   p.split_k > 0 ? p.split_k : (SWAP ? 0 : kTileDefaultGroup), kc, a.status,
                                    static_cast<const float *>(nullptr), static_cast<const float *>(nullptr));
 }
 

@@ -375,6 +375,46 @@ def test_tile_tactic_space(lib):
     assert e.value.status == -6
 
 
+def test_two_chunk_stage_rules(lib):
+    """chunks_per_stage: 0 or 1 is one 64-wide K chunk per ring stage, 2 is two (the ring kernels only, K a
+    multiple of 64); the stage count then counts double stages against the same shared memory, and a
+    split-K plan may not have more ranks than double stages."""
+    mk = lambda k, **f: lib.make_plan(k, **f)
+    tile = dict(threads=192, rows_per_cta=192, tokens_per_cta=128)
+    assert lib.plan_check(256, 14336, 4096, mk("tile", stages=2, chunks_per_stage=2, **tile)).grid == 150
+    with pytest.raises(lib.BF16LinearError):  # 3 double stages of 40 KB chunks do not fit 227 KB
+        lib.plan_check(256, 14336, 4096, mk("tile", stages=3, chunks_per_stage=2, **tile))
+    tt = dict(threads=192, rows_per_cta=128, tokens_per_cta=64)
+    assert lib.plan_check(64, 14336, 4096, mk("tile_t", stages=4, chunks_per_stage=2, **tt)).grid == 112
+    with pytest.raises(lib.BF16LinearError):
+        lib.plan_check(64, 14336, 4096, mk("tile_t", stages=5, chunks_per_stage=2, **tt))
+    sk = dict(threads=128, rows_per_cta=64, tokens_per_cta=16)
+    assert lib.plan_check(16, 2112, 7168, mk("splitk", split_k=8, stages=4, chunks_per_stage=2, **sk)).grid == 264
+    # 2880 = 45 chunks = 23 double stages: 23 ranks at most
+    assert lib.plan_check(1, 128, 2880, mk("splitk_ws", split_k=23, stages=1, chunks_per_stage=2, **sk)).grid == 46
+    with pytest.raises(lib.BF16LinearError):
+        lib.plan_check(1, 128, 2880, mk("splitk_ws", split_k=24, stages=1, chunks_per_stage=2, **sk))
+    assert lib.plan_check(1, 128, 2880, mk("splitk_ws", split_k=45, stages=1, **sk)).grid == 90
+    for bad in (dict(chunks_per_stage=3), dict(chunks_per_stage=-1)):
+        with pytest.raises(lib.BF16LinearError):
+            lib.plan_check(16, 2112, 7168, mk("splitk", split_k=8, stages=2, **dict(sk, **bad)))
+    for other in (mk("dotprod", threads=128, rows_per_cta=2, chunks_per_stage=2),
+                  mk("tile2", threads=192, rows_per_cta=256, tokens_per_cta=256, stages=4, chunks_per_stage=2),
+                  mk("dotmma", threads=128, rows_per_cta=8, split_k=4, stages=1, chunks_per_stage=2)):
+        with pytest.raises(lib.BF16LinearError) as e:
+            lib.plan_check(16, 2112, 7168, other)
+        assert e.value.status == -1
+    with pytest.raises(lib.BF16LinearError) as e:  # K % 64 != 0: no chunked view of the matrices
+        lib.plan_check(16, 2112, 7176, mk("splitk", split_k=8, stages=2, chunks_per_stage=2, **sk))
+    assert e.value.status == -6
+    assert lib.plan_check(16, 2112, 7176, mk("splitk", split_k=8, stages=2, chunks_per_stage=1, **sk)).grid == 264
+    # the dispatcher's plans always pass their own check, whatever chunks they carry
+    for (M, N, K) in [(16, 2112, 7168), (64, 14336, 4096), (256, 14336, 4096), (32, 2112, 7168)]:
+        q = lib.plan(M, N, K)
+        assert q.chunks_per_stage in (0, 1, 2)
+        assert lib.plan_check(M, N, K, q).grid == q.grid
+
+
 def test_launch_flags_validated_without_gpu(lib):
     """Unknown flag bits, and the early-weights mode together with the serial one, are refused before any
     CUDA call; the plan check applies the same rule to a plan's flags."""
