@@ -990,13 +990,17 @@ def mxfp8_arm(args, points):
 
     x and W are quantised once on the device with the library's own bf16_quant_mxfp8; the weight
     codes and scales are rotated over copies totalling >= 256 MB; one CUDA graph of R back-to-back
-    calls per shape; algorithmic bytes NK + N(K/32) + MK + M(K/32) + 2MN (+2N bias)."""
+    calls per shape; algorithmic bytes NK + N(K/32) + MK + M(K/32) + 2MN (+2N bias), flops 2MNK.
+    Shapes above the e4m3 ridge (twice the measured bf16 peak, the nominal ratio, over the HBM copy
+    peak) are reported against that tensor peak, the others against HBM.  With --sweep-fp8 the tile
+    form's tactics (rows per tile, ring depth, raster group) are timed too and the best is reported."""
     import moe_router_gemm_gb300 as lib
     from moe_router_gemm_gb300 import build as _build
     _build.build()
     device = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.Stream(device)
     peaks = load_peaks()
+    fp8_tflops = 2.0 * peaks["bf16_tflops"]
     res = {}
     for pt in points:
         M, N, K, bias = pt["M"], pt["N"], pt["K"], pt["bias"]
@@ -1010,34 +1014,55 @@ def mxfp8_arm(args, points):
         Ws = [ws0] + [ws0.clone() for _ in range(R - 1)]
         bd = b.to(device) if b is not None else None
         out = torch.empty(M, N, dtype=torch.bfloat16, device=device)
-        with torch.cuda.stream(stream):
-            for i in range(2):
-                lib.bf16_linear_mxfp8(xq, xs, Wq[i % R], Ws[i % R], bd, out=out, stream=stream)
-            torch.cuda.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for i in range(R):
-                    lib.bf16_linear_mxfp8(xq, xs, Wq[i], Ws[i], bd, out=out, stream=stream)
-            g.replay()
-            torch.cuda.synchronize()
-            ms = []
-            for _ in range(max(3, args.steps)):
-                a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                g.replay()
-                e.record(stream)
+
+        def time_us(plan=None):
+            with torch.cuda.stream(stream):
+                for i in range(2):
+                    lib.bf16_linear_mxfp8(xq, xs, Wq[i % R], Ws[i % R], bd, out=out, stream=stream, plan_=plan)
                 torch.cuda.synchronize()
-                ms.append(a.elapsed_time(e))
-        us = 1000.0 * statistics.median(ms) / R
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for i in range(R):
+                        lib.bf16_linear_mxfp8(xq, xs, Wq[i], Ws[i], bd, out=out, stream=stream, plan_=plan)
+                g.replay()
+                torch.cuda.synchronize()
+                ms = []
+                for _ in range(max(3, args.steps)):
+                    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    g.replay()
+                    e.record(stream)
+                    torch.cuda.synchronize()
+                    ms.append(a.elapsed_time(e))
+            del g
+            return 1000.0 * statistics.median(ms) / R
+
+        us = time_us()
         nbytes = N * K + N * (K // 32) + M * K + M * (K // 32) + 2 * M * N + (2 * N if bias else 0)
-        res[f"M{M}_N{N}_K{K}"] = {"us": round(us, 3), "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
-                                  "pct_hbm_roofline": round(100.0 * nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 1),
-                                  "split_k": lib.mxfp8_split(M, N, K)}
+        flops = 2.0 * M * N * K
+        tensor = flops / nbytes > fp8_tflops * 1e12 / (peaks["hbm_gbs"] * 1e9)
+        rec = {"us": round(us, 3), "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
+               "TFLOPs": round(flops / (us * 1e-6) / 1e12, 1), "bound": "tensor" if tensor else "hbm",
+               "frac": round(flops / (us * 1e-6) / 1e12 / fp8_tflops if tensor
+                             else nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
+        if args.sweep_fp8 and M > 16 and K % 128 == 0:
+            tried = []
+            for bq, most in ((128, 6), (256, 4)):
+                for st in (most, most - 1):
+                    for grp in (0, 1, 4, 16):
+                        p = lib.make_plan("tile", threads=320, rows_per_cta=bq, stages=st, split_k=grp)
+                        tried.append((time_us(p), f"tile bq={bq} stages={st} group={grp}"))
+            tried.sort()
+            rec["best_tile_us"], rec["best_tile"] = round(tried[0][0], 3), tried[0][1]
+            rec["tile_top5"] = [[round(u, 3), d] for u, d in tried[:5]]
+        res[f"M{M}_N{N}_K{K}" + ("_bias" if bias else "")] = rec
         del Wq, Ws
         torch.cuda.empty_cache()
     mean = statistics.mean(v["us"] for v in res.values()) if res else None
     print(json.dumps({"mode": "mxfp8", "metric": "MXFP8 linear us per call (L2-cold)",
                       "mean_us": None if mean is None else round(mean, 4), "unit": "us/call",
+                      "peaks": {"hbm_gbs": peaks["hbm_gbs"], "e4m3_tflops": fp8_tflops,
+                                "e4m3_note": "twice the measured bf16 burst (nominal e4m3:bf16 ratio)"},
                       "workload": workload_desc(args.workload), "shapes": res}))
 
 
@@ -1054,7 +1079,8 @@ def main():
     ap.add_argument("--workload", default="router", choices=["router", "smallest", "decode", "mlp", "prefill", "all"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--sweep-fp8", action="store_true", help="with --fp8: also time every (split, threads)")
+    ap.add_argument("--sweep-fp8", action="store_true",
+                    help="with --fp8: also time every (split, threads); with --mxfp8: the tile form's tactics")
     ap.add_argument("--fp8", action="store_true",
                     help="time the per-tensor FP8 linear (bf16_linear_fp8) on the workload's shapes instead")
     ap.add_argument("--mxfp8", action="store_true",

@@ -471,7 +471,8 @@ int bf16_linear_probe_read(const void *src, size_t bytes, int grid, int threads,
  *   16-byte aligned; out must not overlap the inputs.  Any M.  Small M:
  *   warp-level e4m3 MMAs, one per scale block, K split over a cluster, in
  *   groups of 16 tokens.  M > 16 with at least 32 tiles of 128 x 256 and
- *   K % 128 == 0: the tcgen05 tile form, one block-scaled MMA
+ *   K % 128 == 0: the tcgen05 tile form (256 W rows per tile, a three-stage
+ *   ring), one block-scaled MMA
  *   (kind::mxf8f6f4.block_scale) per scale block with the scales staged into
  *   tensor memory (xs and ws 4-byte aligned, else BF16L_EALIGN).  Launches one
  *   kernel, allocates nothing.  Block-scale products 2^(xs+ws-254) outside

@@ -614,6 +614,19 @@ __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
     }
 }
 
+// Bias of one 32-column slice n0..n0+31 of the output, one value per lane
+// (lane l holds bias[n0 + l], 0 past N or without bias): one coalesced load per
+// warp instead of 32 scalar loads per thread.  bias_add32 hands the values to
+// every lane with shuffles; both must be called by all 32 lanes of the warp.
+__device__ __forceinline__ float bias_lane(const uint16_t *bias, int n0, int N) {
+    const int n = n0 + (int)(threadIdx.x & 31u);
+    return (bias && n < N) ? bf16_to_f32(__ldg(bias + n)) : 0.0f;
+}
+__device__ __forceinline__ void bias_add32(float (&v)[32], float lane_bias) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] += __shfl_sync(0xFFFFFFFFu, lane_bias, j);
+}
+
 // Programmatic dependent launch hooks (no-ops when the launch did not enable PDL).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {

@@ -421,33 +421,35 @@ __global__ void __launch_bounds__(kMxtThreads, 1)
             int p0, q0;
             mxt_coords(t, p_tiles, q_tiles, G, BQ, p0, q0);
             const int b = tile_iter % kNbuf, use = tile_iter / kNbuf;
+            // The tile's bias, one value per lane and 32-column slice, read while the MMAs run.
+            pdl_wait();  // bias may be written by the previous kernel
+            float lbs[BQ / 32];
+#pragma unroll
+            for (int i = 0; i < BQ / 32; ++i) lbs[i] = bias_lane(bias, q0 + 32 * i, N);
             const bool ok = mbar_wait(&sh.acc_full[b], use & 1, status, kSiteAccum);
             tc_fence_after();
-            const bool have = ok && !*((volatile int32_t *)&sh.aborted);
+            // warp-uniform, so that the bias shuffles below run on all 32 lanes
+            const bool have = __all_sync(0xFFFFFFFFu, ok && !*((volatile int32_t *)&sh.aborted));
             const int m = p0 + row;
             const uint32_t acc = tmem + (uint32_t)(b * BQ) + ((uint32_t)(quarter * 32) << 16);
             if (have) {
-                pdl_wait();
-#pragma unroll 1
+#pragma unroll
                 for (int c = 0; c < BQ; c += 32) {
+                    const float lb = lbs[c / 32];
                     uint32_t r0[16], r1[16];
                     tmem_ld16(acc + (uint32_t)c, r0);
                     tmem_ld16(acc + (uint32_t)(c + 16), r1);
                     tmem_ld_wait16(r0);
                     tmem_ld_wait16(r1);
                     const int n = q0 + c;
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        v[j] = __uint_as_float(r0[j]);
+                        v[16 + j] = __uint_as_float(r1[j]);
+                    }
+                    if (bias && n < N) bias_add32(v, lb);  // warp-uniform condition
                     if (m < M && n < N) {
-                        float v[32];
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            v[j] = __uint_as_float(r0[j]);
-                            v[16 + j] = __uint_as_float(r1[j]);
-                        }
-                        if (bias) {
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (n + j < N) v[j] += bf16_to_f32(bias[n + j]);
-                        }
                         uint16_t *o = out + (size_t)m * N + n;
                         if (vec_ok && n + 32 <= N) {
 #pragma unroll

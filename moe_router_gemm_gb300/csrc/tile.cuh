@@ -216,17 +216,25 @@ __global__ void __launch_bounds__(kTileThreads, 1)
             int p0, q0;
             tile_coords(t, p_tiles, q_tiles, G, BN, p0, q0);
             const int b = tile_iter & 1;
+            const int p = p0 + row;  // x row (plain) or W row (swap) of this thread
+            // The tile's bias, read while the MMAs run: plain form one value per lane and 32-column slice
+            // (bias_lane), swap form this thread's W row.
+            pdl_wait();  // bias may be written by the previous kernel
+            constexpr int kSlices = (BN + 31) / 32;
+            float lbs[kSlices];
+#pragma unroll
+            for (int i = 0; i < kSlices; ++i) lbs[i] = SWAP ? 0.0f : bias_lane(bias, q0 + 32 * i, N);
+            const float bias_row = (SWAP && bias && p < N) ? bf16_to_f32(bias[p]) : 0.0f;
             const bool ok = mbar_wait(&sh.acc_full[b], (tile_iter / 2) & 1, status, kSiteAccum);
             tc_fence_after();
-            const bool have = ok && !*((volatile int32_t *)&sh.aborted);
-            const int p = p0 + row;  // x row (plain) or W row (swap) of this thread
+            // warp-uniform, so that the bias shuffles below run on all 32 lanes
+            const bool have = __all_sync(0xFFFFFFFFu, ok && !*((volatile int32_t *)&sh.aborted));
             const uint32_t acc = tmem + (uint32_t)(b * kAccStride) + ((uint32_t)(quarter * 32) << 16);
             if (have) {
-                pdl_wait();
                 const float sxw = F8 ? __ldg(scale_x) * __ldg(scale_w) : 1.0f;
-                const float bias_row = (SWAP && bias && p < N) ? bf16_to_f32(bias[p]) : 0.0f;
-                // cnt (16 or 32) accumulator columns starting at column c, this thread's row
-                auto emit = [&](int c, const float *vin, int cnt) {
+                // cnt (16 or 32) accumulator columns starting at column c, this thread's row;
+                // lb: the plain form's bias for columns q0 + c + lane (bias_lane)
+                auto emit = [&](int c, const float *vin, int cnt, float lb) {
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = j < cnt ? vin[j] * sxw : 0.0f;
@@ -240,12 +248,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                         }
                     } else {
                         const int n = q0 + c;
+                        if (bias && n < N) bias_add32(v, lb);  // warp-uniform condition
                         if (p < M && n < N) {
-                            if (bias) {
-#pragma unroll
-                                for (int j = 0; j < 32; ++j)
-                                    if (j < cnt && n + j < N) v[j] += bf16_to_f32(bias[n + j]);
-                            }
                             OutT *o = out + (size_t)p * N + n;
                             if (vec_ok && n + cnt <= N) {
 #pragma unroll
@@ -259,8 +263,9 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                         }
                     }
                 };
-#pragma unroll 1
+#pragma unroll
                 for (int c = 0; c + 32 <= BN; c += 32) {
+                    const float lb = lbs[c / 32];
                     uint32_t r0[16], r1[16];
                     tmem_ld16(acc + (uint32_t)c, r0);
                     tmem_ld16(acc + (uint32_t)(c + 16), r1);
@@ -272,16 +277,17 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                         v[j] = __uint_as_float(r0[j]);
                         v[16 + j] = __uint_as_float(r1[j]);
                     }
-                    emit(c, v, 32);
+                    emit(c, v, 32, lb);
                 }
                 if constexpr (BN % 32 != 0) {  // the last 16 columns
+                    const float lb = lbs[kSlices - 1];  // columns BN - 16 .. BN - 1: lanes 0..15
                     uint32_t r0[16];
                     tmem_ld16(acc + (uint32_t)(BN - 16), r0);
                     tmem_ld_wait16(r0);
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r0[j]);
-                    emit(BN - 16, v, 16);
+                    emit(BN - 16, v, 16, lb);
                 }
             }
             tc_fence_before();
