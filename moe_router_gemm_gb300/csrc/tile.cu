@@ -64,7 +64,7 @@ int launch_tile_fp8(const void *xq, const void *wq, const float *sx, const float
     cfg.numAttrs = 1;
     return (int)cudaLaunchKernelEx(&cfg, tile_kernel<256, false, uint16_t, true>, tx, tw,
                                    static_cast<const uint16_t *>(bias), static_cast<uint16_t *>(out), M, N, K, stages,
-                                   kTileDefaultGroup, 1, status, sx, sw);
+                                   kTileDefaultGroup, status, sx, sw);
 }
 
 }  // namespace bf16l

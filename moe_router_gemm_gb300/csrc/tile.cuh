@@ -75,14 +75,16 @@ __device__ __forceinline__ void tile_coords(int t, int p_tiles, int q_tiles, int
 // holds 128 codes instead of 64 bf16 values, each MMA (kind::f8f6f4) takes 32
 // of them, and the epilogue scales the fp32 sum by *scale_x * *scale_w before
 // bias; the shared-memory geometry of a stage is the same.  K counts elements.
-template <int BN, bool SWAP, typename OutT, bool F8 = false>
+template <int BN, bool SWAP, typename OutT, bool F8 = false, int KC = 1>
 __global__ void __launch_bounds__(kTileThreads, 1)
     tile_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_q,
                 const uint16_t *__restrict__ bias, OutT *__restrict__ out, int M, int N, int K, int stages,
-                int group, int kc, int32_t *status, const float *__restrict__ scale_x,
+                int group, int32_t *status, const float *__restrict__ scale_x,
                 const float *__restrict__ scale_w) {
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N: a multiple of 16 up to 256");
     static_assert(!(SWAP && F8), "the e4m3 form is plain only");
+    static_assert(KC == 1 || (KC == 2 && !F8), "two-chunk stages: bf16 only");
+    constexpr int kc = KC;  // K chunks per ring stage (a template parameter: the issue loops stay minimal)
     constexpr int kChunk = F8 ? 2 * kChunkK : kChunkK;  // elements per 128-byte row
     constexpr int kQBytes = BN * 128;  // one chunk of the N-side operand
     constexpr int kAccStride = tile_acc_stride(BN);
@@ -92,7 +94,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     // A stage holds kc consecutive K chunks: kc P chunk tiles, then kc Q chunk tiles.
-    const int stage_bytes = kc * tile_stage_bytes(BN);
+    constexpr int stage_bytes = kc * tile_stage_bytes(BN);
     TileShared &sh = *reinterpret_cast<TileShared *>(ring + stages * stage_bytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -144,7 +146,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                     if (*((volatile int32_t *)&sh.aborted)) goto producer_done;
                     uint8_t *st = ring + s * stage_bytes;
                     mbar_arrive_expect_tx(&sh.full[s], (uint32_t)stage_bytes);
-                    if (kc == 1) {
+                    if constexpr (kc == 1) {
                         tma_load_2d(st, &tm_p, &sh.full[s], c * kChunk, p0);
                         tma_load_2d(st + kTileABytes, &tm_q, &sh.full[s], c * kChunk, q0);
                     } else {  // chunked maps: {64, rows, chunks}
@@ -182,7 +184,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                     }
                     tc_fence_after();
                     const uint8_t *st = ring + s * stage_bytes;
-#pragma unroll 1
+#pragma unroll
                     for (int j = 0; j < kc; ++j) {
                         const uint64_t adesc = smem_desc_sw128(smem_u32(st + j * kTileABytes));
                         const uint64_t bdesc = smem_desc_sw128(smem_u32(st + kc * kTileABytes + j * kQBytes));
@@ -321,43 +323,52 @@ inline int tile_smem_bytes_bn(int stages, int bn, int kc = 1) {
 
 template <int BN, bool SWAP, typename OutT>
 int tile_set_attr() {
-    return (int)cudaFuncSetAttribute(tile_kernel<BN, SWAP, OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     tile_smem_bytes_bn(tile_max_stages(BN), BN));
+    const int bytes = tile_smem_bytes_bn(tile_max_stages(BN), BN);  // covers every valid (stages, chunks)
+    int e = (int)cudaFuncSetAttribute(tile_kernel<BN, SWAP, OutT, false, 1>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (!e)
+        e = (int)cudaFuncSetAttribute(tile_kernel<BN, SWAP, OutT, false, 2>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    return e;
 }
 
-// One launch of the bf16 form: P rows of 128 from tm_p, Q rows of BN from tm_q.
-template <int BN, bool SWAP, typename OutT>
-int tile_launch_bn(const LaunchArgs &a, const bf16l_plan &p) {
+// One launch of the bf16 form: P rows of 128 from tm_p, Q rows of BN from tm_q, KC chunks per stage.
+template <int BN, bool SWAP, typename OutT, int KC>
+int tile_launch_kc(const LaunchArgs &a, const bf16l_plan &p) {
     CUtensorMap tp, tq;
     const void *pb = SWAP ? a.W : a.x, *qb = SWAP ? a.x : a.W;
     const uint64_t pr = SWAP ? (uint64_t)a.N : (uint64_t)a.M, qr = SWAP ? (uint64_t)a.M : (uint64_t)a.N;
-    const int kc = p.chunks_per_stage == 2 ? 2 : 1;  // validated by the plan check (K % 64 == 0)
     int r;
-    if (kc == 1) {
+    if (KC == 1) {
         r = make_tmap_bf16_2d(&tp, pb, pr, (uint64_t)a.K, kTileBP, kChunkK, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
         if (!r)
             r = make_tmap_bf16_2d(&tq, qb, qr, (uint64_t)a.K, BN, kChunkK, CU_TENSOR_MAP_SWIZZLE_128B,
                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-    } else {
-        r = make_tmap_bf16_chunks(&tp, pb, pr, (uint64_t)a.K, kTileBP, (uint32_t)kc);
-        if (!r) r = make_tmap_bf16_chunks(&tq, qb, qr, (uint64_t)a.K, BN, (uint32_t)kc);
+    } else {  // the chunked view: one box brings KC chunks (the plan check asked for K % 64 == 0)
+        r = make_tmap_bf16_chunks(&tp, pb, pr, (uint64_t)a.K, kTileBP, (uint32_t)KC);
+        if (!r) r = make_tmap_bf16_chunks(&tq, qb, qr, (uint64_t)a.K, BN, (uint32_t)KC);
     }
     if (r) return (int)cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid);
     cfg.blockDim = dim3(kTileThreads);
-    cfg.dynamicSmemBytes = (size_t)tile_smem_bytes_bn(p.stages, BN, kc);
+    cfg.dynamicSmemBytes = (size_t)tile_smem_bytes_bn(p.stages, BN, KC);
     cfg.stream = (cudaStream_t)a.stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl_attr_of((uint32_t)p.flags);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return (int)cudaLaunchKernelEx(&cfg, tile_kernel<BN, SWAP, OutT>, tp, tq, static_cast<const uint16_t *>(a.bias),
-                                   static_cast<OutT *>(a.out), a.M, a.N, a.K, p.stages,
-                                   p.split_k > 0 ? p.split_k : (SWAP ? 0 : kTileDefaultGroup), kc, a.status,
+    return (int)cudaLaunchKernelEx(&cfg, tile_kernel<BN, SWAP, OutT, false, KC>, tp, tq,
+                                   static_cast<const uint16_t *>(a.bias), static_cast<OutT *>(a.out), a.M, a.N, a.K,
+                                   p.stages, p.split_k > 0 ? p.split_k : (SWAP ? 0 : kTileDefaultGroup), a.status,
                                    static_cast<const float *>(nullptr), static_cast<const float *>(nullptr));
+}
+
+template <int BN, bool SWAP, typename OutT>
+int tile_launch_bn(const LaunchArgs &a, const bf16l_plan &p) {
+    return p.chunks_per_stage == 2 ? tile_launch_kc<BN, SWAP, OutT, 2>(a, p) : tile_launch_kc<BN, SWAP, OutT, 1>(a, p);
 }
 
 }  // namespace bf16l
