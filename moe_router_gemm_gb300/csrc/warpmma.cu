@@ -107,6 +107,15 @@ __global__ void __launch_bounds__(NT, XR ? 1 : 1024 / NT)
             }
         }
     };
+    // One L2 prefetch per lane of a batch's 32 lines (8 NG rows x U / 2 lines of 128 bytes), issued one batch
+    // ahead so the next loads find their lines in L2.
+    auto prefetch_batch = [&](int qn, int vb) {
+        if (qn >= q1 || vb >= vb1) return;
+        const int row = 8 * NG * qn + lane / (U / 2);
+        const int v = vb + 8 * (lane % (U / 2));  // first 16-byte vector of this lane's 128-byte line
+        if (row < N && v < vb1)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(W + (size_t)row * RB + (size_t)v * 16));
+    };
     int q = q0 + grp;
     if (q < q1) load_batch(8 * NG * q, vb0);
 
@@ -138,6 +147,10 @@ __global__ void __launch_bounds__(NT, XR ? 1 : 1024 / NT)
             for (int i = 0; i < 2; ++i) c[j][i][0] = c[j][i][1] = c[j][i][2] = c[j][i][3] = 0.f;
         for (int vb = vb0; vb < vb1; vb += 4 * U) {  // warp-uniform trip count: mma.sync is warp-wide
             if (!(first && vb == vb0)) load_batch(n0, vb);
+            if (vb + 4 * U < vb1)
+                prefetch_batch(q, vb + 4 * U);
+            else
+                prefetch_batch(q + groups, vb0);
             uint4 xl[XR ? U : 1], xh[XR ? U : 1];
             if constexpr (XR) {  // this batch's x fragments, in flight with the weights
 #pragma unroll
