@@ -107,6 +107,15 @@ __global__ void __launch_bounds__(NT, TT == 1 ? 1024 / NT : 1)
             wv[u] = (vv < wv1 && row < N) ? ldg_stream_v4(wr + vv) : make_uint4(0u, 0u, 0u, 0u);
         }
     };
+    // One L2 prefetch per lane of a batch's 32 lines (8 rows x 4 lines of 128 bytes), issued one batch ahead
+    // so the next loads find their lines in L2.
+    auto prefetch_batch = [&](int qn, int vb) {
+        if (qn >= q1 || vb >= wv1) return;
+        const int row = 8 * qn + lane / (U / 2);
+        const int v = vb + 8 * (lane % (U / 2));  // first 16-byte vector of this lane's line
+        if (row < N && v < wv1)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(W + (size_t)row * RB + (size_t)v * 16));
+    };
     int q = q0 + grp;
     bool pre = q < q1;
     if (pre) load_batch(8 * q, wv0);
@@ -152,6 +161,10 @@ __global__ void __launch_bounds__(NT, TT == 1 ? 1024 / NT : 1)
         if (ok) {
             for (int vb = wv0; vb < wv1; vb += 4 * U) {  // warp-uniform trip count: mma.sync is warp-wide
                 if (!(pre && vb == wv0)) load_batch(n0, vb);
+                if (vb + 4 * U < wv1)
+                    prefetch_batch(q, vb + 4 * U);
+                else
+                    prefetch_batch(q + GW, wv0);
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int vv = vb + 4 * u + t;
