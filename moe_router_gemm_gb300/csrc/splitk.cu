@@ -34,8 +34,12 @@
 //     griddepcontrol.wait, x and the output only after it, and every CTA lets
 //     the next kernel start as soon as its own weight loads are issued.
 //
-// Grid: (S, ceil(N/BN)) with cluster dims (S, 1, 1); rank r takes K chunks
-// [r*C/S, (r+1)*C/S) of the C = ceil(K/64) chunks.
+//   * Two-chunk stages (kc = 2, K % 64 == 0): one 3-D box per operand brings two
+//     consecutive K chunks (the matrix seen as {64, rows, K / 64}); the ranks then
+//     split K in units of two chunks.
+//
+// Grid: (S, ceil(N/BN)) with cluster dims (S, 1, 1); rank r takes ring stages
+// [r*C/S, (r+1)*C/S) of the C = ceil(K / (64 kc)) stages.
 #include "common.cuh"
 #include "kernels.h"
 

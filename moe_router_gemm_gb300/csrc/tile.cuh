@@ -12,7 +12,9 @@
 //
 // This kernel keeps the roles and rebuilds the rest for GB300:
 //   * tile 128 (MMA M) x BN (MMA N), K in 64-wide chunks (one 128-byte swizzle
-//     row) through a ring of `stages` TMA stages of (128 + BN) x 128 bytes;
+//     row) through a ring of `stages` TMA stages of (128 + BN) x 128 bytes; with
+//     KC = 2 a stage holds two chunks, brought by one 3-D box per operand (the
+//     matrix seen as {64, rows, K / 64}), so half as many loads are issued;
 //   * orientation: P is the operand on the MMA M side (128 rows per tile), Q
 //     the one on the N side (BN rows per tile).  Plain form (tile.cu): P = x,
 //     Q = W, so each tile is 128 tokens x BN weight rows.  Swap-AB form
@@ -28,9 +30,11 @@
 //   * persistent grid (at most one CTA per SM) walking the tiles in raster
 //     groups of `group` Q-tiles (Q fastest inside a group, then P), so the
 //     CTAs running together share both operands in L2;
-//   * epilogue: 4 warps, TMEM lane = P row; 16 or 32 columns at a time ->
-//     + bias -> bf16 (RNE) -> stores (16-byte vectors along a row of out in
-//     the plain form; in the swap form each column is one token's row of
+//   * epilogue: 4 warps, TMEM lane = P row; the tile's bias read before the
+//     accumulator wait (one coalesced load per 32 columns, handed to the lanes
+//     by shuffles); 16 or 32 columns at a time -> + bias -> bf16 (RNE) ->
+//     stores (16-byte vectors along a row of out in the plain form; in the
+//     swap form each column is one token's row of
 //     out, and a warp's 32 lanes store 32 consecutive outputs of it).
 // Waits are bounded (1 s) and record their site in the status word.
 #pragma once
