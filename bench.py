@@ -458,6 +458,7 @@ def gpu_arm(args, points, rank, world):
         records = {}
         for name in ("smallest", "decode", "mlp", "prefill"):
             records[name] = workload_record(name, lib, device, stream, peaks, max(3, args.sub_replays))
+        records["prefill_mxfp8"] = mxfp8_record(lib, device, stream, peaks, max(3, args.sub_replays))
 
     return dict(shapes=shapes, per_shape_us=per_shape_us, total_ms=total_ms, launches=launches,
                 clocks=clocks, e2e=e2e, pdl_us=pdl_us, serial_us=serial_us, warm_us=warm_us, floor=floor,
@@ -985,15 +986,79 @@ def fp8_arm(args, points):
                       "workload": workload_desc(args.workload), "shapes": res}))
 
 
-def mxfp8_arm(args, points):
-    """MXFP8 linear (bf16_linear_mxfp8) on the workload's shapes, L2-cold, beside the bf16 call.
+def mxfp8_shape(lib, device, stream, pt, steps, peaks, plan=None):
+    """One shape of the MXFP8 linear (bf16_linear_mxfp8), L2-cold: x and W quantised once on the device
+    with bf16_quant_mxfp8, the weight codes and scales rotated over copies totalling >= 256 MB, one CUDA
+    graph of R back-to-back calls; algorithmic bytes NK + N(K/32) + MK + M(K/32) + 2MN (+2N bias), flops
+    2MNK.  Shapes above the e4m3 ridge (twice the measured bf16 burst peak, the nominal ratio, over the
+    HBM copy peak) are reported against that tensor peak, the others against HBM.  Returns
+    (record, time_fn) where time_fn(plan) re-times the shape with another plan."""
+    M, N, K, bias = pt["M"], pt["N"], pt["K"], pt["bias"]
+    fp8_tflops = 2.0 * peaks["bf16_tflops"]
+    x, W, b = wl.make_inputs(M, N, K, pt["seed"], bias)
+    xq, xs = lib.quant_mxfp8(x.to(device))
+    wq0, ws0 = lib.quant_mxfp8(W.to(device))
+    R = max(2, -(-L2_COLD_BYTES // (N * K)))
+    Wq = [wq0] + [wq0.clone() for _ in range(R - 1)]
+    Ws = [ws0] + [ws0.clone() for _ in range(R - 1)]
+    bd = b.to(device) if b is not None else None
+    out = torch.empty(M, N, dtype=torch.bfloat16, device=device)
 
-    x and W are quantised once on the device with the library's own bf16_quant_mxfp8; the weight
-    codes and scales are rotated over copies totalling >= 256 MB; one CUDA graph of R back-to-back
-    calls per shape; algorithmic bytes NK + N(K/32) + MK + M(K/32) + 2MN (+2N bias), flops 2MNK.
-    Shapes above the e4m3 ridge (twice the measured bf16 peak, the nominal ratio, over the HBM copy
-    peak) are reported against that tensor peak, the others against HBM.  With --sweep-fp8 the tile
-    form's tactics (rows per tile, ring depth, raster group) are timed too and the best is reported."""
+    def time_us(pl=None):
+        with torch.cuda.stream(stream):
+            for i in range(2):
+                lib.bf16_linear_mxfp8(xq, xs, Wq[i % R], Ws[i % R], bd, out=out, stream=stream, plan_=pl)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(R):
+                    lib.bf16_linear_mxfp8(xq, xs, Wq[i], Ws[i], bd, out=out, stream=stream, plan_=pl)
+            g.replay()
+            torch.cuda.synchronize()
+            ms = []
+            for _ in range(max(3, steps)):
+                a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g.replay()
+                e.record(stream)
+                torch.cuda.synchronize()
+                ms.append(a.elapsed_time(e))
+        del g
+        return 1000.0 * statistics.median(ms) / R
+
+    us = time_us(plan)
+    nbytes = N * K + N * (K // 32) + M * K + M * (K // 32) + 2 * M * N + (2 * N if bias else 0)
+    flops = 2.0 * M * N * K
+    tensor = flops / nbytes > fp8_tflops * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    rec = {"M": M, "N": N, "K": K, "bias": bias, "us": round(us, 3), "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
+           "TFLOPs": round(flops / (us * 1e-6) / 1e12, 1), "bound": "tensor" if tensor else "hbm",
+           "frac": round(flops / (us * 1e-6) / 1e12 / fp8_tflops if tensor
+                         else nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
+    return rec, time_us
+
+
+def mxfp8_record(lib, device, stream, peaks, steps):
+    """The MXFP8 linear on the prefill workload's shapes (its tile form), for the default bench line."""
+    rows, tot_flops, tot_us = [], 0.0, 0.0
+    for pt in workload_points("prefill"):
+        rec, time_fn = mxfp8_shape(lib, device, stream, pt, steps, peaks)
+        del time_fn  # frees the shape's weight copies
+        rows.append(rec)
+        tot_flops += 2.0 * rec["M"] * rec["N"] * rec["K"]
+        tot_us += rec["us"]
+        torch.cuda.empty_cache()
+    tf = tot_flops / (tot_us * 1e-6) / 1e12
+    return {"workload": workload_desc("prefill") + "; MXFP8 operands (bf16_quant_mxfp8 of the same inputs)",
+            "unit": "us/call", "shapes": rows, "tensor_TFLOPs": round(tf, 1),
+            "e4m3_peak_TFLOPs": round(2.0 * peaks["bf16_tflops"], 1),
+            "tensor_frac": round(tf / (2.0 * peaks["bf16_tflops"]), 4),
+            "peak_note": "twice the measured bf16 burst peak (the nominal e4m3:bf16 ratio)"}
+
+
+def mxfp8_arm(args, points):
+    """MXFP8 linear (bf16_linear_mxfp8) on the workload's shapes, L2-cold (mxfp8_shape).  With
+    --sweep-fp8 the tile form's tactics (rows per tile, ring depth, raster group) are timed too and the
+    best is reported."""
     import moe_router_gemm_gb300 as lib
     from moe_router_gemm_gb300 import build as _build
     _build.build()
@@ -1006,45 +1071,7 @@ def mxfp8_arm(args, points):
         M, N, K, bias = pt["M"], pt["N"], pt["K"], pt["bias"]
         if K % 32:
             continue
-        x, W, b = wl.make_inputs(M, N, K, pt["seed"], bias)
-        xq, xs = lib.quant_mxfp8(x.to(device))
-        wq0, ws0 = lib.quant_mxfp8(W.to(device))
-        R = max(2, -(-L2_COLD_BYTES // (N * K)))
-        Wq = [wq0] + [wq0.clone() for _ in range(R - 1)]
-        Ws = [ws0] + [ws0.clone() for _ in range(R - 1)]
-        bd = b.to(device) if b is not None else None
-        out = torch.empty(M, N, dtype=torch.bfloat16, device=device)
-
-        def time_us(plan=None):
-            with torch.cuda.stream(stream):
-                for i in range(2):
-                    lib.bf16_linear_mxfp8(xq, xs, Wq[i % R], Ws[i % R], bd, out=out, stream=stream, plan_=plan)
-                torch.cuda.synchronize()
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    for i in range(R):
-                        lib.bf16_linear_mxfp8(xq, xs, Wq[i], Ws[i], bd, out=out, stream=stream, plan_=plan)
-                g.replay()
-                torch.cuda.synchronize()
-                ms = []
-                for _ in range(max(3, args.steps)):
-                    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
-                    g.replay()
-                    e.record(stream)
-                    torch.cuda.synchronize()
-                    ms.append(a.elapsed_time(e))
-            del g
-            return 1000.0 * statistics.median(ms) / R
-
-        us = time_us()
-        nbytes = N * K + N * (K // 32) + M * K + M * (K // 32) + 2 * M * N + (2 * N if bias else 0)
-        flops = 2.0 * M * N * K
-        tensor = flops / nbytes > fp8_tflops * 1e12 / (peaks["hbm_gbs"] * 1e9)
-        rec = {"us": round(us, 3), "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
-               "TFLOPs": round(flops / (us * 1e-6) / 1e12, 1), "bound": "tensor" if tensor else "hbm",
-               "frac": round(flops / (us * 1e-6) / 1e12 / fp8_tflops if tensor
-                             else nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
+        rec, time_us = mxfp8_shape(lib, device, stream, pt, args.steps, peaks)
         if args.sweep_fp8 and M > 16 and K % 128 == 0:
             tried = []
             for bq, most in ((128, 6), (256, 4)):
@@ -1056,7 +1083,7 @@ def mxfp8_arm(args, points):
             rec["best_tile_us"], rec["best_tile"] = round(tried[0][0], 3), tried[0][1]
             rec["tile_top5"] = [[round(u, 3), d] for u, d in tried[:5]]
         res[f"M{M}_N{N}_K{K}" + ("_bias" if bias else "")] = rec
-        del Wq, Ws
+        del time_us
         torch.cuda.empty_cache()
     mean = statistics.mean(v["us"] for v in res.values()) if res else None
     print(json.dumps({"mode": "mxfp8", "metric": "MXFP8 linear us per call (L2-cold)",
