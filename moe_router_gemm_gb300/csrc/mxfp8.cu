@@ -293,7 +293,10 @@ __device__ __forceinline__ void mxt_coords(int t, int p_tiles, int q_tiles, int 
     q0 = qi * bq;
 }
 
-template <int BQ>
+// V4: the scale rows are read 16 bytes (four chunks' words) at a time (K % 512 == 0, xs and ws 16-byte
+// aligned).  One 4-byte word per lane and chunk, from rows 128 or 256 bytes apart (K = 4096 or 8192),
+// measured 40% slower over the whole kernel than at any neighbouring K.
+template <int BQ, bool V4>
 __global__ void __launch_bounds__(kMxtThreads, 1)
     mxtile_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                   const uint8_t *__restrict__ xs, const uint8_t *__restrict__ ws, const uint16_t *__restrict__ bias,
@@ -486,6 +489,57 @@ __global__ void __launch_bounds__(kMxtThreads, 1)
                 inb[j] = rb < N;
                 wb[j] = reinterpret_cast<const uint32_t *>(ws + (size_t)(inb[j] ? rb : 0) * nb);
             }
+            if constexpr (V4) {
+                // words of chunks 4g..4g+3 in one 16-byte load per row; group g + 1 is in flight while g is used
+                const uint4 kOne = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+                const int ng = C / 4;
+                const uint4 *ga = reinterpret_cast<const uint4 *>(wa);
+                const uint4 *gb[kBcols];
+#pragma unroll
+                for (int j = 0; j < kBcols; ++j) gb[j] = reinterpret_cast<const uint4 *>(wb[j]);
+                uint4 ca = (ng > 0 && ra < M) ? __ldg(ga) : kOne, na = (ng > 1 && ra < M) ? __ldg(ga + 1) : kOne;
+                uint4 cbw[kBcols], nbw[kBcols];
+#pragma unroll
+                for (int j = 0; j < kBcols; ++j) {
+                    cbw[j] = (ng > 0 && inb[j]) ? __ldg(gb[j]) : kOne;
+                    nbw[j] = (ng > 1 && inb[j]) ? __ldg(gb[j] + 1) : kOne;
+                }
+                auto pick = [](const uint4 &v, int k) { return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w; };
+                bool stop = false;
+                for (int c = 0; c < C; ++c, ++it) {
+                    const int s = it % stages;
+                    if (it >= stages && !mbar_wait(&sh.empty[s], ((it / stages) - 1) & 1, status, kSiteScale)) {
+                        atomicExch(&sh.aborted, 1);
+                        stop = true;
+                    }
+                    stop = __any_sync(0xffffffffu, stop) || *((volatile int32_t *)&sh.aborted);
+                    if (stop) break;
+                    const int k = c & 3;
+                    const uint32_t sf = tmem + (uint32_t)(kSf + kSlot * s) + qlane;
+                    const uint32_t aw = pick(ca, k);
+                    tmem_st4(sf, aw, aw, aw, aw);  // column `quarter` of the four is the one read
+#pragma unroll
+                    for (int j = 0; j < kBcols; j += 4)
+                        tmem_st4(sf + kBoff + j, pick(cbw[j], k), pick(cbw[j + 1], k), pick(cbw[j + 2], k),
+                                 pick(cbw[j + 3], k));
+                    if (k == 3) {  // next group; fetch the one after
+                        const int gn = c / 4 + 2;
+                        ca = na;
+                        na = (gn < ng && ra < M) ? __ldg(ga + gn) : kOne;
+#pragma unroll
+                        for (int j = 0; j < kBcols; ++j) {
+                            cbw[j] = nbw[j];
+                            nbw[j] = (gn < ng && inb[j]) ? __ldg(gb[j] + gn) : kOne;
+                        }
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sh.sfull[s]);
+                }
+                if (stop) break;
+                continue;
+            }
             // The words of chunks c..c+3 are in flight together (a[d], bw[j][d] = chunk c + d), so the
             // L2 round trip of a chunk's words overlaps the three chunks before it.
             constexpr int PD = 4;
@@ -564,10 +618,16 @@ int init_mxfp8() {
         const int e = (int)cudaFuncSetAttribute(pick_mx(M), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e) return e;
     }
-    int e = (int)cudaFuncSetAttribute(mxtile_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    int e = (int)cudaFuncSetAttribute(mxtile_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       mxtile_smem_bytes(mxtile_max_stages(128), 128));
     if (!e)
-        e = (int)cudaFuncSetAttribute(mxtile_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = (int)cudaFuncSetAttribute(mxtile_kernel<256, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      mxtile_smem_bytes(mxtile_max_stages(256), 256));
+    if (!e)
+        e = (int)cudaFuncSetAttribute(mxtile_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      mxtile_smem_bytes(mxtile_max_stages(128), 128));
+    if (!e)
+        e = (int)cudaFuncSetAttribute(mxtile_kernel<256, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       mxtile_smem_bytes(mxtile_max_stages(256), 256));
     return e;
 }
@@ -593,7 +653,11 @@ int launch_mxfp8_tile(const void *xq, const void *xs, const void *wq, const void
     attr[0].val.programmaticStreamSerializationAllowed = pdl_attr_of(flags);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return (int)cudaLaunchKernelEx(&cfg, bq == 128 ? mxtile_kernel<128> : mxtile_kernel<256>, tx, tw,
+    // 16-byte scale reads when every scale row starts on a 16-byte boundary
+    const bool v4 = K % 512 == 0 && ((reinterpret_cast<uintptr_t>(xs) | reinterpret_cast<uintptr_t>(ws)) & 15u) == 0;
+    auto fn = bq == 128 ? (v4 ? mxtile_kernel<128, true> : mxtile_kernel<128, false>)
+                        : (v4 ? mxtile_kernel<256, true> : mxtile_kernel<256, false>);
+    return (int)cudaLaunchKernelEx(&cfg, fn, tx, tw,
                                    static_cast<const uint8_t *>(xs), static_cast<const uint8_t *>(ws),
                                    static_cast<const uint16_t *>(bias), static_cast<uint16_t *>(out), M, N, K, stages,
                                    group, status);
