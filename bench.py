@@ -140,6 +140,15 @@ def ncu_traffic(kernel_name, shapes):
     return int(sum(vals) / len(vals)) if vals else None
 
 
+# clock-event reasons that make a timed region unrepresentative (sw_power_cap is kept and noted)
+SLOWDOWN_REASONS = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+
+
+def slowdowns(clocks):
+    """The reasons in a ClockSampler record that call for timing the region again."""
+    return sorted(set(clocks.get("reasons", [])) & SLOWDOWN_REASONS)
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -367,25 +376,32 @@ def gpu_arm(args, points, rank, world):
             step()
     torch.cuda.synchronize()
 
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in shapes] for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    sampler = ClockSampler(torch.cuda.current_device())
-    sampler.start()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        t0.record(stream)
-        for k in range(args.steps):
-            step(ev[k])
-        t1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    clocks = sampler.stop()
-    total_ms = t0.elapsed_time(t1)
+    def timed_region():
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in shapes] for _ in range(args.steps)]
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        sampler = ClockSampler(torch.cuda.current_device())
+        sampler.start()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for k in range(args.steps):
+                step(ev[k])
+            t1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        return ev, t0.elapsed_time(t1), sampler.stop()
+
+    ev, total_ms, clocks = timed_region()
+    # A region that saw a hardware or thermal slowdown is timed once more (on every rank, if any saw one).
+    slowed = slowdowns(clocks)
+    if (max_over_ranks(1.0 if slowed else 0.0, device="cuda") if world > 1 else (1.0 if slowed else 0.0)) > 0:
+        ev, total_ms, clocks = timed_region()
+        clocks = dict(clocks, remeasured_after=slowed or ["another rank's slowdown"])
     per_shape_us = []
     for j, s in enumerate(shapes):
         ms = [ev[k][j][0].elapsed_time(ev[k][j][1]) for k in range(args.steps)]

@@ -94,3 +94,30 @@ def test_committed_traffic_matches_the_router_kernel():
     assert t is not None and t > 0
     algo = sum(bench.algo_bytes(m, n, k, False) for (m, n, k) in some) / len(some)
     assert 0.95 < t / algo < 1.2
+
+
+class _FakeSmi:
+    def terminate(self):
+        pass
+
+    def wait(self, timeout=None):
+        return 0
+
+
+def test_clock_record_and_slowdown_retime_rule():
+    """The nvidia-smi lines become the clocks record; hardware and thermal slowdowns call for a
+    second timed region, a power cap alone does not."""
+    s = bench.ClockSampler(0)
+    s.proc = _FakeSmi()
+    s.lines = ["0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+               "0, 1980, 2070, 1390.5, 0x4, Not Active, Not Active, Not Active, Active",
+               "0, 2070, 2070, 1200.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+               "garbage"]
+    c = s.stop()
+    assert c["sm_mhz"] == 2070.0 and c["sm_max_mhz"] == 2070.0 and c["samples"] == 3
+    assert c["reasons"] == ["sw_power_cap"] and bench.slowdowns(c) == []
+    s.lines.append("0, 1500, 2070, 1400.0, 0x88, Active, Not Active, Active, Not Active")
+    c = s.stop()
+    assert c["reasons"] == ["hw_slowdown", "sw_power_cap", "sw_thermal_slowdown"]
+    assert bench.slowdowns(c) == ["hw_slowdown", "sw_thermal_slowdown"]
+    assert bench.slowdowns({"sm_mhz": None, "reasons": ["nvidia-smi unavailable"]}) == []
